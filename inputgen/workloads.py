@@ -1,0 +1,182 @@
+"""The workloads: Commands, views and input recipes, as plain data.
+
+A workload ("spec") is a dict:
+
+``name``      short identifier
+``seed``      generator seed; tensor ``k`` of ``inputs`` draws stream ``k``
+``sizes``     logical sizes shared by every tensor of the Command (row-major)
+``ops``       the Command, in tag order:
+              ``("load", name, dtype)``            Load_Tensor
+              ``("scalar", name, dtype, value)``   Load_Scalar
+              ``("exec", [(eop, name, a, b), ...])`` one T_Execute block;
+                                                   eop in add/sub/mul/neg,
+                                                   b is None for neg
+              ``("store", name, src, dtype)``      Store_Tensor
+``views``     per load/store name: ``strides`` (elements) and ``alloc``
+              (elements in the physical buffer)
+``inputs``    per load name: (distribution kind, lo, hi) for inputgen
+
+Nothing here computes the Command; the oracle side and the CUDA side each
+build their own Command from the same spec.
+"""
+from __future__ import annotations
+
+DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
+
+
+def _dense(sizes):
+    strides, acc = [], 1
+    for s in reversed(sizes):
+        strides.append(acc)
+        acc *= s
+    return tuple(reversed(strides)), acc
+
+
+def add_f32(n: int = 1 << 20) -> dict:
+    """z = x + y, fp32, contiguous 1-D, x and y uniform[-1, 1], seed 0."""
+    st, al = _dense((n,))
+    return dict(
+        name="add_f32", seed=0, sizes=(n,),
+        ops=[("load", "x", "f32"), ("load", "y", "f32"),
+             ("exec", [("add", "z", "x", "y")]),
+             ("store", "out", "z", "f32")],
+        views={k: dict(strides=st, alloc=al) for k in ("x", "y", "out")},
+        inputs={"x": ("uniform_f32", -1.0, 1.0), "y": ("uniform_f32", -1.0, 1.0)},
+    )
+
+
+def chain_f32(n: int = 1 << 26) -> dict:
+    """out = (a*b) - (c + a)*s, s = 0.75, fp32 contiguous, a, b, c normal(0,1).
+
+    Tag ``a`` is referenced twice; it is still read from memory once."""
+    st, al = _dense((n,))
+    return dict(
+        name="chain_f32", seed=1, sizes=(n,),
+        ops=[("load", "a", "f32"), ("load", "b", "f32"), ("load", "c", "f32"),
+             ("scalar", "s", "f32", 0.75),
+             ("exec", [("mul", "ab", "a", "b"),
+                       ("add", "ca", "c", "a"),
+                       ("mul", "cas", "ca", "s"),
+                       ("sub", "r", "ab", "cas")]),
+             ("store", "out", "r", "f32")],
+        views={k: dict(strides=st, alloc=al) for k in ("a", "b", "c", "out")},
+        inputs={k: ("normal_f32", 0.0, 0.0) for k in ("a", "b", "c")},
+    )
+
+
+def wrap_i32(n: int = 1 << 28) -> dict:
+    """out = x*y + z - w in int32 with two's-complement wraparound, seed 2."""
+    st, al = _dense((n,))
+    return dict(
+        name="wrap_i32", seed=2, sizes=(n,),
+        ops=[("load", "x", "i32"), ("load", "y", "i32"), ("load", "z", "i32"),
+             ("load", "w", "i32"),
+             ("exec", [("mul", "xy", "x", "y"),
+                       ("add", "xyz", "xy", "z"),
+                       ("sub", "r", "xyz", "w")]),
+             ("store", "out", "r", "i32")],
+        views={k: dict(strides=st, alloc=al) for k in ("x", "y", "z", "w", "out")},
+        inputs={k: ("u32", 0.0, 0.0) for k in ("x", "y", "z", "w")},
+    )
+
+
+def strided_bf16(m: int = 8192, n: int = 8192, ld_a: int = 8320) -> dict:
+    """out = A*B^T - A + 0.5 in fp32, bf16 in and out, values uniform[-4, 4].
+
+    A is m x n row-major with leading dimension ld_a; B is an n x m row-major
+    tensor read through its transpose view (strides {1, m}); out is dense."""
+    return dict(
+        name="strided_bf16", seed=3, sizes=(m, n),
+        ops=[("load", "A", "bf16"), ("load", "B", "bf16"),
+             ("scalar", "h", "f32", 0.5),
+             ("exec", [("mul", "AB", "A", "B"),
+                       ("sub", "ABA", "AB", "A"),
+                       ("add", "r", "ABA", "h")]),
+             ("store", "out", "r", "bf16")],
+        views={"A": dict(strides=(ld_a, 1), alloc=(m - 1) * ld_a + n if m else 0),
+               "B": dict(strides=(1, m), alloc=m * n),
+               "out": dict(strides=(n, 1), alloc=m * n)},
+        inputs={"A": ("uniform_bf16_trunc", -4.0, 4.0),
+                "B": ("uniform_bf16_trunc", -4.0, 4.0)},
+    )
+
+
+# The 16 E ops of the wide DAG, in tag order; ``t10`` repeats ``t1`` with its
+# operands swapped, so common-subexpression reuse maps it onto ``t1``.
+WIDE_DAG = [
+    ("add", "t1", "a", "b"),
+    ("mul", "t2", "c", "d"),
+    ("sub", "t3", "t1", "t2"),
+    ("mul", "t4", "e", "s"),
+    ("neg", "t5", "f", None),
+    ("add", "t6", "t3", "t4"),
+    ("mul", "t7", "t1", "t5"),
+    ("sub", "t8", "t6", "t7"),
+    ("add", "t9", "t2", "r"),
+    ("add", "t10", "b", "a"),
+    ("mul", "t11", "t10", "t9"),
+    ("neg", "t12", "t3", None),
+    ("add", "t13", "t11", "t12"),
+    ("mul", "t14", "t8", "t13"),
+    ("sub", "t15", "t4", "t5"),
+    ("add", "t16", "t14", "t15"),
+]
+
+
+def wide_dag(n: int = 1 << 27) -> dict:
+    """Six fp32 inputs normal(0,1), scalars 1.5 and -0.25, 16 E ops with
+    shared subexpressions, stores out0 (fp32) <- t16 and out1 (fp16) <- t13."""
+    st, al = _dense((n,))
+    names = ("a", "b", "c", "d", "e", "f")
+    return dict(
+        name="wide_dag", seed=4, sizes=(n,),
+        ops=[("load", k, "f32") for k in names]
+        + [("scalar", "s", "f32", 1.5), ("scalar", "r", "f32", -0.25),
+           ("exec", list(WIDE_DAG)),
+           ("store", "out0", "t16", "f32"), ("store", "out1", "t13", "f16")],
+        views={k: dict(strides=st, alloc=al) for k in names + ("out0", "out1")},
+        inputs={k: ("normal_f32", 0.0, 0.0) for k in names},
+    )
+
+
+# Full-size workloads, in the order they are listed for this path.
+FULL = {
+    "add_f32": add_f32,
+    "chain_f32": chain_f32,
+    "wrap_i32": wrap_i32,
+    "strided_bf16": strided_bf16,
+    "wide_dag": wide_dag,
+}
+
+
+def load_names(spec: dict) -> list:
+    return [op[1] for op in spec["ops"] if op[0] == "load"]
+
+
+def store_names(spec: dict) -> list:
+    return [op[1] for op in spec["ops"] if op[0] == "store"]
+
+
+def tensor_dtypes(spec: dict) -> dict:
+    out = {}
+    for op in spec["ops"]:
+        if op[0] in ("load", "store"):
+            out[op[1]] = op[2] if op[0] == "load" else op[3]
+    return out
+
+
+def numel(spec: dict) -> int:
+    n = 1
+    for s in spec["sizes"]:
+        n *= s
+    return n
+
+
+def algorithmic_bytes(spec: dict, live_loads=None) -> int:
+    """Bytes one pass moves: every live loaded tensor read once and every
+    store written once, over the logical elements (padding not counted)."""
+    dt = tensor_dtypes(spec)
+    n = numel(spec)
+    loads = live_loads if live_loads is not None else load_names(spec)
+    return n * (sum(DTYPE_BYTES[dt[k]] for k in loads)
+                + sum(DTYPE_BYTES[dt[k]] for k in store_names(spec)))

@@ -1,0 +1,351 @@
+/*
+ * cmd_oracle.c - plain, slow CPU oracle for fused Command execution.
+ *
+ * TEST INFRASTRUCTURE: see cmd_oracle.h for who may use it and for the
+ * readings of the pages it follows. Build with -ffp-contract=off and without
+ * fast-math (a compiler that contracts a*b+c into one fused op, or flushes
+ * denormals, would no longer compute the definition).
+ */
+#include "cmd_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- bits <-> values --------------------------------------------------- */
+
+static float as_float(uint32_t u) {
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static uint32_t as_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return u;
+}
+
+/* ---- E operations (rocRoller Design Overview, "Operations": the T_Execute
+ * block's E_ ops act elementwise on vectors or scalars) ------------------- */
+
+/* Float E ops: exact result in binary64 (the product of two 24-bit
+ * significands is exact; a sum is rounded to 53 bits), then one rounding to
+ * binary32 by the C conversion, which rounds to nearest even. */
+uint32_t orc_fadd(uint32_t x, uint32_t y) {
+  double r = (double)as_float(x) + (double)as_float(y);
+  return as_bits((float)r);
+}
+
+uint32_t orc_fsub(uint32_t x, uint32_t y) {
+  double r = (double)as_float(x) - (double)as_float(y);
+  return as_bits((float)r);
+}
+
+uint32_t orc_fmul(uint32_t x, uint32_t y) {
+  double r = (double)as_float(x) * (double)as_float(y);
+  return as_bits((float)r);
+}
+
+/* Negation is the IEEE 754 sign flip. */
+uint32_t orc_fneg(uint32_t x) { return x ^ 0x80000000u; }
+
+/* int32 E ops: two's complement, i.e. arithmetic modulo 2^32 on the bits. */
+uint32_t orc_iadd(uint32_t x, uint32_t y) { return (uint32_t)(x + y); }
+uint32_t orc_isub(uint32_t x, uint32_t y) { return (uint32_t)(x - y); }
+uint32_t orc_imul(uint32_t x, uint32_t y) {
+  return (uint32_t)((uint64_t)x * (uint64_t)y);
+}
+uint32_t orc_ineg(uint32_t x) { return (uint32_t)(0u - x); }
+
+/* ---- conversions ------------------------------------------------------- */
+
+/* Round a non-negative finite value v (exactly representable in binary64)
+ * to the nearest multiple of 2^q, ties to the even multiple. */
+static double round_to_quantum(double v, int q) {
+  double m = ldexp(v, -q);       /* exact: scaling by a power of two */
+  double fl = floor(m);
+  double fr = m - fl;            /* exact: m has at most 24 significant bits */
+  if (fr > 0.5 || (fr == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+  return ldexp(fl, q);
+}
+
+/* Round binary32 value bits to a binary format with p significand bits
+ * (including the implicit one), minimum normal exponent emin and exponent
+ * bias, and return the encoding of the rounded magnitude (sign excluded).
+ * Overflow (rounded value >= 2^(emax+1)) gives the infinity encoding. */
+static uint32_t round_magnitude(uint32_t xb, int p, int emin, int emax) {
+  double v = fabs((double)as_float(xb));
+  if (v == 0.0) return 0u;
+  int e;
+  frexp(v, &e);                  /* v = f * 2^e with f in [0.5, 1) */
+  int E = e - 1;                 /* 2^E <= v < 2^(E+1) */
+  int q = (E >= emin) ? (E - (p - 1)) : (emin - (p - 1));
+  double r = round_to_quantum(v, q);
+  int frac_bits = p - 1;
+  uint32_t exp_all_ones = (uint32_t)(2 * emax + 1); /* biased exponent of inf */
+  if (r >= ldexp(1.0, emax + 1)) return exp_all_ones << frac_bits;
+  if (r < ldexp(1.0, emin)) {
+    /* subnormal: significand = r / 2^(emin - (p-1)), biased exponent 0 */
+    return (uint32_t)ldexp(r, -(emin - (p - 1)));
+  }
+  frexp(r, &e);
+  E = e - 1;
+  uint32_t sig = (uint32_t)ldexp(r, -(E - (p - 1))); /* in [2^(p-1), 2^p) */
+  uint32_t frac = sig - (1u << frac_bits);
+  uint32_t biased = (uint32_t)(E + emax);            /* bias = emax */
+  return (biased << frac_bits) | frac;
+}
+
+/* binary32 -> binary16: p = 11, emin = -14, emax = 15. */
+uint16_t orc_f32_to_f16(uint32_t x) {
+  uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  uint32_t ax = x & 0x7fffffffu;
+  if (ax > 0x7f800000u) return (uint16_t)(sign | 0x7e00u); /* NaN -> quiet NaN */
+  if (ax == 0x7f800000u) return (uint16_t)(sign | 0x7c00u);
+  return (uint16_t)(sign | round_magnitude(x, 11, -14, 15));
+}
+
+/* binary32 -> bfloat16: p = 8, emin = -126, emax = 127. */
+uint16_t orc_f32_to_bf16(uint32_t x) {
+  uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  uint32_t ax = x & 0x7fffffffu;
+  if (ax > 0x7f800000u) return (uint16_t)(sign | 0x7fc0u); /* NaN -> quiet NaN */
+  if (ax == 0x7f800000u) return (uint16_t)(sign | 0x7f80u);
+  return (uint16_t)(sign | round_magnitude(x, 8, -126, 127));
+}
+
+/* binary16 -> binary32, exact. */
+uint32_t orc_f16_to_f32(uint16_t h) {
+  uint32_t sign = ((uint32_t)h & 0x8000u) << 16;
+  int E = (h >> 10) & 0x1f;
+  int F = h & 0x3ff;
+  if (E == 31) return sign | (F ? 0x7fc00000u : 0x7f800000u);
+  double v = (E == 0) ? ldexp((double)F, -24) : ldexp((double)(1024 + F), E - 25);
+  return sign | as_bits((float)v); /* exact: at most 11 significant bits */
+}
+
+/* bfloat16 is by definition the upper half of a binary32 encoding. */
+uint32_t orc_bf16_to_f32(uint16_t h) { return ((uint32_t)h) << 16; }
+
+void orc_f32_to_f16_n(const uint32_t* x, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_f16(x[i]);
+}
+
+void orc_f32_to_bf16_n(const uint32_t* x, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(x[i]);
+}
+
+/* ---- the Command walk -------------------------------------------------- */
+
+enum { CLS_FLOAT = 0, CLS_INT = 1 };
+
+static size_t elem_size(int dtype) {
+  return (dtype == ORC_F16 || dtype == ORC_BF16) ? 2u : 4u;
+}
+
+/* Value class of every tag; checks operand classes and store types. */
+static int classify(const orc_command* c, int* cls) {
+  for (int t = 0; t < c->n_ops; ++t) {
+    const orc_op* op = &c->ops[t];
+    switch (op->kind) {
+      case ORC_LOAD_TENSOR:
+        if (op->dtype < ORC_F32 || op->dtype > ORC_I32) return ORC_ETYPE;
+        cls[t] = (op->dtype == ORC_I32) ? CLS_INT : CLS_FLOAT;
+        break;
+      case ORC_LOAD_SCALAR:
+        if (op->dtype != ORC_F32 && op->dtype != ORC_I32) return ORC_ETYPE;
+        cls[t] = (op->dtype == ORC_I32) ? CLS_INT : CLS_FLOAT;
+        break;
+      case ORC_ADD:
+      case ORC_SUB:
+      case ORC_MUL:
+        if (op->a < 0 || op->a >= t || op->b < 0 || op->b >= t) return ORC_EBAD;
+        if (c->ops[op->a].kind == ORC_STORE || c->ops[op->b].kind == ORC_STORE) return ORC_EBAD;
+        if (cls[op->a] != cls[op->b]) return ORC_ETYPE;
+        cls[t] = cls[op->a];
+        break;
+      case ORC_NEG:
+        if (op->a < 0 || op->a >= t) return ORC_EBAD;
+        if (c->ops[op->a].kind == ORC_STORE) return ORC_EBAD;
+        cls[t] = cls[op->a];
+        break;
+      case ORC_STORE:
+        if (op->a < 0 || op->a >= t) return ORC_EBAD;
+        if (c->ops[op->a].kind == ORC_STORE) return ORC_EBAD;
+        if (op->dtype < ORC_F32 || op->dtype > ORC_I32) return ORC_ETYPE;
+        if ((op->dtype == ORC_I32) != (cls[op->a] == CLS_INT)) return ORC_ETYPE;
+        cls[t] = -1;
+        break;
+      default:
+        return ORC_EBAD;
+    }
+  }
+  return ORC_OK;
+}
+
+/* Element offset of a logical multi-index in a view: sum of index * stride. */
+static int64_t view_offset(const orc_op* op, const int64_t* idx, int rank) {
+  int64_t off = 0;
+  for (int k = 0; k < rank; ++k) off += idx[k] * op->strides[k];
+  return off;
+}
+
+static uint32_t load_elem(const orc_op* op, int64_t off) {
+  const char* base = (const char*)op->ptr + off * (int64_t)elem_size(op->dtype);
+  switch (op->dtype) {
+    case ORC_F16: {
+      uint16_t h;
+      memcpy(&h, base, 2);
+      return orc_f16_to_f32(h);
+    }
+    case ORC_BF16: {
+      uint16_t h;
+      memcpy(&h, base, 2);
+      return orc_bf16_to_f32(h);
+    }
+    default: {
+      uint32_t u;
+      memcpy(&u, base, 4);
+      return u;
+    }
+  }
+}
+
+/* Convert a value to a store's element type, writing elem_size bytes. */
+static void convert_store(int dtype, uint32_t v, void* dst) {
+  if (dtype == ORC_F16) {
+    uint16_t h = orc_f32_to_f16(v);
+    memcpy(dst, &h, 2);
+  } else if (dtype == ORC_BF16) {
+    uint16_t h = orc_f32_to_bf16(v);
+    memcpy(dst, &h, 2);
+  } else {
+    memcpy(dst, &v, 4);
+  }
+}
+
+/* Evaluate all tags at one logical index. When `points` is non-null the s-th
+ * store writes element `pi` of points[s] instead of its view. */
+static void eval_one(const orc_command* c, const int* cls, uint32_t* val,
+                     const int64_t* idx, void* const* points, int64_t pi) {
+  int s = 0;
+  for (int t = 0; t < c->n_ops; ++t) {
+    const orc_op* op = &c->ops[t];
+    switch (op->kind) {
+      case ORC_LOAD_TENSOR:
+        val[t] = load_elem(op, view_offset(op, idx, c->rank));
+        break;
+      case ORC_LOAD_SCALAR:
+        val[t] = op->scalar_bits;
+        break;
+      case ORC_ADD:
+        val[t] = cls[t] == CLS_INT ? orc_iadd(val[op->a], val[op->b])
+                                   : orc_fadd(val[op->a], val[op->b]);
+        break;
+      case ORC_SUB:
+        val[t] = cls[t] == CLS_INT ? orc_isub(val[op->a], val[op->b])
+                                   : orc_fsub(val[op->a], val[op->b]);
+        break;
+      case ORC_MUL:
+        val[t] = cls[t] == CLS_INT ? orc_imul(val[op->a], val[op->b])
+                                   : orc_fmul(val[op->a], val[op->b]);
+        break;
+      case ORC_NEG:
+        val[t] = cls[t] == CLS_INT ? orc_ineg(val[op->a]) : orc_fneg(val[op->a]);
+        break;
+      case ORC_STORE: {
+        size_t es = elem_size(op->dtype);
+        char* dst;
+        if (points) {
+          dst = (char*)points[s] + pi * (int64_t)es;
+        } else {
+          dst = (char*)op->ptr + view_offset(op, idx, c->rank) * (int64_t)es;
+        }
+        convert_store(op->dtype, val[op->a], dst);
+        ++s;
+        break;
+      }
+    }
+  }
+}
+
+/* Row-major logical multi-index of a linear index (Flatten's order). */
+static void unflatten(const orc_command* c, int64_t lin, int64_t* idx) {
+  for (int k = c->rank - 1; k >= 0; --k) {
+    idx[k] = lin % c->sizes[k];
+    lin /= c->sizes[k];
+  }
+}
+
+static int64_t total_elems(const orc_command* c) {
+  int64_t n = 1;
+  for (int k = 0; k < c->rank; ++k) n *= c->sizes[k];
+  return n;
+}
+
+static int check_command(const orc_command* c) {
+  if (!c || c->n_ops < 0 || (c->n_ops > 0 && !c->ops)) return ORC_EBAD;
+  if (c->rank < 0 || c->rank > ORC_MAX_RANK) return ORC_EBAD;
+  for (int k = 0; k < c->rank; ++k)
+    if (c->sizes[k] < 0) return ORC_EBAD;
+  return ORC_OK;
+}
+
+int orc_eval_range(const orc_command* c, int64_t begin, int64_t end) {
+  int rc = check_command(c);
+  if (rc) return rc;
+  int64_t n = total_elems(c);
+  if (begin < 0) begin = 0;
+  if (end > n) end = n;
+  if (begin >= end || c->n_ops == 0) return ORC_OK;
+  int* cls = (int*)malloc(sizeof(int) * (size_t)c->n_ops);
+  uint32_t* val = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)c->n_ops);
+  if (!cls || !val) {
+    free(cls);
+    free(val);
+    return ORC_ENOMEM;
+  }
+  rc = classify(c, cls);
+  if (rc == ORC_OK) {
+    int64_t idx[ORC_MAX_RANK] = {0, 0, 0, 0};
+    for (int64_t e = begin; e < end; ++e) {
+      unflatten(c, e, idx);
+      eval_one(c, cls, val, idx, NULL, 0);
+    }
+  }
+  free(cls);
+  free(val);
+  return rc;
+}
+
+int orc_eval_points(const orc_command* c, const int64_t* lin, int64_t n,
+                    void* const* store_out) {
+  int rc = check_command(c);
+  if (rc) return rc;
+  if (n <= 0 || c->n_ops == 0) return ORC_OK;
+  if (!lin || !store_out) return ORC_EBAD;
+  int64_t total = total_elems(c);
+  int* cls = (int*)malloc(sizeof(int) * (size_t)c->n_ops);
+  uint32_t* val = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)c->n_ops);
+  if (!cls || !val) {
+    free(cls);
+    free(val);
+    return ORC_ENOMEM;
+  }
+  rc = classify(c, cls);
+  if (rc == ORC_OK) {
+    int64_t idx[ORC_MAX_RANK] = {0, 0, 0, 0};
+    for (int64_t i = 0; i < n; ++i) {
+      if (lin[i] < 0 || lin[i] >= total) {
+        rc = ORC_EBAD;
+        break;
+      }
+      unflatten(c, lin[i], idx);
+      eval_one(c, cls, val, idx, store_out, i);
+    }
+  }
+  free(cls);
+  free(val);
+  return rc;
+}
