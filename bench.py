@@ -1,0 +1,469 @@
+"""Benchmark: fused Command throughput on GB300 (HBM GB/s, fraction of the
+HBM roofline, elements/s).
+
+One step = one fused pass of the Command over one batch of synthetic input:
+the workload is the fp32 chain out = (a*b) - (c + a)*s over N = 2^26
+elements (three 256 MiB inputs, one 256 MiB output), inputs resident in HBM.
+The line also carries per-workload measurements of the other Commands
+(add, int32 wraparound, strided bf16 transpose, wide 16-op DAG) at their full
+sizes, an end-to-end figure through the same API with host buffers and the
+copies inside the timed region, the roofline of the executor kernel, SM
+clocks sampled during the timed region, and the CPU oracle timed on a
+bounded sample as a reported baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--headline-only]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path has no exchange step); value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from inputgen import workloads as W  # noqa: E402
+
+HEADLINE = "chain_f32"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "fused Command throughput: HBM GB/s and % of GB300 HBM roofline (elements/s)"
+NP_OF = {"f32": np.float32, "f16": np.float16, "bf16": np.int16, "i32": np.int32}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=list(W.FULL))
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_command_execution_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    from the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    s = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, taken while the
+    timed region runs (start before, stop after)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = (0.0, 0.0)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        t0, t1 = self.window
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        scope = "timed"
+        if len(inside) < 2:
+            inside = [s for t, s in self.samples]
+            scope = "timed+surrounding (timed region shorter than the sampling period)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        mx = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if len(s) > 4 + i and s[4 + i] == "Active"})
+        power = [num(s[2]) for s in inside if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "scope": scope,
+                "power_w_max": max(power) if power else None}
+
+
+def host_inputs(spec, pinned: bool):
+    """Seeded inputs in (pinned) host memory, filled in place by inputgen."""
+    import torch
+
+    import inputgen
+    dts = W.tensor_dtypes(spec)
+    out = {}
+    for k, name in enumerate(W.load_names(spec)):
+        kind, lo, hi = spec["inputs"][name]
+        n = spec["views"][name]["alloc"]
+        t = torch.empty(n, dtype=getattr(torch, {"f32": "float32", "f16": "float16", "bf16": "int16",
+                                                  "i32": "int32"}[dts[name]]), pin_memory=pinned)
+        inputgen.fill_ptr(kind, spec["seed"], k, t.data_ptr(), n, lo, hi)
+        out[name] = t
+    return out
+
+
+def torch_dtype(dt):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.int16, "i32": torch.int32}[dt]
+
+
+class Workload:
+    """A compiled Command with device buffers and pre-built launch arguments."""
+
+    def __init__(self, spec, device):
+        import torch
+
+        import tensor_command_execution_gb300 as T
+        self.spec = spec
+        self.dts = W.tensor_dtypes(spec)
+        self.host = host_inputs(spec, pinned=True)
+        self.dev = {n: t.to(device) for n, t in self.host.items()}
+        for n in W.store_names(spec):
+            self.dev[n] = torch.empty(spec["views"][n]["alloc"], dtype=torch_dtype(self.dts[n]), device=device)
+        self.cmd, self.tags = T.command_from_spec(spec)
+        self.kernel = self.cmd.compile()
+        self.views = {self.tags[n]: T.TensorView(t.data_ptr(), spec["sizes"], spec["views"][n]["strides"])
+                      for n, t in self.dev.items()}
+        self.scal = T.spec_scalars(spec, self.tags)
+        self.args = self.kernel.args(self.views, self.scal)
+        self.plan = self.kernel.plan(self.views, self.scal)
+        self.bytes = self.plan["bytes"]
+        self.elements = self.plan["n_elements"]
+        chunk = 32 * {0: 8, 1: 4, 2: 2}[self.kernel.info()["tier"]]
+        self.launches_per_step = 1 + (1 if (self.plan["path"] == "contig" and self.elements % chunk != 0) else 0)
+
+    def launch(self, stream_handle):
+        self.kernel.launch_args(self.args, stream_handle)
+
+
+def time_device(wl, stream, steps, warmup):
+    """K launches between CUDA events on the launching stream; ms per step."""
+    import torch
+    h = stream.cuda_stream
+    for _ in range(warmup):
+        wl.launch(h)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        wl.launch(h)
+    stop.record(stream)
+    stop.synchronize()
+    return start.elapsed_time(stop) / steps
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = measured_peak()
+
+    spec = W.FULL[args.workload]()
+    wl = Workload(spec, device)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region -------------------------------------------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        wl.launch(stream.cuda_stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        wl.launch(stream.cuda_stream)
+    stop.record(stream)
+    stop.synchronize()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks.mark(t0, t1)
+    clocks.stop()
+    ms = start.elapsed_time(stop) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    gbs = wl.bytes / (ms * 1e-3) / 1e9
+    value = gbs * world
+
+    # ---- end to end: pinned host inputs -> device, launch, output -> host ----
+    outs_host = {n: torch.empty_like(wl.dev[n], device="cpu").pin_memory() for n in W.store_names(spec)}
+    h2d = sum(t.numel() * t.element_size() for t in wl.host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for n, t in wl.host.items():
+                wl.dev[n].copy_(t, non_blocking=True)
+            wl.launch(stream.cuda_stream)
+            for n, t in outs_host.items():
+                t.copy_(wl.dev[n], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_gbs = wl.bytes / (e2e_ms * 1e-3) / 1e9 * world
+
+    # ---- other workloads, same kernels, full sizes (per-rank, informative) ---
+    per = {}
+    if not args.headline_only and rank == 0:
+        for name, f in W.FULL.items():
+            if name == args.workload:
+                continue
+            other = Workload(f(), device)
+            steps = max(20, min(2000, int(0.5 / max(1e-6, other.bytes / (peak * 1e9)))))
+            oms = time_device(other, stream, steps, 10)
+            ogbs = other.bytes / (oms * 1e-3) / 1e9
+            per[name] = {"path": other.plan["path"], "elements": other.elements, "bytes_per_launch": other.bytes,
+                         "us_per_launch": round(oms * 1e3, 2), "gbs": round(ogbs, 1),
+                         "frac_of_measured_peak": round(ogbs / peak, 4),
+                         "frac_of_nominal_8000": round(ogbs / NOMINAL_HBM_GBS, 4),
+                         "elements_per_s": round(other.elements / (oms * 1e-3), 1), "steps": steps}
+            del other
+            torch.cuda.empty_cache()
+
+    # ---- CPU oracle on a bounded sample (rank 0) --------------------------------
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = cpu_baseline(spec, args.cpu_seconds)
+
+    if rank == 0:
+        kernel_name = {"contig": "exec_contig", "tile2d": "exec_tile2d", "generic": "exec_generic"}[wl.plan["path"]]
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
+                      "wide_dag": "f32 (f32+f16 out)"}[args.workload],
+            "data": "synthetic (seeded SplitMix64 inputs; no dataset)",
+            "config": {"workload": f"{args.workload}: {spec_summary(spec)}", "elements": wl.elements,
+                       "bytes_per_step": wl.bytes, "path": wl.plan["path"],
+                       "l2": "inputs larger than L2 (%d MiB moved per step vs 126 MiB L2); no flush" %
+                             (wl.bytes >> 20),
+                       "parallelism": f"replicas x{world}"},
+            "elements_per_s": round(wl.elements * world / (ms * 1e-3), 1),
+            "frac_of_nominal_8000": round(gbs / NOMINAL_HBM_GBS, 4),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                         "kernel": kernel_name,
+                         "traffic": profiled_traffic(kernel_name, args.workload),
+                         "algorithmic_bytes_per_launch": wl.bytes},
+            "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps * wl.launches_per_step,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+            "workloads": per,
+            "impl": "ours",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def spec_summary(spec):
+    sizes = "x".join(str(s) for s in spec["sizes"])
+    return f"{sizes} elements, {len(W.load_names(spec))} loads, {len(W.store_names(spec))} stores"
+
+
+def cpu_baseline(spec, seconds):
+    """The oracle, as it stands, on the host: single-threaded element walk over
+    the first M elements of the same workload, M sized to about `seconds`."""
+    import oracle
+    bufs = {}
+    dts = W.tensor_dtypes(spec)
+    import inputgen
+    n_total = W.numel(spec)
+    # a bounded sample: first M logical elements (calibrated)
+    probe = min(n_total, 1 << 16)
+    for k, name in enumerate(W.load_names(spec)):
+        kind, lo, hi = spec["inputs"][name]
+        bufs[name] = inputgen.generate(kind, spec["seed"], k, spec["views"][name]["alloc"], lo, hi).view(
+            NP_OF[dts[name]] if dts[name] != "bf16" else np.uint16)
+    for name in W.store_names(spec):
+        bufs[name] = np.zeros(spec["views"][name]["alloc"], dtype=NP_OF[dts[name]])
+    oc = oracle.OracleCommand(spec, bufs)
+    t = time.perf_counter()
+    oc.eval_range(0, probe)
+    rate = probe / max(1e-9, time.perf_counter() - t)
+    m = int(min(n_total, max(probe, rate * seconds)))
+    t = time.perf_counter()
+    oc.eval_range(0, m)
+    dt = time.perf_counter() - t
+    bpe = W.algorithmic_bytes(spec) / n_total
+    return {"value": round(m * bpe / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {m} of {n_total} logical elements of the same workload, single thread, "
+                      f"{dt:.1f} s", "elements_per_s": round(m / dt, 1)}
+
+
+def run_reference(args):
+    """The oracle (the CPU reference of this path) timed on the host cores on
+    the same workload, metric and unit; each step a bounded sample."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import inputgen
+    import oracle
+    spec = W.FULL[args.workload]()
+    dts = W.tensor_dtypes(spec)
+    bufs = {}
+    for k, name in enumerate(W.load_names(spec)):
+        kind, lo, hi = spec["inputs"][name]
+        bufs[name] = inputgen.generate(kind, spec["seed"], k, spec["views"][name]["alloc"], lo, hi).view(
+            NP_OF[dts[name]] if dts[name] != "bf16" else np.uint16)
+    for name in W.store_names(spec):
+        bufs[name] = np.zeros(spec["views"][name]["alloc"], dtype=NP_OF[dts[name]])
+    oc = oracle.OracleCommand(spec, bufs)
+    n_total = W.numel(spec)
+    probe = min(n_total, 1 << 16)
+    t = time.perf_counter()
+    oc.eval_range(0, probe)
+    rate = probe / max(1e-9, time.perf_counter() - t)
+    budget = 120.0 / max(1, args.steps + args.warmup)  # whole run about two minutes
+    m = int(min(n_total, max(4096, rate * budget)))
+    for s in range(args.warmup):
+        oc.eval_range(s * m % n_total, s * m % n_total + m)
+    t = time.perf_counter()
+    for s in range(args.steps):
+        b = (s * m) % max(1, n_total - m)
+        oc.eval_range(b, b + m)
+    dt = (time.perf_counter() - t) / args.steps
+    bpe = W.algorithmic_bytes(spec) / n_total
+    val = m * bpe / dt / 1e9
+    line = {"metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {spec_summary(spec)}"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{m} consecutive logical elements per step of {n_total}"},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

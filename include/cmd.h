@@ -1,0 +1,240 @@
+/*
+ * cmd.h - fused tensor Command execution on one GPU (GB300, sm_103a): C ABI.
+ *
+ * A Command is built up from operations, each of which creates a tag that
+ * later operations refer to (rocRoller, "Design Overview", section "Command
+ * Class"). The operations here are the ones that section and section
+ * "Operations" describe: loading a tensor or a scalar, a T_Execute block of
+ * E_ operations applied elementwise to vectors or scalars, and storing a
+ * tensor. Load and store operations take their data as runtime arguments
+ * supplied at launch (section "CommandArgument"): a device pointer with the
+ * tensor's sizes and strides, or a scalar value. Tensor indexing follows the
+ * coordinate-transform reading of section "Kernel Graph": a tensor element
+ * at logical multi-index (i_0, ..., i_{r-1}) lives at element offset
+ * sum_k i_k * stride_k, and logical elements are ordered row-major (the
+ * Flatten transform).
+ *
+ * cmd_compile lowers a Command to a compact register-slot program (dead-tag
+ * elimination, common-subexpression reuse, slot allocation by liveness) held
+ * in GPU constant memory; cmd_launch runs it as one fused pass over the
+ * tensors (section "Command Kernel": a compiled Command is launched many
+ * times with different runtime arguments).
+ *
+ * Arithmetic. Float Commands compute in binary32 with one round-to-nearest-
+ * even rounding per E op and no fused multiply-add; denormals are kept.
+ * binary16 and bfloat16 loads widen exactly; stores to them round once, to
+ * nearest even (overflow to infinity). int32 Commands wrap modulo 2^32.
+ * E_Neg flips the sign bit of a float and is 0 - x for an int.
+ *
+ * Ownership. The library owns Command and kernel objects (create/destroy
+ * pairs below). The caller owns every device buffer and stream; buffers must
+ * stay valid until the launched work has completed on its stream. Scalar
+ * values are copied at launch.
+ *
+ * Errors. Every call returns a cmd_status; CMD_OK is 0. A failing call leaves
+ * its object unchanged and records a message for cmd_last_error() (per
+ * thread). Nothing is thrown across this interface. A launch is asynchronous:
+ * cmd_launch reports launch-phase errors and cmd_sync_status reports the
+ * completion phase.
+ *
+ * Threading. A Command or kernel object may be used by one thread at a time;
+ * distinct objects may be used concurrently.
+ */
+#ifndef CMD_H
+#define CMD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CMD_ABI_VERSION 1
+
+/* limits */
+#define CMD_MAX_RANK 4      /* logical dims of a tensor view */
+#define CMD_MAX_TAGS 128    /* operations (tags) in one Command */
+#define CMD_MAX_LOADS 16    /* live Load_Tensor ops after dead-tag elimination */
+#define CMD_MAX_STORES 8    /* Store_Tensor ops */
+#define CMD_MAX_SCALARS 16  /* live Load_Scalar ops */
+#define CMD_MAX_SLOTS 32    /* simultaneously live values in the lowered program */
+#define CMD_MAX_KERNELS 48  /* compiled kernels alive at once, per device */
+
+typedef enum cmd_status {
+  CMD_OK = 0,
+  CMD_ERR_NULL = 1,           /* a required pointer argument is NULL */
+  CMD_ERR_BAD_TAG = 2,        /* a tag does not name a usable earlier result */
+  CMD_ERR_TYPE = 3,           /* int/float mix, or a dtype not allowed here */
+  CMD_ERR_SHAPE = 4,          /* rank, size or stride mismatch / out of range */
+  CMD_ERR_ALIAS = 5,          /* a store overlaps another tensor argument */
+  CMD_ERR_ALIGN = 6,          /* a pointer is not aligned to its element size */
+  CMD_ERR_STATE = 7,          /* wrong object state (e.g. wrong device) */
+  CMD_ERR_LIMIT = 8,          /* a CMD_MAX_* limit would be exceeded */
+  CMD_ERR_CUDA = 9,           /* the CUDA runtime reported an error */
+  CMD_ERR_DEVICE_TIMEOUT = 10,/* a device-side wait gave up */
+  CMD_ERR_NOMEM = 11,         /* host allocation failed */
+  CMD_ERR_ARG = 12            /* runtime arguments missing, repeated or unknown */
+} cmd_status;
+
+typedef enum cmd_dtype { CMD_F32 = 0, CMD_F16 = 1, CMD_BF16 = 2, CMD_I32 = 3 } cmd_dtype;
+
+/* Elementwise operations of a T_Execute block. */
+typedef enum cmd_eop { CMD_E_ADD = 0, CMD_E_SUB = 1, CMD_E_MUL = 2, CMD_E_NEG = 3 } cmd_eop;
+
+typedef int32_t cmd_tag;
+typedef struct cmd_command* cmd_command_t;
+typedef struct cmd_kernel* cmd_kernel_t;
+
+/* Operand of an E op inside the same cmd_add_execute call: the result of the
+ * block's i-th op (i smaller than the referring op's index). */
+#define CMD_LOCAL(i) ((cmd_tag)(-1 - (i)))
+
+/* One E op: result = a (op) b; for CMD_E_NEG, result = -a and b is ignored.
+ * a and b are tags of earlier Load_Tensor, Load_Scalar or E results, or
+ * CMD_LOCAL(i). */
+typedef struct cmd_xop {
+  int32_t op; /* cmd_eop */
+  cmd_tag a;
+  cmd_tag b;
+} cmd_xop;
+
+/* Runtime argument of a Load_Tensor or Store_Tensor tag: a device pointer and
+ * the view. sizes are the logical sizes (equal for every tensor of the
+ * Command); strides are in elements, >= 0, one per logical dim. */
+typedef struct cmd_tensor_arg {
+  cmd_tag tag;
+  int32_t rank;
+  void* ptr;
+  int64_t sizes[CMD_MAX_RANK];
+  int64_t strides[CMD_MAX_RANK];
+} cmd_tensor_arg;
+
+/* Runtime argument of a Load_Scalar tag. Use .f32 for a CMD_F32 scalar and
+ * .i32 for a CMD_I32 scalar. */
+typedef struct cmd_scalar_arg {
+  cmd_tag tag;
+  union {
+    float f32;
+    int32_t i32;
+    uint32_t bits;
+  } v;
+} cmd_scalar_arg;
+
+typedef struct cmd_runtime_args {
+  const cmd_tensor_arg* tensors;
+  int32_t n_tensors;
+  const cmd_scalar_arg* scalars;
+  int32_t n_scalars;
+} cmd_runtime_args;
+
+/* Result of lowering, for inspection (cmd_lower / cmd_kernel_info). */
+typedef struct cmd_program_info {
+  int32_t n_live_ops;   /* E ops left after dead-tag elimination and reuse */
+  int32_t n_loads;      /* live Load_Tensor ops (each read once per element) */
+  int32_t n_scalars;    /* live Load_Scalar ops */
+  int32_t n_stores;
+  int32_t n_slots;      /* register slots the program needs */
+  int32_t n_words;      /* program words, including the end marker */
+  int32_t tier;         /* executor family: 0 = 4 slots, 1 = 8 slots, 2 = 32 slots */
+  int32_t n_moves;      /* copies the two-address form needed */
+} cmd_program_info;
+
+/* Which executor a launch would use (cmd_plan_launch). */
+typedef enum cmd_path {
+  CMD_PATH_NONE = 0,    /* nothing to do (no elements or no stores) */
+  CMD_PATH_CONTIG = 1,  /* every view dense row-major and aligned: vector loads/stores */
+  CMD_PATH_TILE2D = 2,  /* 2-D views, row-direct or transposed, staged through shared memory */
+  CMD_PATH_GENERIC = 3  /* any other sizes/strides: per-element offsets */
+} cmd_path;
+
+typedef struct cmd_launch_plan {
+  int32_t path;           /* cmd_path */
+  int32_t merged_rank;    /* rank after dropping size-1 dims and merging dims */
+  int64_t merged_sizes[CMD_MAX_RANK];
+  int64_t n_elements;     /* logical elements */
+  int64_t bytes;          /* live loads read once + stores written once */
+  int32_t n_transposed;   /* loads staged through shared memory (tile path) */
+} cmd_launch_plan;
+
+int32_t cmd_abi_version(void);
+const char* cmd_status_string(cmd_status s);
+/* Message of the last failing call on this thread ("" if none). */
+const char* cmd_last_error(void);
+
+/* ---- building a Command (host only) -------------------------------------- */
+
+/* Create an empty Command; *out receives the handle. */
+cmd_status cmd_create(cmd_command_t* out);
+/* Destroy a Command (NULL is ignored). Compiled kernels stay valid. */
+void cmd_destroy(cmd_command_t cmd);
+
+/* Tag the next operation added to cmd will receive. */
+cmd_status cmd_next_tag(cmd_command_t cmd, cmd_tag* out);
+
+/* Load_Tensor of element type dtype and logical rank 0..CMD_MAX_RANK. */
+cmd_status cmd_add_load_tensor(cmd_command_t cmd, cmd_dtype dtype, int32_t rank, cmd_tag* out);
+
+/* Load_Scalar of type CMD_F32 or CMD_I32 (broadcast to every element). */
+cmd_status cmd_add_load_scalar(cmd_command_t cmd, cmd_dtype dtype, cmd_tag* out);
+
+/* One T_Execute block of n E ops (1..CMD_MAX_TAGS). Op i receives tag
+ * first + i, written to out_tags[i] when out_tags is non-NULL. Operands of one
+ * op must both be float-valued or both int-valued. On error nothing is added. */
+cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd_tag* out_tags);
+
+/* Store_Tensor of tag src as element type dtype, logical rank `rank`. A float
+ * value may be stored as CMD_F32, CMD_F16 or CMD_BF16; an int value as CMD_I32. */
+cmd_status cmd_add_store(cmd_command_t cmd, cmd_tag src, cmd_dtype dtype, int32_t rank, cmd_tag* out);
+
+/* ---- lowering ---------------------------------------------------------- */
+
+/* Lower cmd on the host only (no GPU needed): fills *info and, when words is
+ * non-NULL, up to cap program words. For inspection and tests. */
+cmd_status cmd_lower(cmd_command_t cmd, cmd_program_info* info, uint32_t* words, int32_t cap);
+
+/* Lower cmd and place the program in constant memory of the current CUDA
+ * device. Synchronises that device (it may reuse the constant slot of a
+ * destroyed kernel), so do not call it during stream capture. The Command may
+ * be destroyed afterwards. All tensors of the Command must share one rank. */
+cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out);
+
+/* Lower cmd into a kernel handle without touching any GPU. Such a kernel can
+ * be inspected (cmd_kernel_info, cmd_kernel_dump) and planned
+ * (cmd_plan_launch) but not launched (CMD_ERR_STATE). */
+cmd_status cmd_lower_kernel(cmd_command_t cmd, cmd_kernel_t* out);
+
+/* Release a kernel and its constant-memory slot (NULL is ignored). Work
+ * already launched with it must not still be pending. */
+void cmd_kernel_destroy(cmd_kernel_t k);
+
+cmd_status cmd_kernel_info(cmd_kernel_t k, cmd_program_info* info);
+
+/* Text listing of the lowered program into buf (NUL-terminated, truncated to
+ * size); *needed receives the full length + 1 when non-NULL. */
+cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* needed);
+
+/* ---- launching --------------------------------------------------------- */
+
+/* Validate args against the kernel and report the executor it would use,
+ * without touching the GPU. */
+cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_launch_plan* plan);
+
+/* Validate args and enqueue one fused pass on stream cuda_stream (a
+ * cudaStream_t; NULL = the legacy default stream), on the device the kernel
+ * was compiled for, which must be current. Every live Load_Tensor, Store_Tensor
+ * and Load_Scalar tag needs exactly one argument; arguments for dead tags may
+ * be omitted. Stores must not overlap any other tensor argument (an identical
+ * view of the same element type, used in place, is allowed) and must not
+ * overlap themselves. Returns after the launch is enqueued (asynchronous). A
+ * launch with zero elements does nothing. Safe to capture in a CUDA graph. */
+cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_stream);
+
+/* Wait for cuda_stream and report the completion phase of work launched on
+ * it: CMD_OK, or CMD_ERR_CUDA with the runtime's message. */
+cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CMD_H */

@@ -1,0 +1,98 @@
+"""Build the CUDA executor library (libcmdexec.so) in-tree.
+
+The three executor translation units and the host C ABI compile in parallel
+for sm_103a only, then link into one shared library next to this file.
+Float arithmetic is compiled with contraction off (-fmad=false) and without
+fast-math, so denormals are kept and every add/sub/mul rounds once.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+OUT_DIR = os.path.join(HERE, "_lib")
+OBJ_DIR = os.path.join(HERE, "_build")
+LIB_PATH = os.path.join(OUT_DIR, "libcmdexec.so")
+
+CU_SOURCES = ["exec_contig.cu", "exec_tile2d.cu", "exec_generic.cu"]
+CPP_SOURCES = ["cmd_api.cpp"]
+HEADERS = ["cmd_internal.h", "exec_common.cuh"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def cuda_home() -> str:
+    env = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH")
+    if env and os.path.isdir(env):
+        return env
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return "/usr/local/cuda"
+
+
+def _sources():
+    return ([os.path.join(CSRC, s) for s in CU_SOURCES + CPP_SOURCES + HEADERS]
+            + [os.path.join(ROOT, "include", "cmd.h"), os.path.abspath(__file__)])
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return False
+    t = os.path.getmtime(LIB_PATH)
+    return all(os.path.getmtime(s) <= t for s in _sources())
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link libcmdexec.so unless it is newer than every source."""
+    if not force and up_to_date():
+        return LIB_PATH
+    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    home = cuda_home()
+    nvcc = os.path.join(home, "bin", "nvcc")
+    inc = ["-I" + os.path.join(home, "include"), "-I" + os.path.join(ROOT, "include")]
+    jobs = []
+    for s in CU_SOURCES:
+        obj = os.path.join(OBJ_DIR, s + ".o")
+        log = os.path.join(OBJ_DIR, s + ".ptxas.txt")
+        cmd = ([nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-prec-div=true",
+                                "-prec-sqrt=true", "-ftz=false", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
+                                "-c", os.path.join(CSRC, s), "-o", obj] + inc)
+        jobs.append((cmd, obj, log))
+    for s in CPP_SOURCES:
+        obj = os.path.join(OBJ_DIR, s + ".o")
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-Wno-unused-parameter",
+               "-c", os.path.join(CSRC, s), "-o", obj] + inc
+        jobs.append((cmd, obj, None))
+
+    def run(job):
+        cmd, obj, log = job
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if log:
+            with open(log, "w") as f:
+                f.write(r.stderr)
+        if r.returncode != 0:
+            raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+        if verbose and r.stderr:
+            print(r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(run, jobs))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    link = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart_static", "-lrt", "-lpthread", "-ldl"]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    import sys
+    print(build(force="--force" in sys.argv, verbose=True))

@@ -1,0 +1,1069 @@
+// cmd_api.cpp - the C ABI of cmd.h: Command building, lowering to the
+// register-slot program, launch validation and executor selection.
+//
+// Lowering follows the rocRoller "Design Overview" pipeline in spirit
+// (sections "Kernel Graph", "Expression", "Registers", "Command Kernel"): the
+// Command's tag graph is rewritten (dead tags dropped, identical operations
+// reused), values are given registers by their lifetimes, and a compact
+// program is emitted for the hand-written executors to run.
+#include "../../include/cmd.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "cmd_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+cmd_status fail(cmd_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+enum OpKind { kLoad = 0, kScalar = 1, kExec = 2, kStore = 3 };
+enum ValClass { kFloat = 0, kInt = 1, kNone = 2 };
+
+struct Op {
+  int kind;
+  int dtype;  // load/store element type, scalar type
+  int rank;   // load/store logical rank
+  int eop;    // kExec: cmd_eop
+  int a, b;   // kExec operands (b = -1 for NEG); kStore: a = source
+  int cls;    // value class of the result
+};
+
+const char* dtype_name(int dt) {
+  switch (dt) {
+    case CMD_F32: return "f32";
+    case CMD_F16: return "f16";
+    case CMD_BF16: return "bf16";
+    case CMD_I32: return "i32";
+  }
+  return "?";
+}
+
+int elem_size(int dt) { return (dt == CMD_F16 || dt == CMD_BF16) ? 2 : 4; }
+
+bool valid_dtype(int dt) { return dt >= CMD_F32 && dt <= CMD_I32; }
+
+// One instruction of the two-address program, before encoding.
+struct Instr {
+  enum Kind { kBin, kUn, kBinS, kMovS, kSt } kind;
+  int op;   // BinOp / UnOp / StoreType
+  int d;    // destination slot
+  int s;    // source slot
+  int aux;  // scalar index or output index
+};
+
+struct Program {
+  std::vector<int> load_tags;    // slot j holds the j-th live load
+  std::vector<int> scalar_tags;  // scalar index k
+  std::vector<int> store_tags;   // output index o
+  std::vector<Instr> code;
+  std::vector<uint32_t> words;
+  int n_live_e = 0;
+  int n_slots = 0;
+  int n_moves = 0;
+  int tier = cmdx::kTier4;
+};
+
+}  // namespace
+
+struct cmd_command {
+  std::vector<Op> ops;
+};
+
+struct cmd_kernel {
+  std::vector<Op> ops;
+  Program prog;
+  int rank = 0;
+  int device = -1;
+  int slot = -1;
+};
+
+namespace {
+
+// ---- constant-memory program slots, per device -----------------------------
+std::mutex g_slot_mu;
+std::map<int, std::vector<int>> g_slot_state;  // 0 never used, 1 in use, 2 freed
+
+int acquire_slot(int device, bool* reused) {
+  std::lock_guard<std::mutex> g(g_slot_mu);
+  auto& st = g_slot_state[device];
+  if (st.empty()) st.assign(cmdx::kMaxPrograms, 0);
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int i = 0; i < cmdx::kMaxPrograms; ++i) {
+      if ((pass == 0 && st[i] == 0) || (pass == 1 && st[i] == 2)) {
+        *reused = st[i] == 2;
+        st[i] = 1;
+        return i;
+      }
+    }
+  }
+  return -1;
+}
+
+void release_slot(int device, int slot) {
+  std::lock_guard<std::mutex> g(g_slot_mu);
+  auto it = g_slot_state.find(device);
+  if (it != g_slot_state.end() && slot >= 0 && slot < (int)it->second.size()) it->second[slot] = 2;
+}
+
+// ---- lowering --------------------------------------------------------------
+
+cmd_status check_command(const cmd_command* c, int* rank_out) {
+  int rank = -1;
+  bool any_store = false;
+  for (size_t t = 0; t < c->ops.size(); ++t) {
+    const Op& op = c->ops[t];
+    if (op.kind == kLoad || op.kind == kStore) {
+      if (rank < 0) rank = op.rank;
+      if (op.rank != rank)
+        return fail(CMD_ERR_SHAPE, "tag " + std::to_string(t) + " has rank " + std::to_string(op.rank) +
+                                       " but an earlier tensor has rank " + std::to_string(rank) +
+                                       "; every tensor of a Command shares the logical sizes");
+    }
+    if (op.kind == kStore) any_store = true;
+  }
+  (void)any_store;
+  *rank_out = rank < 0 ? 0 : rank;
+  return CMD_OK;
+}
+
+cmd_status lower(const std::vector<Op>& ops, Program* P) {
+  const int n = (int)ops.size();
+  // common-subexpression reuse: an E op with the same (op, operands) as an
+  // earlier one takes that one's value; Add and Mul are commutative exactly
+  // (bit for bit in IEEE 754 and modulo 2^32), so their operands are ordered.
+  std::vector<int> rep(n);
+  std::map<std::tuple<int, int, int>, int> seen;
+  for (int t = 0; t < n; ++t) {
+    const Op& op = ops[t];
+    rep[t] = t;
+    if (op.kind != kExec) continue;
+    int a = rep[op.a];
+    int b = op.eop == CMD_E_NEG ? -1 : rep[op.b];
+    if ((op.eop == CMD_E_ADD || op.eop == CMD_E_MUL) && b < a) std::swap(a, b);
+    auto key = std::make_tuple(op.eop, a, b);
+    auto it = seen.find(key);
+    if (it != seen.end())
+      rep[t] = it->second;
+    else
+      seen.emplace(key, t);
+  }
+  // dead-tag elimination: keep what a store reaches
+  std::vector<char> live(n, 0);
+  for (int t = n - 1; t >= 0; --t) {
+    const Op& op = ops[t];
+    if (op.kind == kStore) {
+      live[t] = 1;
+      live[rep[op.a]] = 1;
+    } else if (op.kind == kExec && live[t] && rep[t] == t) {
+      live[rep[op.a]] = 1;
+      if (op.eop != CMD_E_NEG) live[rep[op.b]] = 1;
+    }
+  }
+  std::vector<int> slot_of(n, -1), sidx(n, -1);
+  P->load_tags.clear();
+  P->scalar_tags.clear();
+  P->store_tags.clear();
+  P->code.clear();
+  P->n_live_e = 0;
+  P->n_moves = 0;
+  for (int t = 0; t < n; ++t) {
+    if (!live[t]) continue;
+    if (ops[t].kind == kLoad) {
+      slot_of[t] = (int)P->load_tags.size();
+      P->load_tags.push_back(t);
+    } else if (ops[t].kind == kScalar) {
+      sidx[t] = (int)P->scalar_tags.size();
+      P->scalar_tags.push_back(t);
+    } else if (ops[t].kind == kStore) {
+      P->store_tags.push_back(t);
+    } else if (rep[t] == t) {
+      ++P->n_live_e;
+    }
+  }
+  if ((int)P->load_tags.size() > cmdx::kMaxLoads)
+    return fail(CMD_ERR_LIMIT, "more than " + std::to_string(cmdx::kMaxLoads) + " live Load_Tensor ops");
+  if ((int)P->store_tags.size() > cmdx::kMaxStores)
+    return fail(CMD_ERR_LIMIT, "more than " + std::to_string(cmdx::kMaxStores) + " Store_Tensor ops");
+  if ((int)P->scalar_tags.size() > cmdx::kMaxScalars)
+    return fail(CMD_ERR_LIMIT, "more than " + std::to_string(cmdx::kMaxScalars) + " live Load_Scalar ops");
+
+  // emission order: stores of loaded or scalar values first, then each live
+  // E op in tag order followed by the stores of its value
+  struct Event { bool store; int tag; };
+  std::vector<Event> ev;
+  for (int t : P->store_tags) {
+    int src = rep[ops[t].a];
+    if (ops[src].kind != kExec) ev.push_back({true, t});
+  }
+  std::vector<std::vector<int>> stores_of(n);
+  for (int t : P->store_tags) {
+    int src = rep[ops[t].a];
+    if (ops[src].kind == kExec) stores_of[src].push_back(t);
+  }
+  for (int t = 0; t < n; ++t) {
+    if (ops[t].kind != kExec || !live[t] || rep[t] != t) continue;
+    ev.push_back({false, t});
+    for (int s : stores_of[t]) ev.push_back({true, s});
+  }
+  std::vector<int> last_use(n, -1);
+  for (int i = 0; i < (int)ev.size(); ++i) {
+    const Op& op = ops[ev[i].tag];
+    if (ev[i].store) {
+      last_use[rep[op.a]] = i;
+    } else {
+      last_use[rep[op.a]] = i;
+      if (op.eop != CMD_E_NEG) last_use[rep[op.b]] = i;
+    }
+  }
+  // slots
+  bool busy[cmdx::kMaxSlots + 1] = {};
+  int in_use = 0, peak = 0;
+  int n_loads = (int)P->load_tags.size();
+  for (int j = 0; j < n_loads; ++j) busy[j] = true;
+  in_use = peak = n_loads;
+  bool overflow = false;
+  auto alloc = [&]() -> int {
+    for (int i = 0; i < cmdx::kMaxSlots; ++i) {
+      if (!busy[i]) {
+        busy[i] = true;
+        ++in_use;
+        peak = std::max(peak, in_use);
+        return i;
+      }
+    }
+    overflow = true;
+    return cmdx::kMaxSlots;  // never encoded: lowering fails below
+  };
+  auto release = [&](int s) {
+    if (s >= 0 && s < cmdx::kMaxSlots && busy[s]) {
+      busy[s] = false;
+      --in_use;
+    }
+  };
+  auto is_scalar = [&](int t) { return ops[t].kind == kScalar; };
+  auto emit = [&](Instr::Kind k, int op, int d, int s, int aux) { P->code.push_back({k, op, d, s, aux}); };
+  auto store_type = [&](int dt) { return dt; /* cmd_dtype numbering matches StoreType */ };
+
+  for (int i = 0; i < (int)ev.size(); ++i) {
+    const int t = ev[i].tag;
+    const Op& op = ops[t];
+    if (ev[i].store) {
+      int src = rep[op.a];
+      int o = (int)(std::find(P->store_tags.begin(), P->store_tags.end(), t) - P->store_tags.begin());
+      if (is_scalar(src)) {
+        int d = alloc();
+        emit(Instr::kMovS, cmdx::kMov, d, 0, sidx[src]);
+        emit(Instr::kSt, store_type(op.dtype), 0, d, o);
+        release(d);
+      } else {
+        emit(Instr::kSt, store_type(op.dtype), 0, slot_of[src], o);
+        if (last_use[src] == i) release(slot_of[src]);
+      }
+      continue;
+    }
+    const bool ints = op.cls == kInt;
+    const int a = rep[op.a];
+    if (op.eop == CMD_E_NEG) {
+      const int neg = ints ? cmdx::kINeg : cmdx::kFNeg;
+      int d;
+      if (is_scalar(a)) {
+        d = alloc();
+        emit(Instr::kMovS, cmdx::kMov, d, 0, sidx[a]);
+        emit(Instr::kUn, neg, d, d, 0);
+      } else if (last_use[a] == i) {
+        d = slot_of[a];
+        emit(Instr::kUn, neg, d, d, 0);
+      } else {
+        d = alloc();
+        emit(Instr::kUn, neg, d, slot_of[a], 0);
+      }
+      slot_of[t] = d;
+      continue;
+    }
+    const int b = rep[op.b];
+    int bop, rsub;
+    if (op.eop == CMD_E_ADD) bop = ints ? cmdx::kIAdd : cmdx::kFAdd;
+    else if (op.eop == CMD_E_SUB) bop = ints ? cmdx::kISub : cmdx::kFSub;
+    else bop = ints ? cmdx::kIMul : cmdx::kFMul;
+    rsub = ints ? cmdx::kIRsub : cmdx::kFRsub;
+    const bool commut = op.eop != CMD_E_SUB;
+    const bool sa = is_scalar(a), sb = is_scalar(b);
+    const bool die_a = !sa && last_use[a] == i;
+    const bool die_b = !sb && last_use[b] == i;
+    auto src = [&](int bo, int d, int x) {  // d = d (bo) x
+      if (is_scalar(x)) emit(Instr::kBinS, bo, d, 0, sidx[x]);
+      else emit(Instr::kBin, bo, d, slot_of[x], 0);
+    };
+    int d;
+    if (die_a) {
+      d = slot_of[a];
+      src(bop, d, b);
+      if (die_b && b != a) release(slot_of[b]);
+    } else if (die_b) {
+      d = slot_of[b];
+      src(commut ? bop : rsub, d, a);
+    } else {
+      d = alloc();
+      ++P->n_moves;
+      if (sa && sb) {
+        emit(Instr::kMovS, cmdx::kMov, d, 0, sidx[a]);
+        src(bop, d, b);
+      } else if (sa) {
+        emit(Instr::kUn, cmdx::kMov, d, slot_of[b], 0);
+        src(commut ? bop : rsub, d, a);
+      } else {
+        emit(Instr::kUn, cmdx::kMov, d, slot_of[a], 0);
+        src(bop, d, b);
+      }
+    }
+    slot_of[t] = d;
+  }
+  if (overflow || peak > cmdx::kMaxSlots)
+    return fail(CMD_ERR_LIMIT, "the program needs more than " + std::to_string(cmdx::kMaxSlots) +
+                                   " simultaneously live values");
+  P->n_slots = std::max(peak, 1);
+  P->tier = P->n_slots <= 4 ? cmdx::kTier4 : P->n_slots <= 8 ? cmdx::kTier8 : cmdx::kTier32;
+
+  // encode
+  P->words.clear();
+  const int S = cmdx::tier_slots(P->tier);
+  for (const Instr& in : P->code) {
+    uint32_t w = 0;
+    if (P->tier != cmdx::kTier32) {
+      switch (in.kind) {
+        case Instr::kBin: w = cmdx::fz_bin(S, in.op, in.d, in.s); break;
+        case Instr::kUn: w = cmdx::fz_un(S, in.op, in.d, in.s); break;
+        case Instr::kBinS: w = cmdx::fz_bin_scalar(S, in.op, in.d) | uint32_t(in.aux) << 16; break;
+        case Instr::kMovS: w = cmdx::fz_movs(S, in.d) | uint32_t(in.aux) << 16; break;
+        case Instr::kSt: w = cmdx::fz_store(S, in.op, in.s) | uint32_t(in.aux) << 16; break;
+      }
+    } else {
+      switch (in.kind) {
+        case Instr::kBin: w = cmdx::wd_word(cmdx::kWBin0 + in.op, in.d, in.s, 0); break;
+        case Instr::kUn: w = cmdx::wd_word(cmdx::kWUn0 + in.op, in.d, in.s, 0); break;
+        case Instr::kBinS: w = cmdx::wd_word((cmdx::kWBin0 + in.op) | cmdx::kWScalar, in.d, 0, in.aux); break;
+        case Instr::kMovS: w = cmdx::wd_word((cmdx::kWUn0 + cmdx::kMov) | cmdx::kWScalar, in.d, 0, in.aux); break;
+        case Instr::kSt: w = cmdx::wd_word(cmdx::kWStore0 + in.op, 0, in.s, in.aux); break;
+      }
+    }
+    P->words.push_back(w);
+  }
+  P->words.push_back(P->tier != cmdx::kTier32 ? cmdx::fz_end(S) : cmdx::wd_word(cmdx::kWEnd, 0, 0, 0));
+  if ((int)P->words.size() > cmdx::kMaxWords)
+    return fail(CMD_ERR_LIMIT, "the lowered program has " + std::to_string(P->words.size()) +
+                                   " words; the limit is " + std::to_string(cmdx::kMaxWords));
+  return CMD_OK;
+}
+
+void fill_info(const Program& P, cmd_program_info* info) {
+  info->n_live_ops = P.n_live_e;
+  info->n_loads = (int32_t)P.load_tags.size();
+  info->n_scalars = (int32_t)P.scalar_tags.size();
+  info->n_stores = (int32_t)P.store_tags.size();
+  info->n_slots = P.n_slots;
+  info->n_words = (int32_t)P.words.size();
+  info->tier = P.tier;
+  info->n_moves = P.n_moves;
+}
+
+// ---- launch validation and planning ----------------------------------------
+
+struct View {
+  int tag;
+  int dtype;
+  void* ptr;
+  int64_t st[cmdx::kMaxRank];
+};
+
+struct Plan {
+  int path = CMD_PATH_NONE;
+  int64_t n = 0;
+  int mrank = 0;
+  int64_t msizes[cmdx::kMaxRank] = {1, 1, 1, 1};
+  std::vector<View> loads, stores;       // in slot / output order
+  int64_t ml[cmdx::kMaxLoads][cmdx::kMaxRank];    // merged strides of loads
+  int64_t ms[cmdx::kMaxStores][cmdx::kMaxRank];   // merged strides of stores
+  uint32_t scal[cmdx::kMaxScalars] = {};
+  int n_trans = 0;
+  int64_t bytes = 0;
+};
+
+// Largest element offset reached by a view (+1), over dims of size > 1.
+int64_t view_extent(const int64_t* sizes, const int64_t* st, int rank) {
+  int64_t e = 0;
+  for (int k = 0; k < rank; ++k)
+    if (sizes[k] > 1) e += (sizes[k] - 1) * st[k];
+  return e + 1;
+}
+
+// Sufficient condition for a view to address distinct elements: with dims of
+// size > 1 sorted by stride, each stride exceeds the span of the smaller ones.
+bool view_injective(const int64_t* sizes, const int64_t* st, int rank) {
+  std::vector<std::pair<int64_t, int64_t>> d;
+  for (int k = 0; k < rank; ++k)
+    if (sizes[k] > 1) d.push_back({st[k], sizes[k]});
+  std::sort(d.begin(), d.end());
+  int64_t span = 0;  // largest offset reachable by the smaller dims
+  for (auto& x : d) {
+    if (x.first <= span) return false;
+    span += (x.second - 1) * x.first;
+  }
+  return true;
+}
+
+cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* pl) {
+  const auto& ops = k->ops;
+  const int n = (int)ops.size();
+  const int rank = k->rank;
+  if (!args) return fail(CMD_ERR_NULL, "args is NULL");
+  if (args->n_tensors < 0 || args->n_scalars < 0) return fail(CMD_ERR_ARG, "negative argument count");
+  if (args->n_tensors > 0 && !args->tensors) return fail(CMD_ERR_NULL, "args->tensors is NULL");
+  if (args->n_scalars > 0 && !args->scalars) return fail(CMD_ERR_NULL, "args->scalars is NULL");
+  std::vector<int> targ(n, -1), sarg(n, -1);
+  int64_t sizes[cmdx::kMaxRank] = {1, 1, 1, 1};
+  bool have_sizes = false;
+  for (int i = 0; i < args->n_tensors; ++i) {
+    const cmd_tensor_arg& a = args->tensors[i];
+    if (a.tag < 0 || a.tag >= n || (ops[a.tag].kind != kLoad && ops[a.tag].kind != kStore))
+      return fail(CMD_ERR_BAD_TAG, "tensor argument " + std::to_string(i) + " names tag " + std::to_string(a.tag) +
+                                       ", which is not a Load_Tensor or Store_Tensor of this kernel");
+    if (targ[a.tag] >= 0) return fail(CMD_ERR_ARG, "tag " + std::to_string(a.tag) + " has two tensor arguments");
+    targ[a.tag] = i;
+    if (a.rank != rank)
+      return fail(CMD_ERR_SHAPE, "tensor argument for tag " + std::to_string(a.tag) + " has rank " +
+                                     std::to_string(a.rank) + ", the Command's tensors have rank " + std::to_string(rank));
+    for (int d = 0; d < rank; ++d) {
+      if (a.sizes[d] < 0) return fail(CMD_ERR_SHAPE, "negative size for tag " + std::to_string(a.tag));
+      if (a.strides[d] < 0)
+        return fail(CMD_ERR_SHAPE, "negative stride for tag " + std::to_string(a.tag) + " (strides must be >= 0)");
+    }
+    if (!have_sizes) {
+      for (int d = 0; d < rank; ++d) sizes[cmdx::kMaxRank - rank + d] = a.sizes[d];
+      have_sizes = true;
+    } else {
+      for (int d = 0; d < rank; ++d)
+        if (sizes[cmdx::kMaxRank - rank + d] != a.sizes[d])
+          return fail(CMD_ERR_SHAPE, "tag " + std::to_string(a.tag) + " has logical size " + std::to_string(a.sizes[d]) +
+                                         " in dim " + std::to_string(d) + ", another tensor has " +
+                                         std::to_string(sizes[cmdx::kMaxRank - rank + d]));
+    }
+  }
+  for (int i = 0; i < args->n_scalars; ++i) {
+    const cmd_scalar_arg& a = args->scalars[i];
+    if (a.tag < 0 || a.tag >= n || ops[a.tag].kind != kScalar)
+      return fail(CMD_ERR_BAD_TAG, "scalar argument " + std::to_string(i) + " names tag " + std::to_string(a.tag) +
+                                       ", which is not a Load_Scalar of this kernel");
+    if (sarg[a.tag] >= 0) return fail(CMD_ERR_ARG, "tag " + std::to_string(a.tag) + " has two scalar arguments");
+    sarg[a.tag] = i;
+  }
+  const Program& P = k->prog;
+  for (int t : P.load_tags)
+    if (targ[t] < 0) return fail(CMD_ERR_ARG, "no tensor argument for live Load_Tensor tag " + std::to_string(t));
+  for (int t : P.store_tags)
+    if (targ[t] < 0) return fail(CMD_ERR_ARG, "no tensor argument for Store_Tensor tag " + std::to_string(t));
+  for (int t : P.scalar_tags)
+    if (sarg[t] < 0) return fail(CMD_ERR_ARG, "no scalar argument for live Load_Scalar tag " + std::to_string(t));
+
+  int64_t N = 1;
+  for (int d = 0; d < cmdx::kMaxRank; ++d) N *= sizes[d];
+  pl->n = N;
+  pl->loads.clear();
+  pl->stores.clear();
+  auto mkview = [&](int t) {
+    const cmd_tensor_arg& a = args->tensors[targ[t]];
+    View v;
+    v.tag = t;
+    v.dtype = ops[t].dtype;
+    v.ptr = a.ptr;
+    for (int d = 0; d < cmdx::kMaxRank; ++d) v.st[d] = 0;
+    for (int d = 0; d < rank; ++d) v.st[cmdx::kMaxRank - rank + d] = a.strides[d];
+    return v;
+  };
+  for (int t : P.load_tags) pl->loads.push_back(mkview(t));
+  for (int t : P.store_tags) pl->stores.push_back(mkview(t));
+  for (size_t j = 0; j < P.scalar_tags.size(); ++j) pl->scal[j] = args->scalars[sarg[P.scalar_tags[j]]].v.bits;
+  pl->bytes = 0;
+  for (auto& v : pl->loads) pl->bytes += N * elem_size(v.dtype);
+  for (auto& v : pl->stores) pl->bytes += N * elem_size(v.dtype);
+  if (N == 0 || P.store_tags.empty()) {
+    pl->path = CMD_PATH_NONE;
+    pl->mrank = 0;
+    return CMD_OK;
+  }
+  // pointers
+  auto check_ptr = [&](const View& v) -> cmd_status {
+    if (!v.ptr) return fail(CMD_ERR_NULL, "NULL pointer for tag " + std::to_string(v.tag));
+    if (reinterpret_cast<uintptr_t>(v.ptr) % (uintptr_t)elem_size(v.dtype))
+      return fail(CMD_ERR_ALIGN, "pointer for tag " + std::to_string(v.tag) + " is not aligned to its " +
+                                     std::to_string(elem_size(v.dtype)) + "-byte elements");
+    return CMD_OK;
+  };
+  for (auto& v : pl->loads) if (cmd_status s = check_ptr(v)) return s;
+  for (auto& v : pl->stores) if (cmd_status s = check_ptr(v)) return s;
+  // stores: injective, and not overlapping any other live tensor (an
+  // identical view of the same element type read in place is allowed)
+  for (size_t i = 0; i < pl->stores.size(); ++i) {
+    const View& s = pl->stores[i];
+    if (!view_injective(sizes, s.st, cmdx::kMaxRank))
+      return fail(CMD_ERR_ALIAS, "the view of Store_Tensor tag " + std::to_string(s.tag) +
+                                     " addresses some elements more than once");
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(s.ptr);
+    const uintptr_t s1 = s0 + (uintptr_t)(view_extent(sizes, s.st, cmdx::kMaxRank) * elem_size(s.dtype));
+    auto overlaps = [&](const View& o) {
+      const uintptr_t o0 = reinterpret_cast<uintptr_t>(o.ptr);
+      const uintptr_t o1 = o0 + (uintptr_t)(view_extent(sizes, o.st, cmdx::kMaxRank) * elem_size(o.dtype));
+      return o0 < s1 && s0 < o1;
+    };
+    auto identical = [&](const View& o) {
+      if (o.ptr != s.ptr || elem_size(o.dtype) != elem_size(s.dtype)) return false;
+      for (int d = 0; d < cmdx::kMaxRank; ++d)
+        if (sizes[d] > 1 && o.st[d] != s.st[d]) return false;
+      return true;
+    };
+    for (size_t j = 0; j < pl->stores.size(); ++j)
+      if (j != i && overlaps(pl->stores[j]))
+        return fail(CMD_ERR_ALIAS, "Store_Tensor tags " + std::to_string(s.tag) + " and " +
+                                       std::to_string(pl->stores[j].tag) + " overlap in memory");
+    for (const View& l : pl->loads)
+      if (overlaps(l) && !identical(l))
+        return fail(CMD_ERR_ALIAS, "Store_Tensor tag " + std::to_string(s.tag) + " overlaps Load_Tensor tag " +
+                                       std::to_string(l.tag) + " without being the identical view");
+  }
+  // merge dims: drop size-1 dims, then fuse neighbours that every view walks
+  // as one (outer stride == inner stride * inner size)
+  int64_t ms[cmdx::kMaxRank];
+  int msrc[cmdx::kMaxRank];
+  int m = 0;
+  for (int d = 0; d < cmdx::kMaxRank; ++d)
+    if (sizes[d] != 1) {
+      ms[m] = sizes[d];
+      msrc[m] = d;
+      ++m;
+    }
+  std::vector<View*> all;
+  for (auto& v : pl->loads) all.push_back(&v);
+  for (auto& v : pl->stores) all.push_back(&v);
+  // working strides per view over the kept dims
+  std::vector<std::vector<int64_t>> wst(all.size());
+  for (size_t i = 0; i < all.size(); ++i)
+    for (int q = 0; q < m; ++q) wst[i].push_back(all[i]->st[msrc[q]]);
+  for (int q = m - 2; q >= 0; --q) {
+    bool ok = true;
+    for (size_t i = 0; i < all.size() && ok; ++i) ok = wst[i][q] == wst[i][q + 1] * ms[q + 1];
+    if (!ok) continue;
+    ms[q] *= ms[q + 1];
+    for (size_t i = 0; i < all.size(); ++i) {
+      wst[i][q] = wst[i][q + 1];
+      wst[i].erase(wst[i].begin() + q + 1);
+    }
+    for (int r = q + 1; r + 1 < m; ++r) ms[r] = ms[r + 1];
+    --m;
+  }
+  pl->mrank = m;
+  for (int d = 0; d < cmdx::kMaxRank; ++d) pl->msizes[d] = 1;
+  for (int q = 0; q < m; ++q) pl->msizes[cmdx::kMaxRank - m + q] = ms[q];
+  for (size_t j = 0; j < pl->loads.size(); ++j)
+    for (int d = 0; d < cmdx::kMaxRank; ++d)
+      pl->ml[j][d] = d < cmdx::kMaxRank - m ? 0 : wst[j][d - (cmdx::kMaxRank - m)];
+  for (size_t j = 0; j < pl->stores.size(); ++j)
+    for (int d = 0; d < cmdx::kMaxRank; ++d)
+      pl->ms[j][d] = d < cmdx::kMaxRank - m ? 0 : wst[pl->loads.size() + j][d - (cmdx::kMaxRank - m)];
+
+  auto aligned = [](const void* p, int bytes) { return reinterpret_cast<uintptr_t>(p) % (uintptr_t)bytes == 0; };
+  // contiguous: one merged dim (or none) walked with stride 1 by every view,
+  // and every pointer aligned for the vector width (4 elements per access)
+  bool contig = m <= 1;
+  for (size_t i = 0; i < all.size() && contig; ++i) {
+    if (m == 1 && wst[i][0] != 1) contig = false;
+    if (!aligned(all[i]->ptr, 4 * elem_size(all[i]->dtype))) contig = false;
+  }
+  if (contig) {
+    pl->path = CMD_PATH_CONTIG;
+    return CMD_OK;
+  }
+  // tile: two merged dims; every store row-direct (inner stride 1); every
+  // load row-direct or transposed (outer stride 1); 16-byte aligned rows
+  if (m == 2 && P.tier != cmdx::kTier32) {
+    bool ok = true;
+    int n_trans = 0;
+    for (size_t i = 0; i < all.size() && ok; ++i) {
+      const bool is_store = i >= pl->loads.size();
+      const int es = elem_size(all[i]->dtype);
+      const int64_t so = wst[i][0], si = wst[i][1];
+      if (!aligned(all[i]->ptr, 16)) ok = false;
+      else if (si == 1 && (so * es) % 16 == 0) {
+        // row-direct
+      } else if (!is_store && so == 1 && si != 1 && (si * es) % 16 == 0) {
+        ++n_trans;
+      } else {
+        ok = false;
+      }
+    }
+    if (ok && n_trans <= 4) {
+      pl->path = CMD_PATH_TILE2D;
+      pl->n_trans = n_trans;
+      return CMD_OK;
+    }
+  }
+  pl->path = CMD_PATH_GENERIC;
+  return CMD_OK;
+}
+
+// Magic number of the Granlund-Montgomery round-up division for 64-bit
+// dividends: l = ceil(log2 d), m = floor(2^64 (2^l - d) / d) + 1.
+cmdx::FastDiv make_fastdiv(int64_t d) {
+  cmdx::FastDiv f{};
+  f.d = d;
+  if (d <= 1) return f;
+  uint32_t l = 0;
+  while (l < 63 && (int64_t(1) << l) < d) ++l;
+  if ((int64_t(1) << l) < d) l = 64;
+  unsigned __int128 two_l = (unsigned __int128)1 << l;
+  unsigned __int128 m = (((unsigned __int128)1 << 64) * (two_l - (unsigned __int128)d)) / (unsigned __int128)d + 1;
+  f.m = (uint64_t)m;
+  f.l = l;
+  return f;
+}
+
+cudaError_t upload_all(int slot, const std::vector<uint32_t>& w) {
+  cudaError_t e = cmdx::contig_upload(slot, w.data(), (int)w.size());
+  if (e == cudaSuccess) e = cmdx::tile2d_upload(slot, w.data(), (int)w.size());
+  if (e == cudaSuccess) e = cmdx::generic_upload(slot, w.data(), (int)w.size());
+  return e;
+}
+
+cmd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(CMD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+
+extern "C" {
+
+int32_t cmd_abi_version(void) { return CMD_ABI_VERSION; }
+
+const char* cmd_status_string(cmd_status s) {
+  switch (s) {
+    case CMD_OK: return "CMD_OK";
+    case CMD_ERR_NULL: return "CMD_ERR_NULL";
+    case CMD_ERR_BAD_TAG: return "CMD_ERR_BAD_TAG";
+    case CMD_ERR_TYPE: return "CMD_ERR_TYPE";
+    case CMD_ERR_SHAPE: return "CMD_ERR_SHAPE";
+    case CMD_ERR_ALIAS: return "CMD_ERR_ALIAS";
+    case CMD_ERR_ALIGN: return "CMD_ERR_ALIGN";
+    case CMD_ERR_STATE: return "CMD_ERR_STATE";
+    case CMD_ERR_LIMIT: return "CMD_ERR_LIMIT";
+    case CMD_ERR_CUDA: return "CMD_ERR_CUDA";
+    case CMD_ERR_DEVICE_TIMEOUT: return "CMD_ERR_DEVICE_TIMEOUT";
+    case CMD_ERR_NOMEM: return "CMD_ERR_NOMEM";
+    case CMD_ERR_ARG: return "CMD_ERR_ARG";
+  }
+  return "CMD_ERR_UNKNOWN";
+}
+
+const char* cmd_last_error(void) { return g_last_error.c_str(); }
+
+cmd_status cmd_create(cmd_command_t* out) {
+  if (!out) return fail(CMD_ERR_NULL, "out is NULL");
+  cmd_command* c = new (std::nothrow) cmd_command();
+  if (!c) return fail(CMD_ERR_NOMEM, "out of host memory");
+  *out = c;
+  return CMD_OK;
+}
+
+void cmd_destroy(cmd_command_t cmd) { delete cmd; }
+
+cmd_status cmd_next_tag(cmd_command_t cmd, cmd_tag* out) {
+  if (!cmd || !out) return fail(CMD_ERR_NULL, "cmd or out is NULL");
+  *out = (cmd_tag)cmd->ops.size();
+  return CMD_OK;
+}
+
+static cmd_status push_op(cmd_command_t cmd, const Op& op, cmd_tag* out) {
+  if (cmd->ops.size() >= (size_t)CMD_MAX_TAGS)
+    return fail(CMD_ERR_LIMIT, "a Command holds at most " + std::to_string(CMD_MAX_TAGS) + " operations");
+  try {
+    cmd->ops.push_back(op);
+  } catch (...) {
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  if (out) *out = (cmd_tag)(cmd->ops.size() - 1);
+  return CMD_OK;
+}
+
+cmd_status cmd_add_load_tensor(cmd_command_t cmd, cmd_dtype dtype, int32_t rank, cmd_tag* out) {
+  if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
+  if (!valid_dtype(dtype)) return fail(CMD_ERR_TYPE, "unknown dtype " + std::to_string((int)dtype));
+  if (rank < 0 || rank > CMD_MAX_RANK) return fail(CMD_ERR_SHAPE, "rank must be 0.." + std::to_string(CMD_MAX_RANK));
+  Op op{kLoad, (int)dtype, rank, 0, -1, -1, dtype == CMD_I32 ? kInt : kFloat};
+  return push_op(cmd, op, out);
+}
+
+cmd_status cmd_add_load_scalar(cmd_command_t cmd, cmd_dtype dtype, cmd_tag* out) {
+  if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
+  if (dtype != CMD_F32 && dtype != CMD_I32)
+    return fail(CMD_ERR_TYPE, "a Load_Scalar is CMD_F32 or CMD_I32");
+  Op op{kScalar, (int)dtype, 0, 0, -1, -1, dtype == CMD_I32 ? kInt : kFloat};
+  return push_op(cmd, op, out);
+}
+
+cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd_tag* out_tags) {
+  if (!cmd || !ops) return fail(CMD_ERR_NULL, "cmd or ops is NULL");
+  if (n <= 0) return fail(CMD_ERR_ARG, "a T_Execute block needs at least one E op");
+  const int base = (int)cmd->ops.size();
+  if (base + n > CMD_MAX_TAGS)
+    return fail(CMD_ERR_LIMIT, "a Command holds at most " + std::to_string(CMD_MAX_TAGS) + " operations");
+  std::vector<Op> block;
+  auto resolve = [&](cmd_tag t, int i, int* res) -> cmd_status {
+    if (t < 0) {
+      int li = -1 - t;
+      if (li >= i)
+        return fail(CMD_ERR_BAD_TAG, "E op " + std::to_string(i) + " refers to CMD_LOCAL(" + std::to_string(li) +
+                                         "), which is not an earlier op of the block");
+      *res = base + li;
+      return CMD_OK;
+    }
+    if (t >= base)
+      return fail(CMD_ERR_BAD_TAG, "E op " + std::to_string(i) + " refers to tag " + std::to_string(t) +
+                                       ", which does not exist yet (use CMD_LOCAL for results of this block)");
+    if (cmd->ops[t].kind == kStore)
+      return fail(CMD_ERR_BAD_TAG, "E op " + std::to_string(i) + " refers to tag " + std::to_string(t) +
+                                       ", a Store_Tensor, which has no value");
+    *res = t;
+    return CMD_OK;
+  };
+  auto cls_of = [&](int t) { return t < base ? cmd->ops[t].cls : block[t - base].cls; };
+  for (int i = 0; i < n; ++i) {
+    const cmd_xop& x = ops[i];
+    if (x.op < CMD_E_ADD || x.op > CMD_E_NEG) return fail(CMD_ERR_ARG, "unknown E op " + std::to_string(x.op));
+    Op op{kExec, 0, 0, x.op, -1, -1, kFloat};
+    if (cmd_status s = resolve(x.a, i, &op.a)) return s;
+    if (x.op != CMD_E_NEG) {
+      if (cmd_status s = resolve(x.b, i, &op.b)) return s;
+      if (cls_of(op.a) != cls_of(op.b))
+        return fail(CMD_ERR_TYPE, "E op " + std::to_string(i) + " mixes an int value and a float value");
+    }
+    op.cls = cls_of(op.a);
+    block.push_back(op);
+  }
+  try {
+    cmd->ops.insert(cmd->ops.end(), block.begin(), block.end());
+  } catch (...) {
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  if (out_tags)
+    for (int i = 0; i < n; ++i) out_tags[i] = base + i;
+  return CMD_OK;
+}
+
+cmd_status cmd_add_store(cmd_command_t cmd, cmd_tag src, cmd_dtype dtype, int32_t rank, cmd_tag* out) {
+  if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
+  if (!valid_dtype(dtype)) return fail(CMD_ERR_TYPE, "unknown dtype " + std::to_string((int)dtype));
+  if (rank < 0 || rank > CMD_MAX_RANK) return fail(CMD_ERR_SHAPE, "rank must be 0.." + std::to_string(CMD_MAX_RANK));
+  if (src < 0 || src >= (cmd_tag)cmd->ops.size() || cmd->ops[src].kind == kStore)
+    return fail(CMD_ERR_BAD_TAG, "store source tag " + std::to_string(src) + " is not an earlier value");
+  const int cls = cmd->ops[src].cls;
+  if ((dtype == CMD_I32) != (cls == kInt))
+    return fail(CMD_ERR_TYPE, std::string("cannot store a ") + (cls == kInt ? "int" : "float") + " value as " +
+                                  dtype_name(dtype));
+  Op op{kStore, (int)dtype, rank, 0, src, -1, kNone};
+  return push_op(cmd, op, out);
+}
+
+cmd_status cmd_lower(cmd_command_t cmd, cmd_program_info* info, uint32_t* words, int32_t cap) {
+  if (!cmd || !info) return fail(CMD_ERR_NULL, "cmd or info is NULL");
+  int rank;
+  if (cmd_status s = check_command(cmd, &rank)) return s;
+  Program P;
+  try {
+    if (cmd_status s = lower(cmd->ops, &P)) return s;
+  } catch (...) {
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  fill_info(P, info);
+  if (words)
+    for (int i = 0; i < cap && i < (int)P.words.size(); ++i) words[i] = P.words[i];
+  return CMD_OK;
+}
+
+cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out) {
+  if (!cmd || !out) return fail(CMD_ERR_NULL, "cmd or out is NULL");
+  cmd_kernel* k = new (std::nothrow) cmd_kernel();
+  if (!k) return fail(CMD_ERR_NOMEM, "out of host memory");
+  try {
+    k->ops = cmd->ops;
+    if (cmd_status s = check_command(cmd, &k->rank)) {
+      delete k;
+      return s;
+    }
+    if (cmd_status s = lower(k->ops, &k->prog)) {
+      delete k;
+      return s;
+    }
+  } catch (...) {
+    delete k;
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    delete k;
+    return cuda_fail(e, "cudaGetDevice");
+  }
+  bool reused = false;
+  int slot = acquire_slot(dev, &reused);
+  if (slot < 0) {
+    delete k;
+    return fail(CMD_ERR_LIMIT, "more than " + std::to_string(CMD_MAX_KERNELS) + " compiled kernels on this device");
+  }
+  if (reused) {
+    // a destroyed kernel's launches may still read this slot
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      release_slot(dev, slot);
+      delete k;
+      return cuda_fail(e, "cudaDeviceSynchronize before reusing a program slot");
+    }
+  }
+  e = upload_all(slot, k->prog.words);
+  if (e != cudaSuccess) {
+    release_slot(dev, slot);
+    delete k;
+    return cuda_fail(e, "uploading the program to constant memory");
+  }
+  k->device = dev;
+  k->slot = slot;
+  *out = k;
+  return CMD_OK;
+}
+
+cmd_status cmd_lower_kernel(cmd_command_t cmd, cmd_kernel_t* out) {
+  if (!cmd || !out) return fail(CMD_ERR_NULL, "cmd or out is NULL");
+  cmd_kernel* k = new (std::nothrow) cmd_kernel();
+  if (!k) return fail(CMD_ERR_NOMEM, "out of host memory");
+  try {
+    k->ops = cmd->ops;
+    cmd_status s = check_command(cmd, &k->rank);
+    if (s == CMD_OK) s = lower(k->ops, &k->prog);
+    if (s != CMD_OK) {
+      delete k;
+      return s;
+    }
+  } catch (...) {
+    delete k;
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  *out = k;
+  return CMD_OK;
+}
+
+void cmd_kernel_destroy(cmd_kernel_t k) {
+  if (!k) return;
+  if (k->slot >= 0) release_slot(k->device, k->slot);
+  delete k;
+}
+
+cmd_status cmd_kernel_info(cmd_kernel_t k, cmd_program_info* info) {
+  if (!k || !info) return fail(CMD_ERR_NULL, "k or info is NULL");
+  fill_info(k->prog, info);
+  return CMD_OK;
+}
+
+cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* needed) {
+  if (!k) return fail(CMD_ERR_NULL, "k is NULL");
+  static const char* bin[] = {"fadd", "fsub", "frsub", "fmul", "iadd", "isub", "irsub", "imul"};
+  static const char* un[] = {"fneg", "ineg", "mov"};
+  std::string s;
+  const Program& P = k->prog;
+  char line[160];
+  std::snprintf(line, sizeof line, "; tier %d, %d slots, %d words, %d live E ops, %d moves\n", P.tier, P.n_slots,
+                (int)P.words.size(), P.n_live_e, P.n_moves);
+  s += line;
+  for (size_t j = 0; j < P.load_tags.size(); ++j) {
+    std::snprintf(line, sizeof line, "load    r%zu <- tag %d (%s)\n", j, P.load_tags[j],
+                  dtype_name(k->ops[P.load_tags[j]].dtype));
+    s += line;
+  }
+  for (size_t j = 0; j < P.scalar_tags.size(); ++j) {
+    std::snprintf(line, sizeof line, "scalar  s%zu <- tag %d (%s)\n", j, P.scalar_tags[j],
+                  dtype_name(k->ops[P.scalar_tags[j]].dtype));
+    s += line;
+  }
+  for (size_t i = 0; i < P.code.size(); ++i) {
+    const Instr& in = P.code[i];
+    switch (in.kind) {
+      case Instr::kBin: std::snprintf(line, sizeof line, "%-7s r%d, r%d\n", bin[in.op], in.d, in.s); break;
+      case Instr::kUn: std::snprintf(line, sizeof line, "%-7s r%d, r%d\n", un[in.op], in.d, in.s); break;
+      case Instr::kBinS: std::snprintf(line, sizeof line, "%-7s r%d, s%d\n", bin[in.op], in.d, in.aux); break;
+      case Instr::kMovS: std::snprintf(line, sizeof line, "mov     r%d, s%d\n", in.d, in.aux); break;
+      case Instr::kSt:
+        std::snprintf(line, sizeof line, "store   out%d <- r%d (%s, tag %d)\n", in.aux, in.s, dtype_name(in.op),
+                      P.store_tags[in.aux]);
+        break;
+    }
+    s += line;
+  }
+  s += "end\n";
+  if (needed) *needed = (int64_t)s.size() + 1;
+  if (buf && size > 0) {
+    size_t n = std::min<size_t>((size_t)size - 1, s.size());
+    std::memcpy(buf, s.data(), n);
+    buf[n] = 0;
+  }
+  return CMD_OK;
+}
+
+cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_launch_plan* plan) {
+  if (!k || !plan) return fail(CMD_ERR_NULL, "k or plan is NULL");
+  Plan pl;
+  try {
+    if (cmd_status s = plan_launch(k, args, &pl)) return s;
+  } catch (...) {
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  plan->path = pl.path;
+  plan->merged_rank = pl.mrank;
+  for (int d = 0; d < CMD_MAX_RANK; ++d) plan->merged_sizes[d] = 1;
+  for (int q = 0; q < pl.mrank; ++q) plan->merged_sizes[q] = pl.msizes[cmdx::kMaxRank - pl.mrank + q];
+  plan->n_elements = pl.n;
+  plan->bytes = pl.bytes;
+  plan->n_transposed = pl.n_trans;
+  return CMD_OK;
+}
+
+cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_stream) {
+  if (!k) return fail(CMD_ERR_NULL, "k is NULL");
+  if (k->slot < 0) return fail(CMD_ERR_STATE, "kernel was lowered without a device (cmd_lower_kernel); compile it");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != k->device)
+    return fail(CMD_ERR_STATE, "kernel was compiled for device " + std::to_string(k->device) +
+                                   " but device " + std::to_string(dev) + " is current");
+  Plan pl;
+  try {
+    if (cmd_status s = plan_launch(k, args, &pl)) return s;
+  } catch (...) {
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  if (pl.path == CMD_PATH_NONE) return CMD_OK;
+  const Program& P = k->prog;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if (pl.path == CMD_PATH_CONTIG) {
+    // whole warp chunks on the contiguous executor, a ragged tail (fewer than
+    // one chunk of elements) on the generic one
+    const int64_t chunk = cmdx::contig_chunk(P.tier);
+    const int64_t n_main = pl.n - pl.n % chunk;
+    e = cudaSuccess;
+    if (n_main > 0) {
+      cmdx::ContigParams p;
+      std::memset(&p, 0, sizeof p);
+      for (size_t j = 0; j < pl.loads.size(); ++j) {
+        p.in[j] = pl.loads[j].ptr;
+        p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+      }
+      for (size_t j = 0; j < pl.stores.size(); ++j) p.out[j] = pl.stores[j].ptr;
+      std::memcpy(p.scal, pl.scal, sizeof p.scal);
+      p.n = n_main;
+      p.prog = (uint32_t)k->slot;
+      p.n_loads = (uint32_t)pl.loads.size();
+      e = cmdx::contig_launch(P.tier, p, stream);
+    }
+    if (e == cudaSuccess && pl.n > n_main) {
+      cmdx::GenericParams p;
+      std::memset(&p, 0, sizeof p);
+      for (size_t j = 0; j < pl.loads.size(); ++j) {
+        p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + n_main * elem_size(pl.loads[j].dtype);
+        p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+        p.in_st[j][cmdx::kMaxRank - 1] = 1;
+      }
+      for (size_t j = 0; j < pl.stores.size(); ++j) {
+        p.out[j] = static_cast<char*>(pl.stores[j].ptr) + n_main * elem_size(pl.stores[j].dtype);
+        p.out_st[j][cmdx::kMaxRank - 1] = 1;
+      }
+      for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(1);
+      p.div[cmdx::kMaxRank - 1] = make_fastdiv(pl.n - n_main);
+      std::memcpy(p.scal, pl.scal, sizeof p.scal);
+      p.n = pl.n - n_main;
+      p.prog = (uint32_t)k->slot;
+      p.n_loads = (uint32_t)pl.loads.size();
+      e = cmdx::generic_launch(P.tier, p, stream);
+    }
+  } else if (pl.path == CMD_PATH_TILE2D) {
+    cmdx::Tile2dParams p;
+    std::memset(&p, 0, sizeof p);
+    int stage = 0;
+    for (size_t j = 0; j < pl.loads.size(); ++j) {
+      p.in[j] = pl.loads[j].ptr;
+      p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+      const int64_t so = pl.ml[j][2], si = pl.ml[j][3];
+      if (si == 1) {
+        p.in_ld[j] = so;
+        p.in_stage[j] = -1;
+      } else {
+        p.in_ld[j] = si;
+        p.in_stage[j] = (int8_t)stage++;
+      }
+    }
+    for (int j = (int)pl.loads.size(); j < cmdx::kMaxLoads; ++j) p.in_stage[j] = -1;
+    for (size_t j = 0; j < pl.stores.size(); ++j) {
+      p.out[j] = pl.stores[j].ptr;
+      p.out_ld[j] = pl.ms[j][2];
+    }
+    std::memcpy(p.scal, pl.scal, sizeof p.scal);
+    p.rows = pl.msizes[2];
+    p.cols = pl.msizes[3];
+    p.tiles_c = (p.cols + cmdx::kTileCols - 1) / cmdx::kTileCols;
+    p.n_tiles = p.tiles_c * ((p.rows + cmdx::kTileRows - 1) / cmdx::kTileRows);
+    p.prog = (uint32_t)k->slot;
+    p.n_loads = (uint32_t)pl.loads.size();
+    p.n_trans = (uint32_t)stage;
+    e = cmdx::tile2d_launch(P.tier, p, stream);
+  } else {
+    cmdx::GenericParams p;
+    std::memset(&p, 0, sizeof p);
+    for (size_t j = 0; j < pl.loads.size(); ++j) {
+      p.in[j] = pl.loads[j].ptr;
+      p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+      for (int d = 0; d < cmdx::kMaxRank; ++d) p.in_st[j][d] = pl.ml[j][d];
+    }
+    for (size_t j = 0; j < pl.stores.size(); ++j) {
+      p.out[j] = pl.stores[j].ptr;
+      for (int d = 0; d < cmdx::kMaxRank; ++d) p.out_st[j][d] = pl.ms[j][d];
+    }
+    for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(pl.msizes[d]);
+    std::memcpy(p.scal, pl.scal, sizeof p.scal);
+    p.n = pl.n;
+    p.prog = (uint32_t)k->slot;
+    p.n_loads = (uint32_t)pl.loads.size();
+    e = cmdx::generic_launch(P.tier, p, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return CMD_OK;
+}
+
+cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream) {
+  (void)k;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "work on the stream failed");
+  return CMD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+// cmd_internal.h - program encoding and launch parameters shared by the host
+// lowering (cmd_api.cpp) and the CUDA executors (exec_*.cu). Not public.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#if defined(__CUDACC__)
+#define CMDX_HD __host__ __device__
+#else
+#define CMDX_HD
+#endif
+
+namespace cmdx {
+
+constexpr int kMaxRank = 4;
+constexpr int kMaxLoads = 16;
+constexpr int kMaxStores = 8;
+constexpr int kMaxScalars = 16;
+constexpr int kMaxSlots = 32;
+constexpr int kMaxPrograms = 48;
+constexpr int kMaxWords = 256;
+
+// Executor families by register-slot count. The two small tiers dispatch on
+// one fused (opcode, dst, src) case; the wide tier fetches the source operand
+// and then dispatches on (opcode, dst).
+enum Tier { kTier4 = 0, kTier8 = 1, kTier32 = 2 };
+CMDX_HD constexpr int tier_slots(int tier) { return tier == kTier4 ? 4 : tier == kTier8 ? 8 : 32; }
+// Elements each thread keeps per slot: 32 slot registers in the fused tiers.
+CMDX_HD constexpr int tier_vec(int tier) { return tier == kTier32 ? 2 : tier == kTier8 ? 4 : 8; }
+// Resident 256-thread CTAs per SM each executor is compiled for (caps registers).
+CMDX_HD constexpr int tier_min_blocks(int tier) { return tier == kTier32 ? 2 : 3; }
+
+// Two-address binary ops: d = d (op) x, where x is a slot or a scalar.
+// RSUB is the reversed subtraction d = x - d.
+enum BinOp {
+  kFAdd = 0, kFSub = 1, kFRsub = 2, kFMul = 3,
+  kIAdd = 4, kISub = 5, kIRsub = 6, kIMul = 7,
+  kNumBin = 8
+};
+// Unary ops: d = f(x).
+enum UnOp { kFNeg = 0, kINeg = 1, kMov = 2, kNumUn = 3 };
+// Store element types, as numbered in cmd.h's cmd_dtype.
+enum StoreType { kStF32 = 0, kStF16 = 1, kStBF16 = 2, kStI32 = 3, kNumSt = 4 };
+
+// ---- fused encoding (tiers 4 and 8) ----------------------------------------
+// word = case | aux << 16; aux is a scalar index (scalar ops) or an output
+// index (stores). Case layout, for S slots:
+//   [0, 8 S^2)            binary op b, dst d, src slot s : b S^2 + d S + s
+//   [8 S^2, 11 S^2)       unary op u, dst d, src slot s  : 8 S^2 + u S^2 + d S + s
+//   [11 S^2, +8 S)        binary op b with scalar src, dst d : 11 S^2 + b S + d
+//   [11 S^2 + 8 S, +S)    broadcast scalar into d
+//   [11 S^2 + 9 S, +4 S)  store slot s as type t : 11 S^2 + 9 S + t S + s
+//   11 S^2 + 13 S         end
+CMDX_HD constexpr uint32_t fz_bin(int S, int b, int d, int s) { return uint32_t(b * S * S + d * S + s); }
+CMDX_HD constexpr uint32_t fz_un(int S, int u, int d, int s) { return uint32_t(kNumBin * S * S + u * S * S + d * S + s); }
+CMDX_HD constexpr uint32_t fz_bin_scalar(int S, int b, int d) { return uint32_t(11 * S * S + b * S + d); }
+CMDX_HD constexpr uint32_t fz_movs(int S, int d) { return uint32_t(11 * S * S + 8 * S + d); }
+CMDX_HD constexpr uint32_t fz_store(int S, int t, int s) { return uint32_t(11 * S * S + 9 * S + t * S + s); }
+CMDX_HD constexpr uint32_t fz_end(int S) { return uint32_t(11 * S * S + 13 * S); }
+
+// ---- wide encoding (tier 32) -------------------------------------------------
+// word = kind << 24 | d << 16 | s << 8 | aux. The source operand x is slot s,
+// or scalar aux when the kind has kWScalar set.
+enum WideKind {
+  kWBin0 = 0,    // + BinOp
+  kWUn0 = 8,     // + UnOp
+  kWStore0 = 11, // + StoreType, stores x to output aux
+  kWEnd = 15,
+  kWScalar = 0x40
+};
+CMDX_HD constexpr uint32_t wd_word(int kind, int d, int s, int aux) {
+  return uint32_t(kind) << 24 | uint32_t(d) << 16 | uint32_t(s) << 8 | uint32_t(aux);
+}
+
+// ---- launch parameters (passed by value as __grid_constant__) ---------------
+struct ContigParams {
+  const void* in[kMaxLoads];
+  void* out[kMaxStores];
+  uint32_t scal[kMaxScalars];
+  int64_t n;             // logical elements, a multiple of 32 * V
+  uint32_t prog;         // program slot in constant memory
+  uint32_t n_loads;
+  uint8_t in_dt[kMaxLoads];
+};
+
+struct Tile2dParams {
+  const void* in[kMaxLoads];
+  void* out[kMaxStores];
+  int64_t in_ld[kMaxLoads];   // row stride (row-direct) or column stride (transposed), elements
+  int64_t out_ld[kMaxStores]; // row stride of each store, elements
+  uint32_t scal[kMaxScalars];
+  int64_t rows, cols;
+  int64_t tiles_c;            // tiles per row of tiles
+  int64_t n_tiles;
+  uint32_t prog;
+  uint32_t n_loads;
+  uint32_t n_trans;           // transposed loads, staged through shared memory
+  uint8_t in_dt[kMaxLoads];
+  int8_t in_stage[kMaxLoads]; // shared-memory stage index of a transposed load, -1 if row-direct
+};
+
+// Unsigned division by an invariant divisor d >= 2 with a multiply-high:
+// q = (t + ((n - t) >> 1)) >> (l - 1), t = mulhi64(m, n), l = ceil(log2 d),
+// m = floor(2^64 (2^l - d) / d) + 1 (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, section 4).
+struct FastDiv {
+  uint64_t m;
+  uint32_t l;   // 0 marks d == 1 (dimension skipped)
+  uint32_t pad;
+  int64_t d;
+};
+
+struct GenericParams {
+  const void* in[kMaxLoads];
+  void* out[kMaxStores];
+  int64_t in_st[kMaxLoads][kMaxRank];   // strides, right-aligned to the merged rank
+  int64_t out_st[kMaxStores][kMaxRank];
+  FastDiv div[kMaxRank];                // merged sizes, right-aligned (leading dims = 1)
+  uint32_t scal[kMaxScalars];
+  int64_t n;
+  uint32_t prog;
+  uint32_t n_loads;
+  uint8_t in_dt[kMaxLoads];
+};
+
+// Host entry points of the executor translation units. Each unit keeps its
+// own constant-memory program table; upload writes one slot of it.
+cudaError_t contig_upload(int slot, const uint32_t* words, int n);
+cudaError_t tile2d_upload(int slot, const uint32_t* words, int n);
+cudaError_t generic_upload(int slot, const uint32_t* words, int n);
+// n must be a multiple of contig_chunk(tier) elements.
+cudaError_t contig_launch(int tier, const ContigParams& p, cudaStream_t stream);
+int contig_chunk(int tier);
+cudaError_t tile2d_launch(int tier, const Tile2dParams& p, cudaStream_t stream);
+cudaError_t generic_launch(int tier, const GenericParams& p, cudaStream_t stream);
+
+// Tile geometry of the tile2d executor.
+constexpr int kTileRows = 64;
+constexpr int kTileCols = 64;
+
+}  // namespace cmdx

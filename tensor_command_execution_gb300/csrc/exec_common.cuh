@@ -1,0 +1,273 @@
+// exec_common.cuh - the register-slot interpreter shared by the executors.
+//
+// Every thread keeps V consecutive-per-lane elements of each live value in
+// registers ("slots"). A program word selects one case of a switch whose
+// slot numbers are compile-time constants, so slots never need run-time
+// register indexing (which would spill them to local memory). All threads of
+// a launch run the same program, so the dispatch branch is warp-uniform.
+//
+// rocRoller, "Design Overview": the program plays the part of the scheduled
+// instructions generated from the KernelGraph (sections "Generating
+// Instructions from a KernelGraph" and "Registers"); here it is interpreted by
+// a hand-written kernel instead of being assembled per Command.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "cmd_internal.h"
+
+namespace cmdx {
+
+// ---- element operations on 32-bit slot words ------------------------------
+// Float ops use the round-to-nearest-even intrinsics, which are never fused
+// into a multiply-add; int ops are unsigned, i.e. modulo 2^32.
+template <int OP>
+__device__ __forceinline__ uint32_t bin(uint32_t d, uint32_t x) {
+  if constexpr (OP == kFAdd) return __float_as_uint(__fadd_rn(__uint_as_float(d), __uint_as_float(x)));
+  if constexpr (OP == kFSub) return __float_as_uint(__fsub_rn(__uint_as_float(d), __uint_as_float(x)));
+  if constexpr (OP == kFRsub) return __float_as_uint(__fsub_rn(__uint_as_float(x), __uint_as_float(d)));
+  if constexpr (OP == kFMul) return __float_as_uint(__fmul_rn(__uint_as_float(d), __uint_as_float(x)));
+  if constexpr (OP == kIAdd) return d + x;
+  if constexpr (OP == kISub) return d - x;
+  if constexpr (OP == kIRsub) return x - d;
+  if constexpr (OP == kIMul) return d * x;
+  return 0;
+}
+
+template <int OP>
+__device__ __forceinline__ uint32_t un(uint32_t x) {
+  if constexpr (OP == kFNeg) return x ^ 0x80000000u;  // IEEE negate: sign flip
+  if constexpr (OP == kINeg) return 0u - x;
+  return x;  // kMov
+}
+
+// ---- widening and narrowing ------------------------------------------------
+__device__ __forceinline__ void widen_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  float2 f = __half22float2(h);
+  lo = __float_as_uint(f.x);
+  hi = __float_as_uint(f.y);
+}
+// bfloat16 is the upper half of a binary32 encoding: widening is a shift.
+__device__ __forceinline__ void widen_bf16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = w << 16;
+  hi = w & 0xffff0000u;
+}
+__device__ __forceinline__ uint32_t widen_f16(uint16_t h) {
+  return __float_as_uint(__half2float(__ushort_as_half(h)));
+}
+__device__ __forceinline__ uint32_t widen_bf16(uint16_t h) { return uint32_t(h) << 16; }
+
+__device__ __forceinline__ uint32_t narrow_f16x2(uint32_t lo, uint32_t hi) {
+  __half2 h = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t narrow_bf16x2(uint32_t lo, uint32_t hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint16_t narrow_f16(uint32_t x) {
+  return __half_as_ushort(__float2half_rn(__uint_as_float(x)));
+}
+__device__ __forceinline__ uint16_t narrow_bf16(uint32_t x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(x)));
+}
+
+// Widen one loaded element of type dt (raw bits) to a slot word.
+__device__ __forceinline__ uint32_t widen_any(int dt, uint32_t raw) {
+  if (dt == 1) return widen_f16((uint16_t)raw);
+  if (dt == 2) return widen_bf16((uint16_t)raw);
+  return raw;
+}
+
+// Streaming global accesses: every element is read or written once.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ uint2 ld_stream(const uint2* p) { return __ldcs(p); }
+__device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) { return __ldcs(reinterpret_cast<const unsigned int*>(p)); }
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(uint2* p, uint2 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(uint32_t* p, uint32_t v) { __stcs(reinterpret_cast<unsigned int*>(p), v); }
+
+// Load/store one raw element of type dt at element offset off.
+__device__ __forceinline__ uint32_t ld_elem(const void* base, int dt, int64_t off) {
+  if (dt == 1 || dt == 2) return __ldcs(reinterpret_cast<const unsigned short*>(base) + off);
+  return __ldcs(reinterpret_cast<const unsigned int*>(base) + off);
+}
+template <int T>
+__device__ __forceinline__ void st_elem(void* base, int64_t off, uint32_t x) {
+  if constexpr (T == kStF16) __stcs(reinterpret_cast<unsigned short*>(base) + off, narrow_f16(x));
+  else if constexpr (T == kStBF16) __stcs(reinterpret_cast<unsigned short*>(base) + off, narrow_bf16(x));
+  else __stcs(reinterpret_cast<unsigned int*>(base) + off, x);
+}
+
+// ---- slot lists for the fused dispatch ----------------------------------------
+#define CMDX_SA4(M, ...) M(0, __VA_ARGS__) M(1, __VA_ARGS__) M(2, __VA_ARGS__) M(3, __VA_ARGS__)
+#define CMDX_SB4(M, ...) M(0, __VA_ARGS__) M(1, __VA_ARGS__) M(2, __VA_ARGS__) M(3, __VA_ARGS__)
+#define CMDX_SA8(M, ...) CMDX_SA4(M, __VA_ARGS__) M(4, __VA_ARGS__) M(5, __VA_ARGS__) M(6, __VA_ARGS__) M(7, __VA_ARGS__)
+#define CMDX_SB8(M, ...) CMDX_SB4(M, __VA_ARGS__) M(4, __VA_ARGS__) M(5, __VA_ARGS__) M(6, __VA_ARGS__) M(7, __VA_ARGS__)
+
+#define CMDX_UNROLL _Pragma("unroll")
+
+// d = d (op) r[s]
+#define CMDX_BIN_CASE(s_, d_, op_)                                          \
+  case fz_bin(S, op_, d_, s_): {                                            \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], r[s_][v]); \
+  } break;
+#define CMDX_BIN_D(d_, op_, SB) SB(CMDX_BIN_CASE, d_, op_)
+// d = f(r[s])
+#define CMDX_UN_CASE(s_, d_, op_)                                           \
+  case fz_un(S, op_, d_, s_): {                                             \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = un<op_>(r[s_][v]);   \
+  } break;
+#define CMDX_UN_D(d_, op_, SB) SB(CMDX_UN_CASE, d_, op_)
+// d = d (op) scalar[aux]
+#define CMDX_BINS_CASE(d_, op_)                                             \
+  case fz_bin_scalar(S, op_, d_): {                                         \
+    const uint32_t k = scal[aux];                                           \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], k); \
+  } break;
+#define CMDX_MOVS_CASE(d_, x_)                                              \
+  case fz_movs(S, d_): {                                                    \
+    const uint32_t k = scal[aux];                                           \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = k;                   \
+  } break;
+#define CMDX_ST_CASE(s_, t_)                                                \
+  case fz_store(S, t_, s_):                                                 \
+    pol.template store<t_>(r[s_], aux);                                     \
+    break;
+
+#define CMDX_FUSED_CASES(SA, SB)                                                          \
+  SA(CMDX_BIN_D, kFAdd, SB) SA(CMDX_BIN_D, kFSub, SB) SA(CMDX_BIN_D, kFRsub, SB)          \
+  SA(CMDX_BIN_D, kFMul, SB) SA(CMDX_BIN_D, kIAdd, SB) SA(CMDX_BIN_D, kISub, SB)           \
+  SA(CMDX_BIN_D, kIRsub, SB) SA(CMDX_BIN_D, kIMul, SB)                                    \
+  SA(CMDX_UN_D, kFNeg, SB) SA(CMDX_UN_D, kINeg, SB) SA(CMDX_UN_D, kMov, SB)               \
+  SA(CMDX_BINS_CASE, kFAdd) SA(CMDX_BINS_CASE, kFSub) SA(CMDX_BINS_CASE, kFRsub)          \
+  SA(CMDX_BINS_CASE, kFMul) SA(CMDX_BINS_CASE, kIAdd) SA(CMDX_BINS_CASE, kISub)           \
+  SA(CMDX_BINS_CASE, kIRsub) SA(CMDX_BINS_CASE, kIMul)                                    \
+  SA(CMDX_MOVS_CASE, 0)                                                                   \
+  SA(CMDX_ST_CASE, kStF32) SA(CMDX_ST_CASE, kStF16) SA(CMDX_ST_CASE, kStBF16) SA(CMDX_ST_CASE, kStI32)
+
+// Run the program in `prog` (constant memory) over the thread's slots.
+// Pol supplies store<T>(const uint32_t (&x)[V], int out_index).
+template <int S, int V, class Pol>
+__device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* __restrict__ prog,
+                                          const uint32_t* __restrict__ scal, Pol& pol) {
+  static_assert(S == 4 || S == 8, "fused dispatch is generated for 4 and 8 slots");
+#pragma unroll 1
+  for (int pc = 0;; ++pc) {
+    const uint32_t w = prog[pc];
+    const uint32_t aux = w >> 16;
+    if constexpr (S == 4) {
+      switch (w & 0xffffu) {
+        CMDX_FUSED_CASES(CMDX_SA4, CMDX_SB4)
+        default: return;
+      }
+    } else {
+      switch (w & 0xffffu) {
+        CMDX_FUSED_CASES(CMDX_SA8, CMDX_SB8)
+        default: return;
+      }
+    }
+  }
+}
+
+// ---- wide dispatch (32 slots): fetch the source, then (op, dst) -------------
+#define CMDX_SA32(M, ...)                                                                 \
+  CMDX_SA8(M, __VA_ARGS__) M(8, __VA_ARGS__) M(9, __VA_ARGS__) M(10, __VA_ARGS__)         \
+  M(11, __VA_ARGS__) M(12, __VA_ARGS__) M(13, __VA_ARGS__) M(14, __VA_ARGS__)             \
+  M(15, __VA_ARGS__) M(16, __VA_ARGS__) M(17, __VA_ARGS__) M(18, __VA_ARGS__)             \
+  M(19, __VA_ARGS__) M(20, __VA_ARGS__) M(21, __VA_ARGS__) M(22, __VA_ARGS__)             \
+  M(23, __VA_ARGS__) M(24, __VA_ARGS__) M(25, __VA_ARGS__) M(26, __VA_ARGS__)             \
+  M(27, __VA_ARGS__) M(28, __VA_ARGS__) M(29, __VA_ARGS__) M(30, __VA_ARGS__) M(31, __VA_ARGS__)
+
+#define CMDX_W_FETCH(s_, x_) \
+  case s_: {                 \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) x[v] = r[s_][v]; \
+  } break;
+#define CMDX_W_BIN(d_, op_) \
+  case (kWBin0 + op_) * 32 + d_: { \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], x[v]); \
+  } break;
+#define CMDX_W_UN(d_, op_) \
+  case (kWUn0 + op_) * 32 + d_: { \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = un<op_>(x[v]); \
+  } break;
+
+template <int V, class Pol>
+__device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* __restrict__ prog,
+                                         const uint32_t* __restrict__ scal, Pol& pol) {
+#pragma unroll 1
+  for (int pc = 0;; ++pc) {
+    const uint32_t w = prog[pc];
+    const uint32_t kind = w >> 24;
+    const uint32_t aux = w & 0xffu;
+    const uint32_t base = kind & 0x3fu;
+    if (base == kWEnd) return;
+    uint32_t x[V];
+    if (kind & kWScalar) {
+      const uint32_t k = scal[aux];
+      CMDX_UNROLL for (int v = 0; v < V; ++v) x[v] = k;
+    } else {
+      switch ((w >> 8) & 0xffu) {
+        CMDX_SA32(CMDX_W_FETCH, 0)
+        default: break;
+      }
+    }
+    if (base >= kWStore0) {
+      switch (base - kWStore0) {
+        case kStF32: pol.template store<kStF32>(x, aux); break;
+        case kStF16: pol.template store<kStF16>(x, aux); break;
+        case kStBF16: pol.template store<kStBF16>(x, aux); break;
+        default: pol.template store<kStI32>(x, aux); break;
+      }
+      continue;
+    }
+    switch (base * 32 + ((w >> 16) & 0xffu)) {
+      CMDX_SA32(CMDX_W_BIN, kFAdd) CMDX_SA32(CMDX_W_BIN, kFSub) CMDX_SA32(CMDX_W_BIN, kFRsub)
+      CMDX_SA32(CMDX_W_BIN, kFMul) CMDX_SA32(CMDX_W_BIN, kIAdd) CMDX_SA32(CMDX_W_BIN, kISub)
+      CMDX_SA32(CMDX_W_BIN, kIRsub) CMDX_SA32(CMDX_W_BIN, kIMul)
+      CMDX_SA32(CMDX_W_UN, kFNeg) CMDX_SA32(CMDX_W_UN, kINeg) CMDX_SA32(CMDX_W_UN, kMov)
+      default: break;
+    }
+  }
+}
+
+template <int TIER, int V, class Pol>
+__device__ __forceinline__ void run_program(uint32_t (&r)[tier_slots(TIER)][V], const uint32_t* prog,
+                                            const uint32_t* scal, Pol& pol) {
+  if constexpr (TIER == kTier32) run_wide<V>(r, prog, scal, pol);
+  else run_fused<tier_slots(TIER), V>(r, prog, scal, pol);
+}
+
+// ---- element-to-lane map of the contiguous and generic executors --------------
+// A warp covers 32*V consecutive logical elements. Lane l holds NG groups of G
+// consecutive elements; group h starts at h*32*G + l*G. With G = 4, each
+// group of a 4-byte tensor is one 16-byte access and a warp's access to one
+// group is 512 contiguous bytes.
+template <int V>
+struct LaneMap {
+  static constexpr int G = V < 4 ? V : 4;
+  static constexpr int NG = V / G;
+  static constexpr int W = 32 * V;
+};
+
+// Grid size for a persistent grid-stride kernel: enough CTAs to fill the
+// device at the kernel's occupancy, and no more than the work needs.
+template <class K>
+inline int persistent_grid(K kernel, int block, size_t smem, int64_t work_blocks) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem);
+  if (per_sm < 1) per_sm = 1;
+  if (sms < 1) sms = 1;
+  int64_t g = (int64_t)sms * per_sm;
+  if (work_blocks < g) g = work_blocks;
+  return g < 1 ? 1 : (int)g;
+}
+
+}  // namespace cmdx

@@ -1,0 +1,135 @@
+// exec_contig.cu - contiguous executor: every view is dense row-major and
+// 16-byte aligned, so each lane moves whole 16-byte (4-byte types) or 8-byte
+// (2-byte types) vectors, a warp's access is contiguous, and the grid strides
+// over warp-sized chunks of 32*V logical elements. It runs whole chunks only:
+// the host hands a ragged tail (fewer than 32*V elements) to the generic
+// executor, so the hot loop carries no bounds checks.
+#include "exec_common.cuh"
+
+namespace cmdx {
+
+static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
+
+// Load one slot (V elements per lane) of a dense tensor of type dt.
+template <int V>
+__device__ __forceinline__ void contig_load(uint32_t (&x)[V], const void* base, int dt, int64_t e0) {
+  using M = LaneMap<V>;
+#pragma unroll
+  for (int h = 0; h < M::NG; ++h) {
+    const int64_t e = e0 + (int64_t)h * 32 * M::G;
+    if (dt == 0 || dt == 3) {
+      if constexpr (M::G == 4) {
+        const uint4 q = ld_stream(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + e));
+        x[4 * h] = q.x; x[4 * h + 1] = q.y; x[4 * h + 2] = q.z; x[4 * h + 3] = q.w;
+      } else {
+        const uint2 q = ld_stream(reinterpret_cast<const uint2*>(static_cast<const uint32_t*>(base) + e));
+        x[2 * h] = q.x; x[2 * h + 1] = q.y;
+      }
+    } else {
+      if constexpr (M::G == 4) {
+        const uint2 q = ld_stream(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + e));
+        if (dt == 1) {
+          widen_f16x2(q.x, x[4 * h], x[4 * h + 1]);
+          widen_f16x2(q.y, x[4 * h + 2], x[4 * h + 3]);
+        } else {
+          widen_bf16x2(q.x, x[4 * h], x[4 * h + 1]);
+          widen_bf16x2(q.y, x[4 * h + 2], x[4 * h + 3]);
+        }
+      } else {
+        const uint32_t q = ld_stream(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + e));
+        if (dt == 1) widen_f16x2(q, x[2 * h], x[2 * h + 1]);
+        else widen_bf16x2(q, x[2 * h], x[2 * h + 1]);
+      }
+    }
+  }
+}
+
+template <int V>
+struct ContigStore {
+  const ContigParams& p;
+  int64_t e0;
+
+  template <int T>
+  __device__ __forceinline__ void store(const uint32_t (&x)[V], uint32_t o) const {
+    using M = LaneMap<V>;
+    void* base = p.out[o];
+#pragma unroll
+    for (int h = 0; h < M::NG; ++h) {
+      const int64_t e = e0 + (int64_t)h * 32 * M::G;
+      const uint32_t* v = &x[h * M::G];
+      if constexpr (T == kStF32 || T == kStI32) {
+        if constexpr (M::G == 4)
+          st_stream(reinterpret_cast<uint4*>(static_cast<uint32_t*>(base) + e), make_uint4(v[0], v[1], v[2], v[3]));
+        else
+          st_stream(reinterpret_cast<uint2*>(static_cast<uint32_t*>(base) + e), make_uint2(v[0], v[1]));
+      } else {
+        auto nar = [](uint32_t a, uint32_t b) {
+          if constexpr (T == kStF16) return narrow_f16x2(a, b);
+          else return narrow_bf16x2(a, b);
+        };
+        if constexpr (M::G == 4)
+          st_stream(reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + e),
+                    make_uint2(nar(v[0], v[1]), nar(v[2], v[3])));
+        else
+          st_stream(reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(base) + e), nar(v[0], v[1]));
+      }
+    }
+  }
+};
+
+template <int TIER>
+__global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(const __grid_constant__ ContigParams p) {
+  constexpr int S = tier_slots(TIER);
+  constexpr int V = tier_vec(TIER);
+  constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
+  using M = LaneMap<V>;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t* prog = c_prog[p.prog];
+  const int64_t n_chunks = p.n / M::W;  // the host passes a multiple of W
+  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n_chunks; w += nwarps) {
+    const int64_t e0 = w * M::W + (int64_t)lane * M::G;
+    uint32_t r[S][V];
+#pragma unroll
+    for (int j = 0; j < NL; ++j)
+      if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
+    ContigStore<V> st{p, e0};
+    run_program<TIER, V>(r, prog, p.scal, st);
+  }
+}
+
+int contig_chunk(int tier) {
+  return tier == kTier4 ? 32 * tier_vec(kTier4) : tier == kTier8 ? 32 * tier_vec(kTier8) : 32 * tier_vec(kTier32);
+}
+
+cudaError_t contig_upload(int slot, const uint32_t* words, int n) {
+  return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
+}
+
+template <int TIER>
+static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
+  constexpr int V = tier_vec(TIER);
+  constexpr int kBlock = 256;
+  static int grid_cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
+  int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
+  if (full_grid == 0) {
+    full_grid = persistent_grid(contig_kernel<TIER>, kBlock, 0, INT64_MAX);
+    if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
+  }
+  const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
+  contig_kernel<TIER><<<grid, kBlock, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t contig_launch(int tier, const ContigParams& p, cudaStream_t stream) {
+  switch (tier) {
+    case kTier4: return launch_tier<kTier4>(p, stream);
+    case kTier8: return launch_tier<kTier8>(p, stream);
+    default: return launch_tier<kTier32>(p, stream);
+  }
+}
+
+}  // namespace cmdx

@@ -1,0 +1,111 @@
+// exec_generic.cu - executor for any sizes/strides (rank <= 4 after merging,
+// strides >= 0, including stride-0 broadcasts and permuted views).
+//
+// Each element's offset in every view is computed from its logical index as
+// sum_k i_k * stride_k, with the multi-index taken from the row-major linear
+// index (rocRoller, "Design Overview", section "Kernel Graph": Dimension nodes
+// with size and stride, and the Flatten transform's row-major order). Lane l
+// of a warp handles elements base + 32 v + l, so views that are contiguous in
+// the innermost dim are still read with consecutive addresses across a warp.
+#include "exec_common.cuh"
+
+namespace cmdx {
+
+static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
+
+// q = e / d with the divisor's precomputed multiply-high form.
+__device__ __forceinline__ uint64_t fast_div(const FastDiv& f, uint64_t e) {
+  const uint64_t t = __umul64hi(f.m, e);
+  return (t + ((e - t) >> 1)) >> (f.l - 1);
+}
+
+// Offset of linear element e in a view with right-aligned strides st: the
+// row-major multi-index of e dotted with the strides.
+__device__ __forceinline__ int64_t gen_offset(const GenericParams& p, const int64_t* st, int64_t e) {
+  int64_t off = 0;
+  uint64_t rem = (uint64_t)e;
+#pragma unroll
+  for (int k = kMaxRank - 1; k > 0; --k) {
+    if (p.div[k].l == 0) continue;  // size-1 dim
+    const uint64_t q = fast_div(p.div[k], rem);
+    off += (int64_t)(rem - q * (uint64_t)p.div[k].d) * st[k];
+    rem = q;
+  }
+  return off + (int64_t)rem * st[0];
+}
+
+template <int V>
+struct GenericStore {
+  const GenericParams& p;
+  int64_t base;
+  int lane;
+
+  template <int T>
+  __device__ __forceinline__ void store(const uint32_t (&x)[V], uint32_t o) const {
+    void* ptr = p.out[o];
+    const int64_t* st = p.out_st[o];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int64_t e = base + 32 * v + lane;
+      if (e < p.n) st_elem<T>(ptr, gen_offset(p, st, e), x[v]);
+    }
+  }
+};
+
+template <int TIER>
+__global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(const __grid_constant__ GenericParams p) {
+  constexpr int S = tier_slots(TIER);
+  constexpr int V = tier_vec(TIER);
+  constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t* prog = c_prog[p.prog];
+  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w * 32 * V < p.n; w += nwarps) {
+    const int64_t base = w * 32 * V;
+    uint32_t r[S][V];
+#pragma unroll
+    for (int j = 0; j < NL; ++j) {
+      if (j < (int)p.n_loads) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int64_t e = base + 32 * v + lane;
+          r[j][v] = e < p.n ? widen_any(p.in_dt[j], ld_elem(p.in[j], p.in_dt[j], gen_offset(p, p.in_st[j], e))) : 0u;
+        }
+      }
+    }
+    GenericStore<V> st{p, base, lane};
+    run_program<TIER, V>(r, prog, p.scal, st);
+  }
+}
+
+cudaError_t generic_upload(int slot, const uint32_t* words, int n) {
+  return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
+}
+
+template <int TIER>
+static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
+  constexpr int V = tier_vec(TIER);
+  constexpr int kBlock = 256;
+  static int grid_cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
+  int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
+  if (full_grid == 0) {
+    full_grid = persistent_grid(generic_kernel<TIER>, kBlock, 0, INT64_MAX);
+    if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
+  }
+  const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
+  generic_kernel<TIER><<<grid, kBlock, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t generic_launch(int tier, const GenericParams& p, cudaStream_t stream) {
+  switch (tier) {
+    case kTier4: return launch_tier<kTier4>(p, stream);
+    case kTier8: return launch_tier<kTier8>(p, stream);
+    default: return launch_tier<kTier32>(p, stream);
+  }
+}
+
+}  // namespace cmdx

@@ -1,0 +1,386 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element
+by element on the same seeded inputs. Bit-exact for int32 and fp32; within
+1 ulp (and in fact exact) for fp16/bf16 stores."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_command_execution_gb300 as T
+from inputgen import workloads as W
+import gpuutil
+import specutil
+
+pytestmark = pytest.mark.gpu
+
+
+# ---- the workloads at sizes the oracle finishes in seconds ------------------------
+
+@pytest.mark.parametrize("spec,path", [
+    (W.add_f32((1 << 20) + 37), "contig"),
+    (W.add_f32(1 << 20), "contig"),
+    (W.chain_f32((1 << 18) + 5), "contig"),
+    (W.wrap_i32((1 << 18) + 3), "contig"),
+    (W.strided_bf16(320, 264, 272), "tile2d"),
+    (W.strided_bf16(200, 136, 144), "tile2d"),
+    (W.strided_bf16(192, 128, 136), "tile2d"),
+    (W.strided_bf16(100, 70, 75), "generic"),
+    (W.wide_dag((1 << 18) + 11), "contig"),
+    (W.wide_dag(37), "contig"),
+], ids=lambda x: x["name"] + str(x["sizes"]) if isinstance(x, dict) else x)
+def test_workload_small(spec, path):
+    plan = gpuutil.parity(spec)
+    assert plan["path"] == path
+
+
+# ---- the workloads at full size, sampled --------------------------------------------
+
+@pytest.mark.parametrize("name", list(W.FULL))
+def test_workload_full_size_sampled(name):
+    spec = W.FULL[name]()
+    plan, checked = gpuutil.sampled_parity(spec, n_samples=1 << 18)
+    assert plan["path"] == ("tile2d" if name == "strided_bf16" else "contig")
+    assert checked > 1 << 17
+
+
+# ---- tile executor over dtypes, ragged tiles and several transposed loads -------------
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16", "i32"])
+@pytest.mark.parametrize("rows,cols", [(64, 64), (130, 72), (8, 200), (257, 40)])
+def test_tile_paths(dt, rows, cols):
+    rng = np.random.default_rng(rows * 1000 + cols)
+    es = 2 if dt in ("f16", "bf16") else 4
+    al = 16 // es  # strides must keep 16-byte rows
+    ldA = (cols + al + al - 1) // al * al
+    ldB = (rows + al - 1) // al * al
+    ldC = (rows + 2 * al - 1) // al * al
+    cls_int = dt == "i32"
+    st = "i32" if cls_int else "f32"
+    spec = dict(name=f"tile_{dt}", seed=0, sizes=(rows, cols),
+                ops=[("load", "A", dt), ("load", "B", dt), ("load", "C", dt),
+                     ("scalar", "s", st, 3 if cls_int else 0.5),
+                     ("exec", [("mul", "AB", "A", "B"), ("sub", "t", "AB", "C"), ("add", "r", "t", "s"),
+                               ("neg", "q", "B", None)]),
+                     ("store", "out", "r", "i32" if cls_int else dt),
+                     ("store", "out2", "q", "i32" if cls_int else "f32")],
+                views={"A": dict(strides=(ldA, 1), alloc=(rows - 1) * ldA + cols),
+                       "B": dict(strides=(1, ldB), alloc=(cols - 1) * ldB + rows),
+                       "C": dict(strides=(1, ldC), alloc=(cols - 1) * ldC + rows),
+                       "out": dict(strides=(cols, 1), alloc=rows * cols),
+                       "out2": dict(strides=(ldA, 1), alloc=(rows - 1) * ldA + cols)},
+                inputs={})
+    bufs = {}
+    for name in ("A", "B", "C"):
+        n = spec["views"][name]["alloc"]
+        if cls_int:
+            bufs[name] = rng.integers(-2**31, 2**31, size=n).astype(np.int32)
+        else:
+            f = rng.standard_normal(n).astype(np.float32) * 4
+            if dt == "f32":
+                bufs[name] = f
+            elif dt == "f16":
+                bufs[name] = f.astype(np.float16)
+            else:
+                bufs[name] = (f.view(np.uint32) >> 16).astype(np.uint16)
+    for name in ("out", "out2"):
+        odt = W.tensor_dtypes(spec)[name]
+        bufs[name] = specutil.sentinel_array(odt, spec["views"][name]["alloc"])
+    plan = gpuutil.parity(spec, bufs)
+    assert plan["path"] == "tile2d" and plan["n_transposed"] == 2
+
+
+# ---- randomized Commands ---------------------------------------------------------------
+
+def _dense_strides(shape):
+    st, acc = [], 1
+    for s in reversed(shape):
+        st.append(acc)
+        acc *= s
+    return tuple(reversed(st)), acc
+
+
+def _random_view(rng, sizes, allow_broadcast):
+    rank = len(sizes)
+    mode = rng.choice(["dense", "padded", "permuted", "broadcast"] if allow_broadcast
+                      else ["dense", "padded", "permuted"])
+    if mode == "dense":
+        st, n = _dense_strides(sizes)
+        return st, n
+    if mode == "padded":
+        pad = int(rng.integers(1, 9))
+        st = [0] * rank
+        acc = 1
+        for k in range(rank - 1, -1, -1):
+            st[k] = acc
+            acc = acc * sizes[k] + (pad if k == rank - 1 else 0)
+        n = sum((s - 1) * t for s, t in zip(sizes, st)) + 1
+        return tuple(st), n
+    if mode == "permuted":
+        perm = rng.permutation(rank)
+        phys = [sizes[p] for p in perm]
+        pst, n = _dense_strides(phys)
+        st = [0] * rank
+        for q, p in enumerate(perm):
+            st[p] = pst[q]
+        return tuple(st), n
+    st, n = _dense_strides(sizes)
+    st = list(st)
+    for k in range(rank):
+        if rng.random() < 0.5:
+            st[k] = 0
+    n = sum((s - 1) * t for s, t in zip(sizes, st)) + 1
+    return tuple(st), n
+
+
+def _random_values(rng, dt, n):
+    if dt == "i32":
+        return rng.integers(-2**31, 2**31, size=n).astype(np.int32)
+    f = (rng.standard_normal(n) * rng.choice([1.0, 100.0, 1e-3])).astype(np.float32)
+    if dt == "f32":
+        return f
+    if dt == "f16":
+        return f.astype(np.float16)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def random_case(seed):
+    rng = np.random.default_rng(seed)
+    rank = int(rng.integers(0, 4))
+    sizes = tuple(int(x) for x in rng.integers(1, 24, size=rank))
+    if rank and rng.random() < 0.3:
+        sizes = sizes[:-1] + (int(rng.integers(100, 700)),)
+    is_int = rng.random() < 0.3
+    ops, views, bufs, vals = [], {}, {}, []
+    n_loads = int(rng.integers(1, 7))
+    for i in range(n_loads):
+        dt = "i32" if is_int else str(rng.choice(["f32", "f16", "bf16"]))
+        name = f"L{i}"
+        ops.append(("load", name, dt))
+        st, n = _random_view(rng, sizes, allow_broadcast=True)
+        views[name] = dict(strides=st, alloc=n)
+        bufs[name] = _random_values(rng, dt, n)
+        vals.append(name)
+    for i in range(int(rng.integers(0, 3))):
+        name = f"S{i}"
+        if is_int:
+            ops.append(("scalar", name, "i32", int(rng.integers(-2**31, 2**31))))
+        else:
+            ops.append(("scalar", name, "f32", float(np.float32(rng.standard_normal()))))
+        vals.append(name)
+    block = []
+    for i in range(int(rng.integers(1, 22))):
+        eop = str(rng.choice(["add", "sub", "mul", "neg"]))
+        a = str(rng.choice(vals))
+        b = None if eop == "neg" else str(rng.choice(vals))
+        name = f"E{i}"
+        block.append((eop, name, a, b))
+        vals.append(name)
+    ops.append(("exec", block))
+    for i in range(int(rng.integers(1, 4))):
+        src = vals[-1 - int(rng.integers(0, min(4, len(vals))))]
+        dt = "i32" if is_int else str(rng.choice(["f32", "f16", "bf16"]))
+        name = f"O{i}"
+        ops.append(("store", name, src, dt))
+        st, n = _random_view(rng, sizes, allow_broadcast=False)
+        views[name] = dict(strides=st, alloc=n)
+        bufs[name] = specutil.sentinel_array(dt, n)
+    return dict(name=f"random{seed}", seed=seed, sizes=sizes, ops=ops, views=views, inputs={}), bufs
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_commands(seed):
+    spec, bufs = random_case(seed)
+    gpuutil.parity(spec, bufs)
+
+
+# ---- edge cases -------------------------------------------------------------------------
+
+def test_empty_launch_is_a_no_op():
+    spec = W.add_f32(0)
+    bufs = {k: np.zeros(0, np.float32) for k in ("x", "y", "out")}
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    views = {tags[n]: T.TensorView(0, (0,), (1,)) for n in ("x", "y", "out")}
+    assert k.plan(views)["path"] == "none"
+    k.launch(views)
+    k.sync()
+    del bufs
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 255, 256, 257, 1023, 1025, 4097])
+def test_ragged_lengths(n):
+    gpuutil.parity(W.wide_dag(n))
+    gpuutil.parity(W.chain_f32(n))
+
+
+def test_rank0_single_element():
+    spec = W.chain_f32(1)
+    spec["sizes"] = ()
+    for k in spec["views"]:
+        spec["views"][k] = dict(strides=(), alloc=1)
+    gpuutil.parity(spec)
+
+
+def test_fill_copy_and_in_place():
+    n = 5000
+    spec = dict(name="fill", seed=0, sizes=(n,),
+                ops=[("load", "x", "f32"), ("scalar", "s", "f32", -2.5),
+                     ("store", "fill", "s", "bf16"), ("store", "copy", "x", "f16"),
+                     ("exec", [("mul", "y", "x", "s")]), ("store", "x_out", "y", "f32")],
+                views={k: dict(strides=(1,), alloc=n) for k in ("x", "fill", "copy", "x_out")},
+                inputs={"x": ("normal_f32", 0, 0)})
+    bufs = specutil.host_buffers(spec)
+    gpuutil.parity(spec, bufs)
+    # in place: the store's view is the load's view
+    dts = W.tensor_dtypes(spec)
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    dev = {name: gpuutil.to_device(bufs[name], dts[name]) for name in ("x", "fill", "copy")}
+    views = {tags[nm]: T.TensorView(dev[nm].data_ptr(), (n,), (1,)) for nm in dev}
+    views[tags["x_out"]] = views[tags["x"]]
+    k.launch(views, {tags["s"]: -2.5})
+    k.sync()
+    torch.cuda.synchronize()
+    ref = {kk: v.copy() for kk, v in bufs.items()}
+    oracle.OracleCommand(spec, ref).eval_range()
+    gpuutil.compare(dev["x"].cpu().numpy(), ref["x_out"], "f32", "in place")
+
+
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_misaligned_bases_use_the_generic_path(off):
+    spec = W.wide_dag(10000)
+    plan = gpuutil.parity(spec, offsets={"a": off, "out1": off})
+    assert plan["path"] == "generic"
+
+
+def test_wide_tier_program():
+    rng = np.random.default_rng(5)
+    n = 3000
+    names = [f"x{i}" for i in range(16)]
+    block = [("add", "c0", "x0", "x15")] + [("mul", f"c{i}", f"c{i-1}", names[i]) for i in range(1, 16)]
+    block += [("sub", f"d{i}", names[i], f"c{i}") for i in range(16)]
+    block += [("add", "e0", "d0", "d1")] + [("add", f"e{i}", f"e{i-1}", f"d{i+1}") for i in range(1, 15)]
+    spec = dict(name="wide", seed=0, sizes=(n,),
+                ops=[("load", k, "f32") for k in names] + [("exec", block), ("store", "out", "e14", "f32"),
+                                                            ("store", "out2", "c15", "bf16")],
+                views={k: dict(strides=(1,), alloc=n) for k in names + ["out", "out2"]}, inputs={})
+    bufs = {k: (rng.standard_normal(n) * 1.5).astype(np.float32) for k in names}
+    bufs["out"] = specutil.sentinel_array("f32", n)
+    bufs["out2"] = specutil.sentinel_array("bf16", n)
+    c, _ = T.command_from_spec(spec)
+    assert c.lower()[0]["tier"] == 2
+    assert gpuutil.parity(spec, bufs)["path"] == "contig"
+
+
+def test_special_values():
+    """Denormals, signed zeros, infinities and NaNs flow through every op
+    like the oracle's IEEE arithmetic (NaN payloads are not compared)."""
+    specials = np.array([0, 0x80000000, 1, 0x80000001, 0x007FFFFF, 0x00800000, 0x7F7FFFFF, 0xFF7FFFFF,
+                         0x7F800000, 0xFF800000, 0x7FC00000, 0x3F800000, 0x33800000, 0x477FF000,
+                         0x477FEFFF, 0x387FC000, 0x33000000, 0x00400000], dtype=np.uint32)
+    x = np.repeat(specials, specials.size)
+    y = np.tile(specials, specials.size)
+    n = x.size
+    spec = dict(name="specials", seed=0, sizes=(n,),
+                ops=[("load", "x", "f32"), ("load", "y", "f32"),
+                     ("exec", [("add", "s", "x", "y"), ("sub", "d", "x", "y"), ("mul", "p", "x", "y"),
+                               ("neg", "m", "p", None)]),
+                     ("store", "o1", "s", "f32"), ("store", "o2", "d", "f16"), ("store", "o3", "p", "bf16"),
+                     ("store", "o4", "m", "f32")],
+                views={k: dict(strides=(1,), alloc=n) for k in ("x", "y", "o1", "o2", "o3", "o4")}, inputs={})
+    bufs = {"x": x.view(np.float32), "y": y.view(np.float32)}
+    for k, dt in (("o1", "f32"), ("o2", "f16"), ("o3", "bf16"), ("o4", "f32")):
+        bufs[k] = specutil.sentinel_array(dt, n)
+    gpuutil.parity(spec, bufs)
+
+
+def test_int_edge_values():
+    e = np.array([0, 1, -1, 2**31 - 1, -2**31, 0x10000, -0x10000, 46341, -46341], dtype=np.int64)
+    x = np.repeat(e, e.size).astype(np.int32)
+    y = np.tile(e, e.size).astype(np.int32)
+    n = x.size
+    spec = dict(name="ints", seed=0, sizes=(n,),
+                ops=[("load", "x", "i32"), ("load", "y", "i32"), ("scalar", "k", "i32", -2**31),
+                     ("exec", [("mul", "p", "x", "y"), ("sub", "d", "p", "k"), ("neg", "m", "x", None),
+                               ("add", "a", "m", "d")]),
+                     ("store", "o", "a", "i32"), ("store", "o2", "m", "i32")],
+                views={k: dict(strides=(1,), alloc=n) for k in ("x", "y", "o", "o2")}, inputs={})
+    bufs = {"x": x, "y": y, "o": specutil.sentinel_array("i32", n), "o2": specutil.sentinel_array("i32", n)}
+    gpuutil.parity(spec, bufs)
+
+
+def test_sixteen_loads_and_eight_stores():
+    rng = np.random.default_rng(11)
+    n = 2049
+    names = [f"x{i}" for i in range(16)]
+    block = [("add", "s0", "x0", "x1")] + [("add", f"s{i}", f"s{i-1}", names[i + 1]) for i in range(1, 15)]
+    stores = [(f"o{j}", f"s{14 - j}", ["f32", "f16", "bf16"][j % 3]) for j in range(8)]
+    spec = dict(name="many", seed=0, sizes=(n,),
+                ops=[("load", k, "f32") for k in names] + [("exec", block)]
+                + [("store", o, s, dt) for o, s, dt in stores],
+                views={k: dict(strides=(1,), alloc=n) for k in names + [o for o, _, _ in stores]}, inputs={})
+    bufs = {k: rng.standard_normal(n).astype(np.float32) for k in names}
+    for o, _, dt in stores:
+        bufs[o] = specutil.sentinel_array(dt, n)
+    gpuutil.parity(spec, bufs)
+
+
+def test_launch_on_a_side_stream_and_relaunch():
+    spec = W.chain_f32(70000)
+    bufs = specutil.host_buffers(spec)
+    s = torch.cuda.Stream()
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    for _ in range(3):
+        got, _ = gpuutil.run_cuda(spec, bufs, stream=s, kernel=k)
+    ref = {kk: v.copy() for kk, v in bufs.items()}
+    oracle.OracleCommand(spec, ref).eval_range()
+    gpuutil.compare(got["out"], ref["out"], "f32", "side stream")
+
+
+def test_many_kernels_and_slot_reuse():
+    """Compile more kernels than the constant table holds over time: destroyed
+    kernels free their program slots for later compiles."""
+    spec = W.add_f32(4096)
+    bufs = specutil.host_buffers(spec)
+    for i in range(120):
+        c, _ = T.command_from_spec(spec)
+        k = c.compile()
+        if i % 40 == 0:
+            got, _ = gpuutil.run_cuda(spec, bufs, kernel=k)
+            gpuutil.compare(got["out"], bufs["x"] + bufs["y"], "f32", f"kernel {i}")
+        del k, c
+
+
+def test_exhaustive_store_conversion():
+    """Every binary32 bit pattern stored as f16 and as bf16 through the GPU
+    path equals the oracle's converter (NaNs compared as a class)."""
+    from concurrent.futures import ThreadPoolExecutor
+    chunk = 1 << 27
+    spec = dict(name="conv", seed=0, sizes=(chunk,),
+                ops=[("load", "x", "f32"), ("store", "h", "x", "f16"), ("store", "b", "x", "bf16")],
+                views={k: dict(strides=(1,), alloc=chunk) for k in ("x", "h", "b")}, inputs={})
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    x = torch.empty(chunk, dtype=torch.int32, device="cuda")
+    h = torch.empty(chunk, dtype=torch.int16, device="cuda")
+    b = torch.empty(chunk, dtype=torch.int16, device="cuda")
+    views = {tags["x"]: T.TensorView(x.data_ptr(), (chunk,), (1,)),
+             tags["h"]: T.TensorView(h.data_ptr(), (chunk,), (1,)),
+             tags["b"]: T.TensorView(b.data_ptr(), (chunk,), (1,))}
+    ramp = torch.arange(chunk, dtype=torch.int64, device="cuda")
+    pool = ThreadPoolExecutor(max_workers=16)
+    for start in range(0, 1 << 32, chunk):
+        x.copy_((ramp + start - (1 << 31)).to(torch.int32) ^ (-(1 << 31)))  # bit pattern start + i
+        k.launch(views)
+        k.sync()
+        got_h = h.cpu().numpy().view(np.uint16)
+        got_b = b.cpu().numpy().view(np.uint16)
+        bits = (np.arange(chunk, dtype=np.uint64) + start).astype(np.uint32)
+        parts = np.array_split(bits, 16)
+        want_h = np.concatenate(list(pool.map(oracle.f32_to_f16_bits, parts)))
+        want_b = np.concatenate(list(pool.map(oracle.f32_to_bf16_bits, parts)))
+        gpuutil.compare(got_h, want_h, "f16", f"f16 from {start:#x}")
+        gpuutil.compare(got_b, want_b, "bf16", f"bf16 from {start:#x}")

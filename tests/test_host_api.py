@@ -1,0 +1,275 @@
+"""Host-side tests of the C ABI: the library loads and exports every declared
+symbol, Command building rejects bad input, lowering has the expected
+structure, and launch planning validates arguments and picks executors. No
+GPU is used (kernels come from cmd_lower_kernel; pointers are never read)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_command_execution_gb300 as T
+from inputgen import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "cmd.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cmd_[a-z_]+)\s*\(", text)) - {"CMD_LOCAL"})
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 18
+    L = ctypes.CDLL(T.library_path() if os.path.exists(T.library_path()) else T._build.build())
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(T.SIGNATURES), set(names) ^ set(T.SIGNATURES)
+    assert T.cmd_abi_version() == 1
+
+
+def test_status_strings():
+    L = T.lib()
+    assert L.cmd_status_string(0) == b"CMD_OK"
+    assert L.cmd_status_string(5) == b"CMD_ERR_ALIAS"
+
+
+# ---- builder errors ------------------------------------------------------------
+
+def _err(fn, *a):
+    with pytest.raises(T.CmdError) as e:
+        fn(*a)
+    return e.value.name
+
+
+def test_builder_rejects_bad_input():
+    c = T.Command()
+    x = c.load_tensor("f32", 1)
+    i = c.load_tensor("i32", 1)
+    assert _err(c.load_tensor, "f32", 5) == "CMD_ERR_SHAPE"
+    assert _err(c.load_scalar, "f16") == "CMD_ERR_TYPE"
+    # int/float mix
+    assert _err(c.execute, [("add", x, i)]) == "CMD_ERR_TYPE"
+    # reference to a tag that does not exist yet
+    assert _err(c.execute, [("add", x, 99)]) == "CMD_ERR_BAD_TAG"
+    # local reference to a later op of the block
+    assert _err(c.execute, [("add", x, T.CMD_LOCAL(0))]) == "CMD_ERR_BAD_TAG"
+    # a failed block adds nothing
+    before = T.cmd_next_tag(c.handle)
+    assert _err(c.execute, [("add", x, x), ("add", x, i)]) == "CMD_ERR_TYPE"
+    assert T.cmd_next_tag(c.handle) == before
+    y, z = c.execute([("mul", x, x), ("neg", T.CMD_LOCAL(0), None)])
+    assert (y, z) == (before, before + 1)
+    s = c.store(z, "bf16", 1)
+    # a store has no value
+    assert _err(c.execute, [("neg", s, None)]) == "CMD_ERR_BAD_TAG"
+    # int value stored as float and float stored as int
+    assert _err(c.store, i, "f32", 1) == "CMD_ERR_TYPE"
+    assert _err(c.store, y, "i32", 1) == "CMD_ERR_TYPE"
+    assert _err(c.execute, []) == "CMD_ERR_ARG"
+
+
+def test_tag_limit():
+    c = T.Command()
+    x = c.load_tensor("f32", 1)
+    for _ in range(W_LIMIT - 1):
+        c.execute([("neg", x, None)])
+    assert _err(c.execute, [("neg", x, None)]) == "CMD_ERR_LIMIT"
+
+
+W_LIMIT = 128
+
+
+def test_mixed_ranks_rejected_at_lowering():
+    c = T.Command()
+    x = c.load_tensor("f32", 2)
+    c.store(x, "f32", 1)
+    assert _err(c.lower) == "CMD_ERR_SHAPE"
+
+
+# ---- lowering structure ---------------------------------------------------------
+
+def test_lowering_of_the_workloads():
+    expect = {  # live E ops, loads, slots, tier, moves
+        "add_f32": (1, 2, 2, 0, 0),
+        "chain_f32": (4, 3, 3, 0, 0),
+        "wrap_i32": (3, 4, 4, 0, 0),
+        "strided_bf16": (3, 2, 2, 0, 0),
+        "wide_dag": (15, 6, 7, 1, 3),
+    }
+    for name, f in W.FULL.items():
+        c, _ = T.command_from_spec(f(1024) if name != "strided_bf16" else f(64, 64, 64))
+        info, words = c.lower()
+        got = (info["n_live_ops"], info["n_loads"], info["n_slots"], info["tier"], info["n_moves"])
+        assert got == expect[name], (name, info)
+        assert info["n_words"] == len(words) == info["n_live_ops"] + info["n_moves"] + info["n_stores"] + 1
+
+
+def test_dead_tags_and_reuse():
+    c = T.Command()
+    a = c.load_tensor("f32", 1)
+    b = c.load_tensor("f32", 1)
+    dead_load = c.load_tensor("f32", 1)
+    s = c.load_scalar("f32")
+    t = c.execute([("add", a, b), ("add", b, a), ("mul", T.CMD_LOCAL(0), T.CMD_LOCAL(1)),
+                   ("sub", dead_load, a), ("mul", a, s), ("mul", s, a), ("sub", T.CMD_LOCAL(4), T.CMD_LOCAL(5))])
+    c.store(t[2], "f32", 1)
+    c.store(t[6], "f32", 1)
+    info, _ = c.lower()
+    # b+a reuses a+b; s*a reuses a*s; the sub of the dead load is dropped
+    assert info["n_loads"] == 2
+    assert info["n_live_ops"] == 4
+    assert info["n_scalars"] == 1
+
+
+def test_sub_is_not_treated_as_commutative():
+    c = T.Command()
+    a = c.load_tensor("f32", 1)
+    b = c.load_tensor("f32", 1)
+    t = c.execute([("sub", a, b), ("sub", b, a)])
+    c.store(t[0], "f32", 1)
+    c.store(t[1], "f32", 1)
+    info, _ = c.lower()
+    assert info["n_live_ops"] == 2
+
+
+def test_wide_program_uses_the_32_slot_tier():
+    # 12 loads all live until the end: needs more than 8 slots
+    c = T.Command()
+    xs = [c.load_tensor("f32", 1) for _ in range(12)]
+    ops = [("add", xs[0], xs[11])] + [("add", T.CMD_LOCAL(i), xs[(i + 1) % 12]) for i in range(11)]
+    ops += [("mul", xs[k], xs[k]) for k in range(12)]
+    t = c.execute(ops)
+    c.store(t[11], "f32", 1)
+    for k in range(12, 19):
+        c.store(t[k], "f32", 1)
+    info, _ = c.lower()
+    assert info["tier"] == 2 and info["n_slots"] > 8
+
+
+def test_store_of_loads_and_scalars_only():
+    c = T.Command()
+    x = c.load_tensor("f16", 1)
+    s = c.load_scalar("f32")
+    c.store(x, "f32", 1)
+    c.store(s, "bf16", 1)
+    info, _ = c.lower()
+    assert info["n_live_ops"] == 0 and info["n_stores"] == 2
+
+
+def test_dump_lists_the_program():
+    c, _ = T.command_from_spec(W.chain_f32(1024))
+    text = c.lower_kernel().dump()
+    assert "fmul    r1, r0" in text and "store   out0 <- r1 (f32" in text
+
+
+# ---- launch planning (host only) -------------------------------------------------
+
+BASE = 1 << 30  # fake, 16-byte-aligned device addresses; never dereferenced
+
+
+def _plan(spec, ptrs=None, overrides=None):
+    c, tags = T.command_from_spec(spec)
+    k = c.lower_kernel()
+    views = {}
+    addr = BASE
+    for name in W.load_names(spec) + W.store_names(spec):
+        v = spec["views"][name]
+        p = (ptrs or {}).get(name, addr)
+        views[tags[name]] = T.TensorView(p, spec["sizes"], v["strides"])
+        addr += (v["alloc"] * 4 + 4096) // 4096 * 4096
+    for name, view in (overrides or {}).items():
+        views[tags[name]] = view
+    return k.plan(views, T.spec_scalars(spec, tags))
+
+
+def test_plans_of_the_workloads():
+    assert _plan(W.add_f32(1 << 20))["path"] == "contig"
+    assert _plan(W.chain_f32(1000))["path"] == "contig"  # ragged length still contiguous
+    p = _plan(W.strided_bf16(256, 192, 200))
+    assert p["path"] == "tile2d" and p["n_transposed"] == 1 and p["merged_sizes"] == [256, 192]
+    assert p["bytes"] == 256 * 192 * 6
+    p = _plan(W.wide_dag(1 << 20))
+    assert p["path"] == "contig" and p["bytes"] == 30 << 20
+
+
+def test_dims_merge_to_contiguous():
+    spec = W.add_f32(24)
+    spec["sizes"] = (2, 3, 4)
+    for k in spec["views"]:
+        spec["views"][k] = dict(strides=(12, 4, 1), alloc=24)
+    p = _plan(spec)
+    assert p["path"] == "contig" and p["merged_rank"] == 1 and p["merged_sizes"] == [24]
+
+
+def test_padded_rows_use_the_tile_path_and_permutations_the_generic():
+    spec = W.add_f32(0)
+    spec["sizes"] = (64, 64)
+    spec["views"] = {"x": dict(strides=(72, 1), alloc=64 * 72), "y": dict(strides=(64, 1), alloc=4096),
+                     "out": dict(strides=(64, 1), alloc=4096)}
+    assert _plan(spec)["path"] == "tile2d"
+    spec["sizes"] = (4, 8, 16)
+    spec["views"] = {"x": dict(strides=(1, 64, 4), alloc=512), "y": dict(strides=(128, 16, 1), alloc=512),
+                     "out": dict(strides=(128, 16, 1), alloc=512)}
+    # the last two dims merge for every view: a 4 x 128 transposed read
+    p = _plan(spec)
+    assert p["path"] == "tile2d" and p["merged_sizes"] == [4, 128] and p["n_transposed"] == 1
+    spec["views"]["x"] = dict(strides=(1, 4, 32), alloc=512)
+    p = _plan(spec)
+    assert p["path"] == "generic" and p["merged_rank"] == 3
+
+
+def test_unaligned_pointer_falls_back_to_generic():
+    assert _plan(W.add_f32(4096), ptrs={"x": BASE + (1 << 28) + 4})["path"] == "generic"
+
+
+def test_launch_validation_errors():
+    spec = W.add_f32(1024)
+    with pytest.raises(T.CmdError) as e:
+        _plan(spec, ptrs={"x": BASE + 2})
+    assert e.value.name == "CMD_ERR_ALIGN"
+    with pytest.raises(T.CmdError) as e:
+        _plan(spec, overrides={"y": T.TensorView(BASE, (1000,), (1,))})
+    assert e.value.name == "CMD_ERR_SHAPE"
+    with pytest.raises(T.CmdError) as e:
+        _plan(spec, overrides={"out": T.TensorView(BASE + 8, (1024,), (1,))})  # overlaps x
+    assert e.value.name == "CMD_ERR_ALIAS"
+    with pytest.raises(T.CmdError) as e:
+        _plan(spec, overrides={"out": T.TensorView(BASE + (1 << 29), (1024,), (0,))})  # not injective
+    assert e.value.name == "CMD_ERR_ALIAS"
+    with pytest.raises(T.CmdError) as e:
+        _plan(spec, overrides={"out": T.TensorView(0, (1024,), (1,))})
+    assert e.value.name == "CMD_ERR_NULL"
+    # an identical view read and written in place is allowed
+    p = _plan(spec, overrides={"out": T.TensorView(BASE, (1024,), (1,))})
+    assert p["path"] == "contig"
+
+
+def test_missing_and_unknown_arguments():
+    spec = W.chain_f32(64)
+    c, tags = T.command_from_spec(spec)
+    k = c.lower_kernel()
+    views = {tags[n]: T.TensorView(BASE + i * 4096, (64,), (1,)) for i, n in enumerate(["a", "b", "c", "out"])}
+    with pytest.raises(T.CmdError) as e:
+        k.plan(views, {})
+    assert e.value.name == "CMD_ERR_ARG"  # scalar s missing
+    with pytest.raises(T.CmdError) as e:
+        k.plan({**views, tags["r"]: T.TensorView(BASE, (64,), (1,))}, {tags["s"]: 0.75})
+    assert e.value.name == "CMD_ERR_BAD_TAG"  # an E result is not a tensor argument
+    # a dead load's argument may be omitted; zero elements plan to nothing
+    empty = {t: T.TensorView(BASE, (0,), (1,)) for t in views}
+    assert k.plan(empty, {tags["s"]: 0.75})["path"] == "none"
+
+
+def test_lowered_kernel_cannot_launch():
+    c, tags = T.command_from_spec(W.add_f32(64))
+    k = c.lower_kernel()
+    views = {tags[n]: T.TensorView(BASE + i * 4096, (64,), (1,)) for i, n in enumerate(["x", "y", "out"])}
+    with pytest.raises(T.CmdError) as e:
+        k.launch(views, stream=0)
+    assert e.value.name == "CMD_ERR_STATE"
