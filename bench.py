@@ -54,7 +54,20 @@ def parse():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the device-timed region (no e2e, CPU baseline or other workloads): for profiling")
+    ap.add_argument("--size", type=int, default=0,
+                    help="override the workload size (elements; rows = cols for the strided workload)")
     return ap.parse_args()
+
+
+def make_spec(name, size):
+    f = W.FULL[name]
+    if not size:
+        return f()
+    if name == "strided_bf16":
+        return f(size, size, size + 128)
+    return f(size)
 
 
 def measured_peak():
@@ -244,7 +257,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     peak, peak_kind = measured_peak()
 
-    spec = W.FULL[args.workload]()
+    spec = make_spec(args.workload, args.size)
     wl = Workload(spec, device)
     torch.cuda.synchronize()
 
@@ -278,6 +291,14 @@ def run_ours(args):
         ms = float(t.item())
     gbs = wl.bytes / (ms * 1e-3) / 1e9
     value = gbs * world
+
+    if args.no_extras:
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "elements": wl.elements, "ms_per_step": ms,
+                              "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "path": wl.plan["path"]}))
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # ---- end to end: pinned host inputs -> device, launch, output -> host ----
     outs_host = {n: torch.empty_like(wl.dev[n], device="cpu").pin_memory() for n in W.store_names(spec)}
