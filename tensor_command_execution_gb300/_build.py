@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(OUT_DIR, "libcmdexec.so")
 
 CU_SOURCES = ["exec_contig.cu", "exec_tile2d.cu", "exec_generic.cu"]
 CPP_SOURCES = ["cmd_api.cpp"]
-HEADERS = ["cmd_internal.h", "exec_common.cuh"]
+HEADERS = ["cmd_internal.h", "exec_common.cuh", "interp_asm.cuh", "gen_interp.py"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,6 +49,10 @@ def up_to_date() -> bool:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link libcmdexec.so unless it is newer than every source."""
+    gen = os.path.join(CSRC, "gen_interp.py")
+    inc_file = os.path.join(CSRC, "interp_asm.cuh")
+    if not os.path.exists(inc_file) or os.path.getmtime(inc_file) < os.path.getmtime(gen):
+        subprocess.run(["python3", gen], check=True, capture_output=True)
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)

@@ -27,8 +27,11 @@ constexpr int kMaxWords = 256;
 // and then dispatches on (opcode, dst).
 enum Tier { kTier4 = 0, kTier8 = 1, kTier32 = 2 };
 CMDX_HD constexpr int tier_slots(int tier) { return tier == kTier4 ? 4 : tier == kTier8 ? 8 : 32; }
-// Elements each thread keeps per slot: 32 slot registers in the fused tiers.
-CMDX_HD constexpr int tier_vec(int tier) { return tier == kTier32 ? 2 : tier == kTier8 ? 4 : 8; }
+// Elements each thread keeps per slot in the contiguous executor.
+CMDX_HD constexpr int tier_vec(int tier) { return tier == kTier32 ? 2 : 8; }
+// ... and in the tile and generic executors, whose addressing needs more
+// registers: the 8-slot tier keeps 4 elements per slot there.
+CMDX_HD constexpr int tier_vec_strided(int tier) { return tier == kTier8 ? 4 : tier_vec(tier); }
 // Resident 256-thread CTAs per SM each executor is compiled for (caps registers).
 CMDX_HD constexpr int tier_min_blocks(int tier) { return tier == kTier32 ? 2 : 3; }
 

@@ -1,10 +1,12 @@
 // exec_common.cuh - the register-slot interpreter shared by the executors.
 //
-// Every thread keeps V consecutive-per-lane elements of each live value in
-// registers ("slots"). A program word selects one case of a switch whose
-// slot numbers are compile-time constants, so slots never need run-time
-// register indexing (which would spill them to local memory). All threads of
-// a launch run the same program, so the dispatch branch is warp-uniform.
+// Every thread keeps V elements of each live value in registers ("slots").
+// A program word selects one case of a jump table whose slot numbers are
+// fixed in the code, so slots never need run-time register indexing (which
+// would spill them to local memory). All threads of a launch run the same
+// program, so the dispatch branch is warp-uniform. In the 4- and 8-slot
+// tiers the loop is inline PTX (interp_asm.cuh, generated): each case updates
+// its destination registers in place and the dispatch moves no data.
 //
 // rocRoller, "Design Overview": the program plays the part of the scheduled
 // instructions generated from the KernelGraph (sections "Generating
@@ -19,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "cmd_internal.h"
+#include "interp_asm.cuh"
 
 namespace cmdx {
 
@@ -106,69 +109,41 @@ __device__ __forceinline__ void st_elem(void* base, int64_t off, uint32_t x) {
 
 // ---- slot lists for the fused dispatch ----------------------------------------
 #define CMDX_SA4(M, ...) M(0, __VA_ARGS__) M(1, __VA_ARGS__) M(2, __VA_ARGS__) M(3, __VA_ARGS__)
-#define CMDX_SB4(M, ...) M(0, __VA_ARGS__) M(1, __VA_ARGS__) M(2, __VA_ARGS__) M(3, __VA_ARGS__)
 #define CMDX_SA8(M, ...) CMDX_SA4(M, __VA_ARGS__) M(4, __VA_ARGS__) M(5, __VA_ARGS__) M(6, __VA_ARGS__) M(7, __VA_ARGS__)
-#define CMDX_SB8(M, ...) CMDX_SB4(M, __VA_ARGS__) M(4, __VA_ARGS__) M(5, __VA_ARGS__) M(6, __VA_ARGS__) M(7, __VA_ARGS__)
 
 #define CMDX_UNROLL _Pragma("unroll")
 
-// d = d (op) r[s]
-#define CMDX_BIN_CASE(s_, d_, op_)                                          \
-  case fz_bin(S, op_, d_, s_): {                                            \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], r[s_][v]); \
-  } break;
-#define CMDX_BIN_D(d_, op_, SB) SB(CMDX_BIN_CASE, d_, op_)
-// d = f(r[s])
-#define CMDX_UN_CASE(s_, d_, op_)                                           \
-  case fz_un(S, op_, d_, s_): {                                             \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = un<op_>(r[s_][v]);   \
-  } break;
-#define CMDX_UN_D(d_, op_, SB) SB(CMDX_UN_CASE, d_, op_)
-// d = d (op) scalar[aux]
-#define CMDX_BINS_CASE(d_, op_)                                             \
-  case fz_bin_scalar(S, op_, d_): {                                         \
-    const uint32_t k = scal[aux];                                           \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], k); \
-  } break;
-#define CMDX_MOVS_CASE(d_, x_)                                              \
-  case fz_movs(S, d_): {                                                    \
-    const uint32_t k = scal[aux];                                           \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = k;                   \
-  } break;
-#define CMDX_ST_CASE(s_, t_)                                                \
-  case fz_store(S, t_, s_):                                                 \
-    pol.template store<t_>(r[s_], aux);                                     \
+// store slot s as type t (case number relative to the first store case)
+#define CMDX_ST_CASE(s_, t_)         \
+  case (t_) * S + (s_):              \
+    pol.template store<t_>(r[s_], aux); \
     break;
 
-#define CMDX_FUSED_CASES(SA, SB)                                                          \
-  SA(CMDX_BIN_D, kFAdd, SB) SA(CMDX_BIN_D, kFSub, SB) SA(CMDX_BIN_D, kFRsub, SB)          \
-  SA(CMDX_BIN_D, kFMul, SB) SA(CMDX_BIN_D, kIAdd, SB) SA(CMDX_BIN_D, kISub, SB)           \
-  SA(CMDX_BIN_D, kIRsub, SB) SA(CMDX_BIN_D, kIMul, SB)                                    \
-  SA(CMDX_UN_D, kFNeg, SB) SA(CMDX_UN_D, kINeg, SB) SA(CMDX_UN_D, kMov, SB)               \
-  SA(CMDX_BINS_CASE, kFAdd) SA(CMDX_BINS_CASE, kFSub) SA(CMDX_BINS_CASE, kFRsub)          \
-  SA(CMDX_BINS_CASE, kFMul) SA(CMDX_BINS_CASE, kIAdd) SA(CMDX_BINS_CASE, kISub)           \
-  SA(CMDX_BINS_CASE, kIRsub) SA(CMDX_BINS_CASE, kIMul)                                    \
-  SA(CMDX_MOVS_CASE, 0)                                                                   \
+#define CMDX_ST_CASES(SA) \
   SA(CMDX_ST_CASE, kStF32) SA(CMDX_ST_CASE, kStF16) SA(CMDX_ST_CASE, kStBF16) SA(CMDX_ST_CASE, kStI32)
 
-// Run the program in `prog` (constant memory) over the thread's slots.
-// Pol supplies store<T>(const uint32_t (&x)[V], int out_index).
+// Run the program in `prog` (constant memory) over the thread's slots. The
+// compute words run inside the inline-PTX loop of interp_asm.cuh; each store
+// word comes back here and is performed by Pol::store<T>(slot, out_index).
 template <int S, int V, class Pol>
 __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* __restrict__ prog,
                                           const uint32_t* __restrict__ scal, Pol& pol) {
   static_assert(S == 4 || S == 8, "fused dispatch is generated for 4 and 8 slots");
+  uint32_t idx = 0;
 #pragma unroll 1
-  for (int pc = 0;; ++pc) {
-    const uint32_t w = prog[pc];
+  for (;;) {
+    const uint32_t w = AsmInterp<S, V>::run(r, idx, prog, scal);
+    const uint32_t c = (w & 0xffffu) - fz_store(S, 0, 0);
+    if (c >= 4u * S) return;  // the end word
     const uint32_t aux = w >> 16;
     if constexpr (S == 4) {
-      switch (w & 0xffffu) {
-        CMDX_FUSED_CASES(CMDX_SA4, CMDX_SB4)
+      switch (c) {
+        CMDX_ST_CASES(CMDX_SA4)
         default: return;
       }
     } else {
-      switch (w & 0xffffu) {
-        CMDX_FUSED_CASES(CMDX_SA8, CMDX_SB8)
+      switch (c) {
+        CMDX_ST_CASES(CMDX_SA8)
         default: return;
       }
     }

@@ -55,7 +55,7 @@ struct GenericStore {
 template <int TIER>
 __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(const __grid_constant__ GenericParams p) {
   constexpr int S = tier_slots(TIER);
-  constexpr int V = tier_vec(TIER);
+  constexpr int V = tier_vec_strided(TIER);
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -84,7 +84,7 @@ cudaError_t generic_upload(int slot, const uint32_t* words, int n) {
 
 template <int TIER>
 static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
-  constexpr int V = tier_vec(TIER);
+  constexpr int V = tier_vec_strided(TIER);
   constexpr int kBlock = 256;
   static int grid_cache[64] = {0};
   int dev = 0;

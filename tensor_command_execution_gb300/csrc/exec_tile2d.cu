@@ -161,7 +161,7 @@ template <int TIER>
 __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int S = tier_slots(TIER);
-  constexpr int V = tier_vec(TIER);
+  constexpr int V = tier_vec_strided(TIER);
   static_assert(V == 4 || V == 8, "the tile executor keeps 4 or 8 columns per thread");
   using TM = TileMap<V>;
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
