@@ -230,8 +230,19 @@ cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_lau
 cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_stream);
 
 /* Wait for cuda_stream and report the completion phase of work launched on
- * it: CMD_OK, or CMD_ERR_CUDA with the runtime's message. */
+ * it with k: CMD_OK; CMD_ERR_CUDA with the runtime's message; or
+ * CMD_ERR_DEVICE_TIMEOUT when a device-side wait of the tile executor (an
+ * mbarrier wait on its shared-memory pipeline) ran past the time limit and
+ * the kernel stopped instead of hanging. The kernel's device error word is
+ * cleared when it is reported. */
 cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream);
+
+/* Process-wide settings of the device-side waits: the time limit of every
+ * bounded wait (default 2 s), and a test hook: with force_timeout != 0 the
+ * tile executor's consumer warps wait on a barrier that nothing completes, so
+ * the timeout path runs (the launch then writes no output and
+ * cmd_sync_status returns CMD_ERR_DEVICE_TIMEOUT). */
+cmd_status cmd_configure_waits(uint64_t timeout_ns, int32_t force_timeout);
 
 #ifdef __cplusplus
 }

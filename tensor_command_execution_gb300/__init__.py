@@ -107,6 +107,7 @@ SIGNATURES = {
     "cmd_plan_launch": (_I, [_P, ctypes.POINTER(cmd_runtime_args), ctypes.POINTER(cmd_launch_plan)]),
     "cmd_launch": (_I, [_P, ctypes.POINTER(cmd_runtime_args), _P]),
     "cmd_sync_status": (_I, [_P, _P]),
+    "cmd_configure_waits": (_I, [ctypes.c_uint64, ctypes.c_int32]),
 }
 
 _lib = None
@@ -241,6 +242,10 @@ def cmd_launch(k: int, args: cmd_runtime_args, stream: int | None) -> None:
 
 def cmd_sync_status(k: int, stream: int | None) -> None:
     _check(lib().cmd_sync_status(k, stream or None), "cmd_sync_status")
+
+
+def cmd_configure_waits(timeout_ns: int, force_timeout: bool = False) -> None:
+    _check(lib().cmd_configure_waits(int(timeout_ns), 1 if force_timeout else 0), "cmd_configure_waits")
 
 
 # ---- argument marshalling ----------------------------------------------------

@@ -9,6 +9,7 @@
 #include "../../include/cmd.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -88,9 +89,14 @@ struct cmd_kernel {
   int rank = 0;
   int device = -1;
   int slot = -1;
+  uint32_t* err = nullptr;  // device error word of the tile executor's bounded waits
 };
 
 namespace {
+
+// ---- device-side wait limit and the test hook that forces a timeout ----------
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int32_t> g_force_timeout{0};
 
 // ---- constant-memory program slots, per device -----------------------------
 std::mutex g_slot_mu;
@@ -595,24 +601,27 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
     return CMD_OK;
   }
   // tile: two merged dims; every store row-direct (inner stride 1); every
-  // load row-direct or transposed (outer stride 1); 16-byte aligned rows
-  if (m == 2 && P.tier != cmdx::kTier32) {
+  // load row-direct or transposed (outer stride 1); 16-byte aligned rows;
+  // one pipeline stage of 64 x 64 boxes of every load fits the stage limit
+  if (m == 2 && P.tier != cmdx::kTier32 && ms[0] < (int64_t(1) << 31) && ms[1] < (int64_t(1) << 31)) {
     bool ok = true;
-    int n_trans = 0;
+    int n_trans = 0, stage = 0;
     for (size_t i = 0; i < all.size() && ok; ++i) {
       const bool is_store = i >= pl->loads.size();
       const int es = elem_size(all[i]->dtype);
       const int64_t so = wst[i][0], si = wst[i][1];
+      if (!is_store) stage += cmdx::tile_stage_bytes(es);
+      // (the row pitch at least covers a row, as the TMA descriptors want)
       if (!aligned(all[i]->ptr, 16)) ok = false;
-      else if (si == 1 && (so * es) % 16 == 0) {
+      else if (si == 1 && so >= ms[1] && (so * es) % 16 == 0) {
         // row-direct
-      } else if (!is_store && so == 1 && si != 1 && (si * es) % 16 == 0) {
+      } else if (!is_store && so == 1 && si != 1 && si >= ms[0] && (si * es) % 16 == 0) {
         ++n_trans;
       } else {
         ok = false;
       }
     }
-    if (ok && n_trans <= 4) {
+    if (ok && !pl->loads.empty() && stage <= cmdx::kTileStageLimit) {
       pl->path = CMD_PATH_TILE2D;
       pl->n_trans = n_trans;
       return CMD_OK;
@@ -843,10 +852,13 @@ cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out) {
     }
   }
   e = upload_all(slot, k->prog.words);
+  if (e == cudaSuccess) e = cudaMalloc(&k->err, 256);
+  if (e == cudaSuccess) e = cudaMemset(k->err, 0, 256);
   if (e != cudaSuccess) {
+    if (k->err) cudaFree(k->err);
     release_slot(dev, slot);
     delete k;
-    return cuda_fail(e, "uploading the program to constant memory");
+    return cuda_fail(e, "uploading the program / allocating the device error word");
   }
   k->device = dev;
   k->slot = slot;
@@ -876,6 +888,13 @@ cmd_status cmd_lower_kernel(cmd_command_t cmd, cmd_kernel_t* out) {
 
 void cmd_kernel_destroy(cmd_kernel_t k) {
   if (!k) return;
+  if (k->err) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != k->device) cudaSetDevice(k->device);
+    cudaFree(k->err);
+    if (cur != k->device && cur >= 0) cudaSetDevice(cur);
+  }
   if (k->slot >= 0) release_slot(k->device, k->slot);
   delete k;
 }
@@ -1007,35 +1026,28 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       e = cmdx::generic_launch(P.tier, p, stream);
     }
   } else if (pl.path == CMD_PATH_TILE2D) {
-    cmdx::Tile2dParams p;
-    std::memset(&p, 0, sizeof p);
-    int stage = 0;
+    cmdx::Tile2dLaunch L;
+    std::memset(&L, 0, sizeof L);
     for (size_t j = 0; j < pl.loads.size(); ++j) {
-      p.in[j] = pl.loads[j].ptr;
-      p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+      L.in[j] = pl.loads[j].ptr;
+      L.in_dt[j] = (uint8_t)pl.loads[j].dtype;
       const int64_t so = pl.ml[j][2], si = pl.ml[j][3];
-      if (si == 1) {
-        p.in_ld[j] = so;
-        p.in_stage[j] = -1;
-      } else {
-        p.in_ld[j] = si;
-        p.in_stage[j] = (int8_t)stage++;
-      }
+      L.in_trans[j] = si != 1;
+      L.in_ld[j] = si == 1 ? so : si;
     }
-    for (int j = (int)pl.loads.size(); j < cmdx::kMaxLoads; ++j) p.in_stage[j] = -1;
     for (size_t j = 0; j < pl.stores.size(); ++j) {
-      p.out[j] = pl.stores[j].ptr;
-      p.out_ld[j] = pl.ms[j][2];
+      L.out[j] = pl.stores[j].ptr;
+      L.out_ld[j] = pl.ms[j][2];
     }
-    std::memcpy(p.scal, pl.scal, sizeof p.scal);
-    p.rows = pl.msizes[2];
-    p.cols = pl.msizes[3];
-    p.tiles_c = (p.cols + cmdx::kTileCols - 1) / cmdx::kTileCols;
-    p.n_tiles = p.tiles_c * ((p.rows + cmdx::kTileRows - 1) / cmdx::kTileRows);
-    p.prog = (uint32_t)k->slot;
-    p.n_loads = (uint32_t)pl.loads.size();
-    p.n_trans = (uint32_t)stage;
-    e = cmdx::tile2d_launch(P.tier, p, stream);
+    std::memcpy(L.scal, pl.scal, sizeof L.scal);
+    L.rows = pl.msizes[2];
+    L.cols = pl.msizes[3];
+    L.prog = (uint32_t)k->slot;
+    L.n_loads = (uint32_t)pl.loads.size();
+    L.err = k->err;
+    L.debug = (uint32_t)g_force_timeout.load();
+    L.timeout_ns = g_wait_limit_ns.load();
+    e = cmdx::tile2d_launch(P.tier, L, stream);
   } else {
     cmdx::GenericParams p;
     std::memset(&p, 0, sizeof p);
@@ -1060,9 +1072,34 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
 }
 
 cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream) {
-  (void)k;
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "work on the stream failed");
+  if (k && k->err) {
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, k->err, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word) {
+      cudaMemset(k->err, 0, sizeof word);
+      std::string what;
+      if (word & 1u) what += " consumer-wait";
+      if (word & 2u) what += " producer-wait";
+      if (word & 4u) what += " drain-wait";
+      if (word & 8u) what += " forced-wait";
+      return fail(CMD_ERR_DEVICE_TIMEOUT, "a device-side wait gave up after its time limit:" + what +
+                                              " (error word 0x" + [&] {
+                                                char b[16];
+                                                std::snprintf(b, sizeof b, "%x", word);
+                                                return std::string(b);
+                                              }() + ")");
+    }
+  }
+  return CMD_OK;
+}
+
+cmd_status cmd_configure_waits(uint64_t timeout_ns, int32_t force_timeout) {
+  if (timeout_ns == 0) return fail(CMD_ERR_ARG, "timeout_ns must be > 0");
+  g_wait_limit_ns.store(timeout_ns);
+  g_force_timeout.store(force_timeout ? 1 : 0);
   return CMD_OK;
 }
 

@@ -88,21 +88,29 @@ struct ContigParams {
   uint8_t in_dt[kMaxLoads];
 };
 
-struct Tile2dParams {
+// What the tile executor needs from the host: every load view is row-direct
+// (element (i, j) at i*ld + j) or transposed (element (i, j) at i + j*ld);
+// every store is row-direct. The executor builds its TMA descriptors from it.
+struct Tile2dLaunch {
   const void* in[kMaxLoads];
+  int64_t in_ld[kMaxLoads];
+  uint8_t in_dt[kMaxLoads];
+  uint8_t in_trans[kMaxLoads];
   void* out[kMaxStores];
-  int64_t in_ld[kMaxLoads];   // row stride (row-direct) or column stride (transposed), elements
-  int64_t out_ld[kMaxStores]; // row stride of each store, elements
+  int64_t out_ld[kMaxStores];
   uint32_t scal[kMaxScalars];
   int64_t rows, cols;
-  int64_t tiles_c;            // tiles per row of tiles
-  int64_t n_tiles;
   uint32_t prog;
   uint32_t n_loads;
-  uint32_t n_trans;           // transposed loads, staged through shared memory
-  uint8_t in_dt[kMaxLoads];
-  int8_t in_stage[kMaxLoads]; // shared-memory stage index of a transposed load, -1 if row-direct
+  uint32_t* err;        // device error word of the kernel handle
+  uint32_t debug;       // test hook: 1 = consumers wait on a barrier nobody arrives on
+  uint64_t timeout_ns;  // limit of every device-side wait
 };
+
+// Bytes one pipeline stage of the tile executor holds for a load of element
+// size es (a 64 x 64 box); the executor takes at most kTileStageLimit.
+constexpr int tile_stage_bytes(int es) { return 64 * 64 * es; }
+constexpr int kTileStageLimit = 48 * 1024;
 
 // Unsigned division by an invariant divisor d >= 2 with a multiply-high:
 // q = (t + ((n - t) >> 1)) >> (l - 1), t = mulhi64(m, n), l = ceil(log2 d),
@@ -136,7 +144,7 @@ cudaError_t generic_upload(int slot, const uint32_t* words, int n);
 // n must be a multiple of contig_chunk(tier) elements.
 cudaError_t contig_launch(int tier, const ContigParams& p, cudaStream_t stream);
 int contig_chunk(int tier);
-cudaError_t tile2d_launch(int tier, const Tile2dParams& p, cudaStream_t stream);
+cudaError_t tile2d_launch(int tier, const Tile2dLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int tier, const GenericParams& p, cudaStream_t stream);
 
 // Tile geometry of the tile2d executor.

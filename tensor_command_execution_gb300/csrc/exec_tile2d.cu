@@ -1,129 +1,191 @@
-// exec_tile2d.cu - 2-D strided executor for views that are row-direct
-// (element (i, j) at i*ld + j) or transposed (element (i, j) at i + j*ld).
+// exec_tile2d.cu - 2-D strided executor: views that are row-direct (element
+// (i, j) at i*ld + j) or transposed (element (i, j) at i + j*ld), stores
+// row-direct.
 //
-// A CTA of 256 threads walks 64 x 64 tiles of the logical index space. Each
-// thread owns V (8 or 4) consecutive columns of one row per pass, so
-// row-direct loads and every store are vector accesses and a warp touches
-// whole 128-byte (or larger) row segments. A transposed view is read along its physical
-// rows (logical columns), which are contiguous in the logical row index: the
-// tile's 64 physical row segments are copied into shared memory with 16-byte
-// loads and then read transposed. The stage's 16-byte chunks are swizzled by
-// XOR with (physical row / 8) mod 8, so the column groups a warp reads at
-// once fall in distinct banks (at most two-way for V = 4) and the 16-byte
-// stage writes stay aligned.
+// The logical index space is cut into 64 x 64 tiles that persistent CTAs walk
+// in a grid stride. One producer warp stages every load of a tile into shared
+// memory with TMA (cp.async.bulk.tensor.2d, 128-byte swizzle, no multicast),
+// through a ring of pipeline stages guarded by mbarriers: "full" completes
+// when a stage's bytes have landed, "empty" when all consumer warps have read
+// it. Eight consumer warps read the stage, run the program and store straight
+// to global memory with 16-byte vector stores. A transposed view arrives in
+// its physical layout (one box row per logical column) and is read across box
+// rows; each lane starts that walk at a different box row so that the eight
+// lanes of a tile row hit distinct banks, then rotates its registers back.
+//
+// Every wait on an mbarrier is bounded by a time limit; a wait that runs out
+// records a code in the kernel's device error word and the CTA stops (after
+// waiting, again bounded, for the copies it issued), so a stuck copy cannot
+// hang the GPU. cmd_sync_status reports it.
 //
 // rocRoller, "Design Overview", section "Kernel Graph": the coordinate
 // transforms map each logical index to a tensor offset through sizes and
-// strides; tiling and the shared-memory transpose are how this executor
-// makes those transforms coalesce on the GPU (the pages' own generator stages
-// tiles through LDS on AMD hardware).
+// strides; tiling and staging through shared memory is how this executor
+// makes those transforms coalesce (the pages' own generator stages tiles
+// through LDS on AMD hardware).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "exec_common.cuh"
 
 namespace cmdx {
 
 static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
 
-constexpr int kStageBytes = kTileRows * kTileCols * 4;  // one stage, sized for 4-byte elements
-static_assert(kTileRows == 64 && kTileCols == 64, "the thread map below assumes 64 x 64 tiles");
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 4;
+constexpr int kBarrierBytes = 1024;   // barriers; stages start 1024-byte aligned
+constexpr int kBoxBytes = 8192;       // one 64-row box of 128-byte rows
 
-// Copy the tile's physical rows of a transposed view into a stage.
-__device__ __forceinline__ void stage_tile(unsigned char* stage, const void* base, int dt, int64_t ld,
-                                           int64_t i0, int64_t j0, int64_t rows, int64_t cols, bool full, int tid) {
-  const int es = (dt == 1 || dt == 2) ? 2 : 4;
-  const int chunks_per_row = kTileRows * es / 16;  // 8 (2-byte) or 16 (4-byte)
-  const int elems_per_chunk = 16 / es;
-  const int n_chunks = kTileCols * chunks_per_row;
-  for (int c = tid; c < n_chunks; c += 256) {
-    const int q = c / chunks_per_row;     // physical row in the tile = logical column j0 + q
-    const int ch = c - q * chunks_per_row;
-    unsigned char* dst = stage + q * (kTileRows * es) + ((ch ^ ((q >> 3) & 7)) << 4);
-    const int64_t i = i0 + (int64_t)ch * elems_per_chunk;
-    const int64_t j = j0 + q;
-    if (full) {
-      const unsigned char* src = static_cast<const unsigned char*>(base) + (j * ld + i) * es;
-      *reinterpret_cast<uint4*>(dst) = ld_stream(reinterpret_cast<const uint4*>(src));
-    } else {
-      if (es == 2) {
-        uint16_t v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          v[e] = (j < cols && i + e < rows) ? (uint16_t)ld_elem(base, dt, j * ld + i + e) : (uint16_t)0;
-        uint4 w;
-        w.x = v[0] | (uint32_t)v[1] << 16; w.y = v[2] | (uint32_t)v[3] << 16;
-        w.z = v[4] | (uint32_t)v[5] << 16; w.w = v[6] | (uint32_t)v[7] << 16;
-        *reinterpret_cast<uint4*>(dst) = w;
-      } else {
-        uint32_t v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = (j < cols && i + e < rows) ? ld_elem(base, dt, j * ld + i + e) : 0u;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
-      }
-    }
-  }
-}
+// error codes (bits of the error word)
+constexpr uint32_t kErrConsumerWait = 1u << 0;
+constexpr uint32_t kErrProducerWait = 1u << 1;
+constexpr uint32_t kErrDrainWait = 1u << 2;
+constexpr uint32_t kErrDebugWait = 1u << 3;
 
-// Thread map of a 64 x 64 tile for V columns per thread.
-template <int V>
-struct TileMap {
-  static constexpr int TPR = kTileCols / V;        // threads per tile row
-  static constexpr int RPP = 256 / TPR;            // rows per pass
-  static constexpr int PASSES = kTileRows / RPP;
+struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
+  CUtensorMap maps[kMaxLoads];
+  void* out[kMaxStores];
+  int64_t out_ld[kMaxStores];
+  uint32_t scal[kMaxScalars];
+  uint32_t* err;
+  int64_t rows, cols, tiles_c, n_tiles;
+  uint64_t timeout_ns;
+  uint32_t prog, n_loads, n_stages, stage_bytes, tx_bytes, debug;
+  uint32_t load_off[kMaxLoads];  // byte offset of load j in a stage
+  uint8_t in_dt[kMaxLoads];
+  uint8_t in_trans[kMaxLoads];
 };
 
-// Read logical (li, V*cj + k), k < V, from a stage and widen.
-template <int V>
-__device__ __forceinline__ void read_stage(uint32_t (&x)[V], const unsigned char* stage, int dt, int li, int cj) {
-  const int es = (dt == 1 || dt == 2) ? 2 : 4;
-  const int elems_per_chunk = 16 / es;
-  const int ch = li / elems_per_chunk;
-  const int within = (li - ch * elems_per_chunk) * es;
-#pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const int q = V * cj + k;  // physical row of the stage
-    const unsigned char* at = stage + q * (kTileRows * es) + ((ch ^ ((q >> 3) & 7)) << 4) + within;
-    if (es == 2) {
-      const uint16_t h = *reinterpret_cast<const uint16_t*>(at);
-      x[k] = dt == 1 ? widen_f16(h) : widen_bf16(h);
-    } else {
-      x[k] = *reinterpret_cast<const uint32_t*>(at);
-    }
+// ---- mbarrier / TMA primitives (inline PTX) ----------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of parity `parity` to complete, for at most timeout_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > timeout_ns) return false;
   }
 }
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 
-// Row-direct load of V consecutive columns.
-template <int V>
-__device__ __forceinline__ void row_load(uint32_t (&x)[V], const void* base, int dt, int64_t off, bool full,
-                                         int ncols_left) {
-  if (full) {
-    if (dt == 0 || dt == 3) {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + off);
-#pragma unroll
-      for (int h = 0; h < V / 4; ++h) {
-        const uint4 a = ld_stream(p + h);
-        x[4 * h] = a.x; x[4 * h + 1] = a.y; x[4 * h + 2] = a.z; x[4 * h + 3] = a.w;
-      }
+// ---- reading a stage -----------------------------------------------------------
+// A 64 x 64 box with 128-byte rows and the 128-byte swizzle keeps 16-byte
+// chunk c of row q at q*128 + ((c ^ (q % 8)) * 16); 4-byte views use two boxes
+// of 32 elements per row, the second 8 KB after the first.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// Row-direct: logical (li, 8 cj .. 8 cj + 7).
+__device__ __forceinline__ void read_row(uint32_t (&x)[8], uint32_t stage, int dt, int li, int cj) {
+  const uint32_t sw = li & 7;
+  if (dt == 1 || dt == 2) {
+    const uint4 a = lds128(stage + li * 128 + ((cj ^ sw) << 4));
+    if (dt == 1) {
+      widen_f16x2(a.x, x[0], x[1]); widen_f16x2(a.y, x[2], x[3]);
+      widen_f16x2(a.z, x[4], x[5]); widen_f16x2(a.w, x[6], x[7]);
     } else {
-      uint32_t w[V / 2];
-      if constexpr (V == 8) {
-        const uint4 a = ld_stream(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off));
-        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-      } else {
-        const uint2 a = ld_stream(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + off));
-        w[0] = a.x; w[1] = a.y;
-      }
-#pragma unroll
-      for (int h = 0; h < V / 2; ++h) {
-        if (dt == 1) widen_f16x2(w[h], x[2 * h], x[2 * h + 1]);
-        else widen_bf16x2(w[h], x[2 * h], x[2 * h + 1]);
-      }
+      widen_bf16x2(a.x, x[0], x[1]); widen_bf16x2(a.y, x[2], x[3]);
+      widen_bf16x2(a.z, x[4], x[5]); widen_bf16x2(a.w, x[6], x[7]);
     }
   } else {
-#pragma unroll
-    for (int k = 0; k < V; ++k) x[k] = k < ncols_left ? widen_any(dt, ld_elem(base, dt, off + k)) : 0u;
+    // columns 8 cj.. live in box cj / 4, chunks 2 (cj % 4) and 2 (cj % 4) + 1;
+    // lanes of the second box take their chunks in the other order so a
+    // tile row's eight lanes cover all eight chunk positions at each access
+    const uint32_t box = stage + (cj >> 2) * kBoxBytes + li * 128;
+    const uint32_t c0 = (cj & 3) * 2;
+    const bool flip = (cj >> 2) & 1;
+    const uint4 a = lds128(box + (((c0 + (flip ? 1 : 0)) ^ sw) << 4));
+    const uint4 b = lds128(box + (((c0 + (flip ? 0 : 1)) ^ sw) << 4));
+    const uint4 lo = flip ? b : a, hi = flip ? a : b;
+    x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+    x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
   }
 }
 
-template <int V>
+// Transposed: logical (li, 8 cj + m) is box row q = 8 cj + m, element li.
+// Step k reads m = (k + cj) % 8, so q % 8 differs across a tile row's lanes;
+// the values are then rotated back into column order.
+__device__ __forceinline__ void read_trans(uint32_t (&x)[8], uint32_t stage, int dt, int li, int cj) {
+  uint32_t y[8];
+  if (dt == 1 || dt == 2) {
+    const uint32_t within = (li & 7) * 2;
+    const uint32_t ch = li >> 3;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t q = 8 * cj + ((k + cj) & 7);
+      const uint32_t h = lds16(stage + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+      y[k] = dt == 1 ? widen_f16((uint16_t)h) : widen_bf16((uint16_t)h);
+    }
+  } else {
+    const uint32_t box = stage + (li >> 5) * kBoxBytes;
+    const uint32_t lr = li & 31;
+    const uint32_t within = (lr & 3) * 4;
+    const uint32_t ch = lr >> 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t q = 8 * cj + ((k + cj) & 7);
+      y[k] = lds32(box + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+    }
+  }
+  // x[m] = y[(m - cj) % 8]: rotate by 1, 2 and 4 places as the bits of cj say
+  uint32_t z[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) z[m] = (cj & 1) ? y[(m + 7) & 7] : y[m];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) y[m] = (cj & 2) ? z[(m + 6) & 7] : z[m];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) x[m] = (cj & 4) ? y[(m + 4) & 7] : y[m];
+}
+
 struct TileStore {
   const Tile2dParams& p;
   int64_t i, j;
@@ -131,77 +193,132 @@ struct TileStore {
   int ncols_left;
 
   template <int T>
-  __device__ __forceinline__ void store(const uint32_t (&x)[V], uint32_t o) const {
+  __device__ __forceinline__ void store(const uint32_t (&x)[8], uint32_t o) const {
     void* base = p.out[o];
     const int64_t off = i * p.out_ld[o] + j;
     if (full) {
       if constexpr (T == kStF32 || T == kStI32) {
         uint4* q = reinterpret_cast<uint4*>(static_cast<uint32_t*>(base) + off);
-#pragma unroll
-        for (int h = 0; h < V / 4; ++h) st_stream(q + h, make_uint4(x[4 * h], x[4 * h + 1], x[4 * h + 2], x[4 * h + 3]));
+        st_stream(q, make_uint4(x[0], x[1], x[2], x[3]));
+        st_stream(q + 1, make_uint4(x[4], x[5], x[6], x[7]));
+      } else if constexpr (T == kStF16) {
+        st_stream(reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + off),
+                  make_uint4(narrow_f16x2(x[0], x[1]), narrow_f16x2(x[2], x[3]), narrow_f16x2(x[4], x[5]),
+                             narrow_f16x2(x[6], x[7])));
       } else {
-        uint32_t w[V / 2];
-#pragma unroll
-        for (int h = 0; h < V / 2; ++h)
-          w[h] = T == kStF16 ? narrow_f16x2(x[2 * h], x[2 * h + 1]) : narrow_bf16x2(x[2 * h], x[2 * h + 1]);
-        if constexpr (V == 8)
-          st_stream(reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + off), make_uint4(w[0], w[1], w[2], w[3]));
-        else
-          st_stream(reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + off), make_uint2(w[0], w[1]));
+        st_stream(reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + off),
+                  make_uint4(narrow_bf16x2(x[0], x[1]), narrow_bf16x2(x[2], x[3]), narrow_bf16x2(x[4], x[5]),
+                             narrow_bf16x2(x[6], x[7])));
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < V; ++k)
+      for (int k = 0; k < 8; ++k)
         if (k < ncols_left) st_elem<T>(base, off + k, x[k]);
     }
   }
 };
 
+// Resident CTAs per SM the register budget is sized for.
+constexpr int tile_min_blocks(int tier) { return tier == kTier4 ? 3 : 2; }
+
 template <int TIER>
-__global__ void __launch_bounds__(256, tier_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int S = tier_slots(TIER);
-  constexpr int V = tier_vec_strided(TIER);
-  static_assert(V == 4 || V == 8, "the tile executor keeps 4 or 8 columns per thread");
-  using TM = TileMap<V>;
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
-  const int tid = threadIdx.x;
-  const int cj = tid % TM::TPR;  // column group: columns V cj .. V cj + V - 1 of the tile
-  const int ri = tid / TM::TPR;  // row within a pass
+  const uint32_t base = smem_u32(smem);
+  const uint32_t full_bar = base;                    // kMaxStages x 8 bytes
+  const uint32_t empty_bar = base + 8 * kMaxStages;  // kMaxStages x 8 bytes
+  const uint32_t debug_bar = base + 16 * kMaxStages;
+  const uint32_t stages = base + kBarrierBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ns = p.n_stages;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < ns; ++s) {
+      mbar_init(full_bar + 8 * s, 1);
+      mbar_init(empty_bar + 8 * s, kConsumerWarps);
+    }
+    mbar_init(debug_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---- producer: one lane issues the TMA copies ----
+    if (lane != 0 || p.debug) return;
+    uint32_t n = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
+      const uint32_t s = n % ns, ph = (n / ns) & 1;
+      if (!mbar_wait(empty_bar + 8 * s, ph ^ 1, p.timeout_ns)) {
+        atomicOr(p.err, kErrProducerWait);
+        ok = false;
+        break;
+      }
+      const int64_t tr = t / p.tiles_c;
+      const int32_t i0 = (int32_t)(tr * kTileRows), j0 = (int32_t)((t - tr * p.tiles_c) * kTileCols);
+      const uint32_t fb = full_bar + 8 * s;
+      mbar_arrive_expect_tx(fb, p.tx_bytes);
+      const uint32_t st = stages + s * p.stage_bytes;
+      for (uint32_t j = 0; j < p.n_loads; ++j) {
+        const uint32_t dst = st + p.load_off[j];
+        const bool wide = !(p.in_dt[j] == 1 || p.in_dt[j] == 2);
+        // row-direct boxes are (columns, rows); transposed boxes (rows, columns)
+        const int32_t x = p.in_trans[j] ? i0 : j0, y = p.in_trans[j] ? j0 : i0;
+        tma_load_2d(dst, &p.maps[j], x, y, fb);
+        if (wide) tma_load_2d(dst + kBoxBytes, &p.maps[j], x + 32, y, fb);
+      }
+    }
+    if (!ok) {
+      // wait (bounded) for the copies still in flight into this CTA's stages
+      const uint32_t pend = n < ns ? n : ns;
+      for (uint32_t q = n - pend; q < n; ++q)
+        if (!mbar_wait(full_bar + 8 * (q % ns), (q / ns) & 1, p.timeout_ns)) atomicOr(p.err, kErrDrainWait);
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  const int cj = threadIdx.x & 7;   // columns 8 cj .. 8 cj + 7 of the tile
+  const int ri = threadIdx.x >> 3;  // row within a 32-row pass
   const uint32_t* prog = c_prog[p.prog];
-  for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+  if (p.debug) {
+    // test hook: a wait that nothing satisfies must give up and report
+    if (!mbar_wait(debug_bar, 0, p.timeout_ns) && lane == 0) atomicOr(p.err, kErrDebugWait);
+    return;
+  }
+  uint32_t n = 0;
+  for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
+    const uint32_t s = n % ns, ph = (n / ns) & 1;
+    if (!mbar_wait(full_bar + 8 * s, ph, p.timeout_ns)) {
+      if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+      return;
+    }
     const int64_t tr = t / p.tiles_c;
     const int64_t i0 = tr * kTileRows, j0 = (t - tr * p.tiles_c) * kTileCols;
-    const bool full_tile = i0 + kTileRows <= p.rows && j0 + kTileCols <= p.cols;
-    if (p.n_trans) {
-      __syncthreads();  // the previous tile's stage readers are done
-#pragma unroll
-      for (int j = 0; j < NL; ++j)
-        if (j < (int)p.n_loads && p.in_stage[j] >= 0)
-          stage_tile(smem + p.in_stage[j] * kStageBytes, p.in[j], p.in_dt[j], p.in_ld[j], i0, j0, p.rows, p.cols,
-                     full_tile, tid);
-      __syncthreads();
-    }
+    const uint32_t st = stages + s * p.stage_bytes;
 #pragma unroll 1
-    for (int pass = 0; pass < TM::PASSES; ++pass) {
-      const int li = pass * TM::RPP + ri;
+    for (int pass = 0; pass < kTileRows / 32; ++pass) {
+      const int li = pass * 32 + ri;
       const int64_t i = i0 + li;
-      const int64_t jc = j0 + cj * V;
-      if (i >= p.rows || jc >= p.cols) continue;
-      const int64_t left = p.cols - jc;
-      const bool full = left >= V;
-      const int ncols_left = full ? V : (int)left;
-      uint32_t r[S][V];
+      const int64_t jc = j0 + cj * 8;
+      if (i < p.rows && jc < p.cols) {
+        const int64_t left = p.cols - jc;
+        uint32_t r[S][8];
 #pragma unroll
-      for (int j = 0; j < NL; ++j) {
-        if (j < (int)p.n_loads) {
-          if (p.in_stage[j] >= 0) read_stage<V>(r[j], smem + p.in_stage[j] * kStageBytes, p.in_dt[j], li, cj);
-          else row_load<V>(r[j], p.in[j], p.in_dt[j], i * p.in_ld[j] + jc, full, ncols_left);
+        for (int j = 0; j < NL; ++j) {
+          if (j < (int)p.n_loads) {
+            if (p.in_trans[j]) read_trans(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+            else read_row(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+          }
         }
+        TileStore sto{p, i, jc, left >= 8, left >= 8 ? 8 : (int)left};
+        run_program<TIER, 8>(r, prog, p.scal, sto);
       }
-      TileStore<V> st{p, i, jc, full, ncols_left};
-      run_program<TIER, V>(r, prog, p.scal, st);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar + 8 * s);
   }
 }
 
@@ -209,32 +326,94 @@ cudaError_t tile2d_upload(int slot, const uint32_t* words, int n) {
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
+// ---- host side ----------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
 template <int TIER>
 static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
-  constexpr int kBlock = 256;
-  const size_t smem = (size_t)p.n_trans * kStageBytes;
-  static int grid_cache[64][5] = {};
+  const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes;
+  static int grid_cache[64][kMaxStages + 1] = {};
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  const bool cacheable = dev >= 0 && dev < 64 && p.n_trans <= 4;
-  if (cacheable && !attr_set[dev]) {
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (!cacheable || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         4 * kStageBytes);
+                                         kBarrierBytes + 2 * kTileStageLimit + 4096);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (cacheable) attr_set[dev] = true;
   }
-  int full_grid = cacheable ? grid_cache[dev][p.n_trans] : 0;
+  // occupancy depends on the stage size; cached for the common size only
+  int full_grid = 0;
+  const bool cache_ok = cacheable && p.stage_bytes == 16384;
+  if (cache_ok) full_grid = grid_cache[dev][p.n_stages];
   if (full_grid == 0) {
-    full_grid = persistent_grid(tile2d_kernel<TIER>, kBlock, smem, INT64_MAX);
-    if (cacheable) grid_cache[dev][p.n_trans] = full_grid;
+    full_grid = persistent_grid(tile2d_kernel<TIER>, kThreads, smem, INT64_MAX);
+    if (cache_ok) grid_cache[dev][p.n_stages] = full_grid;
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
-  tile2d_kernel<TIER><<<grid, kBlock, smem, stream>>>(p);
+  tile2d_kernel<TIER><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t tile2d_launch(int tier, const Tile2dParams& p, cudaStream_t stream) {
+cudaError_t tile2d_launch(int tier, const Tile2dLaunch& L, cudaStream_t stream) {
+  static_assert(sizeof(Tile2dParams) < 8192, "kernel parameters stay small");
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  Tile2dParams p;
+  std::memset(&p, 0, sizeof p);
+  uint32_t off = 0;
+  for (uint32_t j = 0; j < L.n_loads; ++j) {
+    const bool half = L.in_dt[j] == 1 || L.in_dt[j] == 2;
+    const uint32_t es = half ? 2 : 4;
+    // row-direct: inner dim = columns, outer = rows; transposed: inner = rows
+    const cuuint64_t inner = L.in_trans[j] ? (cuuint64_t)L.rows : (cuuint64_t)L.cols;
+    const cuuint64_t outer = L.in_trans[j] ? (cuuint64_t)L.cols : (cuuint64_t)L.rows;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {(cuuint64_t)L.in_ld[j] * es};
+    cuuint32_t box[2] = {half ? 64u : 32u, 64u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                        const_cast<void*>(L.in[j]), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    p.load_off[j] = off;
+    off += (uint32_t)tile_stage_bytes((int)es);
+    p.in_dt[j] = L.in_dt[j];
+    p.in_trans[j] = L.in_trans[j];
+  }
+  if (off == 0 || off > (uint32_t)kTileStageLimit) return cudaErrorInvalidValue;
+  p.stage_bytes = off;
+  p.tx_bytes = off;
+  const uint32_t stages_fit = (uint32_t)(2 * kTileStageLimit / off);
+  p.n_stages = stages_fit < 2 ? 2 : stages_fit > kMaxStages ? kMaxStages : stages_fit;
+  for (int j = 0; j < kMaxStores; ++j) {
+    p.out[j] = L.out[j];
+    p.out_ld[j] = L.out_ld[j];
+  }
+  std::memcpy(p.scal, L.scal, sizeof p.scal);
+  p.err = L.err;
+  p.rows = L.rows;
+  p.cols = L.cols;
+  p.tiles_c = (L.cols + kTileCols - 1) / kTileCols;
+  p.n_tiles = p.tiles_c * ((L.rows + kTileRows - 1) / kTileRows);
+  p.timeout_ns = L.timeout_ns;
+  p.prog = L.prog;
+  p.n_loads = L.n_loads;
+  p.debug = L.debug;
   switch (tier) {
     case kTier4: return launch_tier<kTier4>(p, stream);
     default: return launch_tier<kTier8>(p, stream);

@@ -384,3 +384,28 @@ def test_exhaustive_store_conversion():
         want_b = np.concatenate(list(pool.map(oracle.f32_to_bf16_bits, parts)))
         gpuutil.compare(got_h, want_h, "f16", f"f16 from {start:#x}")
         gpuutil.compare(got_b, want_b, "bf16", f"bf16 from {start:#x}")
+
+
+def test_device_wait_timeout_is_reported_and_the_context_recovers():
+    """Force the tile executor's consumer warps to wait on a barrier nothing
+    completes, with a 1 ms limit: the kernel must give up, the error must be
+    reported by cmd_sync_status, and the next launch must work normally."""
+    spec = W.strided_bf16(256, 192, 200)
+    bufs = specutil.host_buffers(spec)
+    dts = W.tensor_dtypes(spec)
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    dev = {n: gpuutil.to_device(bufs[n], dts[n]) for n in W.load_names(spec) + W.store_names(spec)}
+    views = {tags[n]: T.TensorView(t.data_ptr(), spec["sizes"], spec["views"][n]["strides"]) for n, t in dev.items()}
+    scal = T.spec_scalars(spec, tags)
+    assert k.plan(views, scal)["path"] == "tile2d"
+    T.cmd_configure_waits(1_000_000, True)
+    try:
+        k.launch(views, scal)
+        with pytest.raises(T.CmdError) as e:
+            k.sync()
+        assert e.value.name == "CMD_ERR_DEVICE_TIMEOUT"
+    finally:
+        T.cmd_configure_waits(2_000_000_000, False)
+    k.sync()  # the error word was cleared when reported
+    gpuutil.parity(spec, bufs)

@@ -273,3 +273,10 @@ def test_lowered_kernel_cannot_launch():
     with pytest.raises(T.CmdError) as e:
         k.launch(views, stream=0)
     assert e.value.name == "CMD_ERR_STATE"
+
+
+def test_configure_waits_validates():
+    with pytest.raises(T.CmdError) as e:
+        T.cmd_configure_waits(0)
+    assert e.value.name == "CMD_ERR_ARG"
+    T.cmd_configure_waits(2_000_000_000, False)
