@@ -80,14 +80,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {
+    "exec_contig": ["exec_contig.cu", "exec_common.cuh", "interp_asm.cuh", "cmd_internal.h"],
+    "exec_tile2d": ["exec_tile2d.cu", "exec_common.cuh", "interp_asm.cuh", "cmd_internal.h"],
+    "exec_generic": ["exec_generic.cu", "exec_common.cuh", "interp_asm.cuh", "cmd_internal.h"],
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of the sources that make up one executor kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_command_execution_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -101,7 +108,7 @@ def profiled_traffic(kernel: str, workload: str):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     s = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_hash():
+    if not m or not s or s.group(1) != source_hash(kernel):
         return None
     return int(m.group(1))
 
