@@ -198,6 +198,24 @@ cmd_status cmd_lower(cmd_command_t cmd, cmd_program_info* info, uint32_t* words,
  * be destroyed afterwards. All tensors of the Command must share one rank. */
 cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out);
 
+/* Like cmd_compile, but allocates no device memory. For callers that cannot
+ * call cudaMalloc: code running while a CUDA graph is captured in global
+ * capture mode, where the runtime refuses allocations, and programs whose
+ * device memory belongs wholly to their own pool. The only device memory a
+ * kernel needs beyond its inputs and outputs is one 4-byte error word for the
+ * tile executor's bounded waits; kernels from this call keep it in a static
+ * 256-byte array of the library (one word per constant-memory program slot,
+ * so at most CMD_MAX_KERNELS such words) that every GPU which loads the
+ * library holds until the process exits. The first call on a device looks up
+ * the array's device address on that device, so make it before any stream
+ * capture; the call also synchronises the device when it reuses a program
+ * slot, like cmd_compile. The word is cleared here; it then keeps whatever
+ * the kernel's launches report until cmd_sync_status reads and clears it, and
+ * launches of the same kernel that overlap on the GPU share (race on) it.
+ * Launch, inspect and destroy the kernel with the usual calls. The pages have
+ * no counterpart of this entry point. */
+cmd_status cmd_compile_static_scratch(cmd_command_t cmd, cmd_kernel_t* out);
+
 /* Lower cmd into a kernel handle without touching any GPU. Such a kernel can
  * be inspected (cmd_kernel_info, cmd_kernel_dump) and planned
  * (cmd_plan_launch) but not launched (CMD_ERR_STATE). */

@@ -101,6 +101,7 @@ SIGNATURES = {
     "cmd_lower": (_I, [_P, ctypes.POINTER(cmd_program_info), ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]),
     "cmd_compile": (_I, [_P, ctypes.POINTER(_P)]),
     "cmd_lower_kernel": (_I, [_P, ctypes.POINTER(_P)]),
+    "cmd_compile_static_scratch": (_I, [_P, ctypes.POINTER(_P)]),
     "cmd_kernel_destroy": (None, [_P]),
     "cmd_kernel_info": (_I, [_P, ctypes.POINTER(cmd_program_info)]),
     "cmd_kernel_dump": (_I, [_P, ctypes.c_char_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
@@ -203,6 +204,13 @@ def cmd_lower(cmd: int):
 def cmd_compile(cmd: int) -> int:
     h = _P()
     _check(lib().cmd_compile(cmd, ctypes.byref(h)), "cmd_compile")
+    return h.value
+
+
+def cmd_compile_static_scratch(cmd: int) -> int:
+    """cmd_compile without any device allocation (see include/cmd.h)."""
+    h = _P()
+    _check(lib().cmd_compile_static_scratch(cmd, ctypes.byref(h)), "cmd_compile_static_scratch")
     return h.value
 
 

@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libcmdexec.so")
 
-CU_SOURCES = ["exec_contig.cu", "exec_tile2d.cu", "exec_generic.cu"]
+CU_SOURCES = ["exec_contig.cu", "exec_tile2d.cu", "exec_generic.cu", "static_scratch.cu"]
 CPP_SOURCES = ["cmd_api.cpp"]
 HEADERS = ["cmd_internal.h", "exec_common.cuh", "interp_asm.cuh", "gen_interp.py"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -90,6 +90,7 @@ struct cmd_kernel {
   int device = -1;
   int slot = -1;
   uint32_t* err = nullptr;  // device error word of the tile executor's bounded waits
+  bool err_owned = true;    // false when err points into static device memory
 };
 
 namespace {
@@ -660,6 +661,65 @@ cmd_status cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace cmdx {
+
+void set_last_error(cmd_status s, const char* msg) { fail(s, msg); }
+
+// cmd_compile without the device allocation: the kernel's error word is
+// words[slot] of a caller-provided static device array of `capacity` words.
+cmd_status compile_with_static_word(cmd_command_t cmd, cmd_kernel_t* out, uint32_t* words, int capacity) {
+  if (!cmd || !out) return fail(CMD_ERR_NULL, "cmd or out is NULL");
+  cmd_kernel* k = new (std::nothrow) cmd_kernel();
+  if (!k) return fail(CMD_ERR_NOMEM, "out of host memory");
+  try {
+    k->ops = cmd->ops;
+    cmd_status s = check_command(cmd, &k->rank);
+    if (s == CMD_OK) s = lower(k->ops, &k->prog);
+    if (s != CMD_OK) {
+      delete k;
+      return s;
+    }
+  } catch (...) {
+    delete k;
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    delete k;
+    return cuda_fail(e, "cudaGetDevice");
+  }
+  bool reused = false;
+  const int slot = acquire_slot(dev, &reused);
+  if (slot < 0) {
+    delete k;
+    return fail(CMD_ERR_LIMIT, "more than " + std::to_string(CMD_MAX_KERNELS) + " compiled kernels on this device");
+  }
+  if (slot >= capacity) {
+    release_slot(dev, slot);
+    delete k;
+    return fail(CMD_ERR_LIMIT, "the static scratch array holds " + std::to_string(capacity) +
+                                   " error words; program slot " + std::to_string(slot) + " is beyond it");
+  }
+  if (reused) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = upload_all(slot, k->prog.words);
+  // the word keeps whatever the previous kernel in this slot left: clear it
+  if (e == cudaSuccess) e = cudaMemset(words + slot, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    release_slot(dev, slot);
+    delete k;
+    return cuda_fail(e, "uploading the program / clearing the static error word");
+  }
+  k->err = words + slot;
+  k->err_owned = false;
+  k->device = dev;
+  k->slot = slot;
+  *out = k;
+  return CMD_OK;
+}
+
+}  // namespace cmdx
+
 // ============================================================================
 // C ABI
 // ============================================================================
@@ -888,7 +948,7 @@ cmd_status cmd_lower_kernel(cmd_command_t cmd, cmd_kernel_t* out) {
 
 void cmd_kernel_destroy(cmd_kernel_t k) {
   if (!k) return;
-  if (k->err) {
+  if (k->err && k->err_owned) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != k->device) cudaSetDevice(k->device);
