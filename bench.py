@@ -226,7 +226,7 @@ class Workload:
         self.plan = self.kernel.plan(self.views, self.scal)
         self.bytes = self.plan["bytes"]
         self.elements = self.plan["n_elements"]
-        chunk = 32 * {0: 8, 1: 8, 2: 2}[self.kernel.info()["tier"]]
+        chunk = 32 * {0: 8, 1: 8, 2: 8, 3: 2}[self.kernel.info()["tier"]]
         self.launches_per_step = 1 + (1 if (self.plan["path"] == "contig" and self.elements % chunk != 0) else 0)
 
     def launch(self, stream_handle):

@@ -135,7 +135,7 @@ typedef struct cmd_program_info {
   int32_t n_stores;
   int32_t n_slots;      /* register slots the program needs */
   int32_t n_words;      /* program words, including the end marker */
-  int32_t tier;         /* executor family: 0 = 4 slots, 1 = 8 slots, 2 = 32 slots */
+  int32_t tier;         /* executor family: 0 = 2 slots, 1 = 4, 2 = 8, 3 = 32 */
   int32_t n_moves;      /* copies the two-address form needed */
 } cmd_program_info;
 

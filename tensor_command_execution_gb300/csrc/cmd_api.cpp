@@ -342,7 +342,10 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     return fail(CMD_ERR_LIMIT, "the program needs more than " + std::to_string(cmdx::kMaxSlots) +
                                    " simultaneously live values");
   P->n_slots = std::max(peak, 1);
-  P->tier = P->n_slots <= 4 ? cmdx::kTier4 : P->n_slots <= 8 ? cmdx::kTier8 : cmdx::kTier32;
+  P->tier = P->n_slots <= 2   ? cmdx::kTier2
+            : P->n_slots <= 4 ? cmdx::kTier4
+            : P->n_slots <= 8 ? cmdx::kTier8
+                              : cmdx::kTier32;
 
   // encode
   P->words.clear();
@@ -369,9 +372,9 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     P->words.push_back(w);
   }
   P->words.push_back(P->tier != cmdx::kTier32 ? cmdx::fz_end(S) : cmdx::wd_word(cmdx::kWEnd, 0, 0, 0));
-  if ((int)P->words.size() > cmdx::kMaxWords)
+  if ((int)P->words.size() > cmdx::kMaxProgramWords)
     return fail(CMD_ERR_LIMIT, "the lowered program has " + std::to_string(P->words.size()) +
-                                   " words; the limit is " + std::to_string(cmdx::kMaxWords));
+                                   " words; the limit is " + std::to_string(cmdx::kMaxProgramWords));
   return CMD_OK;
 }
 

@@ -25,8 +25,10 @@ constexpr int kMaxWords = 256;
 // Executor families by register-slot count. The two small tiers dispatch on
 // one fused (opcode, dst, src) case; the wide tier fetches the source operand
 // and then dispatches on (opcode, dst).
-enum Tier { kTier4 = 0, kTier8 = 1, kTier32 = 2 };
-CMDX_HD constexpr int tier_slots(int tier) { return tier == kTier4 ? 4 : tier == kTier8 ? 8 : 32; }
+enum Tier { kTier2 = 0, kTier4 = 1, kTier8 = 2, kTier32 = 3 };
+CMDX_HD constexpr int tier_slots(int tier) {
+  return tier == kTier2 ? 2 : tier == kTier4 ? 4 : tier == kTier8 ? 8 : 32;
+}
 // Elements each thread keeps per slot in the contiguous executor.
 CMDX_HD constexpr int tier_vec(int tier) { return tier == kTier32 ? 2 : 8; }
 // ... and in the tile and generic executors, whose addressing needs more
@@ -34,6 +36,9 @@ CMDX_HD constexpr int tier_vec(int tier) { return tier == kTier32 ? 2 : 8; }
 CMDX_HD constexpr int tier_vec_strided(int tier) { return tier == kTier8 ? 4 : tier_vec(tier); }
 // Resident 256-thread CTAs per SM each executor is compiled for (caps registers).
 CMDX_HD constexpr int tier_min_blocks(int tier) { return tier == kTier32 ? 2 : 3; }
+// Program words a program may have: one less than its constant-memory row,
+// so the interpreter's read-ahead of the word after the last stays in the row.
+constexpr int kMaxProgramWords = kMaxWords - 1;
 
 // Two-address binary ops: d = d (op) x, where x is a slot or a scalar.
 // RSUB is the reversed subtraction d = x - d.

@@ -108,6 +108,7 @@ __device__ __forceinline__ void st_elem(void* base, int64_t off, uint32_t x) {
 }
 
 // ---- slot lists for the fused dispatch ----------------------------------------
+#define CMDX_SA2(M, ...) M(0, __VA_ARGS__) M(1, __VA_ARGS__)
 #define CMDX_SA4(M, ...) M(0, __VA_ARGS__) M(1, __VA_ARGS__) M(2, __VA_ARGS__) M(3, __VA_ARGS__)
 #define CMDX_SA8(M, ...) CMDX_SA4(M, __VA_ARGS__) M(4, __VA_ARGS__) M(5, __VA_ARGS__) M(6, __VA_ARGS__) M(7, __VA_ARGS__)
 
@@ -128,7 +129,7 @@ __device__ __forceinline__ void st_elem(void* base, int64_t off, uint32_t x) {
 template <int S, int V, class Pol>
 __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* __restrict__ prog,
                                           const uint32_t* __restrict__ scal, Pol& pol) {
-  static_assert(S == 4 || S == 8, "fused dispatch is generated for 4 and 8 slots");
+  static_assert(S == 2 || S == 4 || S == 8, "fused dispatch is generated for 2, 4 and 8 slots");
   uint32_t idx = 0;
 #pragma unroll 1
   for (;;) {
@@ -136,7 +137,12 @@ __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* _
     const uint32_t c = (w & 0xffffu) - fz_store(S, 0, 0);
     if (c >= 4u * S) return;  // the end word
     const uint32_t aux = w >> 16;
-    if constexpr (S == 4) {
+    if constexpr (S == 2) {
+      switch (c) {
+        CMDX_ST_CASES(CMDX_SA2)
+        default: return;
+      }
+    } else if constexpr (S == 4) {
       switch (c) {
         CMDX_ST_CASES(CMDX_SA4)
         default: return;

@@ -98,9 +98,7 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(cons
   }
 }
 
-int contig_chunk(int tier) {
-  return tier == kTier4 ? 32 * tier_vec(kTier4) : tier == kTier8 ? 32 * tier_vec(kTier8) : 32 * tier_vec(kTier32);
-}
+int contig_chunk(int tier) { return 32 * (tier == kTier32 ? tier_vec(kTier32) : tier_vec(kTier4)); }
 
 cudaError_t contig_upload(int slot, const uint32_t* words, int n) {
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
@@ -126,6 +124,7 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
 
 cudaError_t contig_launch(int tier, const ContigParams& p, cudaStream_t stream) {
   switch (tier) {
+    case kTier2: return launch_tier<kTier2>(p, stream);
     case kTier4: return launch_tier<kTier4>(p, stream);
     case kTier8: return launch_tier<kTier8>(p, stream);
     default: return launch_tier<kTier32>(p, stream);

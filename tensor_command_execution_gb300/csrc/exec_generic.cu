@@ -102,6 +102,7 @@ static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
 
 cudaError_t generic_launch(int tier, const GenericParams& p, cudaStream_t stream) {
   switch (tier) {
+    case kTier2: return launch_tier<kTier2>(p, stream);
     case kTier4: return launch_tier<kTier4>(p, stream);
     case kTier8: return launch_tier<kTier8>(p, stream);
     default: return launch_tier<kTier32>(p, stream);

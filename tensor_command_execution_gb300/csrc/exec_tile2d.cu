@@ -124,6 +124,8 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   return v;
 }
 
+__device__ __forceinline__ void rotate8(uint32_t (&y)[8], int c);
+
 // Row-direct: logical (li, 8 cj .. 8 cj + 7).
 __device__ __forceinline__ void read_row(uint32_t (&x)[8], uint32_t stage, int dt, int li, int cj) {
   const uint32_t sw = li & 7;
@@ -176,14 +178,83 @@ __device__ __forceinline__ void read_trans(uint32_t (&x)[8], uint32_t stage, int
       y[k] = lds32(box + q * 128 + ((ch ^ (q & 7)) << 4) + within);
     }
   }
-  // x[m] = y[(m - cj) % 8]: rotate by 1, 2 and 4 places as the bits of cj say
+  rotate8(y, cj);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) x[m] = y[m];
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+// x[m] = y[(m - c) % 8] for a thread-constant c: rotations by 1, 2 and 4.
+__device__ __forceinline__ void rotate8(uint32_t (&y)[8], int c) {
   uint32_t z[8];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) z[m] = (cj & 1) ? y[(m + 7) & 7] : y[m];
+  for (int m = 0; m < 8; ++m) z[m] = (c & 1) ? y[(m + 7) & 7] : y[m];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) y[m] = (cj & 2) ? z[(m + 6) & 7] : z[m];
+  for (int m = 0; m < 8; ++m) y[m] = (c & 2) ? z[(m + 6) & 7] : z[m];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) x[m] = (cj & 4) ? y[(m + 4) & 7] : y[m];
+  for (int m = 0; m < 8; ++m) z[m] = (c & 4) ? y[(m + 4) & 7] : y[m];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) y[m] = z[m];
+}
+
+// Two rows per thread: x[0..7] is row li, x[8..15] row li + 1 (li even).
+__device__ __forceinline__ void read_row2(uint32_t (&x)[16], uint32_t stage, int dt, int li, int cj) {
+  uint32_t a[8], b[8];
+  read_row(a, stage, dt, li, cj);
+  read_row(b, stage, dt, li + 1, cj);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    x[m] = a[m];
+    x[8 + m] = b[m];
+  }
+}
+
+// Transposed, two rows: rows li and li + 1 of box row q are adjacent, so one
+// 32-bit (2-byte types) or 64-bit (4-byte types) load fetches both.
+__device__ __forceinline__ void read_trans2(uint32_t (&x)[16], uint32_t stage, int dt, int li, int cj) {
+  uint32_t y0[8], y1[8];
+  if (dt == 1 || dt == 2) {
+    const uint32_t within = (li & 7) * 2;
+    const uint32_t ch = li >> 3;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t q = 8 * cj + ((k + cj) & 7);
+      y0[k] = lds32(stage + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+    }
+    rotate8(y0, cj);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (dt == 1) {
+        widen_f16x2(y0[m], x[m], x[8 + m]);
+      } else {
+        widen_bf16x2(y0[m], x[m], x[8 + m]);
+      }
+    }
+  } else {
+    const uint32_t box = stage + (li >> 5) * kBoxBytes;
+    const uint32_t lr = li & 31;
+    const uint32_t within = (lr & 3) * 4;
+    const uint32_t ch = lr >> 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t q = 8 * cj + ((k + cj) & 7);
+      const uint2 v = lds64(box + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+      y0[k] = v.x;
+      y1[k] = v.y;
+    }
+    rotate8(y0, cj);
+    rotate8(y1, cj);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      x[m] = y0[m];
+      x[8 + m] = y1[m];
+    }
+  }
 }
 
 struct TileStore {
@@ -218,8 +289,28 @@ struct TileStore {
   }
 };
 
+// Two rows per thread: x[0..7] to row i, x[8..15] to row i + 1 (if it exists).
+struct TileStore2 {
+  TileStore lo, hi;
+  bool second;
+
+  template <int T>
+  __device__ __forceinline__ void store(const uint32_t (&x)[16], uint32_t o) const {
+    uint32_t a[8], b[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      a[m] = x[m];
+      b[m] = x[8 + m];
+    }
+    lo.template store<T>(a, o);
+    if (second) hi.template store<T>(b, o);
+  }
+};
+
 // Resident CTAs per SM the register budget is sized for.
-constexpr int tile_min_blocks(int tier) { return tier == kTier4 ? 3 : 2; }
+CMDX_HD constexpr int tile_min_blocks(int tier) { return tier == kTier2 ? 3 : 2; }
+// Rows each consumer thread handles per tile pass: 2 in the 2- and 4-slot tiers.
+CMDX_HD constexpr int tile_rows_per_thread(int tier) { return tier == kTier8 ? 1 : 2; }
 
 template <int TIER>
 __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
@@ -280,41 +371,56 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
   }
 
   // ---- consumers ----
-  const int cj = threadIdx.x & 7;   // columns 8 cj .. 8 cj + 7 of the tile
-  const int ri = threadIdx.x >> 3;  // row within a 32-row pass
+  constexpr int RPT = tile_rows_per_thread(TIER);
+  constexpr int V = 8 * RPT;
+  const int cj = threadIdx.x & 7;         // columns 8 cj .. 8 cj + 7 of the tile
+  const int rg = threadIdx.x >> 3;        // row group: rows RPT rg .. RPT rg + RPT - 1 of a pass
   const uint32_t* prog = c_prog[p.prog];
   if (p.debug) {
     // test hook: a wait that nothing satisfies must give up and report
     if (!mbar_wait(debug_bar, 0, p.timeout_ns) && lane == 0) atomicOr(p.err, kErrDebugWait);
     return;
   }
+  const uint32_t n_tiles = (uint32_t)p.n_tiles, tiles_c = (uint32_t)p.tiles_c;
   uint32_t n = 0;
-  for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
+  for (uint32_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++n) {
     const uint32_t s = n % ns, ph = (n / ns) & 1;
     if (!mbar_wait(full_bar + 8 * s, ph, p.timeout_ns)) {
       if (lane == 0) atomicOr(p.err, kErrConsumerWait);
       return;
     }
-    const int64_t tr = t / p.tiles_c;
-    const int64_t i0 = tr * kTileRows, j0 = (t - tr * p.tiles_c) * kTileCols;
+    const uint32_t tr = t / tiles_c;
+    const int64_t i0 = (int64_t)tr * kTileRows, j0 = (int64_t)(t - tr * tiles_c) * kTileCols;
     const uint32_t st = stages + s * p.stage_bytes;
 #pragma unroll 1
-    for (int pass = 0; pass < kTileRows / 32; ++pass) {
-      const int li = pass * 32 + ri;
+    for (int pass = 0; pass < kTileRows / (32 * RPT); ++pass) {
+      const int li = pass * 32 * RPT + RPT * rg;
       const int64_t i = i0 + li;
       const int64_t jc = j0 + cj * 8;
       if (i < p.rows && jc < p.cols) {
         const int64_t left = p.cols - jc;
-        uint32_t r[S][8];
+        const bool fullc = left >= 8;
+        const int nleft = fullc ? 8 : (int)left;
+        uint32_t r[S][V];
 #pragma unroll
         for (int j = 0; j < NL; ++j) {
           if (j < (int)p.n_loads) {
-            if (p.in_trans[j]) read_trans(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
-            else read_row(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+            if constexpr (RPT == 2) {
+              if (p.in_trans[j]) read_trans2(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+              else read_row2(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+            } else {
+              if (p.in_trans[j]) read_trans(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+              else read_row(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+            }
           }
         }
-        TileStore sto{p, i, jc, left >= 8, left >= 8 ? 8 : (int)left};
-        run_program<TIER, 8>(r, prog, p.scal, sto);
+        if constexpr (RPT == 2) {
+          TileStore2 sto{{p, i, jc, fullc, nleft}, {p, i + 1, jc, fullc, nleft}, i + 1 < p.rows};
+          run_program<TIER, V>(r, prog, p.scal, sto);
+        } else {
+          TileStore sto{p, i, jc, fullc, nleft};
+          run_program<TIER, V>(r, prog, p.scal, sto);
+        }
       }
     }
     __syncwarp();
@@ -415,6 +521,7 @@ cudaError_t tile2d_launch(int tier, const Tile2dLaunch& L, cudaStream_t stream) 
   p.n_loads = L.n_loads;
   p.debug = L.debug;
   switch (tier) {
+    case kTier2: return launch_tier<kTier2>(p, stream);
     case kTier4: return launch_tier<kTier4>(p, stream);
     default: return launch_tier<kTier8>(p, stream);
   }

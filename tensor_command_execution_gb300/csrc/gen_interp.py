@@ -17,7 +17,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 OUT = os.path.join(HERE, "interp_asm.cuh")
 
-TIERS = [(4, 8), (8, 8), (8, 4)]
+TIERS = [(2, 8), (2, 16), (4, 8), (4, 16), (8, 8), (8, 4)]
 
 # binary ops d = d (op) x, in BinOp order; "{d}" destination, "{x}" source
 BIN = [
@@ -82,22 +82,27 @@ def gen_tier(S: int, V: int) -> str:
             lab = f"$LS{b}_{d}"
             labels.append(lab)
             ops = " ".join(BIN[b].format(d=reg(d, v), x="%%k") for v in range(V))
-            bodies.append(f"{lab}: shr.u32 %%aux, %%w, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; "
+            bodies.append(f"{lab}: shr.u32 %%aux, %%wc, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; "
                           f"ld.u32 %%k, [%%sa]; {ops} bra.uni $Lloop;")
     # broadcast scalar
     for d in range(S):
         lab = f"$LM{d}"
         labels.append(lab)
         ops = " ".join(f"mov.b32 {reg(d, v)}, %%k;" for v in range(V))
-        bodies.append(f"{lab}: shr.u32 %%aux, %%w, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; "
+        bodies.append(f"{lab}: shr.u32 %%aux, %%wc, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; "
                       f"ld.u32 %%k, [%%sa]; {ops} bra.uni $Lloop;")
-    # stores and end leave the loop
+    # stores and end leave the loop; the table is padded to a power of two
+    # with exits so that masking the case number keeps every jump inside it
     labels += ["$Lexit"] * (4 * S + 1)
     assert len(labels) == n_cases
+    size = 1
+    while size < n_cases:
+        size *= 2
+    labels += ["$Lexit"] * (size - n_cases)
 
     lines = []
     lines.append("{")
-    lines.append(".reg .b32 %%w, %%c, %%aux, %%k;")
+    lines.append(".reg .b32 %%w, %%wc, %%c, %%aux, %%k;")
     lines.append(".reg .b64 %%cbase, %%ca, %%sa;")
     # branch table, 16 labels per line
     tbl = []
@@ -106,16 +111,19 @@ def gen_tier(S: int, V: int) -> str:
     lines.append("$Ltable: .branchtargets " + ",\n".join(tbl) + ";")
     lines.append(f"cvta.to.const.u64 %%cbase, %{o_prog};")
     lines.append(f"mad.wide.u32 %%ca, %{o_idx}, 4, %%cbase;")
-    lines.append("$Lloop:")
     lines.append("ld.const.u32 %%w, [%%ca];")
+    lines.append("$Lloop:")
+    # the case number, masked to the table; the next word is fetched while
+    # this one's case runs (the host keeps every program shorter than its
+    # constant-memory row, so that read stays inside the row)
+    lines.append(f"and.b32 %%c, %%w, {size - 1};")
+    lines.append("mov.b32 %%wc, %%w;")
     lines.append("add.u64 %%ca, %%ca, 4;")
-    lines.append("and.b32 %%c, %%w, 0xffff;")
-    # a word outside the table ends the program instead of jumping anywhere
-    lines.append(f"min.u32 %%c, %%c, {end};")
+    lines.append("ld.const.u32 %%w, [%%ca];")
     lines.append("brx.idx.uni %%c, $Ltable;")
     lines += bodies
     lines.append("$Lexit:")
-    lines.append(f"mov.b32 %{o_word}, %%w;")
+    lines.append(f"mov.b32 %{o_word}, %%wc;")
     # the index of the word after the one that left the loop
     lines.append("sub.u64 %%ca, %%ca, %%cbase;")
     lines.append(f"cvt.u32.u64 %{o_idx}, %%ca;")

@@ -270,7 +270,7 @@ def test_wide_tier_program():
     bufs["out"] = specutil.sentinel_array("f32", n)
     bufs["out2"] = specutil.sentinel_array("bf16", n)
     c, _ = T.command_from_spec(spec)
-    assert c.lower()[0]["tier"] == 2
+    assert c.lower()[0]["tier"] == 3
     assert gpuutil.parity(spec, bufs)["path"] == "contig"
 
 

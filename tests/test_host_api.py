@@ -97,10 +97,10 @@ def test_mixed_ranks_rejected_at_lowering():
 def test_lowering_of_the_workloads():
     expect = {  # live E ops, loads, slots, tier, moves
         "add_f32": (1, 2, 2, 0, 0),
-        "chain_f32": (4, 3, 3, 0, 0),
-        "wrap_i32": (3, 4, 4, 0, 0),
+        "chain_f32": (4, 3, 3, 1, 0),
+        "wrap_i32": (3, 4, 4, 1, 0),
         "strided_bf16": (3, 2, 2, 0, 0),
-        "wide_dag": (15, 6, 7, 1, 3),
+        "wide_dag": (15, 6, 7, 2, 3),
     }
     for name, f in W.FULL.items():
         c, _ = T.command_from_spec(f(1024) if name != "strided_bf16" else f(64, 64, 64))
@@ -149,7 +149,7 @@ def test_wide_program_uses_the_32_slot_tier():
     for k in range(12, 19):
         c.store(t[k], "f32", 1)
     info, _ = c.lower()
-    assert info["tier"] == 2 and info["n_slots"] > 8
+    assert info["tier"] == 3 and info["n_slots"] > 8
 
 
 def test_store_of_loads_and_scalars_only():
