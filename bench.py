@@ -219,8 +219,7 @@ class Workload:
             self.dev[n] = torch.empty(spec["views"][n]["alloc"], dtype=torch_dtype(self.dts[n]), device=device)
         self.cmd, self.tags = T.command_from_spec(spec)
         self.kernel = self.cmd.compile()
-        self.views = {self.tags[n]: T.TensorView(t.data_ptr(), spec["sizes"], spec["views"][n]["strides"])
-                      for n, t in self.dev.items()}
+        self.views = {self.tags[n]: self.view_of(n, t) for n, t in self.dev.items()}
         self.scal = T.spec_scalars(spec, self.tags)
         self.args = self.kernel.args(self.views, self.scal)
         self.plan = self.kernel.plan(self.views, self.scal)
@@ -228,6 +227,14 @@ class Workload:
         self.elements = self.plan["n_elements"]
         chunk = 32 * {0: 8, 1: 8, 2: 8, 3: 2}[self.kernel.info()["tier"]]
         self.launches_per_step = 1 + (1 if (self.plan["path"] == "contig" and self.elements % chunk != 0) else 0)
+
+    def view_of(self, name, t, start=0, count=None):
+        """The view of tensor `name` over buffer t (optionally elements
+        [start, start + count) of a dense 1-D tensor)."""
+        import tensor_command_execution_gb300 as T
+        if count is None:
+            return T.TensorView(t.data_ptr(), self.spec["sizes"], self.spec["views"][name]["strides"])
+        return T.TensorView(t.data_ptr() + start * t.element_size(), (count,), (1,))
 
     def launch(self, stream_handle):
         self.kernel.launch_args(self.args, stream_handle)
@@ -248,6 +255,112 @@ def time_device(wl, stream, steps, warmup):
     stop.record(stream)
     stop.synchronize()
     return start.elapsed_time(stop) / steps
+
+
+def time_graph_rotating(wl, device, min_bytes, replays):
+    """Per-launch time of wl's kernel from a CUDA graph that launches it once
+    on each of R copies of its buffers (R * bytes >= min_bytes)."""
+    import math
+
+    import torch
+    sets = max(2, math.ceil(min_bytes / wl.bytes))
+    arg_sets = []
+    keep = []
+    for _ in range(sets):
+        bufs = {n: t.clone() for n, t in wl.dev.items()}
+        keep.append(bufs)
+        views = {wl.tags[n]: wl.view_of(n, t) for n, t in bufs.items()}
+        arg_sets.append(wl.kernel.args(views, wl.scal))
+    s = torch.cuda.Stream(device)
+    for a in arg_sets:  # warm-up outside the capture
+        wl.kernel.launch_args(a, s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for a in arg_sets:
+            wl.kernel.launch_args(a, s.cuda_stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(replays):
+            g.replay()
+    e1.record(s)
+    e1.synchronize()
+    del keep
+    return e0.elapsed_time(e1) / (replays * sets), sets
+
+
+class E2EPipeline:
+    """One end-to-end step through the public API: the inputs are copied in
+    from pinned host memory chunk by chunk, each chunk is launched once it has
+    landed and its outputs are copied back once computed, on three streams, so
+    host-to-device copies, kernels and device-to-host copies overlap. Dense
+    1-D workloads are split into chunks; others run as one chunk."""
+
+    def __init__(self, wl, device, chunks):
+        import torch
+        self.wl = wl
+        spec = wl.spec
+        names_in = W.load_names(spec)
+        names_out = W.store_names(spec)
+        dense_1d = len(spec["sizes"]) == 1 and all(spec["views"][k]["strides"] == (1,)
+                                                   for k in names_in + names_out)
+        n = wl.elements
+        c = chunks if dense_1d else 1
+        step = -(-n // c)
+        step = -(-step // 256) * 256  # keep chunk starts 16-byte aligned for every dtype
+        self.bounds = [(a, min(n, a + step)) for a in range(0, n, step)] if dense_1d else [(0, n)]
+        self.dense_1d = dense_1d
+        self.outs_host = {k: torch.empty_like(wl.dev[k], device="cpu").pin_memory() for k in names_out}
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in wl.host.values())
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.outs_host.values())
+        self.s_in = torch.cuda.Stream(device)
+        self.s_k = torch.cuda.Stream(device)
+        self.s_out = torch.cuda.Stream(device)
+        self.args = []
+        for a, b in self.bounds:
+            if dense_1d:
+                views = {wl.tags[k]: wl.view_of(k, wl.dev[k], a, b - a) for k in names_in + names_out}
+            else:
+                views = wl.views
+            self.args.append(wl.kernel.args(views, wl.scal))
+        m = len(self.bounds)
+        self.ev_in = [torch.cuda.Event() for _ in range(m)]
+        self.ev_k = [torch.cuda.Event() for _ in range(m)]
+        self.ev_out = [torch.cuda.Event() for _ in range(m)]
+        self.started = False
+
+    def step(self):
+        import torch
+        wl = self.wl
+        for c, (a, b) in enumerate(self.bounds):
+            if self.started:
+                self.s_in.wait_event(self.ev_k[c])    # last step's kernel has read this chunk
+            with torch.cuda.stream(self.s_in):
+                for k, t in wl.host.items():
+                    if self.dense_1d:
+                        wl.dev[k][a:b].copy_(t[a:b], non_blocking=True)
+                    else:
+                        wl.dev[k].copy_(t, non_blocking=True)
+            self.ev_in[c].record(self.s_in)
+            self.s_k.wait_event(self.ev_in[c])
+            if self.started:
+                self.s_k.wait_event(self.ev_out[c])   # last step's outputs of this chunk are home
+            wl.kernel.launch_args(self.args[c], self.s_k.cuda_stream)
+            self.ev_k[c].record(self.s_k)
+            self.s_out.wait_event(self.ev_k[c])
+            with torch.cuda.stream(self.s_out):
+                for k, t in self.outs_host.items():
+                    if self.dense_1d:
+                        t[a:b].copy_(wl.dev[k][a:b], non_blocking=True)
+                    else:
+                        t.copy_(wl.dev[k], non_blocking=True)
+            self.ev_out[c].record(self.s_out)
+        self.started = True
 
 
 def run_ours(args):
@@ -308,30 +421,21 @@ def run_ours(args):
         return
 
     # ---- end to end: pinned host inputs -> device, launch, output -> host ----
-    outs_host = {n: torch.empty_like(wl.dev[n], device="cpu").pin_memory() for n in W.store_names(spec)}
-    h2d = sum(t.numel() * t.element_size() for t in wl.host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for n, t in wl.host.items():
-                wl.dev[n].copy_(t, non_blocking=True)
-            wl.launch(stream.cuda_stream)
-            for n, t in outs_host.items():
-                t.copy_(wl.dev[n], non_blocking=True)
-
+    pipe = E2EPipeline(wl, device, chunks=8)
+    h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
     for _ in range(3):
-        e2e_step()
+        pipe.step()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(pipe.s_in)
     for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
+        pipe.step()
+    e1.record(pipe.s_out)
     e1.synchronize()
+    torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     if world > 1:
         t = torch.tensor([e2e_ms], device=device)
@@ -346,14 +450,23 @@ def run_ours(args):
             if name == args.workload:
                 continue
             other = Workload(f(), device)
-            steps = max(20, min(2000, int(0.5 / max(1e-6, other.bytes / (peak * 1e9)))))
-            oms = time_device(other, stream, steps, 10)
+            l2 = torch.cuda.get_device_properties(device).L2_cache_size
+            if other.bytes < 4 * l2:
+                # smaller than L2: a CUDA graph of launches over rotating
+                # buffer sets (together > 4x L2), so neither launch overhead
+                # nor L2 reuse is timed
+                oms, sets = time_graph_rotating(other, device, 4 * l2, 50)
+                steps, how = sets * 50, f"CUDA graph of {sets} launches over {sets} buffer sets, replayed 50x"
+            else:
+                steps = max(20, min(2000, int(0.5 / max(1e-6, other.bytes / (peak * 1e9)))))
+                oms, how = time_device(other, stream, steps, 10), "stream launches"
             ogbs = other.bytes / (oms * 1e-3) / 1e9
             per[name] = {"path": other.plan["path"], "elements": other.elements, "bytes_per_launch": other.bytes,
                          "us_per_launch": round(oms * 1e3, 2), "gbs": round(ogbs, 1),
                          "frac_of_measured_peak": round(ogbs / peak, 4),
                          "frac_of_nominal_8000": round(ogbs / NOMINAL_HBM_GBS, 4),
-                         "elements_per_s": round(other.elements / (oms * 1e-3), 1), "steps": steps}
+                         "elements_per_s": round(other.elements / (oms * 1e-3), 1), "launches": steps,
+                         "timing": how}
             del other
             torch.cuda.empty_cache()
 
