@@ -87,6 +87,9 @@ KERNEL_SOURCES = {
 }
 
 
+KERNEL_OF_PATH = {"contig": "exec_contig", "tile2d": "exec_tile2d", "generic": "exec_generic"}
+
+
 def source_hash(kernel: str) -> str:
     """Hash of the sources that make up one executor kernel."""
     h = hashlib.sha256()
@@ -466,7 +469,8 @@ def run_ours(args):
                          "frac_of_measured_peak": round(ogbs / peak, 4),
                          "frac_of_nominal_8000": round(ogbs / NOMINAL_HBM_GBS, 4),
                          "elements_per_s": round(other.elements / (oms * 1e-3), 1), "launches": steps,
-                         "timing": how}
+                         "timing": how,
+                         "traffic": profiled_traffic(KERNEL_OF_PATH[other.plan["path"]], name)}
             del other
             torch.cuda.empty_cache()
 
@@ -476,7 +480,7 @@ def run_ours(args):
         cpu = cpu_baseline(spec, args.cpu_seconds)
 
     if rank == 0:
-        kernel_name = {"contig": "exec_contig", "tile2d": "exec_tile2d", "generic": "exec_generic"}[wl.plan["path"]]
+        kernel_name = KERNEL_OF_PATH[wl.plan["path"]]
         line = {
             "metric": METRIC,
             "value": round(value, 2),
