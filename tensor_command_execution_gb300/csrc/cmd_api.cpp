@@ -409,6 +409,9 @@ struct Plan {
   uint32_t scal[cmdx::kMaxScalars] = {};
   int n_trans = 0;
   int64_t bytes = 0;
+  // tile executor: merged-dim indices of the tile's row and column dims and
+  // of the (up to two) batch dims, outer first
+  int tile_row = -1, tile_col = -1, n_batch = 0, batch[2] = {-1, -1};
 };
 
 // Largest element offset reached by a view (+1), over dims of size > 1.
@@ -604,30 +607,79 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
     pl->path = CMD_PATH_CONTIG;
     return CMD_OK;
   }
-  // tile: two merged dims; every store row-direct (inner stride 1); every
-  // load row-direct or transposed (outer stride 1); 16-byte aligned rows;
-  // one pipeline stage of 64 x 64 boxes of every load fits the stage limit
-  if (m == 2 && P.tier != cmdx::kTier32 && ms[0] < (int64_t(1) << 31) && ms[1] < (int64_t(1) << 31)) {
-    bool ok = true;
+  // tile: two of the merged dims form the tile, the rest (at most two) are
+  // batch dims. The column dim is the first store's unit-stride dim; the row
+  // dim is the unit-stride dim of the loads that are not unit-stride along
+  // the column dim (or, without such loads, the store's next smallest stride).
+  if (m >= 2 && P.tier != cmdx::kTier32 && !pl->loads.empty()) {
+    const size_t nl = pl->loads.size();
+    int col = -1, row = -1;
+    for (int q = 0; q < m; ++q)
+      if (wst[nl][q] == 1) col = q;
+    bool ok = col >= 0;
+    for (size_t i = 0; i < nl && ok; ++i) {
+      if (wst[i][col] == 1) continue;
+      int unit = -1;
+      for (int q = 0; q < m; ++q)
+        if (q != col && wst[i][q] == 1) unit = q;
+      if (unit < 0 || (row >= 0 && row != unit)) ok = false;
+      else row = unit;
+    }
+    if (ok && row < 0) {
+      for (int q = 0; q < m; ++q)
+        if (q != col && (row < 0 || wst[nl][q] < wst[nl][row])) row = q;
+    }
+    int bd[2] = {-1, -1}, nbd = 0;
+    for (int q = 0; q < m && ok; ++q)
+      if (q != row && q != col) bd[nbd++] = q;
+    int64_t tiles = 1;
+    if (ok) {
+      const int64_t R = ms[row], C = ms[col];
+      tiles = ((R + cmdx::kTileRows - 1) / cmdx::kTileRows) * ((C + cmdx::kTileCols - 1) / cmdx::kTileCols);
+      for (int b = 0; b < nbd; ++b) tiles *= ms[bd[b]];
+      if (R >= (int64_t(1) << 31) || C >= (int64_t(1) << 31) || tiles >= (int64_t(1) << 31)) ok = false;
+    }
     int n_trans = 0, stage = 0;
     for (size_t i = 0; i < all.size() && ok; ++i) {
-      const bool is_store = i >= pl->loads.size();
+      const bool is_store = i >= nl;
       const int es = elem_size(all[i]->dtype);
-      const int64_t so = wst[i][0], si = wst[i][1];
-      if (!is_store) stage += cmdx::tile_stage_bytes(es);
-      // (the row pitch at least covers a row, as the TMA descriptors want)
-      if (!aligned(all[i]->ptr, 16)) ok = false;
-      else if (si == 1 && so >= ms[1] && (so * es) % 16 == 0) {
-        // row-direct
-      } else if (!is_store && so == 1 && si != 1 && si >= ms[0] && (si * es) % 16 == 0) {
-        ++n_trans;
-      } else {
+      const std::vector<int64_t>& v = wst[i];
+      auto mul16 = [&](int64_t st) { return (st * es) % 16 == 0; };
+      if (!aligned(all[i]->ptr, 16)) {
         ok = false;
+        break;
       }
+      for (int b = 0; b < nbd; ++b)
+        if (!mul16(v[bd[b]])) ok = false;
+      if (is_store) {
+        // stores go out as 16-byte vectors along the column dim
+        if (v[col] != 1 || !mul16(v[row])) ok = false;
+        continue;
+      }
+      stage += cmdx::tile_stage_bytes(es);
+      const bool trans = v[col] != 1;
+      const int other = trans ? col : row;   // the load's non-unit tile dim
+      if (v[other] != 0 && !mul16(v[other])) ok = false;
+      if (trans) ++n_trans;
+      // the load's TMA descriptor walks its dims with nonzero stride in
+      // increasing stride order; each must step over the whole previous dim
+      std::vector<std::pair<int64_t, int64_t>> d;  // (stride, size)
+      d.push_back({1, ms[trans ? row : col]});
+      if (v[other] != 0) d.push_back({v[other], ms[other]});
+      for (int b = 0; b < nbd; ++b)
+        if (v[bd[b]] != 0) d.push_back({v[bd[b]], ms[bd[b]]});
+      std::sort(d.begin() + 1, d.end());
+      for (size_t k2 = 1; k2 < d.size() && ok; ++k2)
+        if (d[k2].first < d[k2 - 1].first * d[k2 - 1].second) ok = false;
     }
-    if (ok && !pl->loads.empty() && stage <= cmdx::kTileStageLimit) {
+    if (ok && stage <= cmdx::kTileStageLimit) {
       pl->path = CMD_PATH_TILE2D;
       pl->n_trans = n_trans;
+      pl->tile_row = row;
+      pl->tile_col = col;
+      pl->n_batch = nbd;
+      pl->batch[0] = bd[0];
+      pl->batch[1] = bd[1];
       return CMD_OK;
     }
   }
@@ -1091,20 +1143,31 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
   } else if (pl.path == CMD_PATH_TILE2D) {
     cmdx::Tile2dLaunch L;
     std::memset(&L, 0, sizeof L);
+    const int off = cmdx::kMaxRank - pl.mrank;  // merged dims are right-aligned in ml/ms
+    const int row = off + pl.tile_row, col = off + pl.tile_col;
+    // batch dims b0 (outer), b1: a single batch dim is b1
+    const int b0 = pl.n_batch == 2 ? off + pl.batch[0] : -1;
+    const int b1 = pl.n_batch >= 1 ? off + pl.batch[pl.n_batch - 1] : -1;
     for (size_t j = 0; j < pl.loads.size(); ++j) {
       L.in[j] = pl.loads[j].ptr;
       L.in_dt[j] = (uint8_t)pl.loads[j].dtype;
-      const int64_t so = pl.ml[j][2], si = pl.ml[j][3];
-      L.in_trans[j] = si != 1;
-      L.in_ld[j] = si == 1 ? so : si;
+      const bool trans = pl.ml[j][col] != 1;
+      L.in_trans[j] = trans;
+      L.in_ld[j] = trans ? pl.ml[j][col] : pl.ml[j][row];
+      L.in_bst[j][0] = b0 >= 0 ? pl.ml[j][b0] : 0;
+      L.in_bst[j][1] = b1 >= 0 ? pl.ml[j][b1] : 0;
     }
     for (size_t j = 0; j < pl.stores.size(); ++j) {
       L.out[j] = pl.stores[j].ptr;
-      L.out_ld[j] = pl.ms[j][2];
+      L.out_ld[j] = pl.ms[j][row];
+      L.out_bst[j][0] = b0 >= 0 ? pl.ms[j][b0] : 0;
+      L.out_bst[j][1] = b1 >= 0 ? pl.ms[j][b1] : 0;
     }
     std::memcpy(L.scal, pl.scal, sizeof L.scal);
-    L.rows = pl.msizes[2];
-    L.cols = pl.msizes[3];
+    L.rows = pl.msizes[row];
+    L.cols = pl.msizes[col];
+    L.nb[0] = b0 >= 0 ? pl.msizes[b0] : 1;
+    L.nb[1] = b1 >= 0 ? pl.msizes[b1] : 1;
     L.prog = (uint32_t)k->slot;
     L.n_loads = (uint32_t)pl.loads.size();
     L.err = k->err;

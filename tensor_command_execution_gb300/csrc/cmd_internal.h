@@ -93,18 +93,25 @@ struct ContigParams {
   uint8_t in_dt[kMaxLoads];
 };
 
-// What the tile executor needs from the host: every load view is row-direct
-// (element (i, j) at i*ld + j) or transposed (element (i, j) at i + j*ld);
-// every store is row-direct. The executor builds its TMA descriptors from it.
+// What the tile executor needs from the host. The logical index space is
+// viewed as [b0][b1][row][col]: two tile dims (row, col) and up to two batch
+// dims (size 1 when absent). Every store has unit stride along col; every
+// load has unit stride along col ("row-direct") or along row ("transposed").
+// The other tile dim of a load may have stride 0 (a broadcast row or column)
+// and batch dims may have stride 0 (broadcast across the batch). The executor
+// builds one TMA descriptor per load from this.
 struct Tile2dLaunch {
   const void* in[kMaxLoads];
-  int64_t in_ld[kMaxLoads];
+  int64_t in_ld[kMaxLoads];      // stride of the load's other tile dim (0 = broadcast)
+  int64_t in_bst[kMaxLoads][2];  // batch strides (0 = broadcast)
   uint8_t in_dt[kMaxLoads];
   uint8_t in_trans[kMaxLoads];
   void* out[kMaxStores];
-  int64_t out_ld[kMaxStores];
+  int64_t out_ld[kMaxStores];     // row stride of each store
+  int64_t out_bst[kMaxStores][2]; // batch strides of each store
   uint32_t scal[kMaxScalars];
-  int64_t rows, cols;
+  int64_t rows, cols;             // sizes of the two tile dims
+  int64_t nb[2];                  // batch sizes (outer first)
   uint32_t prog;
   uint32_t n_loads;
   uint32_t* err;        // device error word of the kernel handle

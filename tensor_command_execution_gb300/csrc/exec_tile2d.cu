@@ -50,14 +50,19 @@ struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap maps[kMaxLoads];
   void* out[kMaxStores];
   int64_t out_ld[kMaxStores];
+  int64_t out_bst[kMaxStores][2];
   uint32_t scal[kMaxScalars];
   uint32_t* err;
-  int64_t rows, cols, tiles_c, n_tiles;
+  int64_t rows, cols;
   uint64_t timeout_ns;
+  uint32_t tiles_r, tiles_c, nb1, n_tiles;
   uint32_t prog, n_loads, n_stages, stage_bytes, tx_bytes, debug;
   uint32_t load_off[kMaxLoads];  // byte offset of load j in a stage
   uint8_t in_dt[kMaxLoads];
   uint8_t in_trans[kMaxLoads];
+  uint8_t in_bcast[kMaxLoads];   // the load's other tile dim has stride 0: a one-row box
+  uint8_t in_rank[kMaxLoads];    // dims of its TMA descriptor
+  uint8_t in_src[kMaxLoads][3];  // coordinate of descriptor dims 1..3: 0 tile, 1 batch b0, 2 batch b1
 };
 
 // ---- mbarrier / TMA primitives (inline PTX) ----------------------------------
@@ -96,12 +101,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     if (global_ns() - t0 > timeout_ns) return false;
   }
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
+// One box of a descriptor of rank 1..4 at coordinates c[0..rank).
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int rank, const int32_t (&c)[4],
+                                         uint32_t bar) {
+  const uint64_t m = reinterpret_cast<uint64_t>(map);
+  switch (rank) {
+    case 1:
+      asm volatile(
+          "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];"
+          ::"r"(dst), "l"(m), "r"(c[0]), "r"(bar) : "memory");
+      break;
+    case 2:
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+          ::"r"(dst), "l"(m), "r"(c[0]), "r"(c[1]), "r"(bar) : "memory");
+      break;
+    case 3:
+      asm volatile(
+          "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+          ::"r"(dst), "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(bar) : "memory");
+      break;
+    default:
+      asm volatile(
+          "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+          "[%6];"
+          ::"r"(dst), "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(bar) : "memory");
+      break;
+  }
 }
 
 // ---- reading a stage -----------------------------------------------------------
@@ -202,11 +228,11 @@ __device__ __forceinline__ void rotate8(uint32_t (&y)[8], int c) {
   for (int m = 0; m < 8; ++m) y[m] = z[m];
 }
 
-// Two rows per thread: x[0..7] is row li, x[8..15] row li + 1 (li even).
-__device__ __forceinline__ void read_row2(uint32_t (&x)[16], uint32_t stage, int dt, int li, int cj) {
+// Two rows per thread: x[0..7] is box row la, x[8..15] box row lb.
+__device__ __forceinline__ void read_row2(uint32_t (&x)[16], uint32_t stage, int dt, int la, int lb, int cj) {
   uint32_t a[8], b[8];
-  read_row(a, stage, dt, li, cj);
-  read_row(b, stage, dt, li + 1, cj);
+  read_row(a, stage, dt, la, cj);
+  read_row(b, stage, dt, lb, cj);
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     x[m] = a[m];
@@ -257,16 +283,29 @@ __device__ __forceinline__ void read_trans2(uint32_t (&x)[16], uint32_t stage, i
   }
 }
 
+// A broadcast column (transposed load whose column stride is 0): the box has
+// one row, element li of it is the value of every column of row li.
+__device__ __forceinline__ uint32_t read_bcast_col(uint32_t stage, int dt, int li) {
+  if (dt == 1 || dt == 2) {
+    const uint32_t h = lds16(stage + ((((uint32_t)li >> 3) ^ 0u) << 4) + (li & 7) * 2);
+    return dt == 1 ? widen_f16((uint16_t)h) : widen_bf16((uint16_t)h);
+  }
+  return lds32(stage + (li >> 5) * kBoxBytes + ((((uint32_t)li & 31) >> 2) << 4) + (li & 3) * 4);
+}
+
+template <bool ND>
 struct TileStore {
   const Tile2dParams& p;
   int64_t i, j;
   bool full;
   int ncols_left;
+  uint32_t b0, b1;
 
   template <int T>
   __device__ __forceinline__ void store(const uint32_t (&x)[8], uint32_t o) const {
     void* base = p.out[o];
-    const int64_t off = i * p.out_ld[o] + j;
+    int64_t off = i * p.out_ld[o] + j;
+    if (ND) off += (int64_t)b0 * p.out_bst[o][0] + (int64_t)b1 * p.out_bst[o][1];
     if (full) {
       if constexpr (T == kStF32 || T == kStI32) {
         uint4* q = reinterpret_cast<uint4*>(static_cast<uint32_t*>(base) + off);
@@ -290,8 +329,9 @@ struct TileStore {
 };
 
 // Two rows per thread: x[0..7] to row i, x[8..15] to row i + 1 (if it exists).
+template <bool ND>
 struct TileStore2 {
-  TileStore lo, hi;
+  TileStore<ND> lo, hi;
   bool second;
 
   template <int T>
@@ -312,7 +352,9 @@ CMDX_HD constexpr int tile_min_blocks(int tier) { return tier == kTier2 ? 3 : 2;
 // Rows each consumer thread handles per tile pass: 2 in the 2- and 4-slot tiers.
 CMDX_HD constexpr int tile_rows_per_thread(int tier) { return tier == kTier8 ? 1 : 2; }
 
-template <int TIER>
+// ND: the launch has batch dims or broadcast loads. Plain 2-D launches
+// compile without that bookkeeping (the consumer warps are issue-bound).
+template <int TIER, bool ND>
 __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int S = tier_slots(TIER);
@@ -340,25 +382,40 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
     if (lane != 0 || p.debug) return;
     uint32_t n = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
+    for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
       const uint32_t s = n % ns, ph = (n / ns) & 1;
       if (!mbar_wait(empty_bar + 8 * s, ph ^ 1, p.timeout_ns)) {
         atomicOr(p.err, kErrProducerWait);
         ok = false;
         break;
       }
-      const int64_t tr = t / p.tiles_c;
-      const int32_t i0 = (int32_t)(tr * kTileRows), j0 = (int32_t)((t - tr * p.tiles_c) * kTileCols);
+      // t = ((b0 * nb1 + b1) * tiles_r + tile row) * tiles_c + tile column
+      const uint32_t tc = t % p.tiles_c, t1 = t / p.tiles_c;
+      const uint32_t tr = ND ? t1 % p.tiles_r : t1, t2 = ND ? t1 / p.tiles_r : 0;
+      const int32_t i0 = (int32_t)(tr * kTileRows), j0 = (int32_t)(tc * kTileCols);
+      const int32_t bc[3] = {0, ND ? (int32_t)(t2 / p.nb1) : 0, ND ? (int32_t)(t2 % p.nb1) : 0};
       const uint32_t fb = full_bar + 8 * s;
       mbar_arrive_expect_tx(fb, p.tx_bytes);
       const uint32_t st = stages + s * p.stage_bytes;
       for (uint32_t j = 0; j < p.n_loads; ++j) {
         const uint32_t dst = st + p.load_off[j];
         const bool wide = !(p.in_dt[j] == 1 || p.in_dt[j] == 2);
-        // row-direct boxes are (columns, rows); transposed boxes (rows, columns)
-        const int32_t x = p.in_trans[j] ? i0 : j0, y = p.in_trans[j] ? j0 : i0;
-        tma_load_2d(dst, &p.maps[j], x, y, fb);
-        if (wide) tma_load_2d(dst + kBoxBytes, &p.maps[j], x + 32, y, fb);
+        // dim 0 runs along the load's unit-stride tile dim; dims 1.. take the
+        // other tile coordinate or a batch coordinate, as routed on the host
+        const int32_t inner = p.in_trans[j] ? i0 : j0, outer = p.in_trans[j] ? j0 : i0;
+        int32_t c[4] = {inner, outer, 0, 0};
+        if (ND) {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            const uint32_t src = p.in_src[j][k];
+            c[k + 1] = src == 0 ? outer : bc[src];
+          }
+        }
+        tma_load(dst, &p.maps[j], ND ? p.in_rank[j] : 2, c, fb);
+        if (wide) {
+          c[0] = inner + 32;
+          tma_load(dst + kBoxBytes, &p.maps[j], p.in_rank[j], c, fb);
+        }
       }
     }
     if (!ok) {
@@ -381,16 +438,17 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
     if (!mbar_wait(debug_bar, 0, p.timeout_ns) && lane == 0) atomicOr(p.err, kErrDebugWait);
     return;
   }
-  const uint32_t n_tiles = (uint32_t)p.n_tiles, tiles_c = (uint32_t)p.tiles_c;
   uint32_t n = 0;
-  for (uint32_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++n) {
+  for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
     const uint32_t s = n % ns, ph = (n / ns) & 1;
     if (!mbar_wait(full_bar + 8 * s, ph, p.timeout_ns)) {
       if (lane == 0) atomicOr(p.err, kErrConsumerWait);
       return;
     }
-    const uint32_t tr = t / tiles_c;
-    const int64_t i0 = (int64_t)tr * kTileRows, j0 = (int64_t)(t - tr * tiles_c) * kTileCols;
+    const uint32_t tc = t % p.tiles_c, t1 = t / p.tiles_c;
+    const uint32_t tr = ND ? t1 % p.tiles_r : t1, t2 = ND ? t1 / p.tiles_r : 0;
+    const uint32_t b0 = ND ? t2 / p.nb1 : 0, b1 = ND ? t2 % p.nb1 : 0;
+    const int64_t i0 = (int64_t)tr * kTileRows, j0 = (int64_t)tc * kTileCols;
     const uint32_t st = stages + s * p.stage_bytes;
 #pragma unroll 1
     for (int pass = 0; pass < kTileRows / (32 * RPT); ++pass) {
@@ -405,20 +463,36 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
 #pragma unroll
         for (int j = 0; j < NL; ++j) {
           if (j < (int)p.n_loads) {
-            if constexpr (RPT == 2) {
-              if (p.in_trans[j]) read_trans2(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
-              else read_row2(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+            const uint32_t at = st + p.load_off[j];
+            if (p.in_trans[j]) {
+              if (ND && p.in_bcast[j]) {
+#pragma unroll
+                for (int q = 0; q < RPT; ++q) {
+                  const uint32_t v = read_bcast_col(at, p.in_dt[j], li + q);
+#pragma unroll
+                  for (int m = 0; m < 8; ++m) r[j][8 * q + m] = v;
+                }
+              } else if constexpr (RPT == 2) {
+                read_trans2(r[j], at, p.in_dt[j], li, cj);
+              } else {
+                read_trans(r[j], at, p.in_dt[j], li, cj);
+              }
             } else {
-              if (p.in_trans[j]) read_trans(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
-              else read_row(r[j], st + p.load_off[j], p.in_dt[j], li, cj);
+              const bool bc0 = ND && p.in_bcast[j];
+              const int la = bc0 ? 0 : li;
+              if constexpr (RPT == 2) {
+                read_row2(r[j], at, p.in_dt[j], la, bc0 ? 0 : li + 1, cj);
+              } else {
+                read_row(r[j], at, p.in_dt[j], la, cj);
+              }
             }
           }
         }
         if constexpr (RPT == 2) {
-          TileStore2 sto{{p, i, jc, fullc, nleft}, {p, i + 1, jc, fullc, nleft}, i + 1 < p.rows};
+          TileStore2<ND> sto{{p, i, jc, fullc, nleft, b0, b1}, {p, i + 1, jc, fullc, nleft, b0, b1}, i + 1 < p.rows};
           run_program<TIER, V>(r, prog, p.scal, sto);
         } else {
-          TileStore sto{p, i, jc, fullc, nleft};
+          TileStore<ND> sto{p, i, jc, fullc, nleft, b0, b1};
           run_program<TIER, V>(r, prog, p.scal, sto);
         }
       }
@@ -447,7 +521,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-template <int TIER>
+template <int TIER, bool ND>
 static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes;
   static int grid_cache[64][kMaxStages + 1] = {};
@@ -456,7 +530,7 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   cudaGetDevice(&dev);
   const bool cacheable = dev >= 0 && dev < 64;
   if (!cacheable || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBarrierBytes + 2 * kTileStageLimit + 4096);
     if (e != cudaSuccess) return e;
     if (cacheable) attr_set[dev] = true;
@@ -466,11 +540,11 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const bool cache_ok = cacheable && p.stage_bytes == 16384;
   if (cache_ok) full_grid = grid_cache[dev][p.n_stages];
   if (full_grid == 0) {
-    full_grid = persistent_grid(tile2d_kernel<TIER>, kThreads, smem, INT64_MAX);
+    full_grid = persistent_grid(tile2d_kernel<TIER, ND>, kThreads, smem, INT64_MAX);
     if (cache_ok) grid_cache[dev][p.n_stages] = full_grid;
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
-  tile2d_kernel<TIER><<<grid, kThreads, smem, stream>>>(p);
+  tile2d_kernel<TIER, ND><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -480,50 +554,82 @@ cudaError_t tile2d_launch(int tier, const Tile2dLaunch& L, cudaStream_t stream) 
   if (!encode) return cudaErrorNotSupported;
   Tile2dParams p;
   std::memset(&p, 0, sizeof p);
-  uint32_t off = 0;
+  uint32_t off = 0, tx = 0;
   for (uint32_t j = 0; j < L.n_loads; ++j) {
     const bool half = L.in_dt[j] == 1 || L.in_dt[j] == 2;
     const uint32_t es = half ? 2 : 4;
-    // row-direct: inner dim = columns, outer = rows; transposed: inner = rows
-    const cuuint64_t inner = L.in_trans[j] ? (cuuint64_t)L.rows : (cuuint64_t)L.cols;
-    const cuuint64_t outer = L.in_trans[j] ? (cuuint64_t)L.cols : (cuuint64_t)L.rows;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {(cuuint64_t)L.in_ld[j] * es};
-    cuuint32_t box[2] = {half ? 64u : 32u, 64u};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
-                        const_cast<void*>(L.in[j]), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const bool trans = L.in_trans[j] != 0;
+    // descriptor dims: 0 = the unit-stride tile dim; then the other tile dim
+    // and the batch dims that have a nonzero stride, by increasing stride
+    struct D { int64_t stride, size; int src; };
+    D d[3];
+    int nd = 0;
+    if (L.in_ld[j] != 0) d[nd++] = {L.in_ld[j], trans ? L.cols : L.rows, 0};
+    if (L.in_bst[j][0] != 0) d[nd++] = {L.in_bst[j][0], L.nb[0], 1};
+    if (L.in_bst[j][1] != 0) d[nd++] = {L.in_bst[j][1], L.nb[1], 2};
+    for (int a = 1; a < nd; ++a)
+      for (int b = a; b > 0 && d[b].stride < d[b - 1].stride; --b) std::swap(d[b], d[b - 1]);
+    cuuint64_t dims[4] = {(cuuint64_t)(trans ? L.rows : L.cols), 1, 1, 1};
+    cuuint64_t strides[3] = {0, 0, 0};
+    cuuint32_t box[4] = {half ? 64u : 32u, 1, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    for (int k = 0; k < nd; ++k) {
+      dims[k + 1] = (cuuint64_t)d[k].size;
+      strides[k] = (cuuint64_t)d[k].stride * es;
+      box[k + 1] = d[k].src == 0 ? 64u : 1u;
+      p.in_src[j][k] = (uint8_t)d[k].src;
+    }
+    const int rank = 1 + nd;
+    CUresult r = encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                        (cuuint32_t)rank, const_cast<void*>(L.in[j]), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    p.in_rank[j] = (uint8_t)rank;
+    p.in_bcast[j] = L.in_ld[j] == 0;
     p.load_off[j] = off;
     off += (uint32_t)tile_stage_bytes((int)es);
+    // bytes the load's boxes deliver per tile: one row when broadcast
+    tx += (uint32_t)(p.in_bcast[j] ? 64 * es : 64 * 64 * es);
     p.in_dt[j] = L.in_dt[j];
     p.in_trans[j] = L.in_trans[j];
   }
   if (off == 0 || off > (uint32_t)kTileStageLimit) return cudaErrorInvalidValue;
   p.stage_bytes = off;
-  p.tx_bytes = off;
+  p.tx_bytes = tx;
   const uint32_t stages_fit = (uint32_t)(2 * kTileStageLimit / off);
   p.n_stages = stages_fit < 2 ? 2 : stages_fit > kMaxStages ? kMaxStages : stages_fit;
   for (int j = 0; j < kMaxStores; ++j) {
     p.out[j] = L.out[j];
     p.out_ld[j] = L.out_ld[j];
+    p.out_bst[j][0] = L.out_bst[j][0];
+    p.out_bst[j][1] = L.out_bst[j][1];
   }
   std::memcpy(p.scal, L.scal, sizeof p.scal);
   p.err = L.err;
   p.rows = L.rows;
   p.cols = L.cols;
-  p.tiles_c = (L.cols + kTileCols - 1) / kTileCols;
-  p.n_tiles = p.tiles_c * ((L.rows + kTileRows - 1) / kTileRows);
+  p.tiles_c = (uint32_t)((L.cols + kTileCols - 1) / kTileCols);
+  p.tiles_r = (uint32_t)((L.rows + kTileRows - 1) / kTileRows);
+  p.nb1 = (uint32_t)L.nb[1];
+  p.n_tiles = (uint32_t)((int64_t)p.tiles_c * p.tiles_r * L.nb[0] * L.nb[1]);
   p.timeout_ns = L.timeout_ns;
   p.prog = L.prog;
   p.n_loads = L.n_loads;
   p.debug = L.debug;
+  bool nd = L.nb[0] > 1 || L.nb[1] > 1;
+  for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
+  if (nd) {
+    switch (tier) {
+      case kTier2: return launch_tier<kTier2, true>(p, stream);
+      case kTier4: return launch_tier<kTier4, true>(p, stream);
+      default: return launch_tier<kTier8, true>(p, stream);
+    }
+  }
   switch (tier) {
-    case kTier2: return launch_tier<kTier2>(p, stream);
-    case kTier4: return launch_tier<kTier4>(p, stream);
-    default: return launch_tier<kTier8>(p, stream);
+    case kTier2: return launch_tier<kTier2, false>(p, stream);
+    case kTier4: return launch_tier<kTier4, false>(p, stream);
+    default: return launch_tier<kTier8, false>(p, stream);
   }
 }
 

@@ -409,3 +409,76 @@ def test_device_wait_timeout_is_reported_and_the_context_recovers():
         T.cmd_configure_waits(2_000_000_000, False)
     k.sync()  # the error word was cleared when reported
     gpuutil.parity(spec, bufs)
+
+
+# ---- batched, permuted and broadcast views on the tile executor --------------------
+
+def _nd_case(name, sizes, views, dts, seed=0):
+    """out = A*B - A over rank-3 views; views/dts map A, B, out."""
+    rng = np.random.default_rng(seed)
+    spec = dict(name=name, seed=0, sizes=sizes,
+                ops=[("load", "A", dts["A"]), ("load", "B", dts["B"]),
+                     ("exec", [("mul", "AB", "A", "B"), ("sub", "r", "AB", "A")]),
+                     ("store", "out", "r", dts["out"])],
+                views={}, inputs={})
+    bufs = {}
+    for k in ("A", "B", "out"):
+        st = views[k]
+        alloc = sum((s - 1) * t for s, t in zip(sizes, st)) + 1
+        spec["views"][k] = dict(strides=st, alloc=alloc)
+        if k == "out":
+            bufs[k] = specutil.sentinel_array(dts[k], alloc)
+        else:
+            bufs[k] = _random_values(rng, dts[k], alloc)
+    return spec, bufs
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["batched_transpose", "perm_210", "batch_broadcast", "row_broadcast",
+                                  "col_broadcast", "padded_batched"])
+@pytest.mark.parametrize("sizes", [(3, 96, 136), (2, 64, 64), (5, 40, 72)])
+def test_nd_views_on_the_tile_executor(dt, case, sizes):
+    B, R, C = sizes
+    dense = (R * C, C, 1)
+    views = {
+        "batched_transpose": {"A": (R * C, 1, R), "B": dense},
+        "perm_210": {"A": (1, B, B * R), "B": dense},
+        "batch_broadcast": {"A": (0, C, 1), "B": dense},
+        "row_broadcast": {"A": (C, 0, 1), "B": dense},
+        "col_broadcast": {"A": (R, 1, 0), "B": dense},
+        "padded_batched": {"A": (R * (C + 8), C + 8, 1), "B": (R * C + 64, 1, R)},
+    }[case]
+    views = dict(views, out=dense)
+    spec, bufs = _nd_case(f"{case}_{dt}", sizes, views, {"A": dt, "B": dt, "out": dt}, seed=B * 1000 + R)
+    plan = gpuutil.parity(spec, bufs)
+    es = 2 if dt == "bf16" else 4
+    aligned = all((s * es) % 16 == 0 for s in (B, R, C, R * C))
+    if case in ("batched_transpose", "padded_batched", "batch_broadcast", "row_broadcast", "col_broadcast") \
+            and aligned:
+        assert plan["path"] == "tile2d", plan
+    if case == "perm_210" and aligned and (B * es) % 16 == 0:
+        assert plan["path"] == "tile2d", plan
+
+
+def test_rank4_batched_transpose_with_two_batch_dims():
+    sizes = (2, 3, 64, 80)
+    A, R, C = sizes[1], sizes[2], sizes[3]
+    dense = (A * R * C, R * C, C, 1)
+    bt = (A * R * C, R * C, 1, R)
+    spec, bufs = _nd_case("rank4", sizes, {"A": bt, "B": dense, "out": dense},
+                          {"A": "f32", "B": "f32", "out": "f32"}, seed=4)
+    plan = gpuutil.parity(spec, bufs)
+    assert plan["path"] == "tile2d" and plan["merged_rank"] == 3  # the two batch dims merge
+
+
+def test_rank4_with_two_batch_dims_that_do_not_merge():
+    sizes = (2, 3, 64, 80)
+    _, A, R, C = sizes
+    dense = (A * R * C, R * C, C, 1)
+    # A is a (3, 2, 80, 64) buffer: its two batch dims are swapped and its
+    # tile is transposed, so nothing merges
+    swapped = (R * C, 2 * R * C, 1, R)
+    spec, bufs = _nd_case("rank4b", sizes, {"A": swapped, "B": dense, "out": dense},
+                          {"A": "f32", "B": "f32", "out": "f32"}, seed=5)
+    plan = gpuutil.parity(spec, bufs)
+    assert plan["path"] == "tile2d" and plan["merged_rank"] == 4

@@ -207,7 +207,7 @@ def test_dims_merge_to_contiguous():
     assert p["path"] == "contig" and p["merged_rank"] == 1 and p["merged_sizes"] == [24]
 
 
-def test_padded_rows_use_the_tile_path_and_permutations_the_generic():
+def test_padded_rows_and_permutations_use_the_tile_path():
     spec = W.add_f32(0)
     spec["sizes"] = (64, 64)
     spec["views"] = {"x": dict(strides=(72, 1), alloc=64 * 72), "y": dict(strides=(64, 1), alloc=4096),
@@ -219,7 +219,12 @@ def test_padded_rows_use_the_tile_path_and_permutations_the_generic():
     # the last two dims merge for every view: a 4 x 128 transposed read
     p = _plan(spec)
     assert p["path"] == "tile2d" and p["merged_sizes"] == [4, 128] and p["n_transposed"] == 1
+    # a rank-3 permutation tiles over (dim 0, dim 2) with dim 1 as the batch
     spec["views"]["x"] = dict(strides=(1, 4, 32), alloc=512)
+    p = _plan(spec)
+    assert p["path"] == "tile2d" and p["merged_rank"] == 3 and p["n_transposed"] == 1
+    # a view with no unit stride at all cannot be staged as a tile
+    spec["views"]["x"] = dict(strides=(2, 8, 64), alloc=1024)
     p = _plan(spec)
     assert p["path"] == "generic" and p["merged_rank"] == 3
 
