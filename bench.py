@@ -67,6 +67,8 @@ def make_spec(name, size):
         return f()
     if name == "strided_bf16":
         return f(size, size, size + 128)
+    if name == "batched_transpose":
+        return f(max(1, size // (1 << 20)))
     return f(size)
 
 
@@ -493,7 +495,7 @@ def run_ours(args):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
-                      "wide_dag": "f32 (f32+f16 out)"}[args.workload],
+                      "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32"}[args.workload],
             "data": "synthetic (seeded SplitMix64 inputs; no dataset)",
             "config": {"workload": f"{args.workload}: {spec_summary(spec)}", "elements": wl.elements,
                        "bytes_per_step": wl.bytes, "path": wl.plan["path"],

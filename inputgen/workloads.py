@@ -139,6 +139,23 @@ def wide_dag(n: int = 1 << 27) -> dict:
     )
 
 
+def batched_transpose(b: int = 64, m: int = 1024, n: int = 1024) -> dict:
+    """out = A^T*B - A^T per batch (A^T: each m x n slice of A read through its
+    transpose, strides {m*n, 1, m}), fp32, normal(0,1), seed 5: the batched
+    coordinate transform of the generalised tile path."""
+    dense = (m * n, n, 1)
+    return dict(
+        name="batched_transpose", seed=5, sizes=(b, m, n),
+        ops=[("load", "A", "f32"), ("load", "B", "f32"),
+             ("exec", [("mul", "AB", "A", "B"), ("sub", "r", "AB", "A")]),
+             ("store", "out", "r", "f32")],
+        views={"A": dict(strides=(m * n, 1, m), alloc=b * m * n),
+               "B": dict(strides=dense, alloc=b * m * n),
+               "out": dict(strides=dense, alloc=b * m * n)},
+        inputs={"A": ("normal_f32", 0.0, 0.0), "B": ("normal_f32", 0.0, 0.0)},
+    )
+
+
 # Full-size workloads, in the order they are listed for this path.
 FULL = {
     "add_f32": add_f32,
@@ -146,6 +163,7 @@ FULL = {
     "wrap_i32": wrap_i32,
     "strided_bf16": strided_bf16,
     "wide_dag": wide_dag,
+    "batched_transpose": batched_transpose,
 }
 
 

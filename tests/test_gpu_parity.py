@@ -41,7 +41,7 @@ def test_workload_small(spec, path):
 def test_workload_full_size_sampled(name):
     spec = W.FULL[name]()
     plan, checked = gpuutil.sampled_parity(spec, n_samples=1 << 18)
-    assert plan["path"] == ("tile2d" if name == "strided_bf16" else "contig")
+    assert plan["path"] == ("tile2d" if name in ("strided_bf16", "batched_transpose") else "contig")
     assert checked > 1 << 17
 
 

@@ -101,9 +101,11 @@ def test_lowering_of_the_workloads():
         "wrap_i32": (3, 4, 4, 1, 0),
         "strided_bf16": (3, 2, 2, 0, 0),
         "wide_dag": (15, 6, 7, 2, 3),
+        "batched_transpose": (2, 2, 2, 0, 0),
     }
+    small = {"strided_bf16": (64, 64, 64), "batched_transpose": (2, 64, 64)}
     for name, f in W.FULL.items():
-        c, _ = T.command_from_spec(f(1024) if name != "strided_bf16" else f(64, 64, 64))
+        c, _ = T.command_from_spec(f(*small[name]) if name in small else f(1024))
         info, words = c.lower()
         got = (info["n_live_ops"], info["n_loads"], info["n_slots"], info["tier"], info["n_moves"])
         assert got == expect[name], (name, info)
@@ -196,6 +198,8 @@ def test_plans_of_the_workloads():
     assert p["bytes"] == 256 * 192 * 6
     p = _plan(W.wide_dag(1 << 20))
     assert p["path"] == "contig" and p["bytes"] == 30 << 20
+    p = _plan(W.batched_transpose(4, 128, 64))
+    assert p["path"] == "tile2d" and p["merged_sizes"] == [4, 128, 64] and p["n_transposed"] == 1
 
 
 def test_dims_merge_to_contiguous():

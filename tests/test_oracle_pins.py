@@ -483,3 +483,13 @@ def test_planted_mistakes_are_caught():
         b2["out"] = specutil.sentinel_array("f32", 2048)
         oracle.OracleCommand(v, b2).eval_range()
         assert not (specutil.bits(b2["out"]) == specutil.bits(ref)).all()
+
+
+def test_workload_batched_transpose_matches_numpy():
+    spec = workloads.batched_transpose(3, 40, 24)
+    bufs = specutil.host_buffers(spec)
+    oracle.OracleCommand(spec, bufs).eval_range()
+    A = bufs["A"].reshape(3, 24, 40).transpose(0, 2, 1)
+    B = bufs["B"].reshape(3, 40, 24)
+    want = np.ascontiguousarray(A * B - A).ravel()
+    assert (specutil.bits(bufs["out"]) == specutil.bits(want)).all()
