@@ -495,7 +495,8 @@ def run_ours(args):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
-                      "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32"}[args.workload],
+                      "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32",
+                      "div_clamp_i32": "f32 (int32 out)"}[args.workload],
             "data": "synthetic (seeded SplitMix64 inputs; no dataset)",
             "config": {"workload": f"{args.workload}: {spec_summary(spec)}", "elements": wl.elements,
                        "bytes_per_step": wl.bytes, "path": wl.plan["path"],

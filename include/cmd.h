@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define CMD_ABI_VERSION 1
+#define CMD_ABI_VERSION 2
 
 /* limits */
 #define CMD_MAX_RANK 4      /* logical dims of a tensor view */
@@ -78,8 +78,34 @@ typedef enum cmd_status {
 
 typedef enum cmd_dtype { CMD_F32 = 0, CMD_F16 = 1, CMD_BF16 = 2, CMD_I32 = 3 } cmd_dtype;
 
-/* Elementwise operations of a T_Execute block. */
-typedef enum cmd_eop { CMD_E_ADD = 0, CMD_E_SUB = 1, CMD_E_MUL = 2, CMD_E_NEG = 3 } cmd_eop;
+/* Elementwise operations of a T_Execute block (rocRoller, "Design Overview",
+ * section "Operations": E_ operations such as Add and Subtract on vectors or
+ * scalars; DIV .. TO_I32 follow the operations an Expression supports,
+ * section "Expression", whose special cases the pages leave open and which
+ * are fixed here). Float ops round once to nearest even; int ops wrap modulo
+ * 2^32.
+ *   ADD, SUB, MUL, NEG  as their names say; NEG flips a float's sign bit.
+ *   DIV     float: IEEE division. int: truncates toward zero; x / 0 = -1 and
+ *           INT_MIN / -1 = INT_MIN (so that every input has one result).
+ *   MIN/MAX float: IEEE 754-2019 minimumNumber / maximumNumber (a NaN loses to
+ *           a number; -0 is less than +0). int: signed.
+ *   ABS     float: sign bit cleared. int: |x| modulo 2^32 (|INT_MIN| = INT_MIN).
+ *   TO_F32  int -> float, rounded to nearest even; a float is unchanged.
+ *   TO_I32  float -> int, truncated toward zero and saturated to the int32
+ *           range, NaN -> 0; an int is unchanged.
+ * NEG, ABS, TO_F32 and TO_I32 take one operand (b is ignored). */
+typedef enum cmd_eop {
+  CMD_E_ADD = 0,
+  CMD_E_SUB = 1,
+  CMD_E_MUL = 2,
+  CMD_E_NEG = 3,
+  CMD_E_DIV = 4,
+  CMD_E_MIN = 5,
+  CMD_E_MAX = 6,
+  CMD_E_ABS = 7,
+  CMD_E_TO_F32 = 8,
+  CMD_E_TO_I32 = 9
+} cmd_eop;
 
 typedef int32_t cmd_tag;
 typedef struct cmd_command* cmd_command_t;
@@ -89,7 +115,7 @@ typedef struct cmd_kernel* cmd_kernel_t;
  * block's i-th op (i smaller than the referring op's index). */
 #define CMD_LOCAL(i) ((cmd_tag)(-1 - (i)))
 
-/* One E op: result = a (op) b; for CMD_E_NEG, result = -a and b is ignored.
+/* One E op: result = a (op) b, or op(a) for the one-operand ops (b ignored).
  * a and b are tags of earlier Load_Tensor, Load_Scalar or E results, or
  * CMD_LOCAL(i). */
 typedef struct cmd_xop {
@@ -137,6 +163,8 @@ typedef struct cmd_program_info {
   int32_t n_words;      /* program words, including the end marker */
   int32_t tier;         /* executor family: 0 = 2 slots, 1 = 4, 2 = 8, 3 = 32 */
   int32_t n_moves;      /* copies the two-address form needed */
+  int32_t divides;      /* 1 if a division op is live: the program runs the
+                           executors' variant with division code, 0 otherwise */
 } cmd_program_info;
 
 /* Which executor a launch would use (cmd_plan_launch). */
@@ -178,8 +206,9 @@ cmd_status cmd_add_load_tensor(cmd_command_t cmd, cmd_dtype dtype, int32_t rank,
 cmd_status cmd_add_load_scalar(cmd_command_t cmd, cmd_dtype dtype, cmd_tag* out);
 
 /* One T_Execute block of n E ops (1..CMD_MAX_TAGS). Op i receives tag
- * first + i, written to out_tags[i] when out_tags is non-NULL. Operands of one
- * op must both be float-valued or both int-valued. On error nothing is added. */
+ * first + i, written to out_tags[i] when out_tags is non-NULL. Operands of a
+ * two-operand op must both be float-valued or both int-valued; TO_F32 makes a
+ * float value and TO_I32 an int value. On error nothing is added. */
 cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd_tag* out_tags);
 
 /* Store_Tensor of tag src as element type dtype, logical rank `rank`. A float

@@ -9,8 +9,9 @@ A workload ("spec") is a dict:
               ``("load", name, dtype)``            Load_Tensor
               ``("scalar", name, dtype, value)``   Load_Scalar
               ``("exec", [(eop, name, a, b), ...])`` one T_Execute block;
-                                                   eop in add/sub/mul/neg,
-                                                   b is None for neg
+                                                   eop in add/sub/mul/div/
+                                                   min/max (binary) or neg/
+                                                   abs/to_f32/to_i32 (b None)
               ``("store", name, src, dtype)``      Store_Tensor
 ``views``     per load/store name: ``strides`` (elements) and ``alloc``
               (elements in the physical buffer)
@@ -156,6 +157,25 @@ def batched_transpose(b: int = 64, m: int = 1024, n: int = 1024) -> dict:
     )
 
 
+def div_clamp_i32(n: int = 1 << 27) -> dict:
+    """q = to_i32(min(max(x / s, lo), hi)) and r = q / 3 (int32, truncating):
+    x normal(0, 1), s = 0.0074 (so the clamp at lo = -128 / hi = 127 is
+    active for about a third of the elements), seed 6. Float division, max,
+    min, the float-to-int conversion and int division in one pass; stores q
+    and r as int32."""
+    st, al = _dense((n,))
+    return dict(
+        name="div_clamp_i32", seed=6, sizes=(n,),
+        ops=[("load", "x", "f32"), ("scalar", "s", "f32", 0.0074), ("scalar", "lo", "f32", -128.0),
+             ("scalar", "hi", "f32", 127.0), ("scalar", "k", "i32", 3),
+             ("exec", [("div", "y", "x", "s"), ("max", "c0", "y", "lo"), ("min", "c", "c0", "hi"),
+                       ("to_i32", "q", "c", None), ("div", "r", "q", "k")]),
+             ("store", "oq", "q", "i32"), ("store", "or", "r", "i32")],
+        views={k: dict(strides=st, alloc=al) for k in ("x", "oq", "or")},
+        inputs={"x": ("normal_f32", 0.0, 0.0)},
+    )
+
+
 # Full-size workloads, in the order they are listed for this path.
 FULL = {
     "add_f32": add_f32,
@@ -164,6 +184,7 @@ FULL = {
     "strided_bf16": strided_bf16,
     "wide_dag": wide_dag,
     "batched_transpose": batched_transpose,
+    "div_clamp_i32": div_clamp_i32,
 }
 
 

@@ -28,7 +28,8 @@ _lock = threading.Lock()
 MAX_RANK = 4
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 NP_DTYPE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i32": np.int32}
-KINDS = {"load": 0, "scalar": 1, "add": 2, "sub": 3, "mul": 4, "neg": 5, "store": 6}
+KINDS = {"load": 0, "scalar": 1, "add": 2, "sub": 3, "mul": 4, "neg": 5, "store": 6,
+         "div": 7, "min": 8, "max": 9, "abs": 10, "to_f32": 11, "to_i32": 12}
 
 
 class _Op(ctypes.Structure):
@@ -69,11 +70,12 @@ def lib():
             L.orc_eval_points.argtypes = [ctypes.POINTER(_Command), ctypes.c_void_p,
                                           ctypes.c_int64, ctypes.c_void_p]
             L.orc_eval_points.restype = ctypes.c_int
-            for name in ("orc_fadd", "orc_fsub", "orc_fmul", "orc_iadd", "orc_isub", "orc_imul"):
+            for name in ("orc_fadd", "orc_fsub", "orc_fmul", "orc_iadd", "orc_isub", "orc_imul",
+                         "orc_fdiv", "orc_idiv", "orc_fmin", "orc_fmax", "orc_imin", "orc_imax"):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
                 f.restype = ctypes.c_uint32
-            for name in ("orc_fneg", "orc_ineg"):
+            for name in ("orc_fneg", "orc_ineg", "orc_fabs", "orc_iabs", "orc_i2f", "orc_f2i"):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.c_uint32]
                 f.restype = ctypes.c_uint32

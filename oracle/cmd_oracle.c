@@ -58,6 +58,57 @@ uint32_t orc_imul(uint32_t x, uint32_t y) {
 }
 uint32_t orc_ineg(uint32_t x) { return (uint32_t)(0u - x); }
 
+/* Division: the binary64 quotient rounded once more to binary32 (innocuous
+ * for division as for + - x: Figueroa's condition 53 >= 2*24 + 2 holds). */
+uint32_t orc_fdiv(uint32_t x, uint32_t y) {
+  double r = (double)as_float(x) / (double)as_float(y);
+  return as_bits((float)r);
+}
+
+uint32_t orc_idiv(uint32_t x, uint32_t y) {
+  int32_t a = (int32_t)x, b = (int32_t)y;
+  if (b == 0) return 0xffffffffu;                 /* x / 0 = -1 */
+  if (a == INT32_MIN && b == -1) return x;        /* INT_MIN / -1 = INT_MIN */
+  return (uint32_t)(a / b);                       /* C truncates toward zero */
+}
+
+/* minimumNumber / maximumNumber (IEEE 754-2019 section 9.6). */
+uint32_t orc_fmin(uint32_t x, uint32_t y) {
+  float a = as_float(x), b = as_float(y);
+  if (isnan(a)) return y;
+  if (isnan(b)) return x;
+  if (a < b) return x;
+  if (b < a) return y;
+  return signbit(a) ? x : y; /* equal: for zeros the negative one is smaller */
+}
+
+uint32_t orc_fmax(uint32_t x, uint32_t y) {
+  float a = as_float(x), b = as_float(y);
+  if (isnan(a)) return y;
+  if (isnan(b)) return x;
+  if (a > b) return x;
+  if (b > a) return y;
+  return signbit(a) ? y : x;
+}
+
+uint32_t orc_imin(uint32_t x, uint32_t y) { return (int32_t)x < (int32_t)y ? x : y; }
+uint32_t orc_imax(uint32_t x, uint32_t y) { return (int32_t)x > (int32_t)y ? x : y; }
+
+uint32_t orc_fabs(uint32_t x) { return x & 0x7fffffffu; }
+uint32_t orc_iabs(uint32_t x) { return ((int32_t)x < 0) ? (uint32_t)(0u - x) : x; }
+
+/* int32 -> binary32: the exact value in binary64, rounded once. */
+uint32_t orc_i2f(uint32_t x) { return as_bits((float)(double)(int32_t)x); }
+
+/* binary32 -> int32: truncate toward zero, saturate, NaN -> 0. */
+uint32_t orc_f2i(uint32_t x) {
+  double v = (double)as_float(x);
+  if (isnan(v)) return 0u;
+  if (v >= 2147483648.0) return 0x7fffffffu;
+  if (v <= -2147483649.0) return 0x80000000u;
+  return (uint32_t)(int32_t)trunc(v);
+}
+
 /* ---- conversions ------------------------------------------------------- */
 
 /* Round a non-negative finite value v (exactly representable in binary64)
@@ -165,10 +216,21 @@ static int classify(const orc_command* c, int* cls) {
         if (cls[op->a] != cls[op->b]) return ORC_ETYPE;
         cls[t] = cls[op->a];
         break;
+      case ORC_DIV:
+      case ORC_MIN:
+      case ORC_MAX:
+        if (op->a < 0 || op->a >= t || op->b < 0 || op->b >= t) return ORC_EBAD;
+        if (c->ops[op->a].kind == ORC_STORE || c->ops[op->b].kind == ORC_STORE) return ORC_EBAD;
+        if (cls[op->a] != cls[op->b]) return ORC_ETYPE;
+        cls[t] = cls[op->a];
+        break;
       case ORC_NEG:
+      case ORC_ABS:
+      case ORC_TO_F32:
+      case ORC_TO_I32:
         if (op->a < 0 || op->a >= t) return ORC_EBAD;
         if (c->ops[op->a].kind == ORC_STORE) return ORC_EBAD;
-        cls[t] = cls[op->a];
+        cls[t] = op->kind == ORC_TO_F32 ? CLS_FLOAT : op->kind == ORC_TO_I32 ? CLS_INT : cls[op->a];
         break;
       case ORC_STORE:
         if (op->a < 0 || op->a >= t) return ORC_EBAD;
@@ -253,6 +315,27 @@ static void eval_one(const orc_command* c, const int* cls, uint32_t* val,
         break;
       case ORC_NEG:
         val[t] = cls[t] == CLS_INT ? orc_ineg(val[op->a]) : orc_fneg(val[op->a]);
+        break;
+      case ORC_DIV:
+        val[t] = cls[t] == CLS_INT ? orc_idiv(val[op->a], val[op->b])
+                                   : orc_fdiv(val[op->a], val[op->b]);
+        break;
+      case ORC_MIN:
+        val[t] = cls[t] == CLS_INT ? orc_imin(val[op->a], val[op->b])
+                                   : orc_fmin(val[op->a], val[op->b]);
+        break;
+      case ORC_MAX:
+        val[t] = cls[t] == CLS_INT ? orc_imax(val[op->a], val[op->b])
+                                   : orc_fmax(val[op->a], val[op->b]);
+        break;
+      case ORC_ABS:
+        val[t] = cls[t] == CLS_INT ? orc_iabs(val[op->a]) : orc_fabs(val[op->a]);
+        break;
+      case ORC_TO_F32:
+        val[t] = cls[op->a] == CLS_INT ? orc_i2f(val[op->a]) : val[op->a];
+        break;
+      case ORC_TO_I32:
+        val[t] = cls[op->a] == CLS_INT ? val[op->a] : orc_f2i(val[op->a]);
         break;
       case ORC_STORE: {
         size_t es = elem_size(op->dtype);

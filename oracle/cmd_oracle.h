@@ -33,6 +33,18 @@
  *   - E_Neg flips the sign bit of a float and is 0 - x for an int;
  *   - half and bfloat16 inputs widen exactly to binary32; stores round once,
  *     to nearest even, overflow to infinity; NaN payloads are not pinned.
+ *   - E_Div: binary32 division rounded once to nearest even (IEEE 754 6.3 /
+ *     7.3 for zeros and infinities); int32 division truncates toward zero,
+ *     x / 0 = -1 and INT_MIN / -1 = INT_MIN (the convention the RISC-V ISA
+ *     manual fixes for its DIV instruction, taken here so that every input
+ *     has one result).
+ *   - E_Min / E_Max: IEEE 754-2019 minimumNumber / maximumNumber: a NaN
+ *     operand loses to a number, and -0 counts as less than +0; int32 signed.
+ *   - E_Abs: the sign bit cleared for a float; |x| modulo 2^32 for an int
+ *     (|INT_MIN| = INT_MIN).
+ *   - E_ToF32: an int converts with one round to nearest even; a float is
+ *     unchanged. E_ToI32: a float truncates toward zero and saturates to the
+ *     int32 range, NaN gives 0; an int is unchanged.
  */
 #ifndef CMD_ORACLE_H
 #define CMD_ORACLE_H
@@ -54,7 +66,13 @@ enum {
   ORC_SUB = 3,
   ORC_MUL = 4,
   ORC_NEG = 5,
-  ORC_STORE = 6
+  ORC_STORE = 6,
+  ORC_DIV = 7,
+  ORC_MIN = 8,
+  ORC_MAX = 9,
+  ORC_ABS = 10,
+  ORC_TO_F32 = 11,
+  ORC_TO_I32 = 12
 };
 
 /* status codes */
@@ -99,6 +117,16 @@ uint32_t orc_iadd(uint32_t x, uint32_t y);
 uint32_t orc_isub(uint32_t x, uint32_t y);
 uint32_t orc_imul(uint32_t x, uint32_t y);
 uint32_t orc_ineg(uint32_t x);
+uint32_t orc_fdiv(uint32_t x, uint32_t y);
+uint32_t orc_idiv(uint32_t x, uint32_t y);
+uint32_t orc_fmin(uint32_t x, uint32_t y);
+uint32_t orc_fmax(uint32_t x, uint32_t y);
+uint32_t orc_imin(uint32_t x, uint32_t y);
+uint32_t orc_imax(uint32_t x, uint32_t y);
+uint32_t orc_fabs(uint32_t x);
+uint32_t orc_iabs(uint32_t x);
+uint32_t orc_i2f(uint32_t x);
+uint32_t orc_f2i(uint32_t x);
 uint16_t orc_f32_to_f16(uint32_t x);
 uint16_t orc_f32_to_bf16(uint32_t x);
 uint32_t orc_f16_to_f32(uint16_t h);

@@ -24,7 +24,8 @@ from . import _build
 CMD_MAX_RANK = 4
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
-EOPS = {"add": 0, "sub": 1, "mul": 2, "neg": 3}
+EOPS = {"add": 0, "sub": 1, "mul": 2, "neg": 3, "div": 4, "min": 5, "max": 6, "abs": 7, "to_f32": 8,
+        "to_i32": 9}
 PATHS = {0: "none", 1: "contig", 2: "tile2d", 3: "generic"}
 STATUS = {0: "CMD_OK", 1: "CMD_ERR_NULL", 2: "CMD_ERR_BAD_TAG", 3: "CMD_ERR_TYPE", 4: "CMD_ERR_SHAPE",
           5: "CMD_ERR_ALIAS", 6: "CMD_ERR_ALIGN", 7: "CMD_ERR_STATE", 8: "CMD_ERR_LIMIT", 9: "CMD_ERR_CUDA",
@@ -67,7 +68,7 @@ class cmd_runtime_args(ctypes.Structure):
 
 class cmd_program_info(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int32) for k in ("n_live_ops", "n_loads", "n_scalars", "n_stores", "n_slots",
-                                              "n_words", "tier", "n_moves")]
+                                              "n_words", "tier", "n_moves", "divides")]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -1,7 +1,10 @@
 """Build the CUDA executor library (libcmdexec.so) in-tree.
 
-The three executor translation units and the host C ABI compile in parallel
-for sm_103a only, then link into one shared library next to this file.
+Each executor source compiles once per tier and division variant
+(CMDX_TIER, CMDX_DIV; the tile executor also per view variant, CMDX_ND):
+the per-tier interpreters are large, so this spreads them over parallel
+compiler processes. With the host sources, all compile in parallel for
+sm_103a only, then link into one shared library next to this file.
 Float arithmetic is compiled with contraction off (-fmad=false) and without
 fast-math, so denormals are kept and every add/sub/mul rounds once.
 """
@@ -19,9 +22,26 @@ OUT_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libcmdexec.so")
 
-CU_SOURCES = ["exec_contig.cu", "exec_tile2d.cu", "exec_generic.cu", "static_scratch.cu"]
-CPP_SOURCES = ["cmd_api.cpp"]
-HEADERS = ["cmd_internal.h", "exec_common.cuh", "interp_asm.cuh", "gen_interp.py"]
+# (source, the defines of each object built from it), longest compiles first
+def _objs(tiers, nds=(None,)):
+    out = []
+    for t in tiers:
+        for div in (1, 0):
+            for nd in nds:
+                d = dict(CMDX_TIER=t)
+                if nd is not None:
+                    d["CMDX_ND"] = nd
+                d["CMDX_DIV"] = div
+                out.append(d)
+    return out
+
+
+CU_SOURCES = [("exec_tile2d.cu", _objs((2,), (0, 1))), ("exec_generic.cu", _objs((2,))),
+              ("exec_contig.cu", _objs((2,))), ("exec_tile2d.cu", _objs((1, 0), (0, 1))),
+              ("exec_generic.cu", _objs((3, 1, 0))), ("exec_contig.cu", _objs((3, 1, 0))),
+              ("static_scratch.cu", [{}])]
+CPP_SOURCES = ["cmd_api.cpp", "exec_host.cpp"]
+HEADERS = ["cmd_internal.h", "exec_common.cuh", "exec_tile2d.h", "interp_asm.cuh", "gen_interp.py"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +56,7 @@ def cuda_home() -> str:
 
 
 def _sources():
-    return ([os.path.join(CSRC, s) for s in CU_SOURCES + CPP_SOURCES + HEADERS]
+    return ([os.path.join(CSRC, s) for s in sorted({c for c, _ in CU_SOURCES}) + CPP_SOURCES + HEADERS]
             + [os.path.join(ROOT, "include", "cmd.h"), os.path.abspath(__file__)])
 
 
@@ -61,13 +81,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = os.path.join(home, "bin", "nvcc")
     inc = ["-I" + os.path.join(home, "include"), "-I" + os.path.join(ROOT, "include")]
     jobs = []
-    for s in CU_SOURCES:
-        obj = os.path.join(OBJ_DIR, s + ".o")
-        log = os.path.join(OBJ_DIR, s + ".ptxas.txt")
-        cmd = ([nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-prec-div=true",
-                                "-prec-sqrt=true", "-ftz=false", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
-                                "-c", os.path.join(CSRC, s), "-o", obj] + inc)
-        jobs.append((cmd, obj, log))
+    for s, variants in CU_SOURCES:
+        for defs in variants:
+            stem = s + "".join(f".{k[5:].lower()}{v}" for k, v in defs.items())
+            obj = os.path.join(OBJ_DIR, stem + ".o")
+            log = os.path.join(OBJ_DIR, stem + ".ptxas.txt")
+            cmd = ([nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-prec-div=true",
+                                    "-prec-sqrt=true", "-ftz=false", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
+                                    "-c", os.path.join(CSRC, s), "-o", obj] + inc
+                   + [f"-D{k}={v}" for k, v in defs.items()])
+            jobs.append((cmd, obj, log))
     for s in CPP_SOURCES:
         obj = os.path.join(OBJ_DIR, s + ".o")
         cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-Wno-unused-parameter",
@@ -86,7 +109,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(run, jobs))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     link = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart_static", "-lrt", "-lpthread", "-ldl"]

@@ -54,6 +54,13 @@ const char* dtype_name(int dt) {
 
 int elem_size(int dt) { return (dt == CMD_F16 || dt == CMD_BF16) ? 2 : 4; }
 
+// E ops that take one operand.
+bool is_unary(int eop) { return eop == CMD_E_NEG || eop == CMD_E_ABS || eop == CMD_E_TO_F32 || eop == CMD_E_TO_I32; }
+// E ops whose two operands commute exactly (IEEE 754 and modulo 2^32).
+bool is_commutative(int eop) {
+  return eop == CMD_E_ADD || eop == CMD_E_MUL || eop == CMD_E_MIN || eop == CMD_E_MAX;
+}
+
 bool valid_dtype(int dt) { return dt >= CMD_F32 && dt <= CMD_I32; }
 
 // One instruction of the two-address program, before encoding.
@@ -75,6 +82,7 @@ struct Program {
   int n_slots = 0;
   int n_moves = 0;
   int tier = cmdx::kTier4;
+  bool divides = false;  // has a division op: runs the executors' division variant
 };
 
 }  // namespace
@@ -158,8 +166,8 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     rep[t] = t;
     if (op.kind != kExec) continue;
     int a = rep[op.a];
-    int b = op.eop == CMD_E_NEG ? -1 : rep[op.b];
-    if ((op.eop == CMD_E_ADD || op.eop == CMD_E_MUL) && b < a) std::swap(a, b);
+    int b = is_unary(op.eop) ? -1 : rep[op.b];
+    if (is_commutative(op.eop) && b < a) std::swap(a, b);
     auto key = std::make_tuple(op.eop, a, b);
     auto it = seen.find(key);
     if (it != seen.end())
@@ -176,7 +184,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
       live[rep[op.a]] = 1;
     } else if (op.kind == kExec && live[t] && rep[t] == t) {
       live[rep[op.a]] = 1;
-      if (op.eop != CMD_E_NEG) live[rep[op.b]] = 1;
+      if (!is_unary(op.eop)) live[rep[op.b]] = 1;
     }
   }
   std::vector<int> slot_of(n, -1), sidx(n, -1);
@@ -232,7 +240,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
       last_use[rep[op.a]] = i;
     } else {
       last_use[rep[op.a]] = i;
-      if (op.eop != CMD_E_NEG) last_use[rep[op.b]] = i;
+      if (!is_unary(op.eop)) last_use[rep[op.b]] = i;
     }
   }
   // slots
@@ -283,30 +291,45 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     }
     const bool ints = op.cls == kInt;
     const int a = rep[op.a];
-    if (op.eop == CMD_E_NEG) {
-      const int neg = ints ? cmdx::kINeg : cmdx::kFNeg;
+    if (is_unary(op.eop)) {
+      const bool a_int = ops[a].cls == kInt;
+      int uop;
+      if (op.eop == CMD_E_NEG) uop = ints ? cmdx::kINeg : cmdx::kFNeg;
+      else if (op.eop == CMD_E_ABS) uop = ints ? cmdx::kIAbs : cmdx::kFAbs;
+      else if (op.eop == CMD_E_TO_F32) uop = a_int ? cmdx::kI2F : cmdx::kMov;
+      else uop = a_int ? cmdx::kMov : cmdx::kF2I;
       int d;
       if (is_scalar(a)) {
         d = alloc();
         emit(Instr::kMovS, cmdx::kMov, d, 0, sidx[a]);
-        emit(Instr::kUn, neg, d, d, 0);
+        if (uop != cmdx::kMov) emit(Instr::kUn, uop, d, d, 0);
       } else if (last_use[a] == i) {
         d = slot_of[a];
-        emit(Instr::kUn, neg, d, d, 0);
+        if (uop != cmdx::kMov) emit(Instr::kUn, uop, d, d, 0);
       } else {
         d = alloc();
-        emit(Instr::kUn, neg, d, slot_of[a], 0);
+        emit(Instr::kUn, uop, d, slot_of[a], 0);
       }
       slot_of[t] = d;
       continue;
     }
     const int b = rep[op.b];
-    int bop, rsub;
-    if (op.eop == CMD_E_ADD) bop = ints ? cmdx::kIAdd : cmdx::kFAdd;
-    else if (op.eop == CMD_E_SUB) bop = ints ? cmdx::kISub : cmdx::kFSub;
-    else bop = ints ? cmdx::kIMul : cmdx::kFMul;
-    rsub = ints ? cmdx::kIRsub : cmdx::kFRsub;
-    const bool commut = op.eop != CMD_E_SUB;
+    int bop, rsub;  // rsub: the reversed form, d = x (op) d
+    switch (op.eop) {
+      case CMD_E_ADD: bop = rsub = ints ? cmdx::kIAdd : cmdx::kFAdd; break;
+      case CMD_E_SUB:
+        bop = ints ? cmdx::kISub : cmdx::kFSub;
+        rsub = ints ? cmdx::kIRsub : cmdx::kFRsub;
+        break;
+      case CMD_E_MUL: bop = rsub = ints ? cmdx::kIMul : cmdx::kFMul; break;
+      case CMD_E_DIV:
+        bop = ints ? cmdx::kIDiv : cmdx::kFDiv;
+        rsub = ints ? cmdx::kIRdiv : cmdx::kFRdiv;
+        break;
+      case CMD_E_MIN: bop = rsub = ints ? cmdx::kIMin : cmdx::kFMin; break;
+      default: bop = rsub = ints ? cmdx::kIMax : cmdx::kFMax; break;
+    }
+    const bool commut = is_commutative(op.eop);
     const bool sa = is_scalar(a), sb = is_scalar(b);
     const bool die_a = !sa && last_use[a] == i;
     const bool die_b = !sb && last_use[b] == i;
@@ -349,6 +372,10 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
 
   // encode
   P->words.clear();
+  P->divides = false;
+  for (const Instr& in : P->code)
+    if ((in.kind == Instr::kBin || in.kind == Instr::kBinS) && in.op >= cmdx::kFDiv && in.op <= cmdx::kIRdiv)
+      P->divides = true;
   const int S = cmdx::tier_slots(P->tier);
   for (const Instr& in : P->code) {
     uint32_t w = 0;
@@ -387,6 +414,7 @@ void fill_info(const Program& P, cmd_program_info* info) {
   info->n_words = (int32_t)P.words.size();
   info->tier = P.tier;
   info->n_moves = P.n_moves;
+  info->divides = P.divides ? 1 : 0;
 }
 
 // ---- launch validation and planning ----------------------------------------
@@ -703,13 +731,6 @@ cmdx::FastDiv make_fastdiv(int64_t d) {
   return f;
 }
 
-cudaError_t upload_all(int slot, const std::vector<uint32_t>& w) {
-  cudaError_t e = cmdx::contig_upload(slot, w.data(), (int)w.size());
-  if (e == cudaSuccess) e = cmdx::tile2d_upload(slot, w.data(), (int)w.size());
-  if (e == cudaSuccess) e = cmdx::generic_upload(slot, w.data(), (int)w.size());
-  return e;
-}
-
 cmd_status cuda_fail(cudaError_t e, const char* what) {
   return fail(CMD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
 }
@@ -757,7 +778,7 @@ cmd_status compile_with_static_word(cmd_command_t cmd, cmd_kernel_t* out, uint32
                                    " error words; program slot " + std::to_string(slot) + " is beyond it");
   }
   if (reused) e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = upload_all(slot, k->prog.words);
+  if (e == cudaSuccess) e = cmdx::upload_program(k->prog.tier, k->prog.divides, slot, k->prog.words.data(), (int)k->prog.words.size());
   // the word keeps whatever the previous kernel in this slot left: clear it
   if (e == cudaSuccess) e = cudaMemset(words + slot, 0, sizeof(uint32_t));
   if (e != cudaSuccess) {
@@ -876,15 +897,15 @@ cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd
   auto cls_of = [&](int t) { return t < base ? cmd->ops[t].cls : block[t - base].cls; };
   for (int i = 0; i < n; ++i) {
     const cmd_xop& x = ops[i];
-    if (x.op < CMD_E_ADD || x.op > CMD_E_NEG) return fail(CMD_ERR_ARG, "unknown E op " + std::to_string(x.op));
+    if (x.op < CMD_E_ADD || x.op > CMD_E_TO_I32) return fail(CMD_ERR_ARG, "unknown E op " + std::to_string(x.op));
     Op op{kExec, 0, 0, x.op, -1, -1, kFloat};
     if (cmd_status s = resolve(x.a, i, &op.a)) return s;
-    if (x.op != CMD_E_NEG) {
+    if (!is_unary(x.op)) {
       if (cmd_status s = resolve(x.b, i, &op.b)) return s;
       if (cls_of(op.a) != cls_of(op.b))
         return fail(CMD_ERR_TYPE, "E op " + std::to_string(i) + " mixes an int value and a float value");
     }
-    op.cls = cls_of(op.a);
+    op.cls = x.op == CMD_E_TO_F32 ? kFloat : x.op == CMD_E_TO_I32 ? kInt : cls_of(op.a);
     block.push_back(op);
   }
   try {
@@ -966,7 +987,7 @@ cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out) {
       return cuda_fail(e, "cudaDeviceSynchronize before reusing a program slot");
     }
   }
-  e = upload_all(slot, k->prog.words);
+  e = cmdx::upload_program(k->prog.tier, k->prog.divides, slot, k->prog.words.data(), (int)k->prog.words.size());
   if (e == cudaSuccess) e = cudaMalloc(&k->err, 256);
   if (e == cudaSuccess) e = cudaMemset(k->err, 0, 256);
   if (e != cudaSuccess) {
@@ -1022,8 +1043,9 @@ cmd_status cmd_kernel_info(cmd_kernel_t k, cmd_program_info* info) {
 
 cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* needed) {
   if (!k) return fail(CMD_ERR_NULL, "k is NULL");
-  static const char* bin[] = {"fadd", "fsub", "frsub", "fmul", "iadd", "isub", "irsub", "imul"};
-  static const char* un[] = {"fneg", "ineg", "mov"};
+  static const char* bin[] = {"fadd", "fsub", "frsub", "fmul", "iadd", "isub", "irsub", "imul",
+                              "fdiv", "frdiv", "idiv", "irdiv", "fmin", "fmax", "imin", "imax"};
+  static const char* un[] = {"fneg", "ineg", "mov", "fabs", "iabs", "i2f", "f2i"};
   std::string s;
   const Program& P = k->prog;
   char line[160];
@@ -1118,7 +1140,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n = n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
-      e = cmdx::contig_launch(P.tier, p, stream);
+      e = cmdx::contig_launch(P.tier, P.divides, p, stream);
     }
     if (e == cudaSuccess && pl.n > n_main) {
       cmdx::GenericParams p;
@@ -1138,7 +1160,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n = pl.n - n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
-      e = cmdx::generic_launch(P.tier, p, stream);
+      e = cmdx::generic_launch(P.tier, P.divides, p, stream);
     }
   } else if (pl.path == CMD_PATH_TILE2D) {
     cmdx::Tile2dLaunch L;
@@ -1173,7 +1195,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     L.err = k->err;
     L.debug = (uint32_t)g_force_timeout.load();
     L.timeout_ns = g_wait_limit_ns.load();
-    e = cmdx::tile2d_launch(P.tier, L, stream);
+    e = cmdx::tile2d_launch(P.tier, P.divides, L, stream);
   } else {
     cmdx::GenericParams p;
     std::memset(&p, 0, sizeof p);
@@ -1191,7 +1213,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     p.n = pl.n;
     p.prog = (uint32_t)k->slot;
     p.n_loads = (uint32_t)pl.loads.size();
-    e = cmdx::generic_launch(P.tier, p, stream);
+    e = cmdx::generic_launch(P.tier, P.divides, p, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return CMD_OK;

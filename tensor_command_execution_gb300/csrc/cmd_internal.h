@@ -41,41 +41,45 @@ CMDX_HD constexpr int tier_min_blocks(int tier) { return tier == kTier32 ? 2 : 3
 constexpr int kMaxProgramWords = kMaxWords - 1;
 
 // Two-address binary ops: d = d (op) x, where x is a slot or a scalar.
-// RSUB is the reversed subtraction d = x - d.
+// The R variants reverse the operands: d = x (op) d.
 enum BinOp {
   kFAdd = 0, kFSub = 1, kFRsub = 2, kFMul = 3,
   kIAdd = 4, kISub = 5, kIRsub = 6, kIMul = 7,
-  kNumBin = 8
+  kFDiv = 8, kFRdiv = 9, kIDiv = 10, kIRdiv = 11,
+  kFMin = 12, kFMax = 13, kIMin = 14, kIMax = 15,
+  kNumBin = 16
 };
 // Unary ops: d = f(x).
-enum UnOp { kFNeg = 0, kINeg = 1, kMov = 2, kNumUn = 3 };
+enum UnOp { kFNeg = 0, kINeg = 1, kMov = 2, kFAbs = 3, kIAbs = 4, kI2F = 5, kF2I = 6, kNumUn = 7 };
 // Store element types, as numbered in cmd.h's cmd_dtype.
 enum StoreType { kStF32 = 0, kStF16 = 1, kStBF16 = 2, kStI32 = 3, kNumSt = 4 };
 
-// ---- fused encoding (tiers 4 and 8) ----------------------------------------
+// ---- fused encoding (tiers 2, 4 and 8) ----------------------------------------
 // word = case | aux << 16; aux is a scalar index (scalar ops) or an output
-// index (stores). Case layout, for S slots:
-//   [0, 8 S^2)            binary op b, dst d, src slot s : b S^2 + d S + s
-//   [8 S^2, 11 S^2)       unary op u, dst d, src slot s  : 8 S^2 + u S^2 + d S + s
-//   [11 S^2, +8 S)        binary op b with scalar src, dst d : 11 S^2 + b S + d
-//   [11 S^2 + 8 S, +S)    broadcast scalar into d
-//   [11 S^2 + 9 S, +4 S)  store slot s as type t : 11 S^2 + 9 S + t S + s
-//   11 S^2 + 13 S         end
+// index (stores). Case layout, for S slots (B = kNumBin, U = kNumUn):
+//   [0, B S^2)                binary op b, dst d, src slot s : b S^2 + d S + s
+//   [B S^2, (B+U) S^2)        unary op u, dst d, src slot s  : B S^2 + u S^2 + d S + s
+//   [(B+U) S^2, +B S)         binary op b with scalar src, dst d
+//   then S cases              broadcast scalar into d
+//   then 4 S cases            store slot s as type t
+//   then                      end
 CMDX_HD constexpr uint32_t fz_bin(int S, int b, int d, int s) { return uint32_t(b * S * S + d * S + s); }
 CMDX_HD constexpr uint32_t fz_un(int S, int u, int d, int s) { return uint32_t(kNumBin * S * S + u * S * S + d * S + s); }
-CMDX_HD constexpr uint32_t fz_bin_scalar(int S, int b, int d) { return uint32_t(11 * S * S + b * S + d); }
-CMDX_HD constexpr uint32_t fz_movs(int S, int d) { return uint32_t(11 * S * S + 8 * S + d); }
-CMDX_HD constexpr uint32_t fz_store(int S, int t, int s) { return uint32_t(11 * S * S + 9 * S + t * S + s); }
-CMDX_HD constexpr uint32_t fz_end(int S) { return uint32_t(11 * S * S + 13 * S); }
+CMDX_HD constexpr uint32_t fz_bin_scalar(int S, int b, int d) { return uint32_t((kNumBin + kNumUn) * S * S + b * S + d); }
+CMDX_HD constexpr uint32_t fz_movs(int S, int d) { return uint32_t((kNumBin + kNumUn) * S * S + kNumBin * S + d); }
+CMDX_HD constexpr uint32_t fz_store(int S, int t, int s) {
+  return uint32_t((kNumBin + kNumUn) * S * S + (kNumBin + 1) * S + t * S + s);
+}
+CMDX_HD constexpr uint32_t fz_end(int S) { return uint32_t((kNumBin + kNumUn) * S * S + (kNumBin + 5) * S); }
 
 // ---- wide encoding (tier 32) -------------------------------------------------
 // word = kind << 24 | d << 16 | s << 8 | aux. The source operand x is slot s,
 // or scalar aux when the kind has kWScalar set.
 enum WideKind {
   kWBin0 = 0,    // + BinOp
-  kWUn0 = 8,     // + UnOp
-  kWStore0 = 11, // + StoreType, stores x to output aux
-  kWEnd = 15,
+  kWUn0 = 16,    // + UnOp
+  kWStore0 = 23, // + StoreType, stores x to output aux
+  kWEnd = 31,
   kWScalar = 0x40
 };
 CMDX_HD constexpr uint32_t wd_word(int kind, int d, int s, int aux) {
@@ -148,16 +152,29 @@ struct GenericParams {
   uint8_t in_dt[kMaxLoads];
 };
 
-// Host entry points of the executor translation units. Each unit keeps its
-// own constant-memory program table; upload writes one slot of it.
-cudaError_t contig_upload(int slot, const uint32_t* words, int n);
-cudaError_t tile2d_upload(int slot, const uint32_t* words, int n);
-cudaError_t generic_upload(int slot, const uint32_t* words, int n);
+// Host entry points of the executors. Each executor source is compiled once
+// per tier and per division variant (CMDX_TIER, CMDX_DIV), so that the large
+// per-tier interpreters compile in parallel and programs without a division
+// run a loop that carries no division code; every such object keeps its own
+// constant-memory program table. The functions below (exec_host.cpp) route
+// a call to the object of a program's tier and variant.
+#define CMDX_DECL_OBJ(t, v)                                                         \
+  cudaError_t contig_upload_t##t##d##v(int slot, const uint32_t* words, int n);     \
+  cudaError_t contig_launch_t##t##d##v(const ContigParams& p, cudaStream_t stream); \
+  cudaError_t generic_upload_t##t##d##v(int slot, const uint32_t* words, int n);    \
+  cudaError_t generic_launch_t##t##d##v(const GenericParams& p, cudaStream_t stream);
+CMDX_DECL_OBJ(0, 0) CMDX_DECL_OBJ(1, 0) CMDX_DECL_OBJ(2, 0) CMDX_DECL_OBJ(3, 0)
+CMDX_DECL_OBJ(0, 1) CMDX_DECL_OBJ(1, 1) CMDX_DECL_OBJ(2, 1) CMDX_DECL_OBJ(3, 1)
+#undef CMDX_DECL_OBJ
+
+// Write a compiled program into slot `slot` of every executor object of its
+// tier and division variant (div: the program has a division op).
+cudaError_t upload_program(int tier, bool div, int slot, const uint32_t* words, int n);
 // n must be a multiple of contig_chunk(tier) elements.
-cudaError_t contig_launch(int tier, const ContigParams& p, cudaStream_t stream);
+cudaError_t contig_launch(int tier, bool div, const ContigParams& p, cudaStream_t stream);
 int contig_chunk(int tier);
-cudaError_t tile2d_launch(int tier, const Tile2dLaunch& L, cudaStream_t stream);
-cudaError_t generic_launch(int tier, const GenericParams& p, cudaStream_t stream);
+cudaError_t tile2d_launch(int tier, bool div, const Tile2dLaunch& L, cudaStream_t stream);
+cudaError_t generic_launch(int tier, bool div, const GenericParams& p, cudaStream_t stream);
 
 // Tile geometry of the tile2d executor.
 constexpr int kTileRows = 64;

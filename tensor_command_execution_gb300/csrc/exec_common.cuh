@@ -23,11 +23,36 @@
 #include "cmd_internal.h"
 #include "interp_asm.cuh"
 
+// The name of this object's entry point: CMDX_TIER_NAME(f_t) is f_t<T>d<D>
+// for CMDX_TIER = T (0..3) and CMDX_DIV = D (0: no division ops, 1: with).
+#define CMDX_TIER_CAT2(a, b) a##b
+#define CMDX_TIER_CAT(a, b) CMDX_TIER_CAT2(a, b)
+#define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), d), CMDX_DIV)
+
 namespace cmdx {
 
 // ---- element operations on 32-bit slot words ------------------------------
 // Float ops use the round-to-nearest-even intrinsics, which are never fused
 // into a multiply-add; int ops are unsigned, i.e. modulo 2^32.
+// minimumNumber / maximumNumber: min.f32 / max.f32 without .ftz return the
+// number when one operand is NaN, order -0 below +0 and keep denormals.
+__device__ __forceinline__ uint32_t fmin_num(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.f32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t fmax_num(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.f32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// int32 division truncating toward zero; x / 0 = -1, INT_MIN / -1 = INT_MIN.
+__device__ __forceinline__ uint32_t idiv(uint32_t a, uint32_t b) {
+  if (b == 0u) return 0xffffffffu;
+  if (b == 0xffffffffu) return 0u - a;
+  return (uint32_t)((int32_t)a / (int32_t)b);
+}
+
 template <int OP>
 __device__ __forceinline__ uint32_t bin(uint32_t d, uint32_t x) {
   if constexpr (OP == kFAdd) return __float_as_uint(__fadd_rn(__uint_as_float(d), __uint_as_float(x)));
@@ -38,6 +63,14 @@ __device__ __forceinline__ uint32_t bin(uint32_t d, uint32_t x) {
   if constexpr (OP == kISub) return d - x;
   if constexpr (OP == kIRsub) return x - d;
   if constexpr (OP == kIMul) return d * x;
+  if constexpr (OP == kFDiv) return __float_as_uint(__fdiv_rn(__uint_as_float(d), __uint_as_float(x)));
+  if constexpr (OP == kFRdiv) return __float_as_uint(__fdiv_rn(__uint_as_float(x), __uint_as_float(d)));
+  if constexpr (OP == kIDiv) return idiv(d, x);
+  if constexpr (OP == kIRdiv) return idiv(x, d);
+  if constexpr (OP == kFMin) return fmin_num(d, x);
+  if constexpr (OP == kFMax) return fmax_num(d, x);
+  if constexpr (OP == kIMin) return (int32_t)d < (int32_t)x ? d : x;
+  if constexpr (OP == kIMax) return (int32_t)d > (int32_t)x ? d : x;
   return 0;
 }
 
@@ -45,6 +78,10 @@ template <int OP>
 __device__ __forceinline__ uint32_t un(uint32_t x) {
   if constexpr (OP == kFNeg) return x ^ 0x80000000u;  // IEEE negate: sign flip
   if constexpr (OP == kINeg) return 0u - x;
+  if constexpr (OP == kFAbs) return x & 0x7fffffffu;
+  if constexpr (OP == kIAbs) return (int32_t)x < 0 ? 0u - x : x;
+  if constexpr (OP == kI2F) return __float_as_uint(__int2float_rn((int32_t)x));
+  if constexpr (OP == kF2I) return (uint32_t)__float2int_rz(__uint_as_float(x));  // saturates, NaN -> 0
   return x;  // kMov
 }
 
@@ -126,14 +163,17 @@ __device__ __forceinline__ void st_elem(void* base, int64_t off, uint32_t x) {
 // Run the program in `prog` (constant memory) over the thread's slots. The
 // compute words run inside the inline-PTX loop of interp_asm.cuh; each store
 // word comes back here and is performed by Pol::store<T>(slot, out_index).
-template <int S, int V, class Pol>
+template <int S, int V, bool DIV, class Pol>
 __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* __restrict__ prog,
                                           const uint32_t* __restrict__ scal, Pol& pol) {
+  // (a division word reaching the variant without division ops leaves the
+  // loop and ends the program here, like the end word; the host never
+  // launches such a pairing)
   static_assert(S == 2 || S == 4 || S == 8, "fused dispatch is generated for 2, 4 and 8 slots");
   uint32_t idx = 0;
 #pragma unroll 1
   for (;;) {
-    const uint32_t w = AsmInterp<S, V>::run(r, idx, prog, scal);
+    const uint32_t w = AsmInterp<S, V, DIV>::run(r, idx, prog, scal);
     const uint32_t c = (w & 0xffffu) - fz_store(S, 0, 0);
     if (c >= 4u * S) return;  // the end word
     const uint32_t aux = w >> 16;
@@ -169,6 +209,14 @@ __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* _
   case s_: {                 \
     CMDX_UNROLL for (int v = 0; v < V; ++v) x[v] = r[s_][v]; \
   } break;
+#define CMDX_W_FETCH_Y(s_, x_) \
+  case s_: {                   \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = r[s_][v]; \
+  } break;
+#define CMDX_W_PUT_Y(s_, x_) \
+  case s_: {                 \
+    CMDX_UNROLL for (int v = 0; v < V; ++v) r[s_][v] = y[v]; \
+  } break;
 #define CMDX_W_BIN(d_, op_) \
   case (kWBin0 + op_) * 32 + d_: { \
     CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], x[v]); \
@@ -178,7 +226,7 @@ __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* _
     CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = un<op_>(x[v]); \
   } break;
 
-template <int V, class Pol>
+template <int V, bool DIV, class Pol>
 __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* __restrict__ prog,
                                          const uint32_t* __restrict__ scal, Pol& pol) {
 #pragma unroll 1
@@ -198,6 +246,29 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
         default: break;
       }
     }
+    if (base >= kWBin0 + kFDiv && base <= kWBin0 + kIRdiv) {
+      // the division ops (kFDiv, kFRdiv, kIDiv, kIRdiv are consecutive): one
+      // body for every destination, fetch, divide, write back; the variant
+      // without them ends the program (the host never launches that pairing)
+      if constexpr (!DIV) return;
+      const uint32_t d = (w >> 16) & 0xffu;
+      uint32_t y[V];
+      switch (d) {
+        CMDX_SA32(CMDX_W_FETCH_Y, 0)
+        default: break;
+      }
+      const uint32_t op = base - kWBin0;
+      CMDX_UNROLL for (int v = 0; v < V; ++v) {
+        const bool rev = op == kFRdiv || op == kIRdiv;
+        const uint32_t a = rev ? x[v] : y[v], b = rev ? y[v] : x[v];
+        y[v] = op >= kIDiv ? idiv(a, b) : bin<kFDiv>(a, b);
+      }
+      switch (d) {
+        CMDX_SA32(CMDX_W_PUT_Y, 0)
+        default: break;
+      }
+      continue;
+    }
     if (base >= kWStore0) {
       switch (base - kWStore0) {
         case kStF32: pol.template store<kStF32>(x, aux); break;
@@ -211,17 +282,21 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
       CMDX_SA32(CMDX_W_BIN, kFAdd) CMDX_SA32(CMDX_W_BIN, kFSub) CMDX_SA32(CMDX_W_BIN, kFRsub)
       CMDX_SA32(CMDX_W_BIN, kFMul) CMDX_SA32(CMDX_W_BIN, kIAdd) CMDX_SA32(CMDX_W_BIN, kISub)
       CMDX_SA32(CMDX_W_BIN, kIRsub) CMDX_SA32(CMDX_W_BIN, kIMul)
+      CMDX_SA32(CMDX_W_BIN, kFMin) CMDX_SA32(CMDX_W_BIN, kFMax)
+      CMDX_SA32(CMDX_W_BIN, kIMin) CMDX_SA32(CMDX_W_BIN, kIMax)
       CMDX_SA32(CMDX_W_UN, kFNeg) CMDX_SA32(CMDX_W_UN, kINeg) CMDX_SA32(CMDX_W_UN, kMov)
+      CMDX_SA32(CMDX_W_UN, kFAbs) CMDX_SA32(CMDX_W_UN, kIAbs) CMDX_SA32(CMDX_W_UN, kI2F)
+      CMDX_SA32(CMDX_W_UN, kF2I)
       default: break;
     }
   }
 }
 
-template <int TIER, int V, class Pol>
+template <int TIER, int V, bool DIV, class Pol>
 __device__ __forceinline__ void run_program(uint32_t (&r)[tier_slots(TIER)][V], const uint32_t* prog,
                                             const uint32_t* scal, Pol& pol) {
-  if constexpr (TIER == kTier32) run_wide<V>(r, prog, scal, pol);
-  else run_fused<tier_slots(TIER), V>(r, prog, scal, pol);
+  if constexpr (TIER == kTier32) run_wide<V, DIV>(r, prog, scal, pol);
+  else run_fused<tier_slots(TIER), V, DIV>(r, prog, scal, pol);
 }
 
 // ---- element-to-lane map of the contiguous and generic executors --------------

@@ -4,7 +4,14 @@
 // over warp-sized chunks of 32*V logical elements. It runs whole chunks only:
 // the host hands a ragged tail (fewer than 32*V elements) to the generic
 // executor, so the hot loop carries no bounds checks.
+//
+// Compiled once per tier and division variant: CMDX_TIER and CMDX_DIV select
+// the kernel this object holds.
 #include "exec_common.cuh"
+
+#if !defined(CMDX_TIER) || !defined(CMDX_DIV)
+#error "exec_contig.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_DIV=<0|1>"
+#endif
 
 namespace cmdx {
 
@@ -77,7 +84,7 @@ struct ContigStore {
   }
 };
 
-template <int TIER>
+template <int TIER, bool DIV>
 __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(const __grid_constant__ ContigParams p) {
   constexpr int S = tier_slots(TIER);
   constexpr int V = tier_vec(TIER);
@@ -94,17 +101,15 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(cons
     for (int j = 0; j < NL; ++j)
       if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
     ContigStore<V> st{p, e0};
-    run_program<TIER, V>(r, prog, p.scal, st);
+    run_program<TIER, V, DIV>(r, prog, p.scal, st);
   }
 }
 
-int contig_chunk(int tier) { return 32 * (tier == kTier32 ? tier_vec(kTier32) : tier_vec(kTier4)); }
-
-cudaError_t contig_upload(int slot, const uint32_t* words, int n) {
+cudaError_t CMDX_TIER_NAME(contig_upload_t)(int slot, const uint32_t* words, int n) {
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
-template <int TIER>
+template <int TIER, bool DIV>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   constexpr int V = tier_vec(TIER);
   constexpr int kBlock = 256;
@@ -114,21 +119,16 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
   if (full_grid == 0) {
-    full_grid = persistent_grid(contig_kernel<TIER>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(contig_kernel<TIER, DIV>, kBlock, 0, INT64_MAX);
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  contig_kernel<TIER><<<grid, kBlock, 0, stream>>>(p);
+  contig_kernel<TIER, DIV><<<grid, kBlock, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t contig_launch(int tier, const ContigParams& p, cudaStream_t stream) {
-  switch (tier) {
-    case kTier2: return launch_tier<kTier2>(p, stream);
-    case kTier4: return launch_tier<kTier4>(p, stream);
-    case kTier8: return launch_tier<kTier8>(p, stream);
-    default: return launch_tier<kTier32>(p, stream);
-  }
+cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
+  return launch_tier<CMDX_TIER, CMDX_DIV != 0>(p, stream);
 }
 
 }  // namespace cmdx

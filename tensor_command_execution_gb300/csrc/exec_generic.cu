@@ -7,7 +7,14 @@
 // with size and stride, and the Flatten transform's row-major order). Lane l
 // of a warp handles elements base + 32 v + l, so views that are contiguous in
 // the innermost dim are still read with consecutive addresses across a warp.
+//
+// Compiled once per tier and division variant: CMDX_TIER and CMDX_DIV select
+// the kernel this object holds.
 #include "exec_common.cuh"
+
+#if !defined(CMDX_TIER) || !defined(CMDX_DIV)
+#error "exec_generic.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_DIV=<0|1>"
+#endif
 
 namespace cmdx {
 
@@ -52,7 +59,7 @@ struct GenericStore {
   }
 };
 
-template <int TIER>
+template <int TIER, bool DIV>
 __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(const __grid_constant__ GenericParams p) {
   constexpr int S = tier_slots(TIER);
   constexpr int V = tier_vec_strided(TIER);
@@ -74,15 +81,15 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(con
       }
     }
     GenericStore<V> st{p, base, lane};
-    run_program<TIER, V>(r, prog, p.scal, st);
+    run_program<TIER, V, DIV>(r, prog, p.scal, st);
   }
 }
 
-cudaError_t generic_upload(int slot, const uint32_t* words, int n) {
+cudaError_t CMDX_TIER_NAME(generic_upload_t)(int slot, const uint32_t* words, int n) {
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
-template <int TIER>
+template <int TIER, bool DIV>
 static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
   constexpr int V = tier_vec_strided(TIER);
   constexpr int kBlock = 256;
@@ -92,21 +99,16 @@ static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
   if (full_grid == 0) {
-    full_grid = persistent_grid(generic_kernel<TIER>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(generic_kernel<TIER, DIV>, kBlock, 0, INT64_MAX);
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  generic_kernel<TIER><<<grid, kBlock, 0, stream>>>(p);
+  generic_kernel<TIER, DIV><<<grid, kBlock, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t generic_launch(int tier, const GenericParams& p, cudaStream_t stream) {
-  switch (tier) {
-    case kTier2: return launch_tier<kTier2>(p, stream);
-    case kTier4: return launch_tier<kTier4>(p, stream);
-    case kTier8: return launch_tier<kTier8>(p, stream);
-    default: return launch_tier<kTier32>(p, stream);
-  }
+cudaError_t CMDX_TIER_NAME(generic_launch_t)(const GenericParams& p, cudaStream_t stream) {
+  return launch_tier<CMDX_TIER, CMDX_DIV != 0>(p, stream);
 }
 
 }  // namespace cmdx

@@ -1,0 +1,156 @@
+// exec_host.cpp - host side of the executors: the tier dispatch of program
+// uploads and launches, and the TMA descriptors of the tile2d executor.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <utility>
+
+#include "exec_tile2d.h"
+
+namespace cmdx {
+
+int contig_chunk(int tier) { return 32 * (tier == kTier32 ? tier_vec(kTier32) : tier_vec(kTier4)); }
+
+namespace {
+
+using Upload = cudaError_t (*)(int, const uint32_t*, int);
+using ContigLaunch = cudaError_t (*)(const ContigParams&, cudaStream_t);
+using GenericLaunch = cudaError_t (*)(const GenericParams&, cudaStream_t);
+using TileLaunch = cudaError_t (*)(const Tile2dParams&, cudaStream_t);
+
+// [division variant][tier]
+constexpr Upload kContigUpload[2][4] = {
+    {contig_upload_t0d0, contig_upload_t1d0, contig_upload_t2d0, contig_upload_t3d0},
+    {contig_upload_t0d1, contig_upload_t1d1, contig_upload_t2d1, contig_upload_t3d1}};
+constexpr Upload kGenericUpload[2][4] = {
+    {generic_upload_t0d0, generic_upload_t1d0, generic_upload_t2d0, generic_upload_t3d0},
+    {generic_upload_t0d1, generic_upload_t1d1, generic_upload_t2d1, generic_upload_t3d1}};
+constexpr ContigLaunch kContigLaunch[2][4] = {
+    {contig_launch_t0d0, contig_launch_t1d0, contig_launch_t2d0, contig_launch_t3d0},
+    {contig_launch_t0d1, contig_launch_t1d1, contig_launch_t2d1, contig_launch_t3d1}};
+constexpr GenericLaunch kGenericLaunch[2][4] = {
+    {generic_launch_t0d0, generic_launch_t1d0, generic_launch_t2d0, generic_launch_t3d0},
+    {generic_launch_t0d1, generic_launch_t1d1, generic_launch_t2d1, generic_launch_t3d1}};
+// [division variant][view variant][tier]; the 32-slot tier has no tile kernel
+constexpr Upload kTileUpload[2][2][3] = {
+    {{tile2d_upload_t0n0d0, tile2d_upload_t1n0d0, tile2d_upload_t2n0d0},
+     {tile2d_upload_t0n1d0, tile2d_upload_t1n1d0, tile2d_upload_t2n1d0}},
+    {{tile2d_upload_t0n0d1, tile2d_upload_t1n0d1, tile2d_upload_t2n0d1},
+     {tile2d_upload_t0n1d1, tile2d_upload_t1n1d1, tile2d_upload_t2n1d1}}};
+constexpr TileLaunch kTileLaunch[2][2][3] = {
+    {{tile2d_launch_t0n0d0, tile2d_launch_t1n0d0, tile2d_launch_t2n0d0},
+     {tile2d_launch_t0n1d0, tile2d_launch_t1n1d0, tile2d_launch_t2n1d0}},
+    {{tile2d_launch_t0n0d1, tile2d_launch_t1n0d1, tile2d_launch_t2n0d1},
+     {tile2d_launch_t0n1d1, tile2d_launch_t1n1d1, tile2d_launch_t2n1d1}}};
+
+bool tier_ok(int tier) { return tier >= kTier2 && tier <= kTier32; }
+
+}  // namespace
+
+cudaError_t upload_program(int tier, bool div, int slot, const uint32_t* words, int n) {
+  if (!tier_ok(tier)) return cudaErrorInvalidValue;
+  cudaError_t e = kContigUpload[div][tier](slot, words, n);
+  if (e == cudaSuccess) e = kGenericUpload[div][tier](slot, words, n);
+  for (int nd = 0; nd < 2 && e == cudaSuccess && tier != kTier32; ++nd) e = kTileUpload[div][nd][tier](slot, words, n);
+  return e;
+}
+
+cudaError_t contig_launch(int tier, bool div, const ContigParams& p, cudaStream_t stream) {
+  if (!tier_ok(tier)) return cudaErrorInvalidValue;
+  return kContigLaunch[div][tier](p, stream);
+}
+
+cudaError_t generic_launch(int tier, bool div, const GenericParams& p, cudaStream_t stream) {
+  if (!tier_ok(tier)) return cudaErrorInvalidValue;
+  return kGenericLaunch[div][tier](p, stream);
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+cudaError_t tile2d_launch(int tier, bool div, const Tile2dLaunch& L, cudaStream_t stream) {
+  static_assert(sizeof(Tile2dParams) < 8192, "kernel parameters stay small");
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  Tile2dParams p;
+  std::memset(&p, 0, sizeof p);
+  uint32_t off = 0, tx = 0;
+  for (uint32_t j = 0; j < L.n_loads; ++j) {
+    const bool half = L.in_dt[j] == 1 || L.in_dt[j] == 2;
+    const uint32_t es = half ? 2 : 4;
+    const bool trans = L.in_trans[j] != 0;
+    // descriptor dims: 0 = the unit-stride tile dim; then the other tile dim
+    // and the batch dims that have a nonzero stride, by increasing stride
+    struct D { int64_t stride, size; int src; };
+    D d[3];
+    int nd = 0;
+    if (L.in_ld[j] != 0) d[nd++] = {L.in_ld[j], trans ? L.cols : L.rows, 0};
+    if (L.in_bst[j][0] != 0) d[nd++] = {L.in_bst[j][0], L.nb[0], 1};
+    if (L.in_bst[j][1] != 0) d[nd++] = {L.in_bst[j][1], L.nb[1], 2};
+    for (int a = 1; a < nd; ++a)
+      for (int b = a; b > 0 && d[b].stride < d[b - 1].stride; --b) std::swap(d[b], d[b - 1]);
+    cuuint64_t dims[4] = {(cuuint64_t)(trans ? L.rows : L.cols), 1, 1, 1};
+    cuuint64_t strides[3] = {0, 0, 0};
+    cuuint32_t box[4] = {half ? 64u : 32u, 1, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    for (int k = 0; k < nd; ++k) {
+      dims[k + 1] = (cuuint64_t)d[k].size;
+      strides[k] = (cuuint64_t)d[k].stride * es;
+      box[k + 1] = d[k].src == 0 ? 64u : 1u;
+      p.in_src[j][k] = (uint8_t)d[k].src;
+    }
+    const int rank = 1 + nd;
+    CUresult r = encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                        (cuuint32_t)rank, const_cast<void*>(L.in[j]), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    p.in_rank[j] = (uint8_t)rank;
+    p.in_bcast[j] = L.in_ld[j] == 0;
+    p.load_off[j] = off;
+    off += (uint32_t)tile_stage_bytes((int)es);
+    // bytes the load's boxes deliver per tile: one row when broadcast
+    tx += (uint32_t)(p.in_bcast[j] ? 64 * es : 64 * 64 * es);
+    p.in_dt[j] = L.in_dt[j];
+    p.in_trans[j] = L.in_trans[j];
+  }
+  if (off == 0 || off > (uint32_t)kTileStageLimit) return cudaErrorInvalidValue;
+  p.stage_bytes = off;
+  p.tx_bytes = tx;
+  const uint32_t stages_fit = (uint32_t)(2 * kTileStageLimit / off);
+  p.n_stages = stages_fit < 2 ? 2 : stages_fit > kMaxStages ? kMaxStages : stages_fit;
+  for (int j = 0; j < kMaxStores; ++j) {
+    p.out[j] = L.out[j];
+    p.out_ld[j] = L.out_ld[j];
+    p.out_bst[j][0] = L.out_bst[j][0];
+    p.out_bst[j][1] = L.out_bst[j][1];
+  }
+  std::memcpy(p.scal, L.scal, sizeof p.scal);
+  p.err = L.err;
+  p.rows = L.rows;
+  p.cols = L.cols;
+  p.tiles_c = (uint32_t)((L.cols + kTileCols - 1) / kTileCols);
+  p.tiles_r = (uint32_t)((L.rows + kTileRows - 1) / kTileRows);
+  p.nb1 = (uint32_t)L.nb[1];
+  p.n_tiles = (uint32_t)((int64_t)p.tiles_c * p.tiles_r * L.nb[0] * L.nb[1]);
+  p.timeout_ns = L.timeout_ns;
+  p.prog = L.prog;
+  p.n_loads = L.n_loads;
+  p.debug = L.debug;
+  bool nd = L.nb[0] > 1 || L.nb[1] > 1;
+  for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
+  if (tier < kTier2 || tier > kTier8) return cudaErrorInvalidValue;  // no 32-slot tile kernel
+  return kTileLaunch[div][nd][tier](p, stream);
+}
+
+}  // namespace cmdx

@@ -23,47 +23,24 @@
 // strides; tiling and staging through shared memory is how this executor
 // makes those transforms coalesce (the pages' own generator stages tiles
 // through LDS on AMD hardware).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <cstring>
-
+//
+// Compiled once per tier (CMDX_TIER 0..2), view variant (CMDX_ND 0: plain
+// 2-D views; 1: batch dims, broadcast loads or descriptors of another rank)
+// and division variant (CMDX_DIV): each object holds one kernel. The TMA
+// descriptors are encoded on the host (exec_host.cpp).
 #include "exec_common.cuh"
+#include "exec_tile2d.h"
+
+#if !defined(CMDX_TIER) || !defined(CMDX_ND) || !defined(CMDX_DIV)
+#error "exec_tile2d.cu is compiled per variant, with -DCMDX_TIER=<0..2> -DCMDX_ND=<0|1> -DCMDX_DIV=<0|1>"
+#endif
+// tile2d_<f>_t<tier>n<nd>d<div>: this object's entry points
+#define CMDX_TILE_NAME(f) \
+  CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), n), CMDX_ND), d), CMDX_DIV)
 
 namespace cmdx {
 
 static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
-
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxStages = 4;
-constexpr int kBarrierBytes = 1024;   // barriers; stages start 1024-byte aligned
-constexpr int kBoxBytes = 8192;       // one 64-row box of 128-byte rows
-
-// error codes (bits of the error word)
-constexpr uint32_t kErrConsumerWait = 1u << 0;
-constexpr uint32_t kErrProducerWait = 1u << 1;
-constexpr uint32_t kErrDrainWait = 1u << 2;
-constexpr uint32_t kErrDebugWait = 1u << 3;
-
-struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
-  CUtensorMap maps[kMaxLoads];
-  void* out[kMaxStores];
-  int64_t out_ld[kMaxStores];
-  int64_t out_bst[kMaxStores][2];
-  uint32_t scal[kMaxScalars];
-  uint32_t* err;
-  int64_t rows, cols;
-  uint64_t timeout_ns;
-  uint32_t tiles_r, tiles_c, nb1, n_tiles;
-  uint32_t prog, n_loads, n_stages, stage_bytes, tx_bytes, debug;
-  uint32_t load_off[kMaxLoads];  // byte offset of load j in a stage
-  uint8_t in_dt[kMaxLoads];
-  uint8_t in_trans[kMaxLoads];
-  uint8_t in_bcast[kMaxLoads];   // the load's other tile dim has stride 0: a one-row box
-  uint8_t in_rank[kMaxLoads];    // dims of its TMA descriptor
-  uint8_t in_src[kMaxLoads][3];  // coordinate of descriptor dims 1..3: 0 tile, 1 batch b0, 2 batch b1
-};
 
 // ---- mbarrier / TMA primitives (inline PTX) ----------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -354,7 +331,7 @@ CMDX_HD constexpr int tile_rows_per_thread(int tier) { return tier == kTier8 ? 1
 
 // ND: the launch has batch dims or broadcast loads. Plain 2-D launches
 // compile without that bookkeeping (the consumer warps are issue-bound).
-template <int TIER, bool ND>
+template <int TIER, bool ND, bool DIV>
 __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int S = tier_slots(TIER);
@@ -490,10 +467,10 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
         }
         if constexpr (RPT == 2) {
           TileStore2<ND> sto{{p, i, jc, fullc, nleft, b0, b1}, {p, i + 1, jc, fullc, nleft, b0, b1}, i + 1 < p.rows};
-          run_program<TIER, V>(r, prog, p.scal, sto);
+          run_program<TIER, V, DIV>(r, prog, p.scal, sto);
         } else {
           TileStore<ND> sto{p, i, jc, fullc, nleft, b0, b1};
-          run_program<TIER, V>(r, prog, p.scal, sto);
+          run_program<TIER, V, DIV>(r, prog, p.scal, sto);
         }
       }
     }
@@ -502,26 +479,13 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
   }
 }
 
-cudaError_t tile2d_upload(int slot, const uint32_t* words, int n) {
+cudaError_t CMDX_TILE_NAME(tile2d_upload_t)(int slot, const uint32_t* words, int n) {
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
 // ---- host side ----------------------------------------------------------------
 
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-template <int TIER, bool ND>
+template <int TIER, bool ND, bool DIV>
 static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes;
   static int grid_cache[64][kMaxStages + 1] = {};
@@ -530,7 +494,7 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   cudaGetDevice(&dev);
   const bool cacheable = dev >= 0 && dev < 64;
   if (!cacheable || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND, DIV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBarrierBytes + 2 * kTileStageLimit + 4096);
     if (e != cudaSuccess) return e;
     if (cacheable) attr_set[dev] = true;
@@ -540,97 +504,16 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const bool cache_ok = cacheable && p.stage_bytes == 16384;
   if (cache_ok) full_grid = grid_cache[dev][p.n_stages];
   if (full_grid == 0) {
-    full_grid = persistent_grid(tile2d_kernel<TIER, ND>, kThreads, smem, INT64_MAX);
+    full_grid = persistent_grid(tile2d_kernel<TIER, ND, DIV>, kThreads, smem, INT64_MAX);
     if (cache_ok) grid_cache[dev][p.n_stages] = full_grid;
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
-  tile2d_kernel<TIER, ND><<<grid, kThreads, smem, stream>>>(p);
+  tile2d_kernel<TIER, ND, DIV><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t tile2d_launch(int tier, const Tile2dLaunch& L, cudaStream_t stream) {
-  static_assert(sizeof(Tile2dParams) < 8192, "kernel parameters stay small");
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
-  Tile2dParams p;
-  std::memset(&p, 0, sizeof p);
-  uint32_t off = 0, tx = 0;
-  for (uint32_t j = 0; j < L.n_loads; ++j) {
-    const bool half = L.in_dt[j] == 1 || L.in_dt[j] == 2;
-    const uint32_t es = half ? 2 : 4;
-    const bool trans = L.in_trans[j] != 0;
-    // descriptor dims: 0 = the unit-stride tile dim; then the other tile dim
-    // and the batch dims that have a nonzero stride, by increasing stride
-    struct D { int64_t stride, size; int src; };
-    D d[3];
-    int nd = 0;
-    if (L.in_ld[j] != 0) d[nd++] = {L.in_ld[j], trans ? L.cols : L.rows, 0};
-    if (L.in_bst[j][0] != 0) d[nd++] = {L.in_bst[j][0], L.nb[0], 1};
-    if (L.in_bst[j][1] != 0) d[nd++] = {L.in_bst[j][1], L.nb[1], 2};
-    for (int a = 1; a < nd; ++a)
-      for (int b = a; b > 0 && d[b].stride < d[b - 1].stride; --b) std::swap(d[b], d[b - 1]);
-    cuuint64_t dims[4] = {(cuuint64_t)(trans ? L.rows : L.cols), 1, 1, 1};
-    cuuint64_t strides[3] = {0, 0, 0};
-    cuuint32_t box[4] = {half ? 64u : 32u, 1, 1, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    for (int k = 0; k < nd; ++k) {
-      dims[k + 1] = (cuuint64_t)d[k].size;
-      strides[k] = (cuuint64_t)d[k].stride * es;
-      box[k + 1] = d[k].src == 0 ? 64u : 1u;
-      p.in_src[j][k] = (uint8_t)d[k].src;
-    }
-    const int rank = 1 + nd;
-    CUresult r = encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
-                        (cuuint32_t)rank, const_cast<void*>(L.in[j]), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    p.in_rank[j] = (uint8_t)rank;
-    p.in_bcast[j] = L.in_ld[j] == 0;
-    p.load_off[j] = off;
-    off += (uint32_t)tile_stage_bytes((int)es);
-    // bytes the load's boxes deliver per tile: one row when broadcast
-    tx += (uint32_t)(p.in_bcast[j] ? 64 * es : 64 * 64 * es);
-    p.in_dt[j] = L.in_dt[j];
-    p.in_trans[j] = L.in_trans[j];
-  }
-  if (off == 0 || off > (uint32_t)kTileStageLimit) return cudaErrorInvalidValue;
-  p.stage_bytes = off;
-  p.tx_bytes = tx;
-  const uint32_t stages_fit = (uint32_t)(2 * kTileStageLimit / off);
-  p.n_stages = stages_fit < 2 ? 2 : stages_fit > kMaxStages ? kMaxStages : stages_fit;
-  for (int j = 0; j < kMaxStores; ++j) {
-    p.out[j] = L.out[j];
-    p.out_ld[j] = L.out_ld[j];
-    p.out_bst[j][0] = L.out_bst[j][0];
-    p.out_bst[j][1] = L.out_bst[j][1];
-  }
-  std::memcpy(p.scal, L.scal, sizeof p.scal);
-  p.err = L.err;
-  p.rows = L.rows;
-  p.cols = L.cols;
-  p.tiles_c = (uint32_t)((L.cols + kTileCols - 1) / kTileCols);
-  p.tiles_r = (uint32_t)((L.rows + kTileRows - 1) / kTileRows);
-  p.nb1 = (uint32_t)L.nb[1];
-  p.n_tiles = (uint32_t)((int64_t)p.tiles_c * p.tiles_r * L.nb[0] * L.nb[1]);
-  p.timeout_ns = L.timeout_ns;
-  p.prog = L.prog;
-  p.n_loads = L.n_loads;
-  p.debug = L.debug;
-  bool nd = L.nb[0] > 1 || L.nb[1] > 1;
-  for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
-  if (nd) {
-    switch (tier) {
-      case kTier2: return launch_tier<kTier2, true>(p, stream);
-      case kTier4: return launch_tier<kTier4, true>(p, stream);
-      default: return launch_tier<kTier8, true>(p, stream);
-    }
-  }
-  switch (tier) {
-    case kTier2: return launch_tier<kTier2, false>(p, stream);
-    case kTier4: return launch_tier<kTier4, false>(p, stream);
-    default: return launch_tier<kTier8, false>(p, stream);
-  }
+cudaError_t CMDX_TILE_NAME(tile2d_launch_t)(const Tile2dParams& p, cudaStream_t stream) {
+  return launch_tier<CMDX_TIER, CMDX_ND != 0, CMDX_DIV != 0>(p, stream);
 }
 
 }  // namespace cmdx

@@ -8,6 +8,14 @@ operands, so each case names its registers directly and the dispatch moves
 no data. A store or end word leaves the loop and is returned to the caller,
 which performs the store in C++ and re-enters at the next word.
 
+Division (int32, and binary32 rounded to nearest) takes a long instruction
+sequence per element, so it is not expanded in every (dst, src) case: for each element the case copies the two
+operands into a pair of staging registers, records a return-site number and
+branches to one shared body, which returns through a second jump table to
+the site, where the quotient is moved into the destination register. One
+element at a time keeps only two staging registers live beside the slots
+(no spills), and one shared body keeps the generated code small.
+
 Run: python gen_interp.py  (writes interp_asm.cuh next to this file)
 """
 from __future__ import annotations
@@ -19,7 +27,13 @@ OUT = os.path.join(HERE, "interp_asm.cuh")
 
 TIERS = [(2, 8), (2, 16), (4, 8), (4, 16), (8, 8), (8, 4)]
 
-# binary ops d = d (op) x, in BinOp order; "{d}" destination, "{x}" source
+N_BIN = 16
+N_UN = 7
+
+# Binary ops d = d (op) x, in BinOp order of cmd_internal.h. A string is an
+# inline body ("{d}" destination, "{x}" source); a tuple ("staged", name,
+# reversed) goes through the shared body `name` with operands (d, x), or
+# (x, d) when reversed.
 BIN = [
     "add.rn.f32 {d}, {d}, {x};",
     "sub.rn.f32 {d}, {d}, {x};",
@@ -29,44 +43,95 @@ BIN = [
     "sub.u32 {d}, {d}, {x};",
     "sub.u32 {d}, {x}, {d};",
     "mul.lo.u32 {d}, {d}, {x};",
+    ("staged", "fdiv", False),
+    ("staged", "fdiv", True),
+    ("staged", "idiv", False),
+    ("staged", "idiv", True),
+    # IEEE minimumNumber / maximumNumber: min.f32 / max.f32 without .ftz
+    # return the number when one operand is NaN and order -0 below +0
+    "min.f32 {d}, {d}, {x};",
+    "max.f32 {d}, {d}, {x};",
+    "min.s32 {d}, {d}, {x};",
+    "max.s32 {d}, {d}, {x};",
 ]
-# unary ops d = f(x), in UnOp order
+assert len(BIN) == N_BIN
+
+# Unary ops d = f(x), in UnOp order.
 UN = [
     "xor.b32 {d}, {x}, 0x80000000;",
     "neg.s32 {d}, {x};",
     "mov.b32 {d}, {x};",
+    "and.b32 {d}, {x}, 0x7fffffff;",
+    # |x| modulo 2^32: (x ^ s) - s with s = x >> 31 (arithmetic)
+    "shr.s32 %%t, {x}, 31; xor.b32 {d}, {x}, %%t; sub.s32 {d}, {d}, %%t;",
+    "cvt.rn.f32.s32 {d}, {x};",
+    # truncation toward zero; the conversion saturates and maps NaN to 0
+    "cvt.rzi.s32.f32 {d}, {x};",
 ]
+assert len(UN) == N_UN
 
 
-def gen_tier(S: int, V: int) -> str:
+def staged_body(name: str) -> str:
+    """Result in %%xa from operands %%xa, %%xb (one element)."""
+    if name == "fdiv":
+        # IEEE binary32 division, rounded once to nearest even
+        return "div.rn.f32 %%xa, %%xa, %%xb;"
+    assert name == "idiv"
+    # truncating division; b == 0 gives -1 and b == -1 gives 0 - a (which
+    # wraps INT_MIN onto itself); the divide itself never sees 0 or -1
+    return ("setp.eq.s32 %%p0, %%xb, 0; setp.eq.s32 %%p1, %%xb, -1; "
+            "selp.b32 %%t, 1, %%xb, %%p0; selp.b32 %%t, 1, %%t, %%p1; "
+            "div.s32 %%t, %%xa, %%t; neg.s32 %%xb, %%xa; selp.b32 %%t, %%xb, %%t, %%p1; "
+            "selp.b32 %%xa, -1, %%t, %%p0;")
+
+
+def gen_tier(S: int, V: int, div: bool) -> str:
     def reg(i, v):
         return f"%{i * V + v}"
 
-    n_bin = 8 * S * S
-    n_un = 3 * S * S
-    base_bs = 11 * S * S
-    base_movs = base_bs + 8 * S
-    base_st = base_movs + S
-    end = 11 * S * S + 13 * S
+    end = (N_BIN + N_UN) * S * S + (N_BIN + 5) * S
     n_cases = end + 1
     slot_ops = S * V
     o_idx = slot_ops        # "+r" program index (words)
     o_word = slot_ops + 1   # "=r" the word that left the loop
     o_prog = slot_ops + 2   # "l" generic address of the program
     o_scal = slot_ops + 3   # "l" generic address of the scalar array
+    load_k = f"shr.u32 %%aux, %%wc, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; ld.u32 %%k, [%%sa];"
 
-    labels = []
-    bodies = []
+    labels, bodies = [], []
+    staged_used = set()
+    ret_sites = []
+
+    def staged_case(name, rev, d, src_regs):
+        """Per element: stage (d, x) (or (x, d) when reversed), branch to the
+        shared body and take the result back at this element's site."""
+        staged_used.add(name)
+        parts = []
+        for v in range(V):
+            first, second = (src_regs[v], reg(d, v)) if rev else (reg(d, v), src_regs[v])
+            site = len(ret_sites)
+            ret_sites.append(f"$LR{site}")
+            parts.append(f"mov.b32 %%xa, {first}; mov.b32 %%xb, {second}; mov.u32 %%rd, {site}; "
+                         f"bra.uni $Lbody_{name}; $LR{site}: mov.b32 {reg(d, v)}, %%xa;")
+        return " ".join(parts) + " bra.uni $Lloop;"
+
     # binary slot-slot
-    for b in range(8):
+    for b in range(N_BIN):
         for d in range(S):
             for s in range(S):
                 lab = f"$LB{b}_{d}_{s}"
                 labels.append(lab)
-                ops = " ".join(BIN[b].format(d=reg(d, v), x=reg(s, v)) for v in range(V))
-                bodies.append(f"{lab}: {ops} bra.uni $Lloop;")
+                op = BIN[b]
+                if isinstance(op, tuple) and not div:
+                    labels[-1] = "$Lexit"
+                    continue
+                if isinstance(op, tuple):
+                    body = staged_case(op[1], op[2], d, [reg(s, v) for v in range(V)])
+                else:
+                    body = " ".join(op.format(d=reg(d, v), x=reg(s, v)) for v in range(V)) + " bra.uni $Lloop;"
+                bodies.append(f"{lab}: {body}")
     # unary
-    for u in range(3):
+    for u in range(N_UN):
         for d in range(S):
             for s in range(S):
                 lab = f"$LU{u}_{d}_{s}"
@@ -77,20 +142,26 @@ def gen_tier(S: int, V: int) -> str:
                     ops = " ".join(UN[u].format(d=reg(d, v), x=reg(s, v)) for v in range(V))
                     bodies.append(f"{lab}: {ops} bra.uni $Lloop;")
     # binary with scalar source
-    for b in range(8):
+    for b in range(N_BIN):
         for d in range(S):
             lab = f"$LS{b}_{d}"
             labels.append(lab)
-            ops = " ".join(BIN[b].format(d=reg(d, v), x="%%k") for v in range(V))
-            bodies.append(f"{lab}: shr.u32 %%aux, %%wc, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; "
-                          f"ld.u32 %%k, [%%sa]; {ops} bra.uni $Lloop;")
+            op = BIN[b]
+            if isinstance(op, tuple) and not div:
+                labels[-1] = "$Lexit"
+                continue
+            if isinstance(op, tuple):
+                body = load_k + " " + staged_case(op[1], op[2], d, ["%%k"] * V)
+            else:
+                body = load_k + " " + " ".join(op.format(d=reg(d, v), x="%%k") for v in range(V)) + \
+                    " bra.uni $Lloop;"
+            bodies.append(f"{lab}: {body}")
     # broadcast scalar
     for d in range(S):
         lab = f"$LM{d}"
         labels.append(lab)
         ops = " ".join(f"mov.b32 {reg(d, v)}, %%k;" for v in range(V))
-        bodies.append(f"{lab}: shr.u32 %%aux, %%wc, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; "
-                      f"ld.u32 %%k, [%%sa]; {ops} bra.uni $Lloop;")
+        bodies.append(f"{lab}: {load_k} {ops} bra.uni $Lloop;")
     # stores and end leave the loop; the table is padded to a power of two
     # with exits so that masking the case number keeps every jump inside it
     labels += ["$Lexit"] * (4 * S + 1)
@@ -100,15 +171,21 @@ def gen_tier(S: int, V: int) -> str:
         size *= 2
     labels += ["$Lexit"] * (size - n_cases)
 
-    lines = []
-    lines.append("{")
-    lines.append(".reg .b32 %%w, %%wc, %%c, %%aux, %%k;")
+    # shared bodies of the staged ops; they return through the site table
+    for name in sorted(staged_used):
+        bodies.append(f"$Lbody_{name}: {staged_body(name)} brx.idx.uni %%rd, $Lret;")
+
+    lines = ["{"]
+    lines.append(".reg .b32 %%w, %%wc, %%c, %%aux, %%k, %%t, %%rd, %%xa, %%xb;")
     lines.append(".reg .b64 %%cbase, %%ca, %%sa;")
-    # branch table, 16 labels per line
+    lines.append(".reg .pred %%p0, %%p1;")
     tbl = []
     for i in range(0, len(labels), 16):
         tbl.append(", ".join(labels[i:i + 16]))
     lines.append("$Ltable: .branchtargets " + ",\n".join(tbl) + ";")
+    if ret_sites:
+        lines.append("$Lret: .branchtargets " + ",\n".join(
+            ", ".join(ret_sites[i:i + 16]) for i in range(0, len(ret_sites), 16)) + ";")
     lines.append(f"cvta.to.const.u64 %%cbase, %{o_prog};")
     lines.append(f"mad.wide.u32 %%ca, %{o_idx}, 4, %%cbase;")
     lines.append("ld.const.u32 %%w, [%%ca];")
@@ -131,18 +208,18 @@ def gen_tier(S: int, V: int) -> str:
     lines.append("}")
     asm = "\n".join(lines)
 
-    def cstr(s):
+    def cstr(text):
         out = []
-        for ln in s.split("\n"):
+        for ln in text.split("\n"):
             out.append('    "' + ln.replace("\\", "\\\\").replace('"', '\\"') + '\\n"')
         return "\n".join(out)
 
     outs = ", ".join(f'"+r"(r[{i}][{v}])' for i in range(S) for v in range(V))
     return f"""
 template <>
-struct AsmInterp<{S}, {V}> {{
+struct AsmInterp<{S}, {V}, {"true" if div else "false"}> {{
   // Run compute words from prog[idx] on; return the first store or end word
-  // (idx then points past it).
+  // (idx then points past it).{"" if div else " Division words are not in this variant: they leave the loop like an end word."}
   static __device__ __forceinline__ uint32_t run(uint32_t (&r)[{S}][{V}], uint32_t& idx, const uint32_t* prog,
                                                  const uint32_t* scal) {{
     uint32_t word;
@@ -162,10 +239,13 @@ def main():
         "// interp_asm.cuh - GENERATED by gen_interp.py; do not edit by hand.\n"
         "// The compute-op interpreter loop as inline PTX for each fused tier.\n"
         "#pragma once\n\n#include <cstdint>\n\nnamespace cmdx {\n\n"
-        "template <int S, int V>\nstruct AsmInterp;\n"
+        "// DIV selects the variant with the division ops; programs without a\n"
+        "// division run the one without, whose loop carries no division code.\n"
+        "template <int S, int V, bool DIV>\nstruct AsmInterp;\n"
     ]
     for S, V in TIERS:
-        parts.append(gen_tier(S, V))
+        for div in (False, True):
+            parts.append(gen_tier(S, V, div))
     parts.append("\n}  // namespace cmdx\n")
     with open(OUT, "w") as f:
         f.write("".join(parts))

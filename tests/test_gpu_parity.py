@@ -29,6 +29,8 @@ pytestmark = pytest.mark.gpu
     (W.strided_bf16(100, 70, 75), "generic"),
     (W.wide_dag((1 << 18) + 11), "contig"),
     (W.wide_dag(37), "contig"),
+    (W.div_clamp_i32((1 << 18) + 9), "contig"),
+    (W.div_clamp_i32(100), "contig"),
 ], ids=lambda x: x["name"] + str(x["sizes"]) if isinstance(x, dict) else x)
 def test_workload_small(spec, path):
     plan = gpuutil.parity(spec)
@@ -482,3 +484,189 @@ def test_rank4_with_two_batch_dims_that_do_not_merge():
                           {"A": "f32", "B": "f32", "out": "f32"}, seed=5)
     plan = gpuutil.parity(spec, bufs)
     assert plan["path"] == "tile2d" and plan["merged_rank"] == 4
+
+
+# ---- division, min/max, abs and conversions ----------------------------------------------
+
+BIN_OPS = ["add", "sub", "mul", "div", "min", "max"]
+UN_OPS = ["neg", "abs", "to_f32", "to_i32"]
+
+
+def random_mixed_case(seed):
+    """A random Command over every E op, with float and int values mixed:
+    binary ops take two values of one class, to_f32 / to_i32 cross over,
+    and each store's type matches its value's class."""
+    rng = np.random.default_rng(10_000 + seed)
+    rank = int(rng.integers(0, 4))
+    sizes = tuple(int(x) for x in rng.integers(1, 24, size=rank))
+    if rank and rng.random() < 0.3:
+        sizes = sizes[:-1] + (int(rng.integers(100, 700)),)
+    ops, views, bufs = [], {}, {}
+    vals = {"f": [], "i": []}
+    for i in range(int(rng.integers(1, 7))):
+        dt = str(rng.choice(["f32", "f16", "bf16", "i32"]))
+        name = f"L{i}"
+        ops.append(("load", name, dt))
+        st, n = _random_view(rng, sizes, allow_broadcast=True)
+        views[name] = dict(strides=st, alloc=n)
+        bufs[name] = _random_values(rng, dt, n)
+        if dt == "i32" and rng.random() < 0.5:
+            bufs[name] = rng.integers(-9, 10, size=n).astype(np.int32)  # small: zeros and -1 as divisors
+        vals["i" if dt == "i32" else "f"].append(name)
+    for i in range(int(rng.integers(0, 3))):
+        name = f"S{i}"
+        if rng.random() < 0.5:
+            ops.append(("scalar", name, "i32", int(rng.choice([0, -1, 3, -7, int(rng.integers(-2**31, 2**31))]))))
+            vals["i"].append(name)
+        else:
+            ops.append(("scalar", name, "f32", float(np.float32(rng.choice([0.0, -0.0, 2.5, rng.standard_normal()])))))
+            vals["f"].append(name)
+    block, last = [], []
+    for i in range(int(rng.integers(1, 22))):
+        name = f"E{i}"
+        eop = str(rng.choice(BIN_OPS + UN_OPS))
+        cls = str(rng.choice([c for c in ("f", "i") if vals[c]]))
+        a = str(rng.choice(vals[cls]))
+        if eop in BIN_OPS:
+            b = str(rng.choice(vals[cls]))
+            out_cls = cls
+        else:
+            b = None
+            out_cls = {"to_f32": "f", "to_i32": "i"}.get(eop, cls)
+        block.append((eop, name, a, b))
+        vals[out_cls].append(name)
+        last.append((name, out_cls))
+    ops.append(("exec", block))
+    for i in range(int(rng.integers(1, 4))):
+        src, cls = last[-1 - int(rng.integers(0, min(4, len(last))))]
+        dt = "i32" if cls == "i" else str(rng.choice(["f32", "f16", "bf16"]))
+        name = f"O{i}"
+        ops.append(("store", name, src, dt))
+        st, n = _random_view(rng, sizes, allow_broadcast=False)
+        views[name] = dict(strides=st, alloc=n)
+        bufs[name] = specutil.sentinel_array(dt, n)
+    return dict(name=f"mixed{seed}", seed=seed, sizes=sizes, ops=ops, views=views, inputs={}), bufs
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_random_mixed_commands(seed):
+    spec, bufs = random_mixed_case(seed)
+    gpuutil.parity(spec, bufs)
+
+
+F_SPECIALS = np.array([0, 0x80000000, 1, 0x80000001, 0x007FFFFF, 0x00800000, 0x7F7FFFFF, 0xFF7FFFFF,
+                       0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000, 0x3F800000, 0xBF800000, 0x40400000,
+                       0x4F000000, 0xCF000000, 0x4EFFFFFF, 0x3F000000, 0xBFC00000, 0x33800000], dtype=np.uint32)
+I_SPECIALS = np.array([0, 1, -1, 2, -2, 7, -7, 2**31 - 1, -2**31, 0x10000, -0x10000, 16777217, -16777219],
+                      dtype=np.int64)
+
+
+def _pairs(vals):
+    return np.repeat(vals, vals.size), np.tile(vals, vals.size)
+
+
+@pytest.mark.parametrize("tier_pad", [0, 9])
+def test_new_float_ops_on_special_values(tier_pad):
+    """Every pair of special floats through div / min / max (both operand
+    orders reach the reversed forms), abs and to_i32; tier_pad extra live
+    values push the program to a wider tier."""
+    xb, yb = _pairs(F_SPECIALS)
+    n = xb.size
+    pad = [f"p{i}" for i in range(tier_pad)]
+    block = [("div", "q", "x", "y"), ("div", "r", "y", "q"), ("min", "lo", "x", "y"), ("max", "hi", "y", "x"),
+             ("abs", "ax", "x", None), ("to_i32", "ti", "x", None), ("div", "qs", "x", "k"),
+             ("min", "ms", "k", "y")]
+    block += [("add", f"s{i}", p, "x") for i, p in enumerate(pad)]
+    acc = "r"
+    for i in range(tier_pad):
+        block.append(("add", f"a{i}", acc, f"s{i}"))
+        acc = f"a{i}"
+    ops = ([("load", "x", "f32"), ("load", "y", "f32")] + [("load", p, "f32") for p in pad]
+           + [("scalar", "k", "f32", -0.0), ("exec", block)]
+           + [("store", o, s, dt) for o, s, dt in (("o_q", "q", "f32"), ("o_r", acc, "f32"), ("o_lo", "lo", "f32"),
+                                                   ("o_hi", "hi", "bf16"), ("o_ax", "ax", "f16"),
+                                                   ("o_ti", "ti", "i32"), ("o_qs", "qs", "f32"),
+                                                   ("o_ms", "ms", "f32"))])
+    names = ["x", "y"] + pad + ["o_q", "o_r", "o_lo", "o_hi", "o_ax", "o_ti", "o_qs", "o_ms"]
+    spec = dict(name="fspecials", seed=0, sizes=(n,), ops=ops,
+                views={k: dict(strides=(1,), alloc=n) for k in names}, inputs={})
+    bufs = {"x": xb.view(np.float32), "y": yb.view(np.float32)}
+    rng = np.random.default_rng(3)
+    for p in pad:
+        bufs[p] = rng.standard_normal(n).astype(np.float32)
+    for o, _, dt in [(op[1], None, op[3]) for op in ops if op[0] == "store"]:
+        bufs[o] = specutil.sentinel_array(dt, n)
+    if tier_pad:
+        c, _ = T.command_from_spec(spec)
+        assert c.lower()[0]["tier"] == 3
+    gpuutil.parity(spec, bufs)
+
+
+@pytest.mark.parametrize("tier_pad", [0, 9])
+def test_new_int_ops_on_edge_values(tier_pad):
+    """Every pair of int32 edge values through division (zero and -1
+    divisors, INT_MIN / -1, both operand orders), min / max, abs and
+    to_f32 (rounding above 2^24)."""
+    x, y = (v.astype(np.int32) for v in _pairs(I_SPECIALS))
+    n = x.size
+    pad = [f"p{i}" for i in range(tier_pad)]
+    block = [("div", "q", "x", "y"), ("div", "r", "y", "x"), ("min", "lo", "x", "y"), ("max", "hi", "x", "y"),
+             ("abs", "ax", "x", None), ("to_f32", "f", "x", None), ("div", "qs", "x", "k"),
+             ("div", "sq", "k", "y")]
+    block += [("add", f"s{i}", p, "q") for i, p in enumerate(pad)]
+    acc = "r"
+    for i in range(tier_pad):
+        block.append(("mul", f"a{i}", acc, f"s{i}"))
+        acc = f"a{i}"
+    ops = ([("load", "x", "i32"), ("load", "y", "i32")] + [("load", p, "i32") for p in pad]
+           + [("scalar", "k", "i32", -1), ("exec", block)]
+           + [("store", o, s, dt) for o, s, dt in (("o_q", "q", "i32"), ("o_r", acc, "i32"), ("o_lo", "lo", "i32"),
+                                                   ("o_hi", "hi", "i32"), ("o_ax", "ax", "i32"),
+                                                   ("o_f", "f", "f32"), ("o_qs", "qs", "i32"),
+                                                   ("o_sq", "sq", "i32"))])
+    names = ["x", "y"] + pad + ["o_q", "o_r", "o_lo", "o_hi", "o_ax", "o_f", "o_qs", "o_sq"]
+    spec = dict(name="ispecials", seed=0, sizes=(n,), ops=ops,
+                views={k: dict(strides=(1,), alloc=n) for k in names}, inputs={})
+    bufs = {"x": x, "y": y}
+    rng = np.random.default_rng(4)
+    for p in pad:
+        bufs[p] = rng.integers(-2**31, 2**31, size=n).astype(np.int32)
+    for o, dt in [(op[1], op[3]) for op in ops if op[0] == "store"]:
+        bufs[o] = specutil.sentinel_array(dt, n)
+    if tier_pad:
+        c, _ = T.command_from_spec(spec)
+        assert c.lower()[0]["tier"] == 3
+    gpuutil.parity(spec, bufs)
+
+
+@pytest.mark.parametrize("path", ["contig", "tile2d", "generic"])
+def test_new_ops_on_each_executor(path):
+    """One Command with every new op, on a dense view (contig), a transposed
+    2-D view (tile2d) and a padded odd-offset view (generic)."""
+    rng = np.random.default_rng(21)
+    m, nn = 96, 136
+    spec = dict(name=f"newops_{path}", seed=0, sizes=(m, nn),
+                ops=[("load", "A", "f32"), ("load", "B", "f32"), ("load", "I", "i32"),
+                     ("exec", [("div", "q", "A", "B"), ("min", "lo", "q", "A"), ("max", "hi", "lo", "B"),
+                               ("abs", "ab", "hi", None), ("to_i32", "ti", "ab", None),
+                               ("div", "id", "I", "ti"), ("max", "im", "id", "I"), ("to_f32", "fi", "im", None),
+                               ("sub", "r", "fi", "q")]),
+                     ("store", "o1", "r", "f32"), ("store", "o2", "im", "i32")],
+                views={}, inputs={})
+    dense = ((nn, 1), m * nn)
+    if path == "contig":
+        a_view = dense
+    elif path == "tile2d":
+        a_view = ((1, m), m * nn)
+    else:
+        a_view = ((nn + 3, 1), (m - 1) * (nn + 3) + nn)
+    spec["views"] = {"A": dict(strides=a_view[0], alloc=a_view[1]), "B": dict(strides=dense[0], alloc=dense[1]),
+                     "I": dict(strides=dense[0], alloc=dense[1]), "o1": dict(strides=dense[0], alloc=dense[1]),
+                     "o2": dict(strides=dense[0], alloc=dense[1])}
+    bufs = {"A": (rng.standard_normal(a_view[1]) * 40).astype(np.float32),
+            "B": (rng.standard_normal(dense[1]) * 3).astype(np.float32),
+            "I": rng.integers(-1000, 1000, size=dense[1]).astype(np.int32),
+            "o1": specutil.sentinel_array("f32", dense[1]), "o2": specutil.sentinel_array("i32", dense[1])}
+    offsets = {"A": 1} if path == "generic" else None
+    plan = gpuutil.parity(spec, bufs, offsets)
+    assert plan["path"] == path

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(T.SIGNATURES), set(names) ^ set(T.SIGNATURES)
-    assert T.cmd_abi_version() == 1
+    assert T.cmd_abi_version() == 2
 
 
 def test_status_strings():
@@ -102,6 +102,7 @@ def test_lowering_of_the_workloads():
         "strided_bf16": (3, 2, 2, 0, 0),
         "wide_dag": (15, 6, 7, 2, 3),
         "batched_transpose": (2, 2, 2, 0, 0),
+        "div_clamp_i32": (5, 1, 1, 0, 0),
     }
     small = {"strided_bf16": (64, 64, 64), "batched_transpose": (2, 64, 64)}
     for name, f in W.FULL.items():
@@ -138,6 +139,41 @@ def test_sub_is_not_treated_as_commutative():
     c.store(t[1], "f32", 1)
     info, _ = c.lower()
     assert info["n_live_ops"] == 2
+
+
+def test_division_flag_and_new_op_reuse():
+    """A live division marks the program for the executors' division
+    variant; a dead one does not. min/max commute (so reuse merges the
+    swapped form), div does not."""
+    c = T.Command()
+    a = c.load_tensor("f32", 1)
+    b = c.load_tensor("f32", 1)
+    i = c.load_tensor("i32", 1)
+    t = c.execute([("min", a, b), ("min", b, a), ("max", a, b), ("div", a, b), ("div", b, a),
+                   ("to_f32", a, None), ("to_i32", i, None), ("abs", i, None)])
+    c.store(t[0], "f32", 1)
+    c.store(t[1], "f32", 1)
+    c.store(t[2], "f32", 1)
+    c.store(t[5], "f32", 1)
+    c.store(t[6], "i32", 1)
+    info, _ = c.lower()
+    assert info["divides"] == 0  # both divisions are dead
+    assert info["n_live_ops"] == 4  # min (once), max and the two (identity) conversions
+    c.store(t[4], "f32", 1)
+    info, _ = c.lower()
+    assert info["divides"] == 1 and info["n_live_ops"] == 5
+    for name, f in W.FULL.items():
+        c2, _ = T.command_from_spec(f(64) if name in ("add_f32", "chain_f32", "wrap_i32", "wide_dag", "div_clamp_i32")
+                                    else f(2, 64, 64) if name == "batched_transpose" else f(64, 64, 64))
+        assert c2.lower()[0]["divides"] == (name == "div_clamp_i32")
+
+
+def test_mixed_classes_rejected():
+    c = T.Command()
+    a = c.load_tensor("f32", 1)
+    i = c.load_tensor("i32", 1)
+    with pytest.raises(T.CmdError):
+        c.execute([("min", a, i)])
 
 
 def test_wide_program_uses_the_32_slot_tier():
@@ -200,6 +236,8 @@ def test_plans_of_the_workloads():
     assert p["path"] == "contig" and p["bytes"] == 30 << 20
     p = _plan(W.batched_transpose(4, 128, 64))
     assert p["path"] == "tile2d" and p["merged_sizes"] == [4, 128, 64] and p["n_transposed"] == 1
+    p = _plan(W.div_clamp_i32(1 << 20))
+    assert p["path"] == "contig" and p["bytes"] == 12 << 20
 
 
 def test_dims_merge_to_contiguous():

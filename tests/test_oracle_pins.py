@@ -493,3 +493,20 @@ def test_workload_batched_transpose_matches_numpy():
     B = bufs["B"].reshape(3, 40, 24)
     want = np.ascontiguousarray(A * B - A).ravel()
     assert (specutil.bits(bufs["out"]) == specutil.bits(want)).all()
+
+
+def test_workload_div_clamp_i32_matches_numpy():
+    """numpy binary32 division, fmax/fmin, truncation to int32 (values are
+    clamped into range first) and truncating int division from |q| // 3."""
+    spec = workloads.div_clamp_i32(20000)
+    bufs = specutil.host_buffers(spec)
+    oracle.OracleCommand(spec, bufs).eval_range()
+    x = bufs["x"]
+    y = np.divide(x, np.float32(0.0074))
+    c = np.fmin(np.fmax(y, np.float32(-128.0)), np.float32(127.0))
+    q = np.trunc(c).astype(np.int32)
+    r = (np.sign(q) * (np.abs(q) // 3)).astype(np.int32)
+    assert (bufs["oq"] == q).all()
+    assert (bufs["or"] == r).all()
+    clamped = (np.abs(q) >= 127).mean()
+    assert 0.2 < clamped < 0.5, clamped  # the clamp is exercised
