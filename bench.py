@@ -41,7 +41,7 @@ HEADLINE = "chain_f32"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "fused Command throughput: HBM GB/s and % of GB300 HBM roofline (elements/s)"
-NP_OF = {"f32": np.float32, "f16": np.float16, "bf16": np.int16, "i32": np.int32}
+NP_OF = {"f32": np.float32, "f16": np.float16, "bf16": np.int16, "i32": np.int32, "b1": np.uint32}
 
 
 def parse():
@@ -206,7 +206,8 @@ def host_inputs(spec, pinned: bool):
 
 def torch_dtype(dt):
     import torch
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.int16, "i32": torch.int32}[dt]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.int16, "i32": torch.int32,
+            "b1": torch.int32}[dt]
 
 
 class Workload:
@@ -230,8 +231,16 @@ class Workload:
         self.plan = self.kernel.plan(self.views, self.scal)
         self.bytes = self.plan["bytes"]
         self.elements = self.plan["n_elements"]
-        chunk = 32 * {0: 8, 1: 8, 2: 8, 3: 2}[self.kernel.info()["tier"]]
+        info = self.kernel.info()
+        chunk = 32 * (2 if info["tier"] == 3 else 16 if (info["tier"] == 0 and info["extended"]) else 8)
         self.launches_per_step = 1 + (1 if (self.plan["path"] == "contig" and self.elements % chunk != 0) else 0)
+
+    def units(self, name, a, b):
+        """Buffer range holding elements [a, b) of a dense 1-D tensor (for a
+        packed-bit store, its 32-bit words; a is then a multiple of 32)."""
+        if self.dts[name] == "b1":
+            return a // 32, (b + 31) // 32
+        return a, b
 
     def view_of(self, name, t, start=0, count=None):
         """The view of tensor `name` over buffer t (optionally elements
@@ -239,7 +248,8 @@ class Workload:
         import tensor_command_execution_gb300 as T
         if count is None:
             return T.TensorView(t.data_ptr(), self.spec["sizes"], self.spec["views"][name]["strides"])
-        return T.TensorView(t.data_ptr() + start * t.element_size(), (count,), (1,))
+        u0, _ = self.units(name, start, start + count)
+        return T.TensorView(t.data_ptr() + u0 * t.element_size(), (count,), (1,))
 
     def launch(self, stream_handle):
         self.kernel.launch_args(self.args, stream_handle)
@@ -348,7 +358,8 @@ class E2EPipeline:
             with torch.cuda.stream(self.s_in):
                 for k, t in wl.host.items():
                     if self.dense_1d:
-                        wl.dev[k][a:b].copy_(t[a:b], non_blocking=True)
+                        u0, u1 = wl.units(k, a, b)
+                        wl.dev[k][u0:u1].copy_(t[u0:u1], non_blocking=True)
                     else:
                         wl.dev[k].copy_(t, non_blocking=True)
             self.ev_in[c].record(self.s_in)
@@ -361,7 +372,8 @@ class E2EPipeline:
             with torch.cuda.stream(self.s_out):
                 for k, t in self.outs_host.items():
                     if self.dense_1d:
-                        t[a:b].copy_(wl.dev[k][a:b], non_blocking=True)
+                        u0, u1 = wl.units(k, a, b)
+                        t[u0:u1].copy_(wl.dev[k][u0:u1], non_blocking=True)
                     else:
                         t.copy_(wl.dev[k], non_blocking=True)
             self.ev_out[c].record(self.s_out)
@@ -496,7 +508,8 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
                       "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32",
-                      "div_clamp_i32": "f32 (int32 out)"}[args.workload],
+                      "div_clamp_i32": "f32 (int32 out)", "threshold_u32": "u32 (int32 out)",
+                      "threshold_bits": "u32 (packed-bit out)"}[args.workload],
             "data": "synthetic (seeded SplitMix64 inputs; no dataset)",
             "config": {"workload": f"{args.workload}: {spec_summary(spec)}", "elements": wl.elements,
                        "bytes_per_step": wl.bytes, "path": wl.plan["path"],

@@ -76,7 +76,15 @@ typedef enum cmd_status {
   CMD_ERR_ARG = 12            /* runtime arguments missing, repeated or unknown */
 } cmd_status;
 
-typedef enum cmd_dtype { CMD_F32 = 0, CMD_F16 = 1, CMD_BF16 = 2, CMD_I32 = 3 } cmd_dtype;
+/* Element types. CMD_B1 is a store type only: one bit per element, packed
+ * into little-endian 32-bit words (element at bit offset k of the view goes
+ * to bit k % 32 of word k / 32); its view must be dense row-major (the bit
+ * offset of an element is its row-major logical index), the buffer 4-byte
+ * aligned and ceil(numel / 32) words long. Each word is written whole: the
+ * bits of the last word past the last element are 0. The packed prediction
+ * store of the Silk page's threshold classification ("AMDGPU Backend",
+ * section "Code Object Format") is this store of a comparison result. */
+typedef enum cmd_dtype { CMD_F32 = 0, CMD_F16 = 1, CMD_BF16 = 2, CMD_I32 = 3, CMD_B1 = 4 } cmd_dtype;
 
 /* Elementwise operations of a T_Execute block (rocRoller, "Design Overview",
  * section "Operations": E_ operations such as Add and Subtract on vectors or
@@ -93,7 +101,15 @@ typedef enum cmd_dtype { CMD_F32 = 0, CMD_F16 = 1, CMD_BF16 = 2, CMD_I32 = 3 } c
  *   TO_F32  int -> float, rounded to nearest even; a float is unchanged.
  *   TO_I32  float -> int, truncated toward zero and saturated to the int32
  *           range, NaN -> 0; an int is unchanged.
- * NEG, ABS, TO_F32 and TO_I32 take one operand (b is ignored). */
+ *   LT, LE, GT, GE, EQ, NE  the int 1 when a (rel) b holds, else 0: IEEE
+ *           comparisons for floats (a NaN operand makes all but NE false;
+ *           -0 == +0), signed for ints.
+ *   ULT, ULE, UGT, UGE      ints compared as unsigned 32-bit numbers (the
+ *           unsigned threshold comparison of the Silk page's threshold
+ *           classification, "AMDGPU Backend", section "Code Object Format").
+ *   SELECT  a if the int c is nonzero, else b; a and b of one class.
+ * NEG, ABS, TO_F32 and TO_I32 take one operand (b is ignored); only SELECT
+ * reads c. */
 typedef enum cmd_eop {
   CMD_E_ADD = 0,
   CMD_E_SUB = 1,
@@ -104,7 +120,18 @@ typedef enum cmd_eop {
   CMD_E_MAX = 6,
   CMD_E_ABS = 7,
   CMD_E_TO_F32 = 8,
-  CMD_E_TO_I32 = 9
+  CMD_E_TO_I32 = 9,
+  CMD_E_LT = 10,
+  CMD_E_LE = 11,
+  CMD_E_GT = 12,
+  CMD_E_GE = 13,
+  CMD_E_EQ = 14,
+  CMD_E_NE = 15,
+  CMD_E_ULT = 16,
+  CMD_E_ULE = 17,
+  CMD_E_UGT = 18,
+  CMD_E_UGE = 19,
+  CMD_E_SELECT = 20
 } cmd_eop;
 
 typedef int32_t cmd_tag;
@@ -115,13 +142,14 @@ typedef struct cmd_kernel* cmd_kernel_t;
  * block's i-th op (i smaller than the referring op's index). */
 #define CMD_LOCAL(i) ((cmd_tag)(-1 - (i)))
 
-/* One E op: result = a (op) b, or op(a) for the one-operand ops (b ignored).
- * a and b are tags of earlier Load_Tensor, Load_Scalar or E results, or
- * CMD_LOCAL(i). */
+/* One E op: result = a (op) b, op(a) for the one-operand ops (b ignored), or
+ * c ? a : b for SELECT (c ignored by every other op). a, b and c are tags of
+ * earlier Load_Tensor, Load_Scalar or E results, or CMD_LOCAL(i). */
 typedef struct cmd_xop {
   int32_t op; /* cmd_eop */
   cmd_tag a;
   cmd_tag b;
+  cmd_tag c;
 } cmd_xop;
 
 /* Runtime argument of a Load_Tensor or Store_Tensor tag: a device pointer and
@@ -163,8 +191,10 @@ typedef struct cmd_program_info {
   int32_t n_words;      /* program words, including the end marker */
   int32_t tier;         /* executor family: 0 = 2 slots, 1 = 4, 2 = 8, 3 = 32 */
   int32_t n_moves;      /* copies the two-address form needed */
-  int32_t divides;      /* 1 if a division op is live: the program runs the
-                           executors' variant with division code, 0 otherwise */
+  int32_t extended;     /* 1 if the program has a live division, comparison or
+                           select, or a packed-bit store: it runs the
+                           executors' extended variant; 0: the base variant,
+                           whose loop carries none of that code */
 } cmd_program_info;
 
 /* Which executor a launch would use (cmd_plan_launch). */
@@ -207,12 +237,15 @@ cmd_status cmd_add_load_scalar(cmd_command_t cmd, cmd_dtype dtype, cmd_tag* out)
 
 /* One T_Execute block of n E ops (1..CMD_MAX_TAGS). Op i receives tag
  * first + i, written to out_tags[i] when out_tags is non-NULL. Operands of a
- * two-operand op must both be float-valued or both int-valued; TO_F32 makes a
- * float value and TO_I32 an int value. On error nothing is added. */
+ * two-operand op must both be float-valued or both int-valued (ULT .. UGE:
+ * int-valued); comparisons make int values, TO_F32 a float value and TO_I32
+ * an int value; SELECT's c must be int-valued and its a and b of one class.
+ * On error nothing is added. */
 cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd_tag* out_tags);
 
 /* Store_Tensor of tag src as element type dtype, logical rank `rank`. A float
- * value may be stored as CMD_F32, CMD_F16 or CMD_BF16; an int value as CMD_I32. */
+ * value may be stored as CMD_F32, CMD_F16 or CMD_BF16; an int value as
+ * CMD_I32 or CMD_B1 (the bit is value != 0). */
 cmd_status cmd_add_store(cmd_command_t cmd, cmd_tag src, cmd_dtype dtype, int32_t rank, cmd_tag* out);
 
 /* ---- lowering ---------------------------------------------------------- */

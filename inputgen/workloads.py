@@ -10,11 +10,15 @@ A workload ("spec") is a dict:
               ``("scalar", name, dtype, value)``   Load_Scalar
               ``("exec", [(eop, name, a, b), ...])`` one T_Execute block;
                                                    eop in add/sub/mul/div/
-                                                   min/max (binary) or neg/
-                                                   abs/to_f32/to_i32 (b None)
+                                                   min/max and the compares
+                                                   lt/le/gt/ge/eq/ne/ult/ule/
+                                                   ugt/uge (binary), neg/abs/
+                                                   to_f32/to_i32 (b None), or
+                                                   ("select", name, a, b, c)
+                                                   for c ? a : b
               ``("store", name, src, dtype)``      Store_Tensor
 ``views``     per load/store name: ``strides`` (elements) and ``alloc``
-              (elements in the physical buffer)
+              (elements in the physical buffer; 32-bit words for a b1 store)
 ``inputs``    per load name: (distribution kind, lo, hi) for inputgen
 
 Nothing here computes the Command; the oracle side and the CUDA side each
@@ -22,7 +26,7 @@ build their own Command from the same spec.
 """
 from __future__ import annotations
 
-DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
+DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}  # b1 stores: 32 elements per 4-byte word
 
 
 def _dense(sizes):
@@ -176,6 +180,39 @@ def div_clamp_i32(n: int = 1 << 27) -> dict:
     )
 
 
+THRESHOLD = 0xA0000000  # 3/8 of uniform u32 values are at or above it
+
+
+def threshold_u32(n: int = 1 << 28) -> dict:
+    """Threshold classification, one prediction word per element: pred =
+    UGE(x, t) stored as int32 0/1, x uniform over all u32 values (int32 bits),
+    t = 0xA0000000 (so about 3/8 of the predictions are 1), seed 7."""
+    st, al = _dense((n,))
+    return dict(
+        name="threshold_u32", seed=7, sizes=(n,),
+        ops=[("load", "x", "i32"), ("scalar", "t", "i32", THRESHOLD - (1 << 32)),
+             ("exec", [("uge", "pred", "x", "t")]),
+             ("store", "out", "pred", "i32")],
+        views={k: dict(strides=st, alloc=al) for k in ("x", "out")},
+        inputs={"x": ("u32", 0.0, 0.0)},
+    )
+
+
+def threshold_bits(n: int = 1 << 28) -> dict:
+    """Threshold classification with packed predictions: the same comparison
+    as threshold_u32, stored one bit per element (b1: 32 predictions per
+    word, bit i of the buffer for element i), seed 8."""
+    st, _ = _dense((n,))
+    return dict(
+        name="threshold_bits", seed=8, sizes=(n,),
+        ops=[("load", "x", "i32"), ("scalar", "t", "i32", THRESHOLD - (1 << 32)),
+             ("exec", [("uge", "pred", "x", "t")]),
+             ("store", "bits", "pred", "b1")],
+        views={"x": dict(strides=st, alloc=n), "bits": dict(strides=st, alloc=(n + 31) // 32)},
+        inputs={"x": ("u32", 0.0, 0.0)},
+    )
+
+
 # Full-size workloads, in the order they are listed for this path.
 FULL = {
     "add_f32": add_f32,
@@ -185,6 +222,8 @@ FULL = {
     "wide_dag": wide_dag,
     "batched_transpose": batched_transpose,
     "div_clamp_i32": div_clamp_i32,
+    "threshold_u32": threshold_u32,
+    "threshold_bits": threshold_bits,
 }
 
 
@@ -211,11 +250,16 @@ def numel(spec: dict) -> int:
     return n
 
 
+def store_bytes(dtype: str, n: int) -> int:
+    """Bytes a store of n elements writes (packed bits: whole 4-byte words)."""
+    return (n + 31) // 32 * 4 if dtype == "b1" else n * DTYPE_BYTES[dtype]
+
+
 def algorithmic_bytes(spec: dict, live_loads=None) -> int:
     """Bytes one pass moves: every live loaded tensor read once and every
     store written once, over the logical elements (padding not counted)."""
     dt = tensor_dtypes(spec)
     n = numel(spec)
     loads = live_loads if live_loads is not None else load_names(spec)
-    return n * (sum(DTYPE_BYTES[dt[k]] for k in loads)
-                + sum(DTYPE_BYTES[dt[k]] for k in store_names(spec)))
+    return (n * sum(DTYPE_BYTES[dt[k]] for k in loads)
+            + sum(store_bytes(dt[k], n) for k in store_names(spec)))

@@ -26,15 +26,19 @@ _lib = None
 _lock = threading.Lock()
 
 MAX_RANK = 4
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
-NP_DTYPE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i32": np.int32}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3, "b1": 4}
+# host buffers: b1 stores are u32 words (32 elements each); eval_points gives b1 as 0/1 bytes
+NP_DTYPE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i32": np.int32, "b1": np.uint32}
+POINT_DTYPE = dict(NP_DTYPE, b1=np.uint8)
 KINDS = {"load": 0, "scalar": 1, "add": 2, "sub": 3, "mul": 4, "neg": 5, "store": 6,
-         "div": 7, "min": 8, "max": 9, "abs": 10, "to_f32": 11, "to_i32": 12}
+         "div": 7, "min": 8, "max": 9, "abs": 10, "to_f32": 11, "to_i32": 12,
+         "lt": 13, "le": 14, "gt": 15, "ge": 16, "eq": 17, "ne": 18,
+         "ult": 19, "ule": 20, "ugt": 21, "uge": 22, "select": 23}
 
 
 class _Op(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("a", ctypes.c_int32), ("b", ctypes.c_int32),
+                ("a", ctypes.c_int32), ("b", ctypes.c_int32), ("c", ctypes.c_int32),
                 ("ptr", ctypes.c_void_p),
                 ("strides", ctypes.c_int64 * MAX_RANK),
                 ("scalar_bits", ctypes.c_uint32)]
@@ -75,6 +79,8 @@ def lib():
                 f = getattr(L, name)
                 f.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
                 f.restype = ctypes.c_uint32
+            L.orc_compare.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint32]
+            L.orc_compare.restype = ctypes.c_uint32
             for name in ("orc_fneg", "orc_ineg", "orc_fabs", "orc_iabs", "orc_i2f", "orc_f2i"):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.c_uint32]
@@ -119,7 +125,7 @@ class OracleCommand:
             kind = op[0]
             if kind == "load":
                 _, name, dt = op
-                o = _Op(kind=KINDS["load"], dtype=DTYPES[dt], a=-1, b=-1)
+                o = _Op(kind=KINDS["load"], dtype=DTYPES[dt], a=-1, b=-1, c=-1)
                 buf = buffers[name]
                 o.ptr = buf.ctypes.data if buf.size else None
                 for k, s in enumerate(spec["views"][name]["strides"]):
@@ -128,19 +134,23 @@ class OracleCommand:
                 ops.append(o)
             elif kind == "scalar":
                 _, name, dt, value = op
-                o = _Op(kind=KINDS["scalar"], dtype=DTYPES[dt], a=-1, b=-1,
+                o = _Op(kind=KINDS["scalar"], dtype=DTYPES[dt], a=-1, b=-1, c=-1,
                         scalar_bits=_scalar_bits(dt, value))
                 tags[name] = len(ops)
                 ops.append(o)
             elif kind == "exec":
-                for eop, name, a, b in op[1]:
+                for e in op[1]:
+                    # (eop, name, a, b) or, for select, (eop, name, a, b, cond)
+                    eop, name, a, b = e[:4]
+                    cond = e[4] if len(e) > 4 else None
                     o = _Op(kind=KINDS[eop], dtype=0, a=tags[a],
-                            b=tags[b] if b is not None else -1)
+                            b=tags[b] if b is not None else -1,
+                            c=tags[cond] if cond is not None else -1)
                     tags[name] = len(ops)
                     ops.append(o)
             elif kind == "store":
                 _, name, src, dt = op
-                o = _Op(kind=KINDS["store"], dtype=DTYPES[dt], a=tags[src], b=-1)
+                o = _Op(kind=KINDS["store"], dtype=DTYPES[dt], a=tags[src], b=-1, c=-1)
                 buf = buffers[name]
                 o.ptr = buf.ctypes.data if buf.size else None
                 for k, s in enumerate(spec["views"][name]["strides"]):
@@ -166,7 +176,7 @@ class OracleCommand:
     def eval_points(self, lin) -> dict:
         """Values of every store at the given logical (row-major) indices."""
         lin = np.ascontiguousarray(lin, dtype=np.int64)
-        outs = {name: np.empty(lin.size, dtype=NP_DTYPE[dt]) for name, dt in self.store_order}
+        outs = {name: np.empty(lin.size, dtype=POINT_DTYPE[dt]) for name, dt in self.store_order}
         ptrs = (ctypes.c_void_p * max(1, len(outs)))(
             *[outs[name].ctypes.data for name, _ in self.store_order])
         rc = lib().orc_eval_points(ctypes.byref(self._cmd), lin.ctypes.data, lin.size,

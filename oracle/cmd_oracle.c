@@ -109,6 +109,41 @@ uint32_t orc_f2i(uint32_t x) {
   return (uint32_t)(int32_t)trunc(v);
 }
 
+/* Comparisons: 1 when the relation holds, else 0. Floats compare as IEEE
+ * values (C's relational operators on float are the IEEE comparisons: a
+ * NaN operand makes every one false but !=); ints as signed or unsigned
+ * 32-bit numbers. */
+uint32_t orc_compare(int32_t kind, int32_t is_int, uint32_t x, uint32_t y) {
+  if (kind >= ORC_ULT) {
+    switch (kind) {
+      case ORC_ULT: return x < y;
+      case ORC_ULE: return x <= y;
+      case ORC_UGT: return x > y;
+      default: return x >= y;
+    }
+  }
+  if (is_int) {
+    int32_t a = (int32_t)x, b = (int32_t)y;
+    switch (kind) {
+      case ORC_LT: return a < b;
+      case ORC_LE: return a <= b;
+      case ORC_GT: return a > b;
+      case ORC_GE: return a >= b;
+      case ORC_EQ: return a == b;
+      default: return a != b;
+    }
+  }
+  float a = as_float(x), b = as_float(y);
+  switch (kind) {
+    case ORC_LT: return a < b;
+    case ORC_LE: return a <= b;
+    case ORC_GT: return a > b;
+    case ORC_GE: return a >= b;
+    case ORC_EQ: return a == b;
+    default: return a != b;
+  }
+}
+
 /* ---- conversions ------------------------------------------------------- */
 
 /* Round a non-negative finite value v (exactly representable in binary64)
@@ -195,6 +230,10 @@ static size_t elem_size(int dtype) {
   return (dtype == ORC_F16 || dtype == ORC_BF16) ? 2u : 4u;
 }
 
+static int operand_ok(const orc_command* c, int32_t tag, int t) {
+  return tag >= 0 && tag < t && c->ops[tag].kind != ORC_STORE;
+}
+
 /* Value class of every tag; checks operand classes and store types. */
 static int classify(const orc_command* c, int* cls) {
   for (int t = 0; t < c->n_ops; ++t) {
@@ -232,11 +271,32 @@ static int classify(const orc_command* c, int* cls) {
         if (c->ops[op->a].kind == ORC_STORE) return ORC_EBAD;
         cls[t] = op->kind == ORC_TO_F32 ? CLS_FLOAT : op->kind == ORC_TO_I32 ? CLS_INT : cls[op->a];
         break;
+      case ORC_LT:
+      case ORC_LE:
+      case ORC_GT:
+      case ORC_GE:
+      case ORC_EQ:
+      case ORC_NE:
+      case ORC_ULT:
+      case ORC_ULE:
+      case ORC_UGT:
+      case ORC_UGE:
+        if (!operand_ok(c, op->a, t) || !operand_ok(c, op->b, t)) return ORC_EBAD;
+        if (cls[op->a] != cls[op->b]) return ORC_ETYPE;
+        if (op->kind >= ORC_ULT && cls[op->a] != CLS_INT) return ORC_ETYPE;
+        cls[t] = CLS_INT;
+        break;
+      case ORC_SELECT:
+        if (!operand_ok(c, op->a, t) || !operand_ok(c, op->b, t) || !operand_ok(c, op->c, t))
+          return ORC_EBAD;
+        if (cls[op->a] != cls[op->b] || cls[op->c] != CLS_INT) return ORC_ETYPE;
+        cls[t] = cls[op->a];
+        break;
       case ORC_STORE:
         if (op->a < 0 || op->a >= t) return ORC_EBAD;
         if (c->ops[op->a].kind == ORC_STORE) return ORC_EBAD;
-        if (op->dtype < ORC_F32 || op->dtype > ORC_I32) return ORC_ETYPE;
-        if ((op->dtype == ORC_I32) != (cls[op->a] == CLS_INT)) return ORC_ETYPE;
+        if (op->dtype < ORC_F32 || op->dtype > ORC_B1) return ORC_ETYPE;
+        if ((op->dtype == ORC_I32 || op->dtype == ORC_B1) != (cls[op->a] == CLS_INT)) return ORC_ETYPE;
         cls[t] = -1;
         break;
       default:
@@ -337,7 +397,37 @@ static void eval_one(const orc_command* c, const int* cls, uint32_t* val,
       case ORC_TO_I32:
         val[t] = cls[op->a] == CLS_INT ? val[op->a] : orc_f2i(val[op->a]);
         break;
+      case ORC_LT:
+      case ORC_LE:
+      case ORC_GT:
+      case ORC_GE:
+      case ORC_EQ:
+      case ORC_NE:
+      case ORC_ULT:
+      case ORC_ULE:
+      case ORC_UGT:
+      case ORC_UGE:
+        val[t] = orc_compare(op->kind, cls[op->a] == CLS_INT, val[op->a], val[op->b]);
+        break;
+      case ORC_SELECT:
+        val[t] = val[op->c] != 0u ? val[op->a] : val[op->b];
+        break;
       case ORC_STORE: {
+        if (op->dtype == ORC_B1) {
+          uint32_t bit = val[op->a] != 0u;
+          if (points) {
+            ((uint8_t*)points[s])[pi] = (uint8_t)bit;
+          } else {
+            int64_t off = view_offset(op, idx, c->rank);
+            char* wp = (char*)op->ptr + (off / 32) * 4;
+            uint32_t w;
+            memcpy(&w, wp, 4);
+            w = (w & ~(1u << (off % 32))) | (bit << (off % 32));
+            memcpy(wp, &w, 4);
+          }
+          ++s;
+          break;
+        }
         size_t es = elem_size(op->dtype);
         char* dst;
         if (points) {
@@ -365,6 +455,16 @@ static int64_t total_elems(const orc_command* c) {
   int64_t n = 1;
   for (int k = 0; k < c->rank; ++k) n *= c->sizes[k];
   return n;
+}
+
+/* The view's strides are the row-major strides of the logical sizes. */
+static int dense_row_major(const orc_command* c, const orc_op* op) {
+  int64_t acc = 1;
+  for (int k = c->rank - 1; k >= 0; --k) {
+    if (c->sizes[k] != 1 && op->strides[k] != acc) return 0;
+    acc *= c->sizes[k];
+  }
+  return 1;
 }
 
 static int check_command(const orc_command* c) {
@@ -395,6 +495,19 @@ int orc_eval_range(const orc_command* c, int64_t begin, int64_t end) {
     for (int64_t e = begin; e < end; ++e) {
       unflatten(c, e, idx);
       eval_one(c, cls, val, idx, NULL, 0);
+    }
+    /* B1 stores over dense row-major views: once the last element is
+     * written, the bits of its word past it are 0 */
+    if (end == n && n % 32 != 0) {
+      for (int t = 0; t < c->n_ops; ++t) {
+        const orc_op* op = &c->ops[t];
+        if (op->kind != ORC_STORE || op->dtype != ORC_B1 || !dense_row_major(c, op)) continue;
+        char* wp = (char*)op->ptr + ((n - 1) / 32) * 4;
+        uint32_t w;
+        memcpy(&w, wp, 4);
+        w &= (1u << (n % 32)) - 1u;
+        memcpy(wp, &w, 4);
+      }
     }
   }
   free(cls);

@@ -45,6 +45,19 @@
  *   - E_ToF32: an int converts with one round to nearest even; a float is
  *     unchanged. E_ToI32: a float truncates toward zero and saturates to the
  *     int32 range, NaN gives 0; an int is unchanged.
+ *   - comparisons (LT, LE, GT, GE, EQ, NE) give the int 1 when they hold and
+ *     0 otherwise: IEEE 754 comparisons for floats (any NaN operand makes all
+ *     of them false except NE, which is true; -0 equals +0), signed for
+ *     ints; ULT, ULE, UGT, UGE compare ints as unsigned 32-bit numbers (the
+ *     Silk page's threshold classification: an unsigned threshold
+ *     comparison of a loaded u32, "AMDGPU Backend", section "Code Object
+ *     Format").
+ *   - SELECT(c, a, b) is a when the int c is nonzero, else b (a and b of one
+ *     class).
+ *   - a B1 store packs one bit per element, (value != 0), at bit offset
+ *     sum(index * stride) of the buffer taken as little-endian u32 words
+ *     (bit k of word k / 32); for a dense row-major view the bits of the
+ *     last word past the last element are 0.
  */
 #ifndef CMD_ORACLE_H
 #define CMD_ORACLE_H
@@ -56,7 +69,7 @@ extern "C" {
 #endif
 
 /* element types */
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_I32 = 3 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_I32 = 3, ORC_B1 = 4 /* store only */ };
 
 /* operation kinds */
 enum {
@@ -72,7 +85,18 @@ enum {
   ORC_MAX = 9,
   ORC_ABS = 10,
   ORC_TO_F32 = 11,
-  ORC_TO_I32 = 12
+  ORC_TO_I32 = 12,
+  ORC_LT = 13,
+  ORC_LE = 14,
+  ORC_GT = 15,
+  ORC_GE = 16,
+  ORC_EQ = 17,
+  ORC_NE = 18,
+  ORC_ULT = 19,
+  ORC_ULE = 20,
+  ORC_UGT = 21,
+  ORC_UGE = 22,
+  ORC_SELECT = 23
 };
 
 /* status codes */
@@ -85,7 +109,8 @@ typedef struct {
   int32_t kind;      /* ORC_LOAD_TENSOR ... ORC_STORE */
   int32_t dtype;     /* element type of a tensor load/store, or of a scalar */
   int32_t a;         /* first operand tag (E ops); source tag (STORE) */
-  int32_t b;         /* second operand tag (ADD/SUB/MUL) */
+  int32_t b;         /* second operand tag (two-operand ops, SELECT) */
+  int32_t c;         /* SELECT: the condition's tag */
   void* ptr;         /* LOAD_TENSOR / STORE: host base address */
   int64_t strides[ORC_MAX_RANK]; /* LOAD_TENSOR / STORE: stride per logical dim, in elements */
   uint32_t scalar_bits;          /* LOAD_SCALAR: the value's bits (binary32 or int32) */
@@ -104,7 +129,7 @@ int orc_eval_range(const orc_command* cmd, int64_t begin, int64_t end);
 
 /* Evaluate the n logical indices lin[0..n) and, instead of writing the views,
  * put the value of the s-th STORE op (in tag order) at element i of
- * store_out[s], in that store's element type. */
+ * store_out[s], in that store's element type (one byte, 0 or 1, for B1). */
 int orc_eval_points(const orc_command* cmd, const int64_t* lin, int64_t n,
                     void* const* store_out);
 
@@ -127,6 +152,8 @@ uint32_t orc_fabs(uint32_t x);
 uint32_t orc_iabs(uint32_t x);
 uint32_t orc_i2f(uint32_t x);
 uint32_t orc_f2i(uint32_t x);
+/* kind: ORC_LT .. ORC_UGE; is_int selects the int (or unsigned) comparison. */
+uint32_t orc_compare(int32_t kind, int32_t is_int, uint32_t x, uint32_t y);
 uint16_t orc_f32_to_f16(uint32_t x);
 uint16_t orc_f32_to_bf16(uint32_t x);
 uint32_t orc_f16_to_f32(uint16_t h);

@@ -22,10 +22,11 @@ import threading
 from . import _build
 
 CMD_MAX_RANK = 4
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3, "b1": 4}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
 EOPS = {"add": 0, "sub": 1, "mul": 2, "neg": 3, "div": 4, "min": 5, "max": 6, "abs": 7, "to_f32": 8,
-        "to_i32": 9}
+        "to_i32": 9, "lt": 10, "le": 11, "gt": 12, "ge": 13, "eq": 14, "ne": 15, "ult": 16, "ule": 17,
+        "ugt": 18, "uge": 19, "select": 20}
 PATHS = {0: "none", 1: "contig", 2: "tile2d", 3: "generic"}
 STATUS = {0: "CMD_OK", 1: "CMD_ERR_NULL", 2: "CMD_ERR_BAD_TAG", 3: "CMD_ERR_TYPE", 4: "CMD_ERR_SHAPE",
           5: "CMD_ERR_ALIAS", 6: "CMD_ERR_ALIGN", 7: "CMD_ERR_STATE", 8: "CMD_ERR_LIMIT", 9: "CMD_ERR_CUDA",
@@ -45,7 +46,7 @@ class CmdError(RuntimeError):
 
 
 class cmd_xop(ctypes.Structure):
-    _fields_ = [("op", ctypes.c_int32), ("a", ctypes.c_int32), ("b", ctypes.c_int32)]
+    _fields_ = [("op", ctypes.c_int32), ("a", ctypes.c_int32), ("b", ctypes.c_int32), ("c", ctypes.c_int32)]
 
 
 class cmd_tensor_arg(ctypes.Structure):
@@ -68,7 +69,7 @@ class cmd_runtime_args(ctypes.Structure):
 
 class cmd_program_info(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int32) for k in ("n_live_ops", "n_loads", "n_scalars", "n_stores", "n_slots",
-                                              "n_words", "tier", "n_moves", "divides")]
+                                              "n_words", "tier", "n_moves", "extended")]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -178,12 +179,16 @@ def cmd_add_load_scalar(cmd: int, dtype: str) -> int:
 
 
 def cmd_add_execute(cmd: int, ops) -> list:
-    """ops: sequence of (eop name, a, b) with b None for neg; returns tags."""
+    """ops: sequence of (eop name, a, b) with b None for the one-operand ops,
+    or ("select", a, b, c) for c ? a : b; returns tags."""
     arr = (cmd_xop * len(ops))()
-    for i, (eop, a, b) in enumerate(ops):
+    for i, op in enumerate(ops):
+        eop, a, b = op[:3]
+        c = op[3] if len(op) > 3 else None
         arr[i].op = EOPS[eop]
         arr[i].a = a
         arr[i].b = -1 if b is None else b
+        arr[i].c = -1 if c is None else c
     out = (ctypes.c_int32 * len(ops))()
     _check(lib().cmd_add_execute(cmd, arr, len(ops), out), "cmd_add_execute")
     return list(out)
@@ -401,8 +406,9 @@ def command_from_spec(spec: dict):
         elif kind == "scalar":
             tags[op[1]] = c.load_scalar(op[2])
         elif kind == "exec":
+            # entries (eop, name, a, b), or (eop, name, a, b, cond) for select
             block = op[1]
-            local = {name: i for i, (_, name, _, _) in enumerate(block)}
+            local = {e[1]: i for i, e in enumerate(block)}
 
             def ref(x, i):
                 if x is None:
@@ -411,9 +417,10 @@ def command_from_spec(spec: dict):
                 if j is not None and j < i:
                     return CMD_LOCAL(j)
                 return tags[x]
-            res = c.execute([(eop, ref(a, i), ref(b, i)) for i, (eop, _, a, b) in enumerate(block)])
-            for (_, name, _, _), t in zip(block, res):
-                tags[name] = t
+            res = c.execute([(e[0], ref(e[2], i), ref(e[3], i), ref(e[4] if len(e) > 4 else None, i))
+                             for i, e in enumerate(block)])
+            for e, t in zip(block, res):
+                tags[e[1]] = t
         elif kind == "store":
             tags[op[1]] = c.store(tags[op[2]], op[3], rank)
         else:

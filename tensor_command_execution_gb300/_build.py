@@ -1,7 +1,7 @@
 """Build the CUDA executor library (libcmdexec.so) in-tree.
 
-Each executor source compiles once per tier and division variant
-(CMDX_TIER, CMDX_DIV; the tile executor also per view variant, CMDX_ND):
+Each executor source compiles once per tier and op-set variant
+(CMDX_TIER, CMDX_EXT; the tile executor also per view variant, CMDX_ND):
 the per-tier interpreters are large, so this spreads them over parallel
 compiler processes. With the host sources, all compile in parallel for
 sm_103a only, then link into one shared library next to this file.
@@ -26,12 +26,12 @@ LIB_PATH = os.path.join(OUT_DIR, "libcmdexec.so")
 def _objs(tiers, nds=(None,)):
     out = []
     for t in tiers:
-        for div in (1, 0):
+        for ext in (1, 0):
             for nd in nds:
                 d = dict(CMDX_TIER=t)
                 if nd is not None:
                     d["CMDX_ND"] = nd
-                d["CMDX_DIV"] = div
+                d["CMDX_EXT"] = ext
                 out.append(d)
     return out
 

@@ -38,7 +38,8 @@ struct Op {
   int dtype;  // load/store element type, scalar type
   int rank;   // load/store logical rank
   int eop;    // kExec: cmd_eop
-  int a, b;   // kExec operands (b = -1 for NEG); kStore: a = source
+  int a, b;   // kExec operands (b = -1 for one-operand ops); kStore: a = source
+  int c;      // SELECT: the condition (else -1)
   int cls;    // value class of the result
 };
 
@@ -48,6 +49,7 @@ const char* dtype_name(int dt) {
     case CMD_F16: return "f16";
     case CMD_BF16: return "bf16";
     case CMD_I32: return "i32";
+    case CMD_B1: return "b1";
   }
   return "?";
 }
@@ -56,18 +58,24 @@ int elem_size(int dt) { return (dt == CMD_F16 || dt == CMD_BF16) ? 2 : 4; }
 
 // E ops that take one operand.
 bool is_unary(int eop) { return eop == CMD_E_NEG || eop == CMD_E_ABS || eop == CMD_E_TO_F32 || eop == CMD_E_TO_I32; }
+bool is_compare(int eop) { return eop >= CMD_E_LT && eop <= CMD_E_UGE; }
 // E ops whose two operands commute exactly (IEEE 754 and modulo 2^32).
 bool is_commutative(int eop) {
-  return eop == CMD_E_ADD || eop == CMD_E_MUL || eop == CMD_E_MIN || eop == CMD_E_MAX;
+  return eop == CMD_E_ADD || eop == CMD_E_MUL || eop == CMD_E_MIN || eop == CMD_E_MAX || eop == CMD_E_EQ ||
+         eop == CMD_E_NE;
 }
 
+// Element types of loads (and of scalars: f32/i32 only, checked apart).
 bool valid_dtype(int dt) { return dt >= CMD_F32 && dt <= CMD_I32; }
+bool valid_store_dtype(int dt) { return dt >= CMD_F32 && dt <= CMD_B1; }
 
-// One instruction of the two-address program, before encoding.
+// One instruction of the two-address program, before encoding. kSlotX
+// stands for the staging slot (the tier's last slot), fixed at encoding.
+constexpr int kSlotX = -2;
 struct Instr {
-  enum Kind { kBin, kUn, kBinS, kMovS, kSt } kind;
-  int op;   // BinOp / UnOp / StoreType
-  int d;    // destination slot
+  enum Kind { kBin, kUn, kBinS, kMovS, kSt, kCmpX, kCmpS, kSel, kSelS } kind;
+  int op;   // BinOp / UnOp / StoreType / CmpOp
+  int d;    // destination slot (kSlotX: the staging slot)
   int s;    // source slot
   int aux;  // scalar index or output index
 };
@@ -82,7 +90,8 @@ struct Program {
   int n_slots = 0;
   int n_moves = 0;
   int tier = cmdx::kTier4;
-  bool divides = false;  // has a division op: runs the executors' division variant
+  bool extended = false;  // uses an extended op or store: runs the executors' extended variant
+  bool uses_x = false;   // comparisons or selects read the staging slot
 };
 
 }  // namespace
@@ -160,15 +169,16 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
   // earlier one takes that one's value; Add and Mul are commutative exactly
   // (bit for bit in IEEE 754 and modulo 2^32), so their operands are ordered.
   std::vector<int> rep(n);
-  std::map<std::tuple<int, int, int>, int> seen;
+  std::map<std::tuple<int, int, int, int>, int> seen;
   for (int t = 0; t < n; ++t) {
     const Op& op = ops[t];
     rep[t] = t;
     if (op.kind != kExec) continue;
     int a = rep[op.a];
     int b = is_unary(op.eop) ? -1 : rep[op.b];
+    int c = op.eop == CMD_E_SELECT ? rep[op.c] : -1;
     if (is_commutative(op.eop) && b < a) std::swap(a, b);
-    auto key = std::make_tuple(op.eop, a, b);
+    auto key = std::make_tuple(op.eop, a, b, c);
     auto it = seen.find(key);
     if (it != seen.end())
       rep[t] = it->second;
@@ -185,6 +195,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     } else if (op.kind == kExec && live[t] && rep[t] == t) {
       live[rep[op.a]] = 1;
       if (!is_unary(op.eop)) live[rep[op.b]] = 1;
+      if (op.eop == CMD_E_SELECT) live[rep[op.c]] = 1;
     }
   }
   std::vector<int> slot_of(n, -1), sidx(n, -1);
@@ -241,6 +252,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     } else {
       last_use[rep[op.a]] = i;
       if (!is_unary(op.eop)) last_use[rep[op.b]] = i;
+      if (op.eop == CMD_E_SELECT) last_use[rep[op.c]] = i;
     }
   }
   // slots
@@ -314,6 +326,70 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
       continue;
     }
     const int b = rep[op.b];
+    if (is_compare(op.eop) || op.eop == CMD_E_SELECT) {
+      // both read the staging slot X, filled right before them
+      const bool sa = is_scalar(a), sb = is_scalar(b);
+      const bool die_a = !sa && last_use[a] == i;
+      const bool die_b = !sb && last_use[b] == i;
+      auto to_x = [&](int x) {  // X = value of tag x
+        P->uses_x = true;
+        ++P->n_moves;
+        if (is_scalar(x)) emit(Instr::kMovS, cmdx::kMov, kSlotX, 0, sidx[x]);
+        else emit(Instr::kUn, cmdx::kMov, kSlotX, slot_of[x], 0);
+      };
+      auto copy_into_new = [&](int x) {  // a fresh slot holding the value of tag x
+        int d = alloc();
+        ++P->n_moves;
+        if (is_scalar(x)) emit(Instr::kMovS, cmdx::kMov, d, 0, sidx[x]);
+        else emit(Instr::kUn, cmdx::kMov, d, slot_of[x], 0);
+        return d;
+      };
+      int d;
+      if (is_compare(op.eop)) {
+        const bool f = ops[a].cls == kFloat;
+        // CmpOp groups list LT LE GT GE EQ NE in cmd_eop order
+        int cop = op.eop >= CMD_E_ULT ? cmdx::kCULt + (op.eop - CMD_E_ULT)
+                                      : (f ? cmdx::kCFLt : cmdx::kCILt) + (op.eop - CMD_E_LT);
+        if (sb) {  // d = a rel scalar b
+          d = die_a ? slot_of[a] : copy_into_new(a);
+          emit(Instr::kCmpS, cop, d, 0, sidx[b]);
+        } else if (sa) {  // d = b (swapped rel) scalar a
+          d = die_b ? slot_of[b] : copy_into_new(b);
+          emit(Instr::kCmpS, cmdx::cmp_swap(cop), d, 0, sidx[a]);
+        } else if (die_a) {
+          to_x(b);
+          d = slot_of[a];
+          emit(Instr::kCmpX, cop, d, 0, 0);
+          if (die_b && b != a) release(slot_of[b]);
+        } else if (die_b) {
+          to_x(a);
+          d = slot_of[b];
+          emit(Instr::kCmpX, cmdx::cmp_swap(cop), d, 0, 0);
+        } else {
+          d = copy_into_new(a);
+          to_x(b);
+          emit(Instr::kCmpX, cop, d, 0, 0);
+        }
+      } else {
+        const int c = rep[op.c];
+        to_x(c);
+        // d holds a (the value when c != 0), then takes b where c == 0
+        if (die_a) d = slot_of[a];
+        else d = copy_into_new(a);
+        if (sb) emit(Instr::kSelS, 0, d, 0, sidx[b]);
+        else emit(Instr::kSel, 0, d, slot_of[b], 0);
+        // operands whose last use this is and whose slot d did not take
+        int dying[2] = {b, c};
+        for (int k = 0; k < 2; ++k) {
+          const int x = dying[k];
+          if (is_scalar(x) || last_use[x] != i || slot_of[x] == d) continue;
+          if (k == 1 && x == b) continue;  // released already as b
+          release(slot_of[x]);
+        }
+      }
+      slot_of[t] = d;
+      continue;
+    }
     int bop, rsub;  // rsub: the reversed form, d = x (op) d
     switch (op.eop) {
       case CMD_E_ADD: bop = rsub = ints ? cmdx::kIAdd : cmdx::kFAdd; break;
@@ -364,7 +440,11 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
   if (overflow || peak > cmdx::kMaxSlots)
     return fail(CMD_ERR_LIMIT, "the program needs more than " + std::to_string(cmdx::kMaxSlots) +
                                    " simultaneously live values");
-  P->n_slots = std::max(peak, 1);
+  // a program that uses the staging slot needs one slot above its values
+  P->n_slots = std::max(peak, 1) + (P->uses_x ? 1 : 0);
+  if (P->n_slots > cmdx::kMaxSlots)
+    return fail(CMD_ERR_LIMIT, "the program needs more than " + std::to_string(cmdx::kMaxSlots - 1) +
+                                   " simultaneously live values besides the staging slot of its comparisons");
   P->tier = P->n_slots <= 2   ? cmdx::kTier2
             : P->n_slots <= 4 ? cmdx::kTier4
             : P->n_slots <= 8 ? cmdx::kTier8
@@ -372,11 +452,26 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
 
   // encode
   P->words.clear();
-  P->divides = false;
-  for (const Instr& in : P->code)
-    if ((in.kind == Instr::kBin || in.kind == Instr::kBinS) && in.op >= cmdx::kFDiv && in.op <= cmdx::kIRdiv)
-      P->divides = true;
+  // the extended variant: division, comparisons, select, packed-bit stores
+  P->extended = false;
+  for (const Instr& in : P->code) {
+    const bool div = (in.kind == Instr::kBin || in.kind == Instr::kBinS) && in.op >= cmdx::kFDiv && in.op <= cmdx::kIRdiv;
+    const bool cmp_sel = in.kind == Instr::kCmpX || in.kind == Instr::kCmpS || in.kind == Instr::kSel ||
+                         in.kind == Instr::kSelS;
+    const bool bits = in.kind == Instr::kSt && in.op == cmdx::kStB1;
+    if (div || cmp_sel || bits) P->extended = true;
+  }
   const int S = cmdx::tier_slots(P->tier);
+  const int X = S - 1;  // the staging slot
+  for (Instr& in : P->code)
+    if (in.d == kSlotX) in.d = X;
+  // an op that reads the staging slot never writes it or reads it as its
+  // other operand: the executors have no case for that
+  for (const Instr& in : P->code) {
+    const bool reads_x = in.kind == Instr::kCmpX || in.kind == Instr::kSel || in.kind == Instr::kSelS;
+    if (reads_x && (in.d == X || (in.kind == Instr::kSel && in.s == X)))
+      return fail(CMD_ERR_STATE, "internal: the lowering placed a value in the staging slot");
+  }
   for (const Instr& in : P->code) {
     uint32_t w = 0;
     if (P->tier != cmdx::kTier32) {
@@ -386,11 +481,19 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
         case Instr::kBinS: w = cmdx::fz_bin_scalar(S, in.op, in.d) | uint32_t(in.aux) << 16; break;
         case Instr::kMovS: w = cmdx::fz_movs(S, in.d) | uint32_t(in.aux) << 16; break;
         case Instr::kSt: w = cmdx::fz_store(S, in.op, in.s) | uint32_t(in.aux) << 16; break;
+        case Instr::kCmpX: w = cmdx::fz_cmpx(S, in.op, in.d); break;
+        case Instr::kCmpS: w = cmdx::fz_cmps(S, in.op, in.d) | uint32_t(in.aux) << 16; break;
+        case Instr::kSel: w = cmdx::fz_sel(S, in.d, in.s); break;
+        case Instr::kSelS: w = cmdx::fz_sels(S, in.d) | uint32_t(in.aux) << 16; break;
       }
     } else {
       switch (in.kind) {
         case Instr::kBin: w = cmdx::wd_word(cmdx::kWBin0 + in.op, in.d, in.s, 0); break;
         case Instr::kUn: w = cmdx::wd_word(cmdx::kWUn0 + in.op, in.d, in.s, 0); break;
+        case Instr::kCmpX: w = cmdx::wd_word(cmdx::kWCmp0 + in.op, in.d, X, 0); break;
+        case Instr::kCmpS: w = cmdx::wd_word((cmdx::kWCmp0 + in.op) | cmdx::kWScalar, in.d, 0, in.aux); break;
+        case Instr::kSel: w = cmdx::wd_word(cmdx::kWSel, in.d, in.s, 0); break;
+        case Instr::kSelS: w = cmdx::wd_word(cmdx::kWSel | cmdx::kWScalar, in.d, 0, in.aux); break;
         case Instr::kBinS: w = cmdx::wd_word((cmdx::kWBin0 + in.op) | cmdx::kWScalar, in.d, 0, in.aux); break;
         case Instr::kMovS: w = cmdx::wd_word((cmdx::kWUn0 + cmdx::kMov) | cmdx::kWScalar, in.d, 0, in.aux); break;
         case Instr::kSt: w = cmdx::wd_word(cmdx::kWStore0 + in.op, 0, in.s, in.aux); break;
@@ -414,7 +517,7 @@ void fill_info(const Program& P, cmd_program_info* info) {
   info->n_words = (int32_t)P.words.size();
   info->tier = P.tier;
   info->n_moves = P.n_moves;
-  info->divides = P.divides ? 1 : 0;
+  info->extended = P.extended ? 1 : 0;
 }
 
 // ---- launch validation and planning ----------------------------------------
@@ -538,7 +641,7 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   for (size_t j = 0; j < P.scalar_tags.size(); ++j) pl->scal[j] = args->scalars[sarg[P.scalar_tags[j]]].v.bits;
   pl->bytes = 0;
   for (auto& v : pl->loads) pl->bytes += N * elem_size(v.dtype);
-  for (auto& v : pl->stores) pl->bytes += N * elem_size(v.dtype);
+  for (auto& v : pl->stores) pl->bytes += v.dtype == CMD_B1 ? (N + 31) / 32 * 4 : N * elem_size(v.dtype);
   if (N == 0 || P.store_tags.empty()) {
     pl->path = CMD_PATH_NONE;
     pl->mrank = 0;
@@ -554,6 +657,25 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   };
   for (auto& v : pl->loads) if (cmd_status s = check_ptr(v)) return s;
   for (auto& v : pl->stores) if (cmd_status s = check_ptr(v)) return s;
+  // packed-bit stores: the bit of an element is its row-major index, so the
+  // view must be the dense row-major one
+  bool any_b1 = false;
+  for (auto& v : pl->stores) {
+    if (v.dtype != CMD_B1) continue;
+    any_b1 = true;
+    int64_t acc = 1;
+    for (int d = cmdx::kMaxRank - 1; d >= 0; --d) {
+      if (sizes[d] != 1 && v.st[d] != acc)
+        return fail(CMD_ERR_SHAPE, "the view of packed-bit Store_Tensor tag " + std::to_string(v.tag) +
+                                       " is not dense row-major (bit i of the buffer is logical element i)");
+      acc *= sizes[d];
+    }
+  }
+  // bytes a view spans from its base
+  auto span_bytes = [&](const View& v) -> int64_t {
+    if (v.dtype == CMD_B1) return (N + 31) / 32 * 4;
+    return view_extent(sizes, v.st, cmdx::kMaxRank) * elem_size(v.dtype);
+  };
   // stores: injective, and not overlapping any other live tensor (an
   // identical view of the same element type read in place is allowed)
   for (size_t i = 0; i < pl->stores.size(); ++i) {
@@ -562,13 +684,14 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
       return fail(CMD_ERR_ALIAS, "the view of Store_Tensor tag " + std::to_string(s.tag) +
                                      " addresses some elements more than once");
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(s.ptr);
-    const uintptr_t s1 = s0 + (uintptr_t)(view_extent(sizes, s.st, cmdx::kMaxRank) * elem_size(s.dtype));
+    const uintptr_t s1 = s0 + (uintptr_t)span_bytes(s);
     auto overlaps = [&](const View& o) {
       const uintptr_t o0 = reinterpret_cast<uintptr_t>(o.ptr);
-      const uintptr_t o1 = o0 + (uintptr_t)(view_extent(sizes, o.st, cmdx::kMaxRank) * elem_size(o.dtype));
+      const uintptr_t o1 = o0 + (uintptr_t)span_bytes(o);
       return o0 < s1 && s0 < o1;
     };
     auto identical = [&](const View& o) {
+      if (s.dtype == CMD_B1) return false;
       if (o.ptr != s.ptr || elem_size(o.dtype) != elem_size(s.dtype)) return false;
       for (int d = 0; d < cmdx::kMaxRank; ++d)
         if (sizes[d] > 1 && o.st[d] != s.st[d]) return false;
@@ -626,10 +749,12 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   auto aligned = [](const void* p, int bytes) { return reinterpret_cast<uintptr_t>(p) % (uintptr_t)bytes == 0; };
   // contiguous: one merged dim (or none) walked with stride 1 by every view,
   // and every pointer aligned for the vector width (4 elements per access)
+  // (a packed-bit store writes single 32-bit words: 4-byte aligned suffices)
   bool contig = m <= 1;
   for (size_t i = 0; i < all.size() && contig; ++i) {
     if (m == 1 && wst[i][0] != 1) contig = false;
-    if (!aligned(all[i]->ptr, 4 * elem_size(all[i]->dtype))) contig = false;
+    const int vec = all[i]->dtype == CMD_B1 ? 4 : 4 * elem_size(all[i]->dtype);
+    if (!aligned(all[i]->ptr, vec)) contig = false;
   }
   if (contig) {
     pl->path = CMD_PATH_CONTIG;
@@ -639,7 +764,8 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   // batch dims. The column dim is the first store's unit-stride dim; the row
   // dim is the unit-stride dim of the loads that are not unit-stride along
   // the column dim (or, without such loads, the store's next smallest stride).
-  if (m >= 2 && P.tier != cmdx::kTier32 && !pl->loads.empty()) {
+  // (not with packed-bit stores: those take the generic executor)
+  if (m >= 2 && P.tier != cmdx::kTier32 && !pl->loads.empty() && !any_b1) {
     const size_t nl = pl->loads.size();
     int col = -1, row = -1;
     for (int q = 0; q < m; ++q)
@@ -778,7 +904,7 @@ cmd_status compile_with_static_word(cmd_command_t cmd, cmd_kernel_t* out, uint32
                                    " error words; program slot " + std::to_string(slot) + " is beyond it");
   }
   if (reused) e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cmdx::upload_program(k->prog.tier, k->prog.divides, slot, k->prog.words.data(), (int)k->prog.words.size());
+  if (e == cudaSuccess) e = cmdx::upload_program(k->prog.tier, k->prog.extended, slot, k->prog.words.data(), (int)k->prog.words.size());
   // the word keeps whatever the previous kernel in this slot left: clear it
   if (e == cudaSuccess) e = cudaMemset(words + slot, 0, sizeof(uint32_t));
   if (e != cudaSuccess) {
@@ -857,7 +983,7 @@ cmd_status cmd_add_load_tensor(cmd_command_t cmd, cmd_dtype dtype, int32_t rank,
   if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
   if (!valid_dtype(dtype)) return fail(CMD_ERR_TYPE, "unknown dtype " + std::to_string((int)dtype));
   if (rank < 0 || rank > CMD_MAX_RANK) return fail(CMD_ERR_SHAPE, "rank must be 0.." + std::to_string(CMD_MAX_RANK));
-  Op op{kLoad, (int)dtype, rank, 0, -1, -1, dtype == CMD_I32 ? kInt : kFloat};
+  Op op{kLoad, (int)dtype, rank, 0, -1, -1, -1, dtype == CMD_I32 ? kInt : kFloat};
   return push_op(cmd, op, out);
 }
 
@@ -865,7 +991,7 @@ cmd_status cmd_add_load_scalar(cmd_command_t cmd, cmd_dtype dtype, cmd_tag* out)
   if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
   if (dtype != CMD_F32 && dtype != CMD_I32)
     return fail(CMD_ERR_TYPE, "a Load_Scalar is CMD_F32 or CMD_I32");
-  Op op{kScalar, (int)dtype, 0, 0, -1, -1, dtype == CMD_I32 ? kInt : kFloat};
+  Op op{kScalar, (int)dtype, 0, 0, -1, -1, -1, dtype == CMD_I32 ? kInt : kFloat};
   return push_op(cmd, op, out);
 }
 
@@ -897,15 +1023,22 @@ cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd
   auto cls_of = [&](int t) { return t < base ? cmd->ops[t].cls : block[t - base].cls; };
   for (int i = 0; i < n; ++i) {
     const cmd_xop& x = ops[i];
-    if (x.op < CMD_E_ADD || x.op > CMD_E_TO_I32) return fail(CMD_ERR_ARG, "unknown E op " + std::to_string(x.op));
-    Op op{kExec, 0, 0, x.op, -1, -1, kFloat};
+    if (x.op < CMD_E_ADD || x.op > CMD_E_SELECT) return fail(CMD_ERR_ARG, "unknown E op " + std::to_string(x.op));
+    Op op{kExec, 0, 0, x.op, -1, -1, -1, kFloat};
     if (cmd_status s = resolve(x.a, i, &op.a)) return s;
     if (!is_unary(x.op)) {
       if (cmd_status s = resolve(x.b, i, &op.b)) return s;
       if (cls_of(op.a) != cls_of(op.b))
         return fail(CMD_ERR_TYPE, "E op " + std::to_string(i) + " mixes an int value and a float value");
     }
-    op.cls = x.op == CMD_E_TO_F32 ? kFloat : x.op == CMD_E_TO_I32 ? kInt : cls_of(op.a);
+    if (x.op >= CMD_E_ULT && x.op <= CMD_E_UGE && cls_of(op.a) != kInt)
+      return fail(CMD_ERR_TYPE, "E op " + std::to_string(i) + ": unsigned comparisons take int values");
+    if (x.op == CMD_E_SELECT) {
+      if (cmd_status s = resolve(x.c, i, &op.c)) return s;
+      if (cls_of(op.c) != kInt)
+        return fail(CMD_ERR_TYPE, "E op " + std::to_string(i) + ": the condition of a SELECT must be int-valued");
+    }
+    op.cls = x.op == CMD_E_TO_F32 ? kFloat : (x.op == CMD_E_TO_I32 || is_compare(x.op)) ? kInt : cls_of(op.a);
     block.push_back(op);
   }
   try {
@@ -920,15 +1053,15 @@ cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd
 
 cmd_status cmd_add_store(cmd_command_t cmd, cmd_tag src, cmd_dtype dtype, int32_t rank, cmd_tag* out) {
   if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
-  if (!valid_dtype(dtype)) return fail(CMD_ERR_TYPE, "unknown dtype " + std::to_string((int)dtype));
+  if (!valid_store_dtype(dtype)) return fail(CMD_ERR_TYPE, "unknown dtype " + std::to_string((int)dtype));
   if (rank < 0 || rank > CMD_MAX_RANK) return fail(CMD_ERR_SHAPE, "rank must be 0.." + std::to_string(CMD_MAX_RANK));
   if (src < 0 || src >= (cmd_tag)cmd->ops.size() || cmd->ops[src].kind == kStore)
     return fail(CMD_ERR_BAD_TAG, "store source tag " + std::to_string(src) + " is not an earlier value");
   const int cls = cmd->ops[src].cls;
-  if ((dtype == CMD_I32) != (cls == kInt))
+  if ((dtype == CMD_I32 || dtype == CMD_B1) != (cls == kInt))
     return fail(CMD_ERR_TYPE, std::string("cannot store a ") + (cls == kInt ? "int" : "float") + " value as " +
                                   dtype_name(dtype));
-  Op op{kStore, (int)dtype, rank, 0, src, -1, kNone};
+  Op op{kStore, (int)dtype, rank, 0, src, -1, -1, kNone};
   return push_op(cmd, op, out);
 }
 
@@ -987,7 +1120,7 @@ cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out) {
       return cuda_fail(e, "cudaDeviceSynchronize before reusing a program slot");
     }
   }
-  e = cmdx::upload_program(k->prog.tier, k->prog.divides, slot, k->prog.words.data(), (int)k->prog.words.size());
+  e = cmdx::upload_program(k->prog.tier, k->prog.extended, slot, k->prog.words.data(), (int)k->prog.words.size());
   if (e == cudaSuccess) e = cudaMalloc(&k->err, 256);
   if (e == cudaSuccess) e = cudaMemset(k->err, 0, 256);
   if (e != cudaSuccess) {
@@ -1046,6 +1179,8 @@ cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* nee
   static const char* bin[] = {"fadd", "fsub", "frsub", "fmul", "iadd", "isub", "irsub", "imul",
                               "fdiv", "frdiv", "idiv", "irdiv", "fmin", "fmax", "imin", "imax"};
   static const char* un[] = {"fneg", "ineg", "mov", "fabs", "iabs", "i2f", "f2i"};
+  static const char* cmp[] = {"flt", "fle", "fgt", "fge", "feq", "fne", "ilt", "ile",
+                              "igt", "ige", "ieq", "ine", "ult", "ule", "ugt", "uge"};
   std::string s;
   const Program& P = k->prog;
   char line[160];
@@ -1069,6 +1204,18 @@ cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* nee
       case Instr::kUn: std::snprintf(line, sizeof line, "%-7s r%d, r%d\n", un[in.op], in.d, in.s); break;
       case Instr::kBinS: std::snprintf(line, sizeof line, "%-7s r%d, s%d\n", bin[in.op], in.d, in.aux); break;
       case Instr::kMovS: std::snprintf(line, sizeof line, "mov     r%d, s%d\n", in.d, in.aux); break;
+      case Instr::kCmpX:
+        std::snprintf(line, sizeof line, "%-7s r%d, r%d\n", cmp[in.op], in.d, cmdx::tier_slots(P.tier) - 1);
+        break;
+      case Instr::kCmpS: std::snprintf(line, sizeof line, "%-7s r%d, s%d\n", cmp[in.op], in.d, in.aux); break;
+      case Instr::kSel:
+        std::snprintf(line, sizeof line, "sel     r%d, r%d  ; r%d = r%d != 0 ? r%d : r%d\n", in.d, in.s, in.d,
+                      cmdx::tier_slots(P.tier) - 1, in.d, in.s);
+        break;
+      case Instr::kSelS:
+        std::snprintf(line, sizeof line, "sel     r%d, s%d  ; r%d = r%d != 0 ? r%d : s%d\n", in.d, in.aux, in.d,
+                      cmdx::tier_slots(P.tier) - 1, in.d, in.aux);
+        break;
       case Instr::kSt:
         std::snprintf(line, sizeof line, "store   out%d <- r%d (%s, tag %d)\n", in.aux, in.s, dtype_name(in.op),
                       P.store_tags[in.aux]);
@@ -1125,7 +1272,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
   if (pl.path == CMD_PATH_CONTIG) {
     // whole warp chunks on the contiguous executor, a ragged tail (fewer than
     // one chunk of elements) on the generic one
-    const int64_t chunk = cmdx::contig_chunk(P.tier);
+    const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended);
     const int64_t n_main = pl.n - pl.n % chunk;
     e = cudaSuccess;
     if (n_main > 0) {
@@ -1140,7 +1287,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n = n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
-      e = cmdx::contig_launch(P.tier, P.divides, p, stream);
+      e = cmdx::contig_launch(P.tier, P.extended, p, stream);
     }
     if (e == cudaSuccess && pl.n > n_main) {
       cmdx::GenericParams p;
@@ -1151,7 +1298,9 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
         p.in_st[j][cmdx::kMaxRank - 1] = 1;
       }
       for (size_t j = 0; j < pl.stores.size(); ++j) {
-        p.out[j] = static_cast<char*>(pl.stores[j].ptr) + n_main * elem_size(pl.stores[j].dtype);
+        // (packed bits: n_main is a multiple of 32, so the tail starts on a word)
+        const int64_t skip = pl.stores[j].dtype == CMD_B1 ? n_main / 8 : n_main * elem_size(pl.stores[j].dtype);
+        p.out[j] = static_cast<char*>(pl.stores[j].ptr) + skip;
         p.out_st[j][cmdx::kMaxRank - 1] = 1;
       }
       for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(1);
@@ -1160,7 +1309,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n = pl.n - n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
-      e = cmdx::generic_launch(P.tier, P.divides, p, stream);
+      e = cmdx::generic_launch(P.tier, P.extended, p, stream);
     }
   } else if (pl.path == CMD_PATH_TILE2D) {
     cmdx::Tile2dLaunch L;
@@ -1195,7 +1344,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     L.err = k->err;
     L.debug = (uint32_t)g_force_timeout.load();
     L.timeout_ns = g_wait_limit_ns.load();
-    e = cmdx::tile2d_launch(P.tier, P.divides, L, stream);
+    e = cmdx::tile2d_launch(P.tier, P.extended, L, stream);
   } else {
     cmdx::GenericParams p;
     std::memset(&p, 0, sizeof p);
@@ -1213,7 +1362,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     p.n = pl.n;
     p.prog = (uint32_t)k->slot;
     p.n_loads = (uint32_t)pl.loads.size();
-    e = cmdx::generic_launch(P.tier, P.divides, p, stream);
+    e = cmdx::generic_launch(P.tier, P.extended, p, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return CMD_OK;

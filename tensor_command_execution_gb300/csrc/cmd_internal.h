@@ -29,11 +29,24 @@ enum Tier { kTier2 = 0, kTier4 = 1, kTier8 = 2, kTier32 = 3 };
 CMDX_HD constexpr int tier_slots(int tier) {
   return tier == kTier2 ? 2 : tier == kTier4 ? 4 : tier == kTier8 ? 8 : 32;
 }
-// Elements each thread keeps per slot in the contiguous executor.
-CMDX_HD constexpr int tier_vec(int tier) { return tier == kTier32 ? 2 : 8; }
-// ... and in the tile and generic executors, whose addressing needs more
-// registers: the 8-slot tier keeps 4 elements per slot there.
-CMDX_HD constexpr int tier_vec_strided(int tier) { return tier == kTier8 ? 4 : tier_vec(tier); }
+// Elements each thread keeps per slot in the contiguous executor: 8 in the
+// fused tiers and 2 in the 32-slot one, except 16 in the extended variant of
+// the 2-slot tier, whose programs (divisions, comparisons, packed-bit stores)
+// do more work per program word: the wider vector spreads each word's
+// dispatch over more elements (measured: packed-bit threshold +22 %), while
+// plain 2-slot programs run faster at the higher occupancy of 8.
+CMDX_HD constexpr int tier_vec(int tier, bool ext) {
+  return tier == kTier32 ? 2 : (tier == kTier2 && ext) ? 16 : 8;
+}
+// Whether the contiguous executor prefetches the next chunk's loads while
+// the program runs on the current one: in the base variant of the 2-slot
+// tier, whose one or two loads leave few bytes in flight per thread
+// otherwise (measured: two-load add +4.6 %; the extended variant's wider
+// vector serves it better, and its registers leave no room for both).
+CMDX_HD constexpr bool contig_prefetch(int tier, bool ext) { return tier == kTier2 && !ext; }
+// ... and in the generic executor, whose addressing needs more registers:
+// 8, and 4 in the 8-slot tier.
+CMDX_HD constexpr int tier_vec_strided(int tier) { return tier == kTier8 ? 4 : tier == kTier32 ? 2 : 8; }
 // Resident 256-thread CTAs per SM each executor is compiled for (caps registers).
 CMDX_HD constexpr int tier_min_blocks(int tier) { return tier == kTier32 ? 2 : 3; }
 // Program words a program may have: one less than its constant-memory row,
@@ -51,18 +64,36 @@ enum BinOp {
 };
 // Unary ops: d = f(x).
 enum UnOp { kFNeg = 0, kINeg = 1, kMov = 2, kFAbs = 3, kIAbs = 4, kI2F = 5, kF2I = 6, kNumUn = 7 };
-// Store element types, as numbered in cmd.h's cmd_dtype.
-enum StoreType { kStF32 = 0, kStF16 = 1, kStBF16 = 2, kStI32 = 3, kNumSt = 4 };
+// Comparisons: d = (d rel x) ? 1 : 0, floats (IEEE, ordered: false on NaN
+// except NE), signed ints, unsigned ints. Swapping the operands maps LT <-> GT
+// and LE <-> GE within each group (cmp_swap).
+enum CmpOp {
+  kCFLt = 0, kCFLe, kCFGt, kCFGe, kCFEq, kCFNe,
+  kCILt = 6, kCILe, kCIGt, kCIGe, kCIEq, kCINe,
+  kCULt = 12, kCULe, kCUGt, kCUGe,
+  kNumCmp = 16
+};
+CMDX_HD constexpr int cmp_swap(int c) { return c % 6 < 2 ? c + 2 : c % 6 < 4 ? c - 2 : c; }
+// Store element types, as numbered in cmd.h's cmd_dtype (B1: packed bits).
+enum StoreType { kStF32 = 0, kStF16 = 1, kStBF16 = 2, kStI32 = 3, kStB1 = 4, kNumSt = 5 };
 
 // ---- fused encoding (tiers 2, 4 and 8) ----------------------------------------
 // word = case | aux << 16; aux is a scalar index (scalar ops) or an output
-// index (stores). Case layout, for S slots (B = kNumBin, U = kNumUn):
+// index (stores). Case layout, for S slots (B = kNumBin, U = kNumUn,
+// C = kNumCmp, T = kNumSt):
 //   [0, B S^2)                binary op b, dst d, src slot s : b S^2 + d S + s
 //   [B S^2, (B+U) S^2)        unary op u, dst d, src slot s  : B S^2 + u S^2 + d S + s
 //   [(B+U) S^2, +B S)         binary op b with scalar src, dst d
 //   then S cases              broadcast scalar into d
-//   then 4 S cases            store slot s as type t
+//   then T S cases            store slot s as type t
 //   then                      end
+//   then C S cases            compare c: d = d rel X (X = slot S - 1, the staging slot)
+//   then C S cases            compare c: d = d rel scalar
+//   then S^2 cases            select: d = X != 0 ? d : slot s
+//   then S cases              select: d = X != 0 ? d : scalar
+// Comparisons and selects read the staging slot X = S - 1, which the lowering
+// fills right before (a program using it keeps slot S - 1 free), so that they
+// take S cases each rather than S^2.
 CMDX_HD constexpr uint32_t fz_bin(int S, int b, int d, int s) { return uint32_t(b * S * S + d * S + s); }
 CMDX_HD constexpr uint32_t fz_un(int S, int u, int d, int s) { return uint32_t(kNumBin * S * S + u * S * S + d * S + s); }
 CMDX_HD constexpr uint32_t fz_bin_scalar(int S, int b, int d) { return uint32_t((kNumBin + kNumUn) * S * S + b * S + d); }
@@ -70,16 +101,26 @@ CMDX_HD constexpr uint32_t fz_movs(int S, int d) { return uint32_t((kNumBin + kN
 CMDX_HD constexpr uint32_t fz_store(int S, int t, int s) {
   return uint32_t((kNumBin + kNumUn) * S * S + (kNumBin + 1) * S + t * S + s);
 }
-CMDX_HD constexpr uint32_t fz_end(int S) { return uint32_t((kNumBin + kNumUn) * S * S + (kNumBin + 5) * S); }
+CMDX_HD constexpr uint32_t fz_end(int S) {
+  return uint32_t((kNumBin + kNumUn) * S * S + (kNumBin + 1 + kNumSt) * S);
+}
+CMDX_HD constexpr uint32_t fz_cmpx(int S, int c, int d) { return fz_end(S) + 1 + uint32_t(c * S + d); }
+CMDX_HD constexpr uint32_t fz_cmps(int S, int c, int d) { return fz_end(S) + 1 + uint32_t((kNumCmp + c) * S + d); }
+CMDX_HD constexpr uint32_t fz_sel(int S, int d, int s) { return fz_end(S) + 1 + uint32_t(2 * kNumCmp * S + d * S + s); }
+CMDX_HD constexpr uint32_t fz_sels(int S, int d) { return fz_end(S) + 1 + uint32_t(2 * kNumCmp * S + S * S + d); }
+CMDX_HD constexpr uint32_t fz_cases(int S) { return fz_sels(S, S); }  // number of cases
 
 // ---- wide encoding (tier 32) -------------------------------------------------
 // word = kind << 24 | d << 16 | s << 8 | aux. The source operand x is slot s,
-// or scalar aux when the kind has kWScalar set.
+// or scalar aux when the kind has kWScalar set. Selects read the staging
+// slot X = 31 as their condition.
 enum WideKind {
   kWBin0 = 0,    // + BinOp
   kWUn0 = 16,    // + UnOp
   kWStore0 = 23, // + StoreType, stores x to output aux
   kWEnd = 31,
+  kWCmp0 = 32,   // + CmpOp: d = d rel x
+  kWSel = 48,    // d = X != 0 ? d : x
   kWScalar = 0x40
 };
 CMDX_HD constexpr uint32_t wd_word(int kind, int d, int s, int aux) {
@@ -153,28 +194,30 @@ struct GenericParams {
 };
 
 // Host entry points of the executors. Each executor source is compiled once
-// per tier and per division variant (CMDX_TIER, CMDX_DIV), so that the large
-// per-tier interpreters compile in parallel and programs without a division
-// run a loop that carries no division code; every such object keeps its own
-// constant-memory program table. The functions below (exec_host.cpp) route
-// a call to the object of a program's tier and variant.
+// per tier and per op-set variant (CMDX_TIER, CMDX_EXT), so that the large
+// per-tier interpreters compile in parallel and programs that use only the
+// base ops (arithmetic, min/max, abs, conversions) run a loop that carries no
+// code for the extended ones (division, comparisons, select, packed-bit
+// stores); every such object keeps its own constant-memory program table.
+// The functions below (exec_host.cpp) route a call to the object of a
+// program's tier and variant.
 #define CMDX_DECL_OBJ(t, v)                                                         \
-  cudaError_t contig_upload_t##t##d##v(int slot, const uint32_t* words, int n);     \
-  cudaError_t contig_launch_t##t##d##v(const ContigParams& p, cudaStream_t stream); \
-  cudaError_t generic_upload_t##t##d##v(int slot, const uint32_t* words, int n);    \
-  cudaError_t generic_launch_t##t##d##v(const GenericParams& p, cudaStream_t stream);
+  cudaError_t contig_upload_t##t##e##v(int slot, const uint32_t* words, int n);     \
+  cudaError_t contig_launch_t##t##e##v(const ContigParams& p, cudaStream_t stream); \
+  cudaError_t generic_upload_t##t##e##v(int slot, const uint32_t* words, int n);    \
+  cudaError_t generic_launch_t##t##e##v(const GenericParams& p, cudaStream_t stream);
 CMDX_DECL_OBJ(0, 0) CMDX_DECL_OBJ(1, 0) CMDX_DECL_OBJ(2, 0) CMDX_DECL_OBJ(3, 0)
 CMDX_DECL_OBJ(0, 1) CMDX_DECL_OBJ(1, 1) CMDX_DECL_OBJ(2, 1) CMDX_DECL_OBJ(3, 1)
 #undef CMDX_DECL_OBJ
 
 // Write a compiled program into slot `slot` of every executor object of its
-// tier and division variant (div: the program has a division op).
-cudaError_t upload_program(int tier, bool div, int slot, const uint32_t* words, int n);
-// n must be a multiple of contig_chunk(tier) elements.
-cudaError_t contig_launch(int tier, bool div, const ContigParams& p, cudaStream_t stream);
-int contig_chunk(int tier);
-cudaError_t tile2d_launch(int tier, bool div, const Tile2dLaunch& L, cudaStream_t stream);
-cudaError_t generic_launch(int tier, bool div, const GenericParams& p, cudaStream_t stream);
+// tier and variant (ext: the program uses an extended op or store).
+cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, int n);
+// n must be a multiple of contig_chunk(tier, ext) elements.
+cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream);
+int contig_chunk(int tier, bool ext);
+cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_t stream);
+cudaError_t generic_launch(int tier, bool ext, const GenericParams& p, cudaStream_t stream);
 
 // Tile geometry of the tile2d executor.
 constexpr int kTileRows = 64;

@@ -23,11 +23,12 @@
 #include "cmd_internal.h"
 #include "interp_asm.cuh"
 
-// The name of this object's entry point: CMDX_TIER_NAME(f_t) is f_t<T>d<D>
-// for CMDX_TIER = T (0..3) and CMDX_DIV = D (0: no division ops, 1: with).
+// The name of this object's entry point: CMDX_TIER_NAME(f_t) is f_t<T>e<E>
+// for CMDX_TIER = T (0..3) and CMDX_EXT = E (0: the base op set, 1: extended,
+// with division, comparisons, select and packed-bit stores).
 #define CMDX_TIER_CAT2(a, b) a##b
 #define CMDX_TIER_CAT(a, b) CMDX_TIER_CAT2(a, b)
-#define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), d), CMDX_DIV)
+#define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), e), CMDX_EXT)
 
 namespace cmdx {
 
@@ -72,6 +73,33 @@ __device__ __forceinline__ uint32_t bin(uint32_t d, uint32_t x) {
   if constexpr (OP == kIMin) return (int32_t)d < (int32_t)x ? d : x;
   if constexpr (OP == kIMax) return (int32_t)d > (int32_t)x ? d : x;
   return 0;
+}
+
+// Comparison c (CmpOp) of d with x: 1 or 0. Float relations are the IEEE
+// ones (a NaN makes all but != false; -0 == +0).
+__device__ __forceinline__ uint32_t cmp_rel(int c, uint32_t d, uint32_t x) {
+  const float fd = __uint_as_float(d), fx = __uint_as_float(x);
+  const int32_t id = (int32_t)d, ix = (int32_t)x;
+  bool r;
+  switch (c) {
+    case kCFLt: r = fd < fx; break;
+    case kCFLe: r = fd <= fx; break;
+    case kCFGt: r = fd > fx; break;
+    case kCFGe: r = fd >= fx; break;
+    case kCFEq: r = fd == fx; break;
+    case kCFNe: r = fd != fx; break;
+    case kCILt: r = id < ix; break;
+    case kCILe: r = id <= ix; break;
+    case kCIGt: r = id > ix; break;
+    case kCIGe: r = id >= ix; break;
+    case kCIEq: r = d == x; break;
+    case kCINe: r = d != x; break;
+    case kCULt: r = d < x; break;
+    case kCULe: r = d <= x; break;
+    case kCUGt: r = d > x; break;
+    default: r = d >= x; break;
+  }
+  return r ? 1u : 0u;
 }
 
 template <int OP>
@@ -157,25 +185,33 @@ __device__ __forceinline__ void st_elem(void* base, int64_t off, uint32_t x) {
     pol.template store<t_>(r[s_], aux); \
     break;
 
-#define CMDX_ST_CASES(SA) \
-  SA(CMDX_ST_CASE, kStF32) SA(CMDX_ST_CASE, kStF16) SA(CMDX_ST_CASE, kStBF16) SA(CMDX_ST_CASE, kStI32)
+// packed-bit stores exist in the extended variant only (the base variant
+// ends the program there; the host never launches that pairing)
+#define CMDX_ST_CASE_B1(s_, t_)                                 \
+  case kStB1 * S + (s_):                                        \
+    if constexpr (EXT) pol.template store<kStB1>(r[s_], aux);   \
+    else return;                                                \
+    break;
+
+#define CMDX_ST_CASES(SA)                                                                       \
+  SA(CMDX_ST_CASE, kStF32) SA(CMDX_ST_CASE, kStF16) SA(CMDX_ST_CASE, kStBF16) SA(CMDX_ST_CASE, kStI32) \
+  SA(CMDX_ST_CASE_B1, 0)
 
 // Run the program in `prog` (constant memory) over the thread's slots. The
 // compute words run inside the inline-PTX loop of interp_asm.cuh; each store
 // word comes back here and is performed by Pol::store<T>(slot, out_index).
-template <int S, int V, bool DIV, class Pol>
+template <int S, int V, bool EXT, class Pol>
 __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* __restrict__ prog,
                                           const uint32_t* __restrict__ scal, Pol& pol) {
-  // (a division word reaching the variant without division ops leaves the
-  // loop and ends the program here, like the end word; the host never
-  // launches such a pairing)
+  // (in the base variant an extended word leaves the loop and ends the
+  // program here, like the end word; the host never launches that pairing)
   static_assert(S == 2 || S == 4 || S == 8, "fused dispatch is generated for 2, 4 and 8 slots");
   uint32_t idx = 0;
 #pragma unroll 1
   for (;;) {
-    const uint32_t w = AsmInterp<S, V, DIV>::run(r, idx, prog, scal);
+    const uint32_t w = AsmInterp<S, V, EXT>::run(r, idx, prog, scal);
     const uint32_t c = (w & 0xffffu) - fz_store(S, 0, 0);
-    if (c >= 4u * S) return;  // the end word
+    if (c >= uint32_t(kNumSt) * S) return;  // the end word
     const uint32_t aux = w >> 16;
     if constexpr (S == 2) {
       switch (c) {
@@ -226,7 +262,7 @@ __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* _
     CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = un<op_>(x[v]); \
   } break;
 
-template <int V, bool DIV, class Pol>
+template <int V, bool EXT, class Pol>
 __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* __restrict__ prog,
                                          const uint32_t* __restrict__ scal, Pol& pol) {
 #pragma unroll 1
@@ -248,9 +284,9 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
     }
     if (base >= kWBin0 + kFDiv && base <= kWBin0 + kIRdiv) {
       // the division ops (kFDiv, kFRdiv, kIDiv, kIRdiv are consecutive): one
-      // body for every destination, fetch, divide, write back; the variant
-      // without them ends the program (the host never launches that pairing)
-      if constexpr (!DIV) return;
+      // body for every destination, fetch, divide, write back; the base
+      // variant ends the program (the host never launches that pairing)
+      if constexpr (!EXT) return;
       const uint32_t d = (w >> 16) & 0xffu;
       uint32_t y[V];
       switch (d) {
@@ -269,9 +305,45 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
       }
       continue;
     }
-    if (base >= kWStore0) {
+    if (base >= kWCmp0 && base < kWCmp0 + kNumCmp) {
+      // comparisons: one body for every destination, like the divisions
+      if constexpr (!EXT) return;
+      const uint32_t d = (w >> 16) & 0xffu;
+      uint32_t y[V];
+      switch (d) {
+        CMDX_SA32(CMDX_W_FETCH_Y, 0)
+        default: break;
+      }
+      CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = cmp_rel((int)(base - kWCmp0), y[v], x[v]);
+      switch (d) {
+        CMDX_SA32(CMDX_W_PUT_Y, 0)
+        default: break;
+      }
+      continue;
+    }
+    if (base == kWSel) {
+      // d = X != 0 ? d : x, X the staging slot 31
+      if constexpr (!EXT) return;
+      const uint32_t d = (w >> 16) & 0xffu;
+      uint32_t y[V];
+      switch (d) {
+        CMDX_SA32(CMDX_W_FETCH_Y, 0)
+        default: break;
+      }
+      CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = r[31][v] != 0u ? y[v] : x[v];
+      switch (d) {
+        CMDX_SA32(CMDX_W_PUT_Y, 0)
+        default: break;
+      }
+      continue;
+    }
+    if (base >= kWStore0 && base < kWStore0 + kNumSt) {
       switch (base - kWStore0) {
         case kStF32: pol.template store<kStF32>(x, aux); break;
+        case kStB1:
+          if constexpr (EXT) pol.template store<kStB1>(x, aux);
+          else return;
+          break;
         case kStF16: pol.template store<kStF16>(x, aux); break;
         case kStBF16: pol.template store<kStBF16>(x, aux); break;
         default: pol.template store<kStI32>(x, aux); break;
@@ -292,11 +364,11 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
   }
 }
 
-template <int TIER, int V, bool DIV, class Pol>
+template <int TIER, int V, bool EXT, class Pol>
 __device__ __forceinline__ void run_program(uint32_t (&r)[tier_slots(TIER)][V], const uint32_t* prog,
                                             const uint32_t* scal, Pol& pol) {
-  if constexpr (TIER == kTier32) run_wide<V, DIV>(r, prog, scal, pol);
-  else run_fused<tier_slots(TIER), V, DIV>(r, prog, scal, pol);
+  if constexpr (TIER == kTier32) run_wide<V, EXT>(r, prog, scal, pol);
+  else run_fused<tier_slots(TIER), V, EXT>(r, prog, scal, pol);
 }
 
 // ---- element-to-lane map of the contiguous and generic executors --------------

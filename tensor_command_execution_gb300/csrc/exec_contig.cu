@@ -5,12 +5,12 @@
 // the host hands a ragged tail (fewer than 32*V elements) to the generic
 // executor, so the hot loop carries no bounds checks.
 //
-// Compiled once per tier and division variant: CMDX_TIER and CMDX_DIV select
+// Compiled once per tier and op-set variant: CMDX_TIER and CMDX_EXT select
 // the kernel this object holds.
 #include "exec_common.cuh"
 
-#if !defined(CMDX_TIER) || !defined(CMDX_DIV)
-#error "exec_contig.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_DIV=<0|1>"
+#if !defined(CMDX_TIER) || !defined(CMDX_EXT)
+#error "exec_contig.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_EXT=<0|1>"
 #endif
 
 namespace cmdx {
@@ -60,48 +60,96 @@ struct ContigStore {
   __device__ __forceinline__ void store(const uint32_t (&x)[V], uint32_t o) const {
     using M = LaneMap<V>;
     void* base = p.out[o];
+    if constexpr (T == kStB1) {
+      // one bit per element: a lane's G bits of group h go to bits
+      // G * (lane % L) .. of word (group start) / 32 + lane / L, L = 32 / G
+      // lanes sharing a word; an xor-shuffle tree ORs them together
+      constexpr int G = M::G, L = 32 / G;
+      const int lane = threadIdx.x & 31;
+      const int64_t chunk = e0 - (int64_t)lane * G;  // a multiple of 32 * V
 #pragma unroll
-    for (int h = 0; h < M::NG; ++h) {
-      const int64_t e = e0 + (int64_t)h * 32 * M::G;
-      const uint32_t* v = &x[h * M::G];
-      if constexpr (T == kStF32 || T == kStI32) {
-        if constexpr (M::G == 4)
-          st_stream(reinterpret_cast<uint4*>(static_cast<uint32_t*>(base) + e), make_uint4(v[0], v[1], v[2], v[3]));
-        else
-          st_stream(reinterpret_cast<uint2*>(static_cast<uint32_t*>(base) + e), make_uint2(v[0], v[1]));
-      } else {
-        auto nar = [](uint32_t a, uint32_t b) {
-          if constexpr (T == kStF16) return narrow_f16x2(a, b);
-          else return narrow_bf16x2(a, b);
-        };
-        if constexpr (M::G == 4)
-          st_stream(reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + e),
-                    make_uint2(nar(v[0], v[1]), nar(v[2], v[3])));
-        else
-          st_stream(reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(base) + e), nar(v[0], v[1]));
+      for (int h = 0; h < M::NG; ++h) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int j = 0; j < G; ++j) bits |= (x[h * G + j] != 0u ? 1u : 0u) << j;
+        bits <<= G * (lane % L);
+#pragma unroll
+        for (int m = 1; m < L; m <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, m);
+        if (lane % L == 0)
+          st_stream(static_cast<uint32_t*>(base) + (chunk + (int64_t)h * 32 * G) / 32 + lane / L, bits);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < M::NG; ++h) {
+        const int64_t e = e0 + (int64_t)h * 32 * M::G;
+        const uint32_t* v = &x[h * M::G];
+        if constexpr (T == kStF32 || T == kStI32) {
+          if constexpr (M::G == 4)
+            st_stream(reinterpret_cast<uint4*>(static_cast<uint32_t*>(base) + e), make_uint4(v[0], v[1], v[2], v[3]));
+          else
+            st_stream(reinterpret_cast<uint2*>(static_cast<uint32_t*>(base) + e), make_uint2(v[0], v[1]));
+        } else {
+          auto nar = [](uint32_t a, uint32_t b) {
+            if constexpr (T == kStF16) return narrow_f16x2(a, b);
+            else return narrow_bf16x2(a, b);
+          };
+          if constexpr (M::G == 4)
+            st_stream(reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + e),
+                      make_uint2(nar(v[0], v[1]), nar(v[2], v[3])));
+          else
+            st_stream(reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(base) + e), nar(v[0], v[1]));
+        }
       }
     }
   }
 };
 
-template <int TIER, bool DIV>
+template <int TIER, bool EXT>
 __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(const __grid_constant__ ContigParams p) {
   constexpr int S = tier_slots(TIER);
-  constexpr int V = tier_vec(TIER);
+  constexpr int V = tier_vec(TIER, EXT);
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
   using M = LaneMap<V>;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t* prog = c_prog[p.prog];
   const int64_t n_chunks = p.n / M::W;  // the host passes a multiple of W
-  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n_chunks; w += nwarps) {
-    const int64_t e0 = w * M::W + (int64_t)lane * M::G;
-    uint32_t r[S][V];
+  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if constexpr (contig_prefetch(TIER, EXT)) {
+    // software pipeline: the next chunk's loads are issued before the
+    // program runs on this one, so their latency overlaps its work and
+    // stores (the base 2-slot tier has the registers for a second set)
+    uint32_t nx[NL][V];
+    if (w < n_chunks) {
 #pragma unroll
-    for (int j = 0; j < NL; ++j)
-      if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
-    ContigStore<V> st{p, e0};
-    run_program<TIER, V, DIV>(r, prog, p.scal, st);
+      for (int j = 0; j < NL; ++j)
+        if (j < (int)p.n_loads) contig_load<V>(nx[j], p.in[j], p.in_dt[j], w * M::W + (int64_t)lane * M::G);
+    }
+    for (; w < n_chunks; w += nwarps) {
+      const int64_t e0 = w * M::W + (int64_t)lane * M::G;
+      uint32_t r[S][V];
+#pragma unroll
+      for (int j = 0; j < NL; ++j)
+#pragma unroll
+        for (int v = 0; v < V; ++v) r[j][v] = nx[j][v];
+      if (w + nwarps < n_chunks) {
+#pragma unroll
+        for (int j = 0; j < NL; ++j)
+          if (j < (int)p.n_loads) contig_load<V>(nx[j], p.in[j], p.in_dt[j], e0 + nwarps * M::W);
+      }
+      ContigStore<V> st{p, e0};
+      run_program<TIER, V, EXT>(r, prog, p.scal, st);
+    }
+  } else {
+    for (; w < n_chunks; w += nwarps) {
+      const int64_t e0 = w * M::W + (int64_t)lane * M::G;
+      uint32_t r[S][V];
+#pragma unroll
+      for (int j = 0; j < NL; ++j)
+        if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
+      ContigStore<V> st{p, e0};
+      run_program<TIER, V, EXT>(r, prog, p.scal, st);
+    }
   }
 }
 
@@ -109,9 +157,9 @@ cudaError_t CMDX_TIER_NAME(contig_upload_t)(int slot, const uint32_t* words, int
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
-template <int TIER, bool DIV>
+template <int TIER, bool EXT>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
-  constexpr int V = tier_vec(TIER);
+  constexpr int V = tier_vec(TIER, EXT);
   constexpr int kBlock = 256;
   static int grid_cache[64] = {0};
   int dev = 0;
@@ -119,16 +167,16 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
   if (full_grid == 0) {
-    full_grid = persistent_grid(contig_kernel<TIER, DIV>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(contig_kernel<TIER, EXT>, kBlock, 0, INT64_MAX);
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  contig_kernel<TIER, DIV><<<grid, kBlock, 0, stream>>>(p);
+  contig_kernel<TIER, EXT><<<grid, kBlock, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
-  return launch_tier<CMDX_TIER, CMDX_DIV != 0>(p, stream);
+  return launch_tier<CMDX_TIER, CMDX_EXT != 0>(p, stream);
 }
 
 }  // namespace cmdx

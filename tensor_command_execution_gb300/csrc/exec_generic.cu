@@ -8,12 +8,12 @@
 // of a warp handles elements base + 32 v + l, so views that are contiguous in
 // the innermost dim are still read with consecutive addresses across a warp.
 //
-// Compiled once per tier and division variant: CMDX_TIER and CMDX_DIV select
+// Compiled once per tier and op-set variant: CMDX_TIER and CMDX_EXT select
 // the kernel this object holds.
 #include "exec_common.cuh"
 
-#if !defined(CMDX_TIER) || !defined(CMDX_DIV)
-#error "exec_generic.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_DIV=<0|1>"
+#if !defined(CMDX_TIER) || !defined(CMDX_EXT)
+#error "exec_generic.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_EXT=<0|1>"
 #endif
 
 namespace cmdx {
@@ -50,6 +50,17 @@ struct GenericStore {
   template <int T>
   __device__ __forceinline__ void store(const uint32_t (&x)[V], uint32_t o) const {
     void* ptr = p.out[o];
+    if constexpr (T == kStB1) {
+      // one bit per element, at its row-major index (the view is dense):
+      // the warp's 32 consecutive elements base + 32 v + lane make one word
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int64_t e = base + 32 * v + lane;
+        const uint32_t bits = __ballot_sync(0xffffffffu, e < p.n && x[v] != 0u);
+        if (lane == 0 && base + 32 * v < p.n) __stcs(static_cast<unsigned int*>(ptr) + (base + 32 * v) / 32, bits);
+      }
+      return;
+    }
     const int64_t* st = p.out_st[o];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -59,7 +70,7 @@ struct GenericStore {
   }
 };
 
-template <int TIER, bool DIV>
+template <int TIER, bool EXT>
 __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(const __grid_constant__ GenericParams p) {
   constexpr int S = tier_slots(TIER);
   constexpr int V = tier_vec_strided(TIER);
@@ -81,7 +92,7 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(con
       }
     }
     GenericStore<V> st{p, base, lane};
-    run_program<TIER, V, DIV>(r, prog, p.scal, st);
+    run_program<TIER, V, EXT>(r, prog, p.scal, st);
   }
 }
 
@@ -89,7 +100,7 @@ cudaError_t CMDX_TIER_NAME(generic_upload_t)(int slot, const uint32_t* words, in
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
-template <int TIER, bool DIV>
+template <int TIER, bool EXT>
 static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
   constexpr int V = tier_vec_strided(TIER);
   constexpr int kBlock = 256;
@@ -99,16 +110,16 @@ static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
   if (full_grid == 0) {
-    full_grid = persistent_grid(generic_kernel<TIER, DIV>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(generic_kernel<TIER, EXT>, kBlock, 0, INT64_MAX);
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  generic_kernel<TIER, DIV><<<grid, kBlock, 0, stream>>>(p);
+  generic_kernel<TIER, EXT><<<grid, kBlock, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t CMDX_TIER_NAME(generic_launch_t)(const GenericParams& p, cudaStream_t stream) {
-  return launch_tier<CMDX_TIER, CMDX_DIV != 0>(p, stream);
+  return launch_tier<CMDX_TIER, CMDX_EXT != 0>(p, stream);
 }
 
 }  // namespace cmdx

@@ -9,7 +9,7 @@
 
 namespace cmdx {
 
-int contig_chunk(int tier) { return 32 * (tier == kTier32 ? tier_vec(kTier32) : tier_vec(kTier4)); }
+int contig_chunk(int tier, bool ext) { return 32 * tier_vec(tier, ext); }
 
 namespace {
 
@@ -18,51 +18,51 @@ using ContigLaunch = cudaError_t (*)(const ContigParams&, cudaStream_t);
 using GenericLaunch = cudaError_t (*)(const GenericParams&, cudaStream_t);
 using TileLaunch = cudaError_t (*)(const Tile2dParams&, cudaStream_t);
 
-// [division variant][tier]
+// [op-set variant][tier]
 constexpr Upload kContigUpload[2][4] = {
-    {contig_upload_t0d0, contig_upload_t1d0, contig_upload_t2d0, contig_upload_t3d0},
-    {contig_upload_t0d1, contig_upload_t1d1, contig_upload_t2d1, contig_upload_t3d1}};
+    {contig_upload_t0e0, contig_upload_t1e0, contig_upload_t2e0, contig_upload_t3e0},
+    {contig_upload_t0e1, contig_upload_t1e1, contig_upload_t2e1, contig_upload_t3e1}};
 constexpr Upload kGenericUpload[2][4] = {
-    {generic_upload_t0d0, generic_upload_t1d0, generic_upload_t2d0, generic_upload_t3d0},
-    {generic_upload_t0d1, generic_upload_t1d1, generic_upload_t2d1, generic_upload_t3d1}};
+    {generic_upload_t0e0, generic_upload_t1e0, generic_upload_t2e0, generic_upload_t3e0},
+    {generic_upload_t0e1, generic_upload_t1e1, generic_upload_t2e1, generic_upload_t3e1}};
 constexpr ContigLaunch kContigLaunch[2][4] = {
-    {contig_launch_t0d0, contig_launch_t1d0, contig_launch_t2d0, contig_launch_t3d0},
-    {contig_launch_t0d1, contig_launch_t1d1, contig_launch_t2d1, contig_launch_t3d1}};
+    {contig_launch_t0e0, contig_launch_t1e0, contig_launch_t2e0, contig_launch_t3e0},
+    {contig_launch_t0e1, contig_launch_t1e1, contig_launch_t2e1, contig_launch_t3e1}};
 constexpr GenericLaunch kGenericLaunch[2][4] = {
-    {generic_launch_t0d0, generic_launch_t1d0, generic_launch_t2d0, generic_launch_t3d0},
-    {generic_launch_t0d1, generic_launch_t1d1, generic_launch_t2d1, generic_launch_t3d1}};
-// [division variant][view variant][tier]; the 32-slot tier has no tile kernel
+    {generic_launch_t0e0, generic_launch_t1e0, generic_launch_t2e0, generic_launch_t3e0},
+    {generic_launch_t0e1, generic_launch_t1e1, generic_launch_t2e1, generic_launch_t3e1}};
+// [op-set variant][view variant][tier]; the 32-slot tier has no tile kernel
 constexpr Upload kTileUpload[2][2][3] = {
-    {{tile2d_upload_t0n0d0, tile2d_upload_t1n0d0, tile2d_upload_t2n0d0},
-     {tile2d_upload_t0n1d0, tile2d_upload_t1n1d0, tile2d_upload_t2n1d0}},
-    {{tile2d_upload_t0n0d1, tile2d_upload_t1n0d1, tile2d_upload_t2n0d1},
-     {tile2d_upload_t0n1d1, tile2d_upload_t1n1d1, tile2d_upload_t2n1d1}}};
+    {{tile2d_upload_t0n0e0, tile2d_upload_t1n0e0, tile2d_upload_t2n0e0},
+     {tile2d_upload_t0n1e0, tile2d_upload_t1n1e0, tile2d_upload_t2n1e0}},
+    {{tile2d_upload_t0n0e1, tile2d_upload_t1n0e1, tile2d_upload_t2n0e1},
+     {tile2d_upload_t0n1e1, tile2d_upload_t1n1e1, tile2d_upload_t2n1e1}}};
 constexpr TileLaunch kTileLaunch[2][2][3] = {
-    {{tile2d_launch_t0n0d0, tile2d_launch_t1n0d0, tile2d_launch_t2n0d0},
-     {tile2d_launch_t0n1d0, tile2d_launch_t1n1d0, tile2d_launch_t2n1d0}},
-    {{tile2d_launch_t0n0d1, tile2d_launch_t1n0d1, tile2d_launch_t2n0d1},
-     {tile2d_launch_t0n1d1, tile2d_launch_t1n1d1, tile2d_launch_t2n1d1}}};
+    {{tile2d_launch_t0n0e0, tile2d_launch_t1n0e0, tile2d_launch_t2n0e0},
+     {tile2d_launch_t0n1e0, tile2d_launch_t1n1e0, tile2d_launch_t2n1e0}},
+    {{tile2d_launch_t0n0e1, tile2d_launch_t1n0e1, tile2d_launch_t2n0e1},
+     {tile2d_launch_t0n1e1, tile2d_launch_t1n1e1, tile2d_launch_t2n1e1}}};
 
 bool tier_ok(int tier) { return tier >= kTier2 && tier <= kTier32; }
 
 }  // namespace
 
-cudaError_t upload_program(int tier, bool div, int slot, const uint32_t* words, int n) {
+cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, int n) {
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
-  cudaError_t e = kContigUpload[div][tier](slot, words, n);
-  if (e == cudaSuccess) e = kGenericUpload[div][tier](slot, words, n);
-  for (int nd = 0; nd < 2 && e == cudaSuccess && tier != kTier32; ++nd) e = kTileUpload[div][nd][tier](slot, words, n);
+  cudaError_t e = kContigUpload[ext][tier](slot, words, n);
+  if (e == cudaSuccess) e = kGenericUpload[ext][tier](slot, words, n);
+  for (int nd = 0; nd < 2 && e == cudaSuccess && tier != kTier32; ++nd) e = kTileUpload[ext][nd][tier](slot, words, n);
   return e;
 }
 
-cudaError_t contig_launch(int tier, bool div, const ContigParams& p, cudaStream_t stream) {
+cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream) {
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
-  return kContigLaunch[div][tier](p, stream);
+  return kContigLaunch[ext][tier](p, stream);
 }
 
-cudaError_t generic_launch(int tier, bool div, const GenericParams& p, cudaStream_t stream) {
+cudaError_t generic_launch(int tier, bool ext, const GenericParams& p, cudaStream_t stream) {
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
-  return kGenericLaunch[div][tier](p, stream);
+  return kGenericLaunch[ext][tier](p, stream);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -78,7 +78,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-cudaError_t tile2d_launch(int tier, bool div, const Tile2dLaunch& L, cudaStream_t stream) {
+cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_t stream) {
   static_assert(sizeof(Tile2dParams) < 8192, "kernel parameters stay small");
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
@@ -150,7 +150,7 @@ cudaError_t tile2d_launch(int tier, bool div, const Tile2dLaunch& L, cudaStream_
   bool nd = L.nb[0] > 1 || L.nb[1] > 1;
   for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
   if (tier < kTier2 || tier > kTier8) return cudaErrorInvalidValue;  // no 32-slot tile kernel
-  return kTileLaunch[div][nd][tier](p, stream);
+  return kTileLaunch[ext][nd][tier](p, stream);
 }
 
 }  // namespace cmdx

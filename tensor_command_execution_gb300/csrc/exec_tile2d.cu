@@ -26,17 +26,17 @@
 //
 // Compiled once per tier (CMDX_TIER 0..2), view variant (CMDX_ND 0: plain
 // 2-D views; 1: batch dims, broadcast loads or descriptors of another rank)
-// and division variant (CMDX_DIV): each object holds one kernel. The TMA
+// and op-set variant (CMDX_EXT): each object holds one kernel. The TMA
 // descriptors are encoded on the host (exec_host.cpp).
 #include "exec_common.cuh"
 #include "exec_tile2d.h"
 
-#if !defined(CMDX_TIER) || !defined(CMDX_ND) || !defined(CMDX_DIV)
-#error "exec_tile2d.cu is compiled per variant, with -DCMDX_TIER=<0..2> -DCMDX_ND=<0|1> -DCMDX_DIV=<0|1>"
+#if !defined(CMDX_TIER) || !defined(CMDX_ND) || !defined(CMDX_EXT)
+#error "exec_tile2d.cu is compiled per variant, with -DCMDX_TIER=<0..2> -DCMDX_ND=<0|1> -DCMDX_EXT=<0|1>"
 #endif
-// tile2d_<f>_t<tier>n<nd>d<div>: this object's entry points
+// tile2d_<f>_t<tier>n<nd>e<ext>: this object's entry points
 #define CMDX_TILE_NAME(f) \
-  CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), n), CMDX_ND), d), CMDX_DIV)
+  CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), n), CMDX_ND), e), CMDX_EXT)
 
 namespace cmdx {
 
@@ -280,6 +280,9 @@ struct TileStore {
 
   template <int T>
   __device__ __forceinline__ void store(const uint32_t (&x)[8], uint32_t o) const {
+    // packed-bit stores never come here: the host plans programs that have
+    // them onto the contiguous or generic executor
+    if constexpr (T == kStB1) return;
     void* base = p.out[o];
     int64_t off = i * p.out_ld[o] + j;
     if (ND) off += (int64_t)b0 * p.out_bst[o][0] + (int64_t)b1 * p.out_bst[o][1];
@@ -331,7 +334,7 @@ CMDX_HD constexpr int tile_rows_per_thread(int tier) { return tier == kTier8 ? 1
 
 // ND: the launch has batch dims or broadcast loads. Plain 2-D launches
 // compile without that bookkeeping (the consumer warps are issue-bound).
-template <int TIER, bool ND, bool DIV>
+template <int TIER, bool ND, bool EXT>
 __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel(const __grid_constant__ Tile2dParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int S = tier_slots(TIER);
@@ -467,10 +470,10 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
         }
         if constexpr (RPT == 2) {
           TileStore2<ND> sto{{p, i, jc, fullc, nleft, b0, b1}, {p, i + 1, jc, fullc, nleft, b0, b1}, i + 1 < p.rows};
-          run_program<TIER, V, DIV>(r, prog, p.scal, sto);
+          run_program<TIER, V, EXT>(r, prog, p.scal, sto);
         } else {
           TileStore<ND> sto{p, i, jc, fullc, nleft, b0, b1};
-          run_program<TIER, V, DIV>(r, prog, p.scal, sto);
+          run_program<TIER, V, EXT>(r, prog, p.scal, sto);
         }
       }
     }
@@ -485,7 +488,7 @@ cudaError_t CMDX_TILE_NAME(tile2d_upload_t)(int slot, const uint32_t* words, int
 
 // ---- host side ----------------------------------------------------------------
 
-template <int TIER, bool ND, bool DIV>
+template <int TIER, bool ND, bool EXT>
 static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes;
   static int grid_cache[64][kMaxStages + 1] = {};
@@ -494,7 +497,7 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   cudaGetDevice(&dev);
   const bool cacheable = dev >= 0 && dev < 64;
   if (!cacheable || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND, DIV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBarrierBytes + 2 * kTileStageLimit + 4096);
     if (e != cudaSuccess) return e;
     if (cacheable) attr_set[dev] = true;
@@ -504,16 +507,16 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const bool cache_ok = cacheable && p.stage_bytes == 16384;
   if (cache_ok) full_grid = grid_cache[dev][p.n_stages];
   if (full_grid == 0) {
-    full_grid = persistent_grid(tile2d_kernel<TIER, ND, DIV>, kThreads, smem, INT64_MAX);
+    full_grid = persistent_grid(tile2d_kernel<TIER, ND, EXT>, kThreads, smem, INT64_MAX);
     if (cache_ok) grid_cache[dev][p.n_stages] = full_grid;
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
-  tile2d_kernel<TIER, ND, DIV><<<grid, kThreads, smem, stream>>>(p);
+  tile2d_kernel<TIER, ND, EXT><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t CMDX_TILE_NAME(tile2d_launch_t)(const Tile2dParams& p, cudaStream_t stream) {
-  return launch_tier<CMDX_TIER, CMDX_ND != 0, CMDX_DIV != 0>(p, stream);
+  return launch_tier<CMDX_TIER, CMDX_ND != 0, CMDX_EXT != 0>(p, stream);
 }
 
 }  // namespace cmdx

@@ -44,8 +44,8 @@ struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
 // (0..2), view variant x (0 for plain 2-D views, 1 for batch dims, broadcast
 // loads or descriptors of rank other than 2) and division variant v.
 #define CMDX_DECL_TILE(t, x, v)                                                         \
-  cudaError_t tile2d_upload_t##t##n##x##d##v(int slot, const uint32_t* words, int n_words); \
-  cudaError_t tile2d_launch_t##t##n##x##d##v(const Tile2dParams& p, cudaStream_t stream);
+  cudaError_t tile2d_upload_t##t##n##x##e##v(int slot, const uint32_t* words, int n_words); \
+  cudaError_t tile2d_launch_t##t##n##x##e##v(const Tile2dParams& p, cudaStream_t stream);
 CMDX_DECL_TILE(0, 0, 0) CMDX_DECL_TILE(0, 1, 0) CMDX_DECL_TILE(1, 0, 0)
 CMDX_DECL_TILE(1, 1, 0) CMDX_DECL_TILE(2, 0, 0) CMDX_DECL_TILE(2, 1, 0)
 CMDX_DECL_TILE(0, 0, 1) CMDX_DECL_TILE(0, 1, 1) CMDX_DECL_TILE(1, 0, 1)

@@ -16,6 +16,15 @@ the site, where the quotient is moved into the destination register. One
 element at a time keeps only two staging registers live beside the slots
 (no spills), and one shared body keeps the generated code small.
 
+Comparisons and selects read the staging slot X (the tier's last slot,
+filled by the word before): `d = d rel X`, `d = d rel scalar`,
+`d = X != 0 ? d : s` and `d = X != 0 ? d : scalar`, S cases each.
+
+Each tier is emitted twice: the extended variant has the division,
+comparison and select cases; in the base variant those cases exit like the
+end word, so its loop carries none of their code (the host runs a program
+on the base variant only when it has none of them).
+
 Run: python gen_interp.py  (writes interp_asm.cuh next to this file)
 """
 from __future__ import annotations
@@ -29,6 +38,7 @@ TIERS = [(2, 8), (2, 16), (4, 8), (4, 16), (8, 8), (8, 4)]
 
 N_BIN = 16
 N_UN = 7
+N_ST = 5   # store types (f32, f16, bf16, i32, packed bits)
 
 # Binary ops d = d (op) x, in BinOp order of cmd_internal.h. A string is an
 # inline body ("{d}" destination, "{x}" source); a tuple ("staged", name,
@@ -70,6 +80,15 @@ UN = [
 ]
 assert len(UN) == N_UN
 
+# Comparisons d = (d rel x) ? 1 : 0, in CmpOp order: float (ordered, so false
+# on NaN, except ne, which is the unordered-or-not-equal test and so true on
+# NaN: the IEEE != ), signed int, unsigned int.
+CMP = [f"{rel}.f32" for rel in ("lt", "le", "gt", "ge", "eq", "neu")] + \
+      [f"{rel}.s32" for rel in ("lt", "le", "gt", "ge", "eq", "ne")] + \
+      [f"{rel}.u32" for rel in ("lt", "le", "gt", "ge")]
+N_CMP = len(CMP)
+assert N_CMP == 16
+
 
 def staged_body(name: str) -> str:
     """Result in %%xa from operands %%xa, %%xb (one element)."""
@@ -85,12 +104,13 @@ def staged_body(name: str) -> str:
             "selp.b32 %%xa, -1, %%t, %%p0;")
 
 
-def gen_tier(S: int, V: int, div: bool) -> str:
+def gen_tier(S: int, V: int, ext: bool) -> str:
     def reg(i, v):
         return f"%{i * V + v}"
 
-    end = (N_BIN + N_UN) * S * S + (N_BIN + 5) * S
-    n_cases = end + 1
+    end = (N_BIN + N_UN) * S * S + (N_BIN + 1 + N_ST) * S
+    n_cases = end + 1 + 2 * N_CMP * S + S * S + S
+    X = S - 1  # the staging slot compares and selects read
     slot_ops = S * V
     o_idx = slot_ops        # "+r" program index (words)
     o_word = slot_ops + 1   # "=r" the word that left the loop
@@ -122,7 +142,7 @@ def gen_tier(S: int, V: int, div: bool) -> str:
                 lab = f"$LB{b}_{d}_{s}"
                 labels.append(lab)
                 op = BIN[b]
-                if isinstance(op, tuple) and not div:
+                if isinstance(op, tuple) and not ext:
                     labels[-1] = "$Lexit"
                     continue
                 if isinstance(op, tuple):
@@ -147,7 +167,7 @@ def gen_tier(S: int, V: int, div: bool) -> str:
             lab = f"$LS{b}_{d}"
             labels.append(lab)
             op = BIN[b]
-            if isinstance(op, tuple) and not div:
+            if isinstance(op, tuple) and not ext:
                 labels[-1] = "$Lexit"
                 continue
             if isinstance(op, tuple):
@@ -162,9 +182,53 @@ def gen_tier(S: int, V: int, div: bool) -> str:
         labels.append(lab)
         ops = " ".join(f"mov.b32 {reg(d, v)}, %%k;" for v in range(V))
         bodies.append(f"{lab}: {load_k} {ops} bra.uni $Lloop;")
-    # stores and end leave the loop; the table is padded to a power of two
-    # with exits so that masking the case number keeps every jump inside it
-    labels += ["$Lexit"] * (4 * S + 1)
+    # stores and end leave the loop
+    labels += ["$Lexit"] * (N_ST * S + 1)
+    # comparisons with the staging slot, then with a scalar; selects on the
+    # staging slot with a slot, then with a scalar. An op that reads the
+    # staging slot never has it as destination or source (the lowering keeps
+    # it free): those cases exit, and the host encoder never emits them.
+    for c in range(N_CMP):
+        for d in range(S):
+            if d == X or not ext:
+                labels.append("$Lexit")
+                continue
+            lab = f"$LCX{c}_{d}"
+            labels.append(lab)
+            ops = " ".join(f"setp.{CMP[c]} %%p0, {reg(d, v)}, {reg(X, v)}; selp.u32 {reg(d, v)}, 1, 0, %%p0;"
+                           for v in range(V))
+            bodies.append(f"{lab}: {ops} bra.uni $Lloop;")
+    for c in range(N_CMP):
+        for d in range(S):  # (no staging slot read: every destination is valid)
+            if not ext:
+                labels.append("$Lexit")
+                continue
+            lab = f"$LCS{c}_{d}"
+            labels.append(lab)
+            ops = " ".join(f"setp.{CMP[c]} %%p0, {reg(d, v)}, %%k; selp.u32 {reg(d, v)}, 1, 0, %%p0;"
+                           for v in range(V))
+            bodies.append(f"{lab}: {load_k} {ops} bra.uni $Lloop;")
+    for d in range(S):
+        for s_ in range(S):
+            if d == X or s_ == X or not ext:
+                labels.append("$Lexit")
+                continue
+            lab = f"$LSEL{d}_{s_}"
+            labels.append(lab)
+            ops = " ".join(f"setp.ne.u32 %%p0, {reg(X, v)}, 0; selp.b32 {reg(d, v)}, {reg(d, v)}, {reg(s_, v)}, %%p0;"
+                           for v in range(V))
+            bodies.append(f"{lab}: {ops} bra.uni $Lloop;")
+    for d in range(S):
+        if d == X or not ext:
+            labels.append("$Lexit")
+            continue
+        lab = f"$LSELS{d}"
+        labels.append(lab)
+        ops = " ".join(f"setp.ne.u32 %%p0, {reg(X, v)}, 0; selp.b32 {reg(d, v)}, {reg(d, v)}, %%k, %%p0;"
+                       for v in range(V))
+        bodies.append(f"{lab}: {load_k} {ops} bra.uni $Lloop;")
+    # the table is padded to a power of two with exits so that masking the
+    # case number keeps every jump inside it
     assert len(labels) == n_cases
     size = 1
     while size < n_cases:
@@ -217,9 +281,9 @@ def gen_tier(S: int, V: int, div: bool) -> str:
     outs = ", ".join(f'"+r"(r[{i}][{v}])' for i in range(S) for v in range(V))
     return f"""
 template <>
-struct AsmInterp<{S}, {V}, {"true" if div else "false"}> {{
+struct AsmInterp<{S}, {V}, {"true" if ext else "false"}> {{
   // Run compute words from prog[idx] on; return the first store or end word
-  // (idx then points past it).{"" if div else " Division words are not in this variant: they leave the loop like an end word."}
+  // (idx then points past it).{"" if ext else " Extended words (division, comparison, select) are not in this variant: they leave the loop like an end word."}
   static __device__ __forceinline__ uint32_t run(uint32_t (&r)[{S}][{V}], uint32_t& idx, const uint32_t* prog,
                                                  const uint32_t* scal) {{
     uint32_t word;
@@ -239,13 +303,14 @@ def main():
         "// interp_asm.cuh - GENERATED by gen_interp.py; do not edit by hand.\n"
         "// The compute-op interpreter loop as inline PTX for each fused tier.\n"
         "#pragma once\n\n#include <cstdint>\n\nnamespace cmdx {\n\n"
-        "// DIV selects the variant with the division ops; programs without a\n"
-        "// division run the one without, whose loop carries no division code.\n"
-        "template <int S, int V, bool DIV>\nstruct AsmInterp;\n"
+        "// EXT selects the variant with the extended ops (division, comparisons,\n"
+        "// select); programs without them run the base variant, whose loop\n"
+        "// carries none of their code.\n"
+        "template <int S, int V, bool EXT>\nstruct AsmInterp;\n"
     ]
     for S, V in TIERS:
-        for div in (False, True):
-            parts.append(gen_tier(S, V, div))
+        for ext in (False, True):
+            parts.append(gen_tier(S, V, ext))
     parts.append("\n}  // namespace cmdx\n")
     with open(OUT, "w") as f:
         f.write("".join(parts))

@@ -10,8 +10,9 @@ import tensor_command_execution_gb300 as T
 from inputgen import workloads as W
 import specutil
 
-TORCH_OF = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.int16, "i32": torch.int32}
-NP_OF = {"f32": np.float32, "f16": np.float16, "bf16": np.int16, "i32": np.int32}
+TORCH_OF = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.int16, "i32": torch.int32,
+            "b1": torch.int32}
+NP_OF = {"f32": np.float32, "f16": np.float16, "bf16": np.int16, "i32": np.int32, "b1": np.int32}
 
 
 def to_device(arr: np.ndarray, dt: str, dev="cuda:0", offset_elems: int = 0) -> torch.Tensor:
@@ -99,5 +100,9 @@ def sampled_parity(spec: dict, n_samples: int = 1 << 20, seed: int = 0):
         sizes = spec["sizes"]
         multi = np.unravel_index(idx, sizes)
         off = sum(m.astype(np.int64) * s for m, s in zip(multi, st))
+        if dts[name] == "b1":  # bit `off` of the packed words
+            g = ((got[name].view(np.uint32)[off // 32] >> (off % 32).astype(np.uint32)) & 1).astype(np.uint8)
+            assert (g == want[name]).all(), f"{spec['name']}:{name} (sampled): {(g != want[name]).sum()} bits differ"
+            continue
         compare(got[name][off], want[name], dts[name], f"{spec['name']}:{name} (sampled)")
     return plan, idx.size

@@ -13,13 +13,13 @@ import inputgen
 from inputgen import workloads
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-NP = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i32": np.int32}
-SENTINEL_BITS = {"f32": 0x7FA5A5A5, "f16": 0x7DA5, "bf16": 0x7FA5, "i32": 0x5A5A5A5A}
+NP = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i32": np.int32, "b1": np.uint32}
+SENTINEL_BITS = {"f32": 0x7FA5A5A5, "f16": 0x7DA5, "bf16": 0x7FA5, "i32": 0x5A5A5A5A, "b1": 0xA5A5A5A5}
 
 
 def sentinel_array(dt: str, n: int) -> np.ndarray:
     """An array of n elements of type dt filled with a recognisable pattern."""
-    if dt in ("f32", "i32"):
+    if dt in ("f32", "i32", "b1"):
         return np.full(n, SENTINEL_BITS[dt], dtype=np.uint32).view(NP[dt])
     return np.full(n, SENTINEL_BITS[dt], dtype=np.uint16).view(NP[dt])
 
@@ -40,7 +40,7 @@ def host_buffers(spec: dict, threads: int | None = None) -> dict:
 
 
 def bits(arr: np.ndarray) -> np.ndarray:
-    return arr.view(np.uint32 if arr.dtype.itemsize == 4 else np.uint16)
+    return arr.view({4: np.uint32, 2: np.uint16, 1: np.uint8}[arr.dtype.itemsize])
 
 
 def same_bits_nan_as_class(got: np.ndarray, want: np.ndarray, dt: str) -> np.ndarray:

@@ -31,6 +31,9 @@ pytestmark = pytest.mark.gpu
     (W.wide_dag(37), "contig"),
     (W.div_clamp_i32((1 << 18) + 9), "contig"),
     (W.div_clamp_i32(100), "contig"),
+    (W.threshold_u32((1 << 18) + 13), "contig"),
+    (W.threshold_bits((1 << 18) + 13), "contig"),
+    (W.threshold_bits(77), "contig"),
 ], ids=lambda x: x["name"] + str(x["sizes"]) if isinstance(x, dict) else x)
 def test_workload_small(spec, path):
     plan = gpuutil.parity(spec)
@@ -670,3 +673,227 @@ def test_new_ops_on_each_executor(path):
     offsets = {"A": 1} if path == "generic" else None
     plan = gpuutil.parity(spec, bufs, offsets)
     assert plan["path"] == path
+
+
+# ---- comparisons, select and packed-bit stores --------------------------------------------
+
+CMP_OPS = ["lt", "le", "gt", "ge", "eq", "ne"]
+UCMP_OPS = ["ult", "ule", "ugt", "uge"]
+
+
+def random_cmp_case(seed):
+    """A random Command over every E op including comparisons and select,
+    float and int values mixed; some int results are stored as packed bits
+    (dense views only, as b1 requires)."""
+    rng = np.random.default_rng(20_000 + seed)
+    rank = int(rng.integers(0, 4))
+    sizes = tuple(int(x) for x in rng.integers(1, 24, size=rank))
+    if rank and rng.random() < 0.4:
+        sizes = sizes[:-1] + (int(rng.integers(100, 700)),)
+    ops, views, bufs = [], {}, {}
+    vals = {"f": [], "i": []}
+    for i in range(int(rng.integers(1, 7))):
+        dt = str(rng.choice(["f32", "f16", "bf16", "i32"]))
+        name = f"L{i}"
+        ops.append(("load", name, dt))
+        st, n = _random_view(rng, sizes, allow_broadcast=True)
+        views[name] = dict(strides=st, alloc=n)
+        bufs[name] = _random_values(rng, dt, n)
+        if dt == "i32" and rng.random() < 0.5:
+            bufs[name] = rng.integers(-3, 4, size=n).astype(np.int32)  # ties in comparisons
+        if dt == "f32" and rng.random() < 0.3:
+            bufs[name][::7] = np.float32(np.nan)
+            bufs[name][1::11] = np.float32(-0.0)
+        vals["i" if dt == "i32" else "f"].append(name)
+    for i in range(int(rng.integers(0, 3))):
+        name = f"S{i}"
+        if rng.random() < 0.5:
+            ops.append(("scalar", name, "i32", int(rng.choice([0, 1, -1, int(rng.integers(-2**31, 2**31))]))))
+            vals["i"].append(name)
+        else:
+            ops.append(("scalar", name, "f32", float(np.float32(rng.choice([0.0, -0.0, 0.5, rng.standard_normal()])))))
+            vals["f"].append(name)
+    block, last = [], []
+    for i in range(int(rng.integers(1, 22))):
+        name = f"E{i}"
+        kind = rng.choice(["bin", "un", "cmp", "ucmp", "sel"], p=[0.3, 0.1, 0.3, 0.1, 0.2])
+        cls = str(rng.choice([c for c in ("f", "i") if vals[c]]))
+        a = str(rng.choice(vals[cls]))
+        if kind == "bin":
+            eop, b, out = str(rng.choice(BIN_OPS)), str(rng.choice(vals[cls])), cls
+            block.append((eop, name, a, b))
+        elif kind == "un":
+            eop = str(rng.choice(UN_OPS))
+            out = {"to_f32": "f", "to_i32": "i"}.get(eop, cls)
+            block.append((eop, name, a, None))
+        elif kind == "cmp" or (kind == "ucmp" and cls == "f"):
+            block.append((str(rng.choice(CMP_OPS)), name, a, str(rng.choice(vals[cls]))))
+            out = "i"
+        elif kind == "ucmp":
+            block.append((str(rng.choice(UCMP_OPS)), name, a, str(rng.choice(vals["i"]))))
+            out = "i"
+        else:
+            if not vals["i"]:
+                continue
+            block.append(("select", name, a, str(rng.choice(vals[cls])), str(rng.choice(vals["i"]))))
+            out = cls
+        vals[out].append(name)
+        last.append((name, out))
+    if not block:
+        block.append(("ne", "E0", vals["i"][0] if vals["i"] else vals["f"][0],
+                      vals["i"][0] if vals["i"] else vals["f"][0]))
+        last.append(("E0", "i"))
+    ops.append(("exec", block))
+    n_el = int(np.prod(sizes)) if sizes else 1
+    for i in range(int(rng.integers(1, 4))):
+        src, cls = last[-1 - int(rng.integers(0, min(4, len(last))))]
+        if cls == "i":
+            dt = "b1" if rng.random() < 0.5 else "i32"
+        else:
+            dt = str(rng.choice(["f32", "f16", "bf16"]))
+        name = f"O{i}"
+        ops.append(("store", name, src, dt))
+        if dt == "b1":
+            st, _ = _dense_strides(sizes)
+            views[name] = dict(strides=st, alloc=(n_el + 31) // 32)
+        else:
+            st, n = _random_view(rng, sizes, allow_broadcast=False)
+            views[name] = dict(strides=st, alloc=n)
+        bufs[name] = specutil.sentinel_array(dt, views[name]["alloc"])
+    return dict(name=f"cmp{seed}", seed=seed, sizes=sizes, ops=ops, views=views, inputs={}), bufs
+
+
+@pytest.mark.parametrize("seed", range(100))
+def test_random_compare_select_commands(seed):
+    spec, bufs = random_cmp_case(seed)
+    gpuutil.parity(spec, bufs)
+
+
+@pytest.mark.parametrize("pad", [0, 4, 9])
+def test_comparisons_and_select_on_special_values(pad):
+    """Every pair of special floats and of int edge values through every
+    comparison (slot and scalar forms, both operand orders) and select;
+    pad extra live values move the program to the 8- and 32-slot tiers."""
+    xb, yb = _pairs(F_SPECIALS)
+    n = xb.size
+    xi = np.resize(np.repeat(I_SPECIALS, I_SPECIALS.size), n).astype(np.int32)
+    yi = np.resize(np.tile(I_SPECIALS, I_SPECIALS.size), n).astype(np.int32)
+    pads = [f"p{i}" for i in range(pad)]
+    block, outs = [], []
+    for rel in CMP_OPS:
+        block += [(rel, f"f{rel}", "x", "y"), (rel, f"fs{rel}", "x", "k"), (rel, f"fr{rel}", "k", "y"),
+                  (rel, f"i{rel}", "xi", "yi")]
+        outs += [f"f{rel}", f"fs{rel}", f"fr{rel}", f"i{rel}"]
+    for rel in UCMP_OPS:
+        block += [(rel, f"u{rel}", "xi", "yi"), (rel, f"us{rel}", "ki", "yi")]
+        outs += [f"u{rel}", f"us{rel}"]
+    block += [("select", "sf", "x", "y", "flt"), ("select", "si", "xi", "yi", "xi"),
+              ("select", "ss", "x", "k", "ige"), ("select", "sk", "k", "y", "ine")]
+    block += [("add", f"q{i}", p, "x") for i, p in enumerate(pads)]
+    acc = "sf"
+    for i in range(pad):
+        block.append(("add", f"a{i}", acc, f"q{i}"))
+        acc = f"a{i}"
+    # every result stored, comparisons alternately as i32 words and packed
+    # bits; at most 8 stores per Command, so the results are split over several
+    all_stores = [(f"o_{o}", o, "b1" if j % 2 else "i32") for j, o in enumerate(outs)]
+    all_stores += [("o_sf", acc, "f32"), ("o_si", "si", "i32"), ("o_ss", "ss", "f32"), ("o_sk", "sk", "bf16")]
+    names = ["x", "y", "xi", "yi"] + pads
+    loads = [("load", "x", "f32"), ("load", "y", "f32"), ("load", "xi", "i32"), ("load", "yi", "i32")]
+    loads += [("load", p, "f32") for p in pads]
+    scal = [("scalar", "k", "f32", -0.0), ("scalar", "ki", "i32", -2**31)]
+    rng = np.random.default_rng(7)
+    base = {"x": xb.view(np.float32), "y": yb.view(np.float32), "xi": xi, "yi": yi}
+    for p in pads:
+        base[p] = rng.standard_normal(n).astype(np.float32)
+    for gi in range(0, len(all_stores), 8):
+        group = all_stores[gi:gi + 8]
+        ops = loads + scal + [("exec", block)] + [("store", o, src, dt) for o, src, dt in group]
+        views = {k: dict(strides=(1,), alloc=n) for k in names}
+        bufs = dict(base)
+        for o, _, dt in group:
+            views[o] = dict(strides=(1,), alloc=(n + 31) // 32 if dt == "b1" else n)
+            bufs[o] = specutil.sentinel_array(dt, views[o]["alloc"])
+        spec = dict(name=f"cmpspecials{gi}", seed=0, sizes=(n,), ops=ops, views=views, inputs={})
+        if pad == 9 and any(src == acc for _, src, _ in group):
+            c, _ = T.command_from_spec(spec)
+            assert c.lower()[0]["tier"] == 3
+        gpuutil.parity(spec, bufs)
+
+
+@pytest.mark.parametrize("n", [1, 31, 32, 33, 255, 256, 257, 1000, 4097, (1 << 20) + 5])
+def test_packed_bits_ragged_lengths(n):
+    """b1 stores over the contiguous executor (with its generic tail) at
+    ragged lengths: whole words, last word's extra bits zero, and the words
+    after the buffer untouched (sentinel guard)."""
+    rng = np.random.default_rng(n)
+    x = rng.integers(-2**31, 2**31, size=n).astype(np.int32)
+    nb = (n + 31) // 32
+    spec = dict(name=f"bits{n}", seed=0, sizes=(n,),
+                ops=[("load", "x", "i32"), ("scalar", "t", "i32", 0),
+                     ("exec", [("lt", "neg", "x", "t"), ("ugt", "big", "x", "t")]),
+                     ("store", "b_neg", "neg", "b1"), ("store", "b_big", "big", "b1")],
+                views={"x": dict(strides=(1,), alloc=n), "b_neg": dict(strides=(1,), alloc=nb + 2),
+                       "b_big": dict(strides=(1,), alloc=nb)}, inputs={})
+    bufs = {"x": x, "b_neg": specutil.sentinel_array("b1", nb + 2), "b_big": specutil.sentinel_array("b1", nb)}
+    plan = gpuutil.parity(spec, bufs)
+    assert plan["path"] == "contig"
+
+
+@pytest.mark.parametrize("case", ["strided_input", "transposed_input", "misaligned"])
+def test_packed_bits_on_the_generic_executor(case):
+    """A b1 store next to views the contiguous executor cannot take: the plan
+    falls to the generic executor (never to the tile one)."""
+    rng = np.random.default_rng(3)
+    m, nn = 70, 133
+    n = m * nn
+    nb = (n + 31) // 32
+    a_view = {"strided_input": ((nn + 5, 1), (m - 1) * (nn + 5) + nn),
+              "transposed_input": ((1, m), n),
+              "misaligned": ((nn, 1), n)}[case]
+    spec = dict(name=f"bits_{case}", seed=0, sizes=(m, nn),
+                ops=[("load", "A", "f32"), ("load", "B", "f32"),
+                     ("exec", [("gt", "g", "A", "B"), ("select", "r", "A", "B", "g")]),
+                     ("store", "bits", "g", "b1"), ("store", "mx", "r", "f32")],
+                views={"A": dict(strides=a_view[0], alloc=a_view[1]), "B": dict(strides=(nn, 1), alloc=n),
+                       "bits": dict(strides=(nn, 1), alloc=nb), "mx": dict(strides=(nn, 1), alloc=n)},
+                inputs={})
+    bufs = {"A": rng.standard_normal(a_view[1]).astype(np.float32), "B": rng.standard_normal(n).astype(np.float32),
+            "bits": specutil.sentinel_array("b1", nb), "mx": specutil.sentinel_array("f32", n)}
+    plan = gpuutil.parity(spec, bufs, {"A": 1} if case == "misaligned" else None)
+    assert plan["path"] == "generic"
+
+
+def test_packed_bits_view_must_be_dense():
+    n = 64
+    spec = dict(name="bad", seed=0, sizes=(2, n // 2),
+                ops=[("load", "x", "i32"), ("exec", [("ne", "p", "x", "x")]), ("store", "bits", "p", "b1")],
+                views={"x": dict(strides=(n // 2, 1), alloc=n), "bits": dict(strides=(1, 2), alloc=2)}, inputs={})
+    bufs = {"x": np.zeros(n, np.int32), "bits": specutil.sentinel_array("b1", 2)}
+    with pytest.raises(T.CmdError) as e:
+        gpuutil.run_cuda(spec, bufs)
+    assert e.value.name == "CMD_ERR_SHAPE"
+
+
+@pytest.mark.parametrize("pad", [0, 2, 6])
+def test_scalar_compare_into_the_tiers_last_slot(pad):
+    """A comparison with a scalar reads no staging slot, so its result may sit
+    in the tier's last slot (a fault of this kind once ended the program
+    there without storing anything)."""
+    n = 1000
+    rng = np.random.default_rng(pad)
+    names = ["x"] + [f"p{i}" for i in range(pad)]
+    block = [("ne", "k", "s", "s"), ("add", "kx", "k", "x")]
+    acc = "kx"
+    for i in range(pad):
+        block.append(("add", f"a{i}", acc, f"p{i}"))
+        acc = f"a{i}"
+    spec = dict(name=f"lastslot{pad}", seed=0, sizes=(n,),
+                ops=[("load", k, "i32") for k in names] + [("scalar", "s", "i32", 3), ("exec", block),
+                                                          ("store", "o", acc, "i32"), ("store", "ob", "k", "b1")],
+                views={**{k: dict(strides=(1,), alloc=n) for k in names + ["o"]},
+                       "ob": dict(strides=(1,), alloc=(n + 31) // 32)}, inputs={})
+    bufs = {k: rng.integers(-100, 100, size=n).astype(np.int32) for k in names}
+    bufs["o"] = specutil.sentinel_array("i32", n)
+    bufs["ob"] = specutil.sentinel_array("b1", (n + 31) // 32)
+    gpuutil.parity(spec, bufs)

@@ -103,6 +103,8 @@ def test_lowering_of_the_workloads():
         "wide_dag": (15, 6, 7, 2, 3),
         "batched_transpose": (2, 2, 2, 0, 0),
         "div_clamp_i32": (5, 1, 1, 0, 0),
+        "threshold_u32": (1, 1, 1, 0, 0),
+        "threshold_bits": (1, 1, 1, 0, 0),
     }
     small = {"strided_bf16": (64, 64, 64), "batched_transpose": (2, 64, 64)}
     for name, f in W.FULL.items():
@@ -141,8 +143,8 @@ def test_sub_is_not_treated_as_commutative():
     assert info["n_live_ops"] == 2
 
 
-def test_division_flag_and_new_op_reuse():
-    """A live division marks the program for the executors' division
+def test_extended_flag_and_new_op_reuse():
+    """A live division marks the program for the executors' extended
     variant; a dead one does not. min/max commute (so reuse merges the
     swapped form), div does not."""
     c = T.Command()
@@ -157,15 +159,15 @@ def test_division_flag_and_new_op_reuse():
     c.store(t[5], "f32", 1)
     c.store(t[6], "i32", 1)
     info, _ = c.lower()
-    assert info["divides"] == 0  # both divisions are dead
+    assert info["extended"] == 0  # both divisions are dead
     assert info["n_live_ops"] == 4  # min (once), max and the two (identity) conversions
     c.store(t[4], "f32", 1)
     info, _ = c.lower()
-    assert info["divides"] == 1 and info["n_live_ops"] == 5
+    assert info["extended"] == 1 and info["n_live_ops"] == 5
     for name, f in W.FULL.items():
-        c2, _ = T.command_from_spec(f(64) if name in ("add_f32", "chain_f32", "wrap_i32", "wide_dag", "div_clamp_i32")
-                                    else f(2, 64, 64) if name == "batched_transpose" else f(64, 64, 64))
-        assert c2.lower()[0]["divides"] == (name == "div_clamp_i32")
+        c2, _ = T.command_from_spec(f(2, 64, 64) if name == "batched_transpose"
+                                    else f(64, 64, 64) if name == "strided_bf16" else f(64))
+        assert c2.lower()[0]["extended"] == (name in ("div_clamp_i32", "threshold_u32", "threshold_bits"))
 
 
 def test_mixed_classes_rejected():
@@ -327,3 +329,58 @@ def test_configure_waits_validates():
         T.cmd_configure_waits(0)
     assert e.value.name == "CMD_ERR_ARG"
     T.cmd_configure_waits(2_000_000_000, False)
+
+
+def test_compare_select_and_packed_bits_lowering():
+    """Slot-slot comparisons and selects read a staging slot above the
+    program's values (one more slot, a wider tier when needed); scalar
+    comparisons do not. All of them, and packed-bit stores, select the
+    extended executor variant."""
+    c = T.Command()
+    a = c.load_tensor("f32", 1)
+    b = c.load_tensor("f32", 1)
+    t = c.execute([("lt", a, b), ("add", a, b)])  # a and b live past the comparison
+    c.store(t[0], "i32", 1)
+    c.store(t[1], "f32", 1)
+    info, _ = c.lower()
+    assert info["extended"] == 1 and info["n_slots"] == 4 and info["tier"] == 1  # a, b, result, staging
+    c = T.Command()
+    x = c.load_tensor("i32", 1)
+    s = c.load_scalar("i32")
+    t = c.execute([("uge", x, s)])
+    c.store(t[0], "b1", 1)
+    info, _ = c.lower()
+    assert info["extended"] == 1 and info["n_slots"] == 1 and info["tier"] == 0
+    c = T.Command()
+    x = c.load_tensor("f32", 1)
+    y = c.load_tensor("f32", 1)
+    k = c.load_tensor("i32", 1)
+    t = c.execute([("select", x, y, k)])
+    c.store(t[0], "f32", 1)
+    info, words = c.lower()
+    assert info["extended"] == 1 and info["tier"] == 1 and info["n_words"] == len(words)
+    c = T.Command()
+    x = c.load_tensor("i32", 1)
+    t = c.execute([("add", x, x)])
+    c.store(t[0], "i32", 1)
+    assert c.lower()[0]["extended"] == 0
+
+
+def test_compare_select_and_packed_bit_type_rules():
+    c = T.Command()
+    f = c.load_tensor("f32", 1)
+    i = c.load_tensor("i32", 1)
+    with pytest.raises(T.CmdError):
+        c.execute([("ult", f, f)])          # unsigned comparisons take ints
+    with pytest.raises(T.CmdError):
+        c.execute([("select", f, f, f)])    # the condition must be int
+    with pytest.raises(T.CmdError):
+        c.execute([("select", f, i, i)])    # a and b of one class
+    with pytest.raises(T.CmdError):
+        c.store(f, "b1", 1)                 # packed bits store int values
+    with pytest.raises(T.CmdError):
+        c.load_tensor("b1", 1)              # b1 is a store type only
+    t = c.execute([("gt", f, f), ("select", i, i, T.CMD_LOCAL(0))])
+    c.store(t[0], "b1", 1)
+    c.store(t[1], "i32", 1)
+    assert c.lower()[0]["n_live_ops"] == 2
