@@ -248,6 +248,42 @@ cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd
  * CMD_I32 or CMD_B1 (the bit is value != 0). */
 cmd_status cmd_add_store(cmd_command_t cmd, cmd_tag src, cmd_dtype dtype, int32_t rank, cmd_tag* out);
 
+/* ---- text form -------------------------------------------------------- */
+
+/* A Command as text and back (rocRoller, "Design Overview", section
+ * "Serialization": a Command converts to and from YAML, for saving, caching
+ * and inspecting kernel definitions). The text is a small fixed subset of
+ * YAML that cmd_to_yaml writes and cmd_from_yaml reads:
+ *
+ *   # comments (from a '#' at a line's start or after a space) and blank lines
+ *   version: 1
+ *   operations:
+ *     - {kind: load_tensor, tag: 0, dtype: f32, rank: 1}
+ *     - {kind: load_scalar, tag: 1, dtype: f32}
+ *     - kind: execute                       (one T_Execute block)
+ *       ops:
+ *         - {tag: 2, op: mul, a: 0, b: 1}
+ *         - {tag: 3, op: neg, a: 2}         (one-operand ops: a only)
+ *         - {tag: 4, op: select, a: 2, b: 3, c: 5}
+ *     - {kind: store_tensor, tag: 5, src: 4, dtype: f32, rank: 1}
+ *
+ * Keys of a {...} mapping may come in any order; tags must be 0, 1, 2, ...
+ * in order (they are the tags the Command gets), operands refer to earlier
+ * tags, op names are those of cmd_eop in lower case (add .. uge, select) and
+ * dtype names f32, f16, bf16, i32, b1. The reader rebuilds the Command
+ * through cmd_create and the cmd_add_* calls, so it applies all of their
+ * checks; the same Command lowers to the same program. */
+
+/* Write cmd's text form into buf (NUL-terminated, truncated to size);
+ * *needed receives the full length + 1 when non-NULL. */
+cmd_status cmd_to_yaml(cmd_command_t cmd, char* buf, int64_t size, int64_t* needed);
+
+/* Build a new Command from len bytes of text form (len < 0: text is
+ * NUL-terminated). On success *out owns it (release with cmd_destroy); on
+ * error nothing is allocated, CMD_ERR_ARG (or the failing builder call's
+ * status) is returned and cmd_last_error() names the line. */
+cmd_status cmd_from_yaml(const char* text, int64_t len, cmd_command_t* out);
+
 /* ---- lowering ---------------------------------------------------------- */
 
 /* Lower cmd on the host only (no GPU needed): fills *info and, when words is

@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import re
 import threading
 
 from . import _build
@@ -107,6 +108,8 @@ SIGNATURES = {
     "cmd_kernel_destroy": (None, [_P]),
     "cmd_kernel_info": (_I, [_P, ctypes.POINTER(cmd_program_info)]),
     "cmd_kernel_dump": (_I, [_P, ctypes.c_char_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
+    "cmd_to_yaml": (_I, [_P, ctypes.c_char_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
+    "cmd_from_yaml": (_I, [ctypes.c_char_p, ctypes.c_int64, ctypes.POINTER(_P)]),
     "cmd_plan_launch": (_I, [_P, ctypes.POINTER(cmd_runtime_args), ctypes.POINTER(cmd_launch_plan)]),
     "cmd_launch": (_I, [_P, ctypes.POINTER(cmd_runtime_args), _P]),
     "cmd_sync_status": (_I, [_P, _P]),
@@ -244,6 +247,21 @@ def cmd_kernel_dump(k: int) -> str:
     return buf.value.decode()
 
 
+def cmd_to_yaml(cmd: int) -> str:
+    need = ctypes.c_int64()
+    _check(lib().cmd_to_yaml(cmd, None, 0, ctypes.byref(need)), "cmd_to_yaml")
+    buf = ctypes.create_string_buffer(need.value)
+    _check(lib().cmd_to_yaml(cmd, buf, need.value, None), "cmd_to_yaml")
+    return buf.value.decode()
+
+
+def cmd_from_yaml(text: str) -> int:
+    data = text.encode()
+    h = _P()
+    _check(lib().cmd_from_yaml(data, len(data), ctypes.byref(h)), "cmd_from_yaml")
+    return h.value
+
+
 def cmd_plan_launch(k: int, args: cmd_runtime_args) -> dict:
     plan = cmd_launch_plan()
     _check(lib().cmd_plan_launch(k, ctypes.byref(args), ctypes.byref(plan)), "cmd_plan_launch")
@@ -308,9 +326,21 @@ def make_runtime_args(tensors: dict, scalars: dict, scalar_dtypes: dict):
 class Command:
     """Builder for one Command (owns a cmd_command_t)."""
 
-    def __init__(self):
-        self.handle = cmd_create()
+    def __init__(self, handle: int | None = None):
+        self.handle = handle if handle is not None else cmd_create()
         self.scalar_dtypes: dict = {}
+
+    def to_yaml(self) -> str:
+        """The Command's text form (see cmd.h)."""
+        return cmd_to_yaml(self.handle)
+
+    @classmethod
+    def from_yaml(cls, text: str) -> "Command":
+        c = cls(cmd_from_yaml(text))
+        # scalar types, for launch arguments: from the canonical text form
+        for m in re.finditer(r"kind: load_scalar, tag: (\d+), dtype: (\w+)", c.to_yaml()):
+            c.scalar_dtypes[int(m.group(1))] = m.group(2)
+        return c
 
     def __del__(self):
         h = getattr(self, "handle", None)

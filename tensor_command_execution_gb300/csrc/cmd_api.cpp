@@ -41,6 +41,7 @@ struct Op {
   int a, b;   // kExec operands (b = -1 for one-operand ops); kStore: a = source
   int c;      // SELECT: the condition (else -1)
   int cls;    // value class of the result
+  int block = -1;  // kExec: which T_Execute block (cmd_add_execute call) it came in
 };
 
 const char* dtype_name(int dt) {
@@ -55,6 +56,11 @@ const char* dtype_name(int dt) {
 }
 
 int elem_size(int dt) { return (dt == CMD_F16 || dt == CMD_BF16) ? 2 : 4; }
+
+// The text form's names of the E ops, in cmd_eop order.
+const char* const kEopNames[] = {"add", "sub", "mul", "neg", "div", "min", "max", "abs", "to_f32", "to_i32", "lt",
+                                 "le", "gt", "ge", "eq", "ne", "ult", "ule", "ugt", "uge", "select"};
+const char* eop_name(int eop) { return eop >= 0 && eop <= CMD_E_SELECT ? kEopNames[eop] : "?"; }
 
 // E ops that take one operand.
 bool is_unary(int eop) { return eop == CMD_E_NEG || eop == CMD_E_ABS || eop == CMD_E_TO_F32 || eop == CMD_E_TO_I32; }
@@ -96,8 +102,15 @@ struct Program {
 
 }  // namespace
 
+namespace cmdx {
+// Record msg for cmd_last_error() and return s (for the host sources that
+// build Commands through the public API, e.g. the text-form reader).
+cmd_status host_fail(cmd_status s, const std::string& msg) { return fail(s, msg); }
+}  // namespace cmdx
+
 struct cmd_command {
   std::vector<Op> ops;
+  int n_blocks = 0;  // T_Execute blocks added so far
 };
 
 struct cmd_kernel {
@@ -1039,6 +1052,7 @@ cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd
         return fail(CMD_ERR_TYPE, "E op " + std::to_string(i) + ": the condition of a SELECT must be int-valued");
     }
     op.cls = x.op == CMD_E_TO_F32 ? kFloat : (x.op == CMD_E_TO_I32 || is_compare(x.op)) ? kInt : cls_of(op.a);
+    op.block = cmd->n_blocks;
     block.push_back(op);
   }
   try {
@@ -1046,6 +1060,7 @@ cmd_status cmd_add_execute(cmd_command_t cmd, const cmd_xop* ops, int32_t n, cmd
   } catch (...) {
     return fail(CMD_ERR_NOMEM, "out of host memory");
   }
+  ++cmd->n_blocks;
   if (out_tags)
     for (int i = 0; i < n; ++i) out_tags[i] = base + i;
   return CMD_OK;
@@ -1171,6 +1186,56 @@ void cmd_kernel_destroy(cmd_kernel_t k) {
 cmd_status cmd_kernel_info(cmd_kernel_t k, cmd_program_info* info) {
   if (!k || !info) return fail(CMD_ERR_NULL, "k or info is NULL");
   fill_info(k->prog, info);
+  return CMD_OK;
+}
+
+cmd_status cmd_to_yaml(cmd_command_t cmd, char* buf, int64_t size, int64_t* needed) {
+  if (!cmd) return fail(CMD_ERR_NULL, "cmd is NULL");
+  std::string s;
+  try {
+    s += "# tensor Command, text form (YAML)\nversion: 1\noperations:\n";
+    char line[200];
+    const auto& ops = cmd->ops;
+    for (size_t t = 0; t < ops.size(); ++t) {
+      const Op& op = ops[t];
+      switch (op.kind) {
+        case kLoad:
+          std::snprintf(line, sizeof line, "  - {kind: load_tensor, tag: %zu, dtype: %s, rank: %d}\n", t,
+                        dtype_name(op.dtype), op.rank);
+          s += line;
+          break;
+        case kScalar:
+          std::snprintf(line, sizeof line, "  - {kind: load_scalar, tag: %zu, dtype: %s}\n", t, dtype_name(op.dtype));
+          s += line;
+          break;
+        case kStore:
+          std::snprintf(line, sizeof line, "  - {kind: store_tensor, tag: %zu, src: %d, dtype: %s, rank: %d}\n", t,
+                        op.a, dtype_name(op.dtype), op.rank);
+          s += line;
+          break;
+        default:
+          if (t == 0 || ops[t - 1].kind != kExec || ops[t - 1].block != op.block) s += "  - kind: execute\n    ops:\n";
+          if (is_unary(op.eop))
+            std::snprintf(line, sizeof line, "      - {tag: %zu, op: %s, a: %d}\n", t, eop_name(op.eop), op.a);
+          else if (op.eop == CMD_E_SELECT)
+            std::snprintf(line, sizeof line, "      - {tag: %zu, op: %s, a: %d, b: %d, c: %d}\n", t,
+                          eop_name(op.eop), op.a, op.b, op.c);
+          else
+            std::snprintf(line, sizeof line, "      - {tag: %zu, op: %s, a: %d, b: %d}\n", t, eop_name(op.eop),
+                          op.a, op.b);
+          s += line;
+          break;
+      }
+    }
+  } catch (...) {
+    return fail(CMD_ERR_NOMEM, "out of host memory");
+  }
+  if (needed) *needed = (int64_t)s.size() + 1;
+  if (buf && size > 0) {
+    size_t n = std::min<size_t>((size_t)size - 1, s.size());
+    std::memcpy(buf, s.data(), n);
+    buf[n] = 0;
+  }
   return CMD_OK;
 }
 

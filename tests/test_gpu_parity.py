@@ -897,3 +897,21 @@ def test_scalar_compare_into_the_tiers_last_slot(pad):
     bufs["o"] = specutil.sentinel_array("i32", n)
     bufs["ob"] = specutil.sentinel_array("b1", (n + 31) // 32)
     gpuutil.parity(spec, bufs)
+
+
+@pytest.mark.parametrize("spec", [W.chain_f32(5000), W.wide_dag(4099), W.strided_bf16(130, 72, 80),
+                                  W.threshold_bits(3000), W.div_clamp_i32(777), W.batched_transpose(2, 64, 96)],
+                         ids=lambda s: s["name"])
+def test_kernel_from_text_form(spec):
+    """A Command written with cmd_to_yaml and read back with cmd_from_yaml
+    compiles to a kernel whose results match the oracle element by element
+    (rocRoller, "Design Overview", section "Serialization")."""
+    c, _ = T.command_from_spec(spec)
+    k = T.Command.from_yaml(c.to_yaml()).compile()
+    bufs = specutil.host_buffers(spec)
+    got, _ = gpuutil.run_cuda(spec, bufs, kernel=k)
+    ref = {n: v.copy() for n, v in bufs.items()}
+    oracle.OracleCommand(spec, ref).eval_range()
+    dts = W.tensor_dtypes(spec)
+    for name in W.store_names(spec):
+        gpuutil.compare(got[name], ref[name], dts[name], f"{spec['name']}:{name} (from text)")
