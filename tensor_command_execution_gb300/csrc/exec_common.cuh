@@ -383,6 +383,33 @@ struct LaneMap {
   static constexpr int W = 32 * V;
 };
 
+// ---- programmatic dependent launch ------------------------------------------
+// Every executor launch may begin while the previous kernel on its stream is
+// still running: its CTAs are scheduled early, and each one first waits
+// (griddepcontrol.wait) until that kernel has completed and its memory is
+// visible, so no data access overlaps it and a Command that reads what the
+// previous one wrote stays correct. Each CTA then lets the next launch start
+// (griddepcontrol.launch_dependents). What overlaps is launch processing and
+// CTA scheduling, which dominate small launches. Without the launch
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <class K, class P>
+inline cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t stream, const P& params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, params);
+}
+
 // Grid size for a persistent grid-stride kernel: enough CTAs to fill the
 // device at the kernel's occupancy, and no more than the work needs.
 template <class K>

@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(cons
   const uint32_t* prog = c_prog[p.prog];
   const int64_t n_chunks = p.n / M::W;  // the host passes a multiple of W
   int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  pdl_wait();
+  pdl_trigger();
   if constexpr (contig_prefetch(TIER, EXT)) {
     // software pipeline: the next chunk's loads are issued before the
     // program runs on this one, so their latency overlaps its work and
@@ -171,8 +173,7 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  contig_kernel<TIER, EXT><<<grid, kBlock, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(contig_kernel<TIER, EXT>, grid, kBlock, 0, stream, p);
 }
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {

@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(con
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t* prog = c_prog[p.prog];
+  pdl_wait();
+  pdl_trigger();
   for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w * 32 * V < p.n; w += nwarps) {
     const int64_t base = w * 32 * V;
     uint32_t r[S][V];
@@ -114,8 +116,7 @@ static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  generic_kernel<TIER, EXT><<<grid, kBlock, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(generic_kernel<TIER, EXT>, grid, kBlock, 0, stream, p);
 }
 
 cudaError_t CMDX_TIER_NAME(generic_launch_t)(const GenericParams& p, cudaStream_t stream) {

@@ -356,6 +356,10 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // (barrier setup above touches only shared memory; every global access,
+  // the producer's TMA loads included, comes after the previous kernel)
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == kConsumerWarps) {
     // ---- producer: one lane issues the TMA copies ----
@@ -511,8 +515,7 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
     if (cache_ok) grid_cache[dev][p.n_stages] = full_grid;
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
-  tile2d_kernel<TIER, ND, EXT><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(tile2d_kernel<TIER, ND, EXT>, grid, kThreads, smem, stream, p);
 }
 
 cudaError_t CMDX_TILE_NAME(tile2d_launch_t)(const Tile2dParams& p, cudaStream_t stream) {
