@@ -85,37 +85,62 @@ cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_
   Tile2dParams p;
   std::memset(&p, 0, sizeof p);
   uint32_t off = 0, tx = 0;
+  // a batched launch: batch dims or broadcast loads (it runs the ND kernel)
+  bool batched = L.nb[0] > 1 || L.nb[1] > 1;
+  for (uint32_t j = 0; j < L.n_loads; ++j)
+    batched = batched || L.in_ld[j] == 0 || L.in_bst[j][0] != 0 || L.in_bst[j][1] != 0;
   for (uint32_t j = 0; j < L.n_loads; ++j) {
     const bool half = L.in_dt[j] == 1 || L.in_dt[j] == 2;
     const uint32_t es = half ? 2 : 4;
     const bool trans = L.in_trans[j] != 0;
     // descriptor dims: 0 = the unit-stride tile dim; then the other tile dim
-    // and the batch dims that have a nonzero stride, by increasing stride
-    struct D { int64_t stride, size; int src; };
-    D d[3];
-    int nd = 0;
-    if (L.in_ld[j] != 0) d[nd++] = {L.in_ld[j], trans ? L.cols : L.rows, 0};
-    if (L.in_bst[j][0] != 0) d[nd++] = {L.in_bst[j][0], L.nb[0], 1};
-    if (L.in_bst[j][1] != 0) d[nd++] = {L.in_bst[j][1], L.nb[1], 2};
-    for (int a = 1; a < nd; ++a)
-      for (int b = a; b > 0 && d[b].stride < d[b - 1].stride; --b) std::swap(d[b], d[b - 1]);
-    cuuint64_t dims[4] = {(cuuint64_t)(trans ? L.rows : L.cols), 1, 1, 1};
-    cuuint64_t strides[3] = {0, 0, 0};
-    cuuint32_t box[4] = {half ? 64u : 32u, 1, 1, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    for (int k = 0; k < nd; ++k) {
-      dims[k + 1] = (cuuint64_t)d[k].size;
-      strides[k] = (cuuint64_t)d[k].stride * es;
-      box[k + 1] = d[k].src == 0 ? 64u : 1u;
-      p.in_src[j][k] = (uint8_t)d[k].src;
-    }
-    const int rank = 1 + nd;
-    CUresult r = encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
-                        (cuuint32_t)rank, const_cast<void*>(L.in[j]), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // and the batch dims that have a nonzero stride, by increasing stride.
+    // A transposed load whose column count is a multiple of 8 has its column
+    // dim split in two, (column / 8, stride 8 ld) then (column % 8, stride
+    // ld), each a box of 8: column 8 g + k then lands in box row g + 8 k,
+    // which the consumers read without bank conflicts or register rotation.
+    // Measured on GB300 it pays for 4-byte loads in batched launches of the
+    // 2-slot tier (+5%); a 2-byte load with 16 KB rows ran 15% slower split
+    // (the box then walks rows eight apart), and the extra read path cost
+    // the plain 2-D kernel 3%, so only that case splits.
+    struct D { int64_t stride, size; int src; uint32_t box; };
+    auto encode_load = [&](bool split) -> CUresult {
+      D d[4];
+      int nd = 0;
+      if (split) {
+        d[nd++] = {8 * L.in_ld[j], L.cols / 8, 3, 8};
+        d[nd++] = {L.in_ld[j], 8, 4, 8};
+      } else if (L.in_ld[j] != 0) {
+        d[nd++] = {L.in_ld[j], trans ? L.cols : L.rows, 0, 64};
+      }
+      const int first_sorted = split ? nd : 0;  // the split pair keeps its order
+      if (L.in_bst[j][0] != 0) d[nd++] = {L.in_bst[j][0], L.nb[0], 1, 1};
+      if (L.in_bst[j][1] != 0) d[nd++] = {L.in_bst[j][1], L.nb[1], 2, 1};
+      for (int a = first_sorted + 1; a < nd; ++a)
+        for (int b = a; b > first_sorted && d[b].stride < d[b - 1].stride; --b) std::swap(d[b], d[b - 1]);
+      cuuint64_t dims[5] = {(cuuint64_t)(trans ? L.rows : L.cols), 1, 1, 1, 1};
+      cuuint64_t strides[4] = {0, 0, 0, 0};
+      cuuint32_t box[5] = {half ? 64u : 32u, 1, 1, 1, 1};
+      cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+      for (int k = 0; k < 4; ++k) p.in_src[j][k] = 0;
+      for (int k = 0; k < nd; ++k) {
+        dims[k + 1] = (cuuint64_t)d[k].size;
+        strides[k] = (cuuint64_t)d[k].stride * es;
+        box[k + 1] = d[k].box;
+        p.in_src[j][k] = (uint8_t)d[k].src;
+      }
+      const int rank = 1 + nd;
+      p.in_rank[j] = (uint8_t)rank;
+      p.in_split[j] = split ? 1 : 0;
+      return encode(&p.maps[j], half ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                    (cuuint32_t)rank, const_cast<void*>(L.in[j]), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    const bool can_split = batched && !half && tier == kTier2 && trans && L.in_ld[j] != 0 && L.cols % 8 == 0;
+    CUresult r = can_split ? encode_load(true) : CUDA_ERROR_INVALID_VALUE;
+    if (r != CUDA_SUCCESS) r = encode_load(false);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    p.in_rank[j] = (uint8_t)rank;
     p.in_bcast[j] = L.in_ld[j] == 0;
     p.load_off[j] = off;
     off += (uint32_t)tile_stage_bytes((int)es);

@@ -78,8 +78,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     if (global_ns() - t0 > timeout_ns) return false;
   }
 }
-// One box of a descriptor of rank 1..4 at coordinates c[0..rank).
-__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int rank, const int32_t (&c)[4],
+// One box of a descriptor of rank 1..5 at coordinates c[0..rank).
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int rank, const int32_t (&c)[5],
                                          uint32_t bar) {
   const uint64_t m = reinterpret_cast<uint64_t>(map);
   switch (rank) {
@@ -98,11 +98,17 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
           "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
           ::"r"(dst), "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(bar) : "memory");
       break;
-    default:
+    case 4:
       asm volatile(
           "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
           "[%6];"
           ::"r"(dst), "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(bar) : "memory");
+      break;
+    default:
+      asm volatile(
+          "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+          "[%7];"
+          ::"r"(dst), "l"(m), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar) : "memory");
       break;
   }
 }
@@ -260,6 +266,36 @@ __device__ __forceinline__ void read_trans2(uint32_t (&x)[16], uint32_t stage, i
   }
 }
 
+// Transposed, split layout (batched launches of the 2-slot tier, 4-byte
+// loads): the host split the load's column dim into (column / 8, column % 8),
+// the group first, so logical (li, 8 cj + k) is box row cj + 8 k. Under the 128-byte swizzle (chunk ^= box row % 8 = cj) a tile
+// row's eight lanes read eight distinct chunks at every step, and step k of
+// a lane is register k: eight loads at fixed offsets from one address, with
+// no rotation afterwards.
+__device__ __forceinline__ uint32_t split_base(uint32_t stage, bool half, int li, int cj) {
+  if (half) return stage + cj * 128 + ((((uint32_t)li >> 3) ^ (uint32_t)cj) << 4) + (li & 7) * 2;
+  const uint32_t lr = li & 31;
+  return stage + (li >> 5) * kBoxBytes + cj * 128 + (((lr >> 2) ^ (uint32_t)cj) << 4) + (lr & 3) * 4;
+}
+
+// Rows li and li + 1: one 32-bit (2-byte types) or 64-bit load per step.
+__device__ __forceinline__ void read_trans2_split(uint32_t (&x)[16], uint32_t stage, int dt, int li, int cj) {
+  const bool half = dt == 1 || dt == 2;
+  const uint32_t a = split_base(stage, half, li, cj);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (half) {
+      const uint32_t v = lds32(a + k * 1024);
+      if (dt == 1) widen_f16x2(v, x[k], x[8 + k]);
+      else widen_bf16x2(v, x[k], x[8 + k]);
+    } else {
+      const uint2 v = lds64(a + k * 1024);
+      x[k] = v.x;
+      x[8 + k] = v.y;
+    }
+  }
+}
+
 // A broadcast column (transposed load whose column stride is 0): the box has
 // one row, element li of it is the value of every column of row li.
 __device__ __forceinline__ uint32_t read_bcast_col(uint32_t stage, int dt, int li) {
@@ -269,6 +305,47 @@ __device__ __forceinline__ uint32_t read_bcast_col(uint32_t stage, int dt, int l
   }
   return lds32(stage + (li >> 5) * kBoxBytes + ((((uint32_t)li & 31) >> 2) << 4) + (li & 3) * 4);
 }
+
+// The tiles a CTA visits, t = blockIdx.x, + gridDim.x, ..., as the digits of
+// t = ((b0 * nb1 + b1) * tiles_r + tr) * tiles_c + tc, advanced by adding
+// the digits of gridDim.x with carries: no division per tile (used by the
+// producer of batched launches; measured, it did not pay elsewhere).
+struct TileWalk {
+  uint32_t tc, tr, b1, b0;   // digits of t (tr holds t / tiles_c when !nd)
+  uint32_t dc, dr, d1, d0;   // digits of the stride
+  __device__ __forceinline__ void init(const Tile2dParams& p, bool nd, uint32_t t, uint32_t g) {
+    tc = t % p.tiles_c;
+    dc = g % p.tiles_c;
+    uint32_t t1 = t / p.tiles_c, g1 = g / p.tiles_c;
+    if (nd) {
+      tr = t1 % p.tiles_r;
+      dr = g1 % p.tiles_r;
+      const uint32_t t2 = t1 / p.tiles_r, g2 = g1 / p.tiles_r;
+      b1 = t2 % p.nb1;
+      b0 = t2 / p.nb1;
+      d1 = g2 % p.nb1;
+      d0 = g2 / p.nb1;
+    } else {
+      tr = t1;
+      dr = g1;
+      b1 = b0 = d1 = d0 = 0;
+    }
+  }
+  __device__ __forceinline__ void next(const Tile2dParams& p, bool nd) {
+    tc += dc;
+    uint32_t c = tc >= p.tiles_c;
+    if (c) tc -= p.tiles_c;
+    tr += dr + c;
+    if (nd) {
+      c = tr >= p.tiles_r;
+      if (c) tr -= p.tiles_r;
+      b1 += d1 + c;
+      c = b1 >= p.nb1;
+      if (c) b1 -= p.nb1;
+      b0 += d0 + c;
+    }
+  }
+};
 
 template <bool ND>
 struct TileStore {
@@ -366,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
     if (lane != 0 || p.debug) return;
     uint32_t n = 0;
     bool ok = true;
+    TileWalk tw;  // (batched launches: it replaces three divisions a tile)
+    if (ND) tw.init(p, true, blockIdx.x, gridDim.x);
     for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
       const uint32_t s = n % ns, ph = (n / ns) & 1;
       if (!mbar_wait(empty_bar + 8 * s, ph ^ 1, p.timeout_ns)) {
@@ -374,10 +453,19 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
         break;
       }
       // t = ((b0 * nb1 + b1) * tiles_r + tile row) * tiles_c + tile column
-      const uint32_t tc = t % p.tiles_c, t1 = t / p.tiles_c;
-      const uint32_t tr = ND ? t1 % p.tiles_r : t1, t2 = ND ? t1 / p.tiles_r : 0;
+      uint32_t tc, tr;
+      int32_t bc[3] = {0, 0, 0};
+      if (ND) {
+        tc = tw.tc;
+        tr = tw.tr;
+        bc[1] = (int32_t)tw.b0;
+        bc[2] = (int32_t)tw.b1;
+        tw.next(p, true);
+      } else {
+        tc = t % p.tiles_c;
+        tr = t / p.tiles_c;
+      }
       const int32_t i0 = (int32_t)(tr * kTileRows), j0 = (int32_t)(tc * kTileCols);
-      const int32_t bc[3] = {0, ND ? (int32_t)(t2 / p.nb1) : 0, ND ? (int32_t)(t2 % p.nb1) : 0};
       const uint32_t fb = full_bar + 8 * s;
       mbar_arrive_expect_tx(fb, p.tx_bytes);
       const uint32_t st = stages + s * p.stage_bytes;
@@ -387,18 +475,22 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
         // dim 0 runs along the load's unit-stride tile dim; dims 1.. take the
         // other tile coordinate or a batch coordinate, as routed on the host
         const int32_t inner = p.in_trans[j] ? i0 : j0, outer = p.in_trans[j] ? j0 : i0;
-        int32_t c[4] = {inner, outer, 0, 0};
+        int32_t c[5] = {inner, outer, 0, 0, 0};
         if (ND) {
+          // descriptor dims 1..: the other tile dim (src 0), a batch dim
+          // (1, 2), or the two halves of a split column dim (3: column / 8,
+          // 4: column % 8, whose box always starts at 0)
 #pragma unroll
-          for (int k = 0; k < 3; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const uint32_t src = p.in_src[j][k];
-            c[k + 1] = src == 0 ? outer : bc[src];
+            c[k + 1] = src == 0 ? outer : src == 3 ? outer / 8 : src == 4 ? 0 : bc[src];
           }
         }
-        tma_load(dst, &p.maps[j], ND ? p.in_rank[j] : 2, c, fb);
+        const int rank = ND ? p.in_rank[j] : 2;
+        tma_load(dst, &p.maps[j], rank, c, fb);
         if (wide) {
           c[0] = inner + 32;
-          tma_load(dst + kBoxBytes, &p.maps[j], p.in_rank[j], c, fb);
+          tma_load(dst + kBoxBytes, &p.maps[j], rank, c, fb);
         }
       }
     }
@@ -456,6 +548,11 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
 #pragma unroll
                   for (int m = 0; m < 8; ++m) r[j][8 * q + m] = v;
                 }
+              } else if constexpr (TIER == kTier2 && ND) {
+                // (the host splits only here: in the plain 2-D kernel and the
+                // wider tiers a second read path cost more than it saved)
+                if (p.in_split[j]) read_trans2_split(r[j], at, p.in_dt[j], li, cj);
+                else read_trans2(r[j], at, p.in_dt[j], li, cj);
               } else if constexpr (RPT == 2) {
                 read_trans2(r[j], at, p.in_dt[j], li, cj);
               } else {

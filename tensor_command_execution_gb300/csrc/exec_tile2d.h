@@ -37,7 +37,10 @@ struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
   uint8_t in_trans[kMaxLoads];
   uint8_t in_bcast[kMaxLoads];   // the load's other tile dim has stride 0: a one-row box
   uint8_t in_rank[kMaxLoads];    // dims of its TMA descriptor
-  uint8_t in_src[kMaxLoads][3];  // coordinate of descriptor dims 1..3: 0 tile, 1 batch b0, 2 batch b1
+  uint8_t in_split[kMaxLoads];   // transposed load with its column dim split in (column / 8, column % 8)
+  // coordinate of descriptor dims 1..4: 0 the other tile dim, 1 batch b0,
+  // 2 batch b1, 3 column / 8, 4 column % 8 (of a split column dim)
+  uint8_t in_src[kMaxLoads][4];
 };
 
 // Entry points of the objects built from exec_tile2d.cu, one per tier t

@@ -441,7 +441,7 @@ def _nd_case(name, sizes, views, dts, seed=0):
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("case", ["batched_transpose", "perm_210", "batch_broadcast", "row_broadcast",
                                   "col_broadcast", "padded_batched"])
-@pytest.mark.parametrize("sizes", [(3, 96, 136), (2, 64, 64), (5, 40, 72)])
+@pytest.mark.parametrize("sizes", [(3, 96, 136), (2, 64, 64), (5, 40, 72), (4, 40, 60), (2, 33, 100)])
 def test_nd_views_on_the_tile_executor(dt, case, sizes):
     B, R, C = sizes
     dense = (R * C, C, 1)
