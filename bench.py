@@ -380,6 +380,30 @@ class E2EPipeline:
         self.started = True
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest
+    rank's); x itself on one rank. Uses the default process group (NCCL on
+    GPUs, gloo on CPU)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the bytes every rank moved over the slowest
+    rank's time (each rank runs its own replica of the workload)."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
+DTYPE_OF = {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
+            "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32", "div_clamp_i32": "f32 (int32 out)",
+            "threshold_u32": "u32 (int32 out)", "threshold_bits": "u32 (packed-bit out)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -421,13 +445,9 @@ def run_ours(args):
         dist.barrier()
     clocks.mark(t0, t1)
     clocks.stop()
-    ms = start.elapsed_time(stop) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(stop) / args.steps, world, device)
     gbs = wl.bytes / (ms * 1e-3) / 1e9
-    value = gbs * world
+    value = whole_job_gbs(wl.bytes, world, ms)
 
     if args.no_extras:
         if rank == 0:
@@ -453,12 +473,8 @@ def run_ours(args):
     e1.record(pipe.s_out)
     e1.synchronize()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_gbs = wl.bytes / (e2e_ms * 1e-3) / 1e9 * world
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, device)
+    e2e_gbs = whole_job_gbs(wl.bytes, world, e2e_ms)
 
     # ---- other workloads, same kernels, full sizes (per-rank, informative) ---
     per = {}
@@ -506,10 +522,7 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
-                      "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32",
-                      "div_clamp_i32": "f32 (int32 out)", "threshold_u32": "u32 (int32 out)",
-                      "threshold_bits": "u32 (packed-bit out)"}[args.workload],
+            "dtype": DTYPE_OF[args.workload],
             "data": "synthetic (seeded SplitMix64 inputs; no dataset)",
             "config": {"workload": f"{args.workload}: {spec_summary(spec)}", "elements": wl.elements,
                        "bytes_per_step": wl.bytes, "path": wl.plan["path"],
@@ -596,7 +609,8 @@ def run_reference(args):
     t = time.perf_counter()
     oc.eval_range(0, probe)
     rate = probe / max(1e-9, time.perf_counter() - t)
-    budget = 120.0 / max(1, args.steps + args.warmup)  # whole run about two minutes
+    # whole run about two minutes by default (12 x --cpu-seconds in all)
+    budget = min(120.0, 12.0 * args.cpu_seconds) / max(1, args.steps + args.warmup)
     m = int(min(n_total, max(4096, rate * budget)))
     for s in range(args.warmup):
         oc.eval_range(s * m % n_total, s * m % n_total + m)
@@ -609,7 +623,7 @@ def run_reference(args):
     val = m * bpe / dt / 1e9
     line = {"metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_OF[args.workload], "data": "synthetic",
             "config": {"workload": f"{args.workload}: {spec_summary(spec)}"},
             "impl": "reference",
             "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
