@@ -179,3 +179,37 @@ def test_threshold_workloads_match_numpy():
             nb = (pred.size + 31) // 32
             packed = np.concatenate([packed, np.zeros(nb * 4 - packed.size, np.uint8)]).view("<u4")
             assert (bufs["bits"].view(np.uint32) == packed).all()
+
+
+def test_planted_op_mistakes_are_caught():
+    """Plausible mistakes in the new ops (each written here as the mistaken
+    formula) disagree with the oracle on inputs the pins above use, so a pin
+    would fail if the oracle made that mistake."""
+    L = oracle.lib()
+    u = lambda v: v & 0xFFFFFFFF  # noqa: E731
+    s32 = lambda v: ((v + 2**31) % 2**32) - 2**31  # noqa: E731
+    # int division flooring instead of truncating (-7 / 2 = -4)
+    assert s32(L.orc_idiv(u(-7), 2)) != -7 // 2
+    # x / 0 as 0 (a common convention) instead of -1
+    assert L.orc_idiv(5, 0) != 0
+    # an ordered != (false on NaN)
+    assert L.orc_compare(oracle.KINDS["ne"], 0, 0x7FC00000, 0x3F800000) == 1
+    # comparing signed where unsigned is asked
+    assert L.orc_compare(oracle.KINDS["ult"], 1, 1, u(-1)) == 1 and L.orc_compare(oracle.KINDS["lt"], 1, 1, u(-1)) == 0
+    # float -> int rounding to nearest instead of truncating (1.5 -> 2)
+    assert L.orc_f2i(0x3FC00000) == 1
+    # int -> float truncating instead of rounding (2^24 + 3 -> 2^24 + 4 under RNE)
+    assert L.orc_i2f(16777219) == 0x4B800002
+    # min as (a < b ? a : b): min(+0, -0) would be -0 only by accident of order
+    assert L.orc_fmin(0, 0x80000000) == 0x80000000 and L.orc_fmax(0x80000000, 0) == 0
+    # select testing only the low bit of the condition
+    n = 4
+    bufs, _ = _run([("select", "s", "a", "b", "c")],
+                   {"a": ("i32", np.full(n, 1, np.int32)), "b": ("i32", np.full(n, 2, np.int32)),
+                    "c": ("i32", np.array([2, -2, 0, 1], np.int32))}, {"o": ("s", "i32")}, n)
+    assert bufs["o"].tolist() == [1, 1, 2, 1]  # c = 2 and -2 are true (low bit 0)
+    # bits most significant first
+    bufs, _ = _run([("ne", "nz", "x", "zero")], {"x": ("i32", np.array([1] + [0] * 31, np.int32)),
+                                                   "zero": ("i32", np.zeros(32, np.int32))},
+                   {"bits": ("nz", "b1")}, 32)
+    assert bufs["bits"].view(np.uint32)[0] == 1  # element 0 is bit 0, not bit 31
