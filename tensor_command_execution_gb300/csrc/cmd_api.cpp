@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -79,7 +80,7 @@ bool valid_store_dtype(int dt) { return dt >= CMD_F32 && dt <= CMD_B1; }
 // stands for the staging slot (the tier's last slot), fixed at encoding.
 constexpr int kSlotX = -2;
 struct Instr {
-  enum Kind { kBin, kUn, kBinS, kMovS, kSt, kCmpX, kCmpS, kSel, kSelS } kind;
+  enum Kind { kBin, kUn, kBinS, kMovS, kSt, kCmpX, kCmpS, kSel, kSelS, kSDiv } kind;
   int op;   // BinOp / UnOp / StoreType / CmpOp
   int d;    // destination slot (kSlotX: the staging slot)
   int s;    // source slot
@@ -98,6 +99,8 @@ struct Program {
   int tier = cmdx::kTier4;
   bool extended = false;  // uses an extended op or store: runs the executors' extended variant
   bool uses_x = false;   // comparisons or selects read the staging slot
+  // scalars derived at launch (after the program's own): {DerivedKind, own scalar index}
+  std::vector<std::pair<int, int>> derived;
 };
 
 }  // namespace
@@ -296,6 +299,8 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
   auto is_scalar = [&](int t) { return ops[t].kind == kScalar; };
   auto emit = [&](Instr::Kind k, int op, int d, int s, int aux) { P->code.push_back({k, op, d, s, aux}); };
   auto store_type = [&](int dt) { return dt; /* cmd_dtype numbering matches StoreType */ };
+  std::map<std::pair<int, int>, int> sdiv_base;  // (float/int, own scalar) -> first derived index
+  P->derived.clear();
 
   for (int i = 0; i < (int)ev.size(); ++i) {
     const int t = ev[i].tag;
@@ -422,6 +427,40 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     const bool sa = is_scalar(a), sb = is_scalar(b);
     const bool die_a = !sa && last_use[a] == i;
     const bool die_b = !sb && last_use[b] == i;
+    if (op.eop == CMD_E_DIV && !sa && sb) {
+      // a tensor value divided by a scalar: through constants the host
+      // derives from the scalar at launch (a reciprocal, or a multiply-high
+      // constant and shift), when the scalar table has room for them
+      const int o = ints ? 1 : 0;
+      const auto key = std::make_pair(o, sidx[b]);
+      auto it = sdiv_base.find(key);
+      int base = it != sdiv_base.end() ? it->second : -1;
+      const int need = o == 0 ? 2 : 3;
+      if (base < 0 && (int)(P->scalar_tags.size() + P->derived.size()) + need <= cmdx::kMaxScalars) {
+        base = (int)(P->scalar_tags.size() + P->derived.size());
+        P->derived.push_back({cmdx::kDerCopy, sidx[b]});
+        if (o == 0) {
+          P->derived.push_back({cmdx::kDerRecip, sidx[b]});
+        } else {
+          P->derived.push_back({cmdx::kDerIMagic, sidx[b]});
+          P->derived.push_back({cmdx::kDerIShift, sidx[b]});
+        }
+        sdiv_base[key] = base;
+      }
+      if (base >= 0) {
+        int d;
+        if (die_a) {
+          d = slot_of[a];
+        } else {
+          d = alloc();
+          ++P->n_moves;
+          emit(Instr::kUn, cmdx::kMov, d, slot_of[a], 0);
+        }
+        emit(Instr::kSDiv, o, d, 0, base);
+        slot_of[t] = d;
+        continue;
+      }
+    }
     auto src = [&](int bo, int d, int x) {  // d = d (bo) x
       if (is_scalar(x)) emit(Instr::kBinS, bo, d, 0, sidx[x]);
       else emit(Instr::kBin, bo, d, slot_of[x], 0);
@@ -468,7 +507,8 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
   // the extended variant: division, comparisons, select, packed-bit stores
   P->extended = false;
   for (const Instr& in : P->code) {
-    const bool div = (in.kind == Instr::kBin || in.kind == Instr::kBinS) && in.op >= cmdx::kFDiv && in.op <= cmdx::kIRdiv;
+    const bool div = ((in.kind == Instr::kBin || in.kind == Instr::kBinS) && in.op >= cmdx::kFDiv && in.op <= cmdx::kIRdiv) ||
+                     in.kind == Instr::kSDiv;
     const bool cmp_sel = in.kind == Instr::kCmpX || in.kind == Instr::kCmpS || in.kind == Instr::kSel ||
                          in.kind == Instr::kSelS;
     const bool bits = in.kind == Instr::kSt && in.op == cmdx::kStB1;
@@ -498,6 +538,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
         case Instr::kCmpS: w = cmdx::fz_cmps(S, in.op, in.d) | uint32_t(in.aux) << 16; break;
         case Instr::kSel: w = cmdx::fz_sel(S, in.d, in.s); break;
         case Instr::kSelS: w = cmdx::fz_sels(S, in.d) | uint32_t(in.aux) << 16; break;
+        case Instr::kSDiv: w = cmdx::fz_sdiv(S, in.op, in.d) | uint32_t(in.aux) << 16; break;
       }
     } else {
       switch (in.kind) {
@@ -507,6 +548,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
         case Instr::kCmpS: w = cmdx::wd_word((cmdx::kWCmp0 + in.op) | cmdx::kWScalar, in.d, 0, in.aux); break;
         case Instr::kSel: w = cmdx::wd_word(cmdx::kWSel, in.d, in.s, 0); break;
         case Instr::kSelS: w = cmdx::wd_word(cmdx::kWSel | cmdx::kWScalar, in.d, 0, in.aux); break;
+        case Instr::kSDiv: w = cmdx::wd_word(cmdx::kWSDiv0 + in.op, in.d, 0, in.aux); break;
         case Instr::kBinS: w = cmdx::wd_word((cmdx::kWBin0 + in.op) | cmdx::kWScalar, in.d, 0, in.aux); break;
         case Instr::kMovS: w = cmdx::wd_word((cmdx::kWUn0 + cmdx::kMov) | cmdx::kWScalar, in.d, 0, in.aux); break;
         case Instr::kSt: w = cmdx::wd_word(cmdx::kWStore0 + in.op, 0, in.s, in.aux); break;
@@ -557,6 +599,36 @@ struct Plan {
   // of the (up to two) batch dims, outer first
   int tile_row = -1, tile_col = -1, n_batch = 0, batch[2] = {-1, -1};
 };
+
+// A scalar derived at launch from the program's scalar v (see DerivedKind).
+uint32_t derive_scalar(int kind, uint32_t v) {
+  if (kind == cmdx::kDerCopy) return v;
+  if (kind == cmdx::kDerRecip) {
+    // RN(1/s): the binary64 quotient rounded once more to binary32 (innocuous,
+    // 53 >= 2*24 + 2); 0 (no fast path) outside [2^-60, 2^60] or for 0, inf, NaN
+    float s;
+    std::memcpy(&s, &v, 4);
+    const double a = std::fabs((double)s);
+    if (!(a >= std::ldexp(1.0, -60) && a <= std::ldexp(1.0, 60))) return 0u;
+    const float r = (float)(1.0 / (double)s);
+    uint32_t rb;
+    std::memcpy(&rb, &r, 4);
+    return rb;
+  }
+  // int32 division by d, truncating (Granlund and Montgomery, "Division by
+  // invariant integers using multiplication", PLDI 1994, section 5):
+  // l = max(ceil(log2 |d|), 1), m = 1 + floor(2^(31 + l) / |d|) - 2^32,
+  // shift l - 1; d = 0 and d = -1 take the general division
+  const int32_t d = (int32_t)v;
+  if (d == 0 || d == -1) return kind == cmdx::kDerIMagic ? 0u : cmdx::kSDivSlow;
+  const uint64_t ad = d < 0 ? (uint64_t)(-(int64_t)d) : (uint64_t)d;
+  int l = 0;
+  while ((uint64_t(1) << l) < ad) ++l;
+  if (l < 1) l = 1;
+  if (kind == cmdx::kDerIShift) return (uint32_t)(l - 1);
+  const int64_t m = 1 + (int64_t)((uint64_t(1) << (31 + l)) / ad) - (int64_t(1) << 32);
+  return (uint32_t)(int32_t)m;
+}
 
 // Largest element offset reached by a view (+1), over dims of size > 1.
 int64_t view_extent(const int64_t* sizes, const int64_t* st, int rank) {
@@ -652,6 +724,8 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   for (int t : P.load_tags) pl->loads.push_back(mkview(t));
   for (int t : P.store_tags) pl->stores.push_back(mkview(t));
   for (size_t j = 0; j < P.scalar_tags.size(); ++j) pl->scal[j] = args->scalars[sarg[P.scalar_tags[j]]].v.bits;
+  for (size_t j = 0; j < P.derived.size(); ++j)
+    pl->scal[P.scalar_tags.size() + j] = derive_scalar(P.derived[j].first, pl->scal[P.derived[j].second]);
   pl->bytes = 0;
   for (auto& v : pl->loads) pl->bytes += N * elem_size(v.dtype);
   for (auto& v : pl->stores) pl->bytes += v.dtype == CMD_B1 ? (N + 31) / 32 * 4 : N * elem_size(v.dtype);
@@ -1269,6 +1343,12 @@ cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* nee
       case Instr::kUn: std::snprintf(line, sizeof line, "%-7s r%d, r%d\n", un[in.op], in.d, in.s); break;
       case Instr::kBinS: std::snprintf(line, sizeof line, "%-7s r%d, s%d\n", bin[in.op], in.d, in.aux); break;
       case Instr::kMovS: std::snprintf(line, sizeof line, "mov     r%d, s%d\n", in.d, in.aux); break;
+      case Instr::kSDiv: {
+        const int own = P.derived[in.aux - (int)P.scalar_tags.size()].second;
+        std::snprintf(line, sizeof line, "%s r%d, s%d  ; through s%d..s%d, derived from s%d at launch\n",
+                      in.op == 0 ? "fdivs  " : "idivs  ", in.d, own, in.aux, in.aux + (in.op == 0 ? 1 : 2), own);
+        break;
+      }
       case Instr::kCmpX:
         std::snprintf(line, sizeof line, "%-7s r%d, r%d\n", cmp[in.op], in.d, cmdx::tier_slots(P.tier) - 1);
         break;

@@ -91,6 +91,10 @@ enum StoreType { kStF32 = 0, kStF16 = 1, kStBF16 = 2, kStI32 = 3, kStB1 = 4, kNu
 //   then C S cases            compare c: d = d rel scalar
 //   then S^2 cases            select: d = X != 0 ? d : slot s
 //   then S cases              select: d = X != 0 ? d : scalar
+//   then 2 S cases            division o of d by a scalar through constants
+//                             the host derives per launch (o = 0: binary32,
+//                             scalars aux, aux + 1 = s, RN(1/s); o = 1:
+//                             int32, scalars aux .. aux + 2 = d, magic, shift)
 // Comparisons and selects read the staging slot X = S - 1, which the lowering
 // fills right before (a program using it keeps slot S - 1 free), so that they
 // take S cases each rather than S^2.
@@ -108,7 +112,18 @@ CMDX_HD constexpr uint32_t fz_cmpx(int S, int c, int d) { return fz_end(S) + 1 +
 CMDX_HD constexpr uint32_t fz_cmps(int S, int c, int d) { return fz_end(S) + 1 + uint32_t((kNumCmp + c) * S + d); }
 CMDX_HD constexpr uint32_t fz_sel(int S, int d, int s) { return fz_end(S) + 1 + uint32_t(2 * kNumCmp * S + d * S + s); }
 CMDX_HD constexpr uint32_t fz_sels(int S, int d) { return fz_end(S) + 1 + uint32_t(2 * kNumCmp * S + S * S + d); }
-CMDX_HD constexpr uint32_t fz_cases(int S) { return fz_sels(S, S); }  // number of cases
+CMDX_HD constexpr uint32_t fz_sdiv(int S, int o, int d) { return fz_sels(S, S) + uint32_t(o * S + d); }
+CMDX_HD constexpr uint32_t fz_cases(int S) { return fz_sdiv(S, 2, 0); }  // number of cases
+
+// Scalars the host derives at launch from a Load_Scalar value, for the
+// divisions by a scalar (stored after the program's own scalars).
+enum DerivedKind {
+  kDerCopy = 0,     // the value itself
+  kDerRecip = 1,    // binary32 RN(1 / s), or 0 when s is outside [2^-60, 2^60] (no fast path)
+  kDerIMagic = 2,   // int32 division by d: the multiplier m - 2^32 (Granlund-Montgomery)
+  kDerIShift = 3,   // ... the post-shift, with kSDivSlow set for d = 0 and d = -1
+};
+constexpr uint32_t kSDivSlow = 0x80000000u;
 
 // ---- wide encoding (tier 32) -------------------------------------------------
 // word = kind << 24 | d << 16 | s << 8 | aux. The source operand x is slot s,
@@ -121,6 +136,7 @@ enum WideKind {
   kWEnd = 31,
   kWCmp0 = 32,   // + CmpOp: d = d rel x
   kWSel = 48,    // d = X != 0 ? d : x
+  kWSDiv0 = 49,  // + o: d = d / scalars aux.. (the fused sdiv cases)
   kWScalar = 0x40
 };
 CMDX_HD constexpr uint32_t wd_word(int kind, int d, int s, int aux) {

@@ -321,6 +321,55 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
       }
       continue;
     }
+    if (base == kWSDiv0 || base == kWSDiv0 + 1) {
+      // division by a scalar through the derived constants at aux..: the fast
+      // sequence when every element of the warp is in range, else the
+      // general division (the same arithmetic as the fused cases)
+      if constexpr (!EXT) return;
+      const uint32_t d = (w >> 16) & 0xffu;
+      uint32_t y[V];
+      switch (d) {
+        CMDX_SA32(CMDX_W_FETCH_Y, 0)
+        default: break;
+      }
+      if (base == kWSDiv0) {
+        const float sv = __uint_as_float(scal[aux]), rv = __uint_as_float(scal[aux + 1]);
+        bool ok = rv != 0.0f;
+        CMDX_UNROLL for (int v = 0; v < V; ++v) {
+          const float a = fabsf(__uint_as_float(y[v]));
+          ok = ok && a >= 0x1p-60f && a <= 0x1p60f;
+        }
+        if (__all_sync(__activemask(), ok)) {
+          CMDX_UNROLL for (int v = 0; v < V; ++v) {
+            const float xv = __uint_as_float(y[v]);
+            float q = __fmul_rn(xv, rv);
+            q = __fmaf_rn(__fmaf_rn(-q, sv, xv), rv, q);
+            q = __fmaf_rn(__fmaf_rn(-q, sv, xv), rv, q);
+            y[v] = __float_as_uint(q);
+          }
+        } else {
+          CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = bin<kFDiv>(y[v], scal[aux]);
+        }
+      } else {
+        const uint32_t sh = scal[aux + 2];
+        if (sh & kSDivSlow) {
+          CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = idiv(y[v], scal[aux]);
+        } else {
+          const int32_t m = (int32_t)scal[aux + 1], ds = (int32_t)scal[aux] >> 31;
+          CMDX_UNROLL for (int v = 0; v < V; ++v) {
+            const int32_t n = (int32_t)y[v];
+            int32_t q = n + __mulhi(m, n);
+            q = (q >> sh) - (n >> 31);
+            y[v] = (uint32_t)((q ^ ds) - ds);
+          }
+        }
+      }
+      switch (d) {
+        CMDX_SA32(CMDX_W_PUT_Y, 0)
+        default: break;
+      }
+      continue;
+    }
     if (base == kWSel) {
       // d = X != 0 ? d : x, X the staging slot 31
       if constexpr (!EXT) return;

@@ -20,6 +20,11 @@ Comparisons and selects read the staging slot X (the tier's last slot,
 filled by the word before): `d = d rel X`, `d = d rel scalar`,
 `d = X != 0 ? d : s` and `d = X != 0 ? d : scalar`, S cases each.
 
+Division by a scalar has its own cases: constants the host derives per
+launch (a reciprocal, or a multiply-high constant and shift) replace the
+division for a warp whose elements all lie in range; otherwise the warp
+branches to the general scalar-division case.
+
 Each tier is emitted twice: the extended variant has the division,
 comparison and select cases; in the base variant those cases exit like the
 end word, so its loop carries none of their code (the host runs a program
@@ -109,7 +114,7 @@ def gen_tier(S: int, V: int, ext: bool) -> str:
         return f"%{i * V + v}"
 
     end = (N_BIN + N_UN) * S * S + (N_BIN + 1 + N_ST) * S
-    n_cases = end + 1 + 2 * N_CMP * S + S * S + S
+    n_cases = end + 1 + 2 * N_CMP * S + S * S + S + 2 * S
     X = S - 1  # the staging slot compares and selects read
     slot_ops = S * V
     o_idx = slot_ops        # "+r" program index (words)
@@ -227,6 +232,44 @@ def gen_tier(S: int, V: int, ext: bool) -> str:
         ops = " ".join(f"setp.ne.u32 %%p0, {reg(X, v)}, 0; selp.b32 {reg(d, v)}, {reg(d, v)}, %%k, %%p0;"
                        for v in range(V))
         bodies.append(f"{lab}: {load_k} {ops} bra.uni $Lloop;")
+    # division of d by a scalar through constants the host derives at launch
+    # (scalars aux, aux + 1, aux + 2): the whole warp takes the fast sequence
+    # or, when any of its elements (or the divisor) is outside its range, the
+    # general scalar-division case of the same destination, which reads the
+    # divisor at aux
+    for o in range(2):
+        for d in range(S):
+            if not ext:
+                labels.append("$Lexit")
+                continue
+            lab = f"$LSD{o}_{d}"
+            labels.append(lab)
+            head = f"shr.u32 %%aux, %%wc, 16; mad.wide.u32 %%sa, %%aux, 4, %{o_scal};"
+            if o == 0:
+                # binary32: q0 = x r, then twice q += (x - q s) r with the
+                # residual formed exactly by an FMA (r = RN(1/s), Markstein)
+                parts = [head, "ld.u32 %%k, [%%sa]; ld.u32 %%t, [%%sa+4]; setp.ne.b32 %%p1, %%t, 0;"]
+                for v in range(V):
+                    x = reg(d, v)
+                    parts.append(f"abs.f32 %%xa, {x}; setp.ge.f32 %%p0, %%xa, 0f21800000; and.pred %%p1, %%p1, %%p0; "
+                                 f"setp.le.f32 %%p0, %%xa, 0f5D800000; and.pred %%p1, %%p1, %%p0;")
+                parts.append(f"activemask.b32 %%aux; vote.sync.all.pred %%p1, %%p1, %%aux; @!%%p1 bra.uni $LS8_{d};")
+                for v in range(V):
+                    x = reg(d, v)
+                    parts.append(f"mul.rn.f32 %%xa, {x}, %%t; neg.f32 %%xb, %%xa; fma.rn.f32 %%xb, %%xb, %%k, {x}; "
+                                 f"fma.rn.f32 %%xa, %%xb, %%t, %%xa; neg.f32 %%xb, %%xa; fma.rn.f32 %%xb, %%xb, %%k, {x}; "
+                                 f"fma.rn.f32 {x}, %%xb, %%t, %%xa;")
+            else:
+                # int32 (Granlund and Montgomery, signed, truncating): q =
+                # ((((n + mulhi(m, n)) >> sh) - (n >> 31)) ^ ds) - ds, ds = d >> 31
+                parts = [head, f"ld.u32 %%t, [%%sa+8]; setp.lt.s32 %%p1, %%t, 0; @%%p1 bra.uni $LS10_{d};",
+                         "ld.u32 %%k, [%%sa+4]; ld.u32 %%rd, [%%sa]; shr.s32 %%rd, %%rd, 31;"]
+                for v in range(V):
+                    x = reg(d, v)
+                    parts.append(f"mul.hi.s32 %%xa, {x}, %%k; add.s32 %%xa, %%xa, {x}; shr.s32 %%xa, %%xa, %%t; "
+                                 f"shr.s32 %%xb, {x}, 31; sub.s32 %%xa, %%xa, %%xb; xor.b32 %%xa, %%xa, %%rd; "
+                                 f"sub.s32 {x}, %%xa, %%rd;")
+            bodies.append(f"{lab}: " + " ".join(parts) + " bra.uni $Lloop;")
     # the table is padded to a power of two with exits so that masking the
     # case number keeps every jump inside it
     assert len(labels) == n_cases

@@ -384,3 +384,32 @@ def test_compare_select_and_packed_bit_type_rules():
     c.store(t[0], "b1", 1)
     c.store(t[1], "i32", 1)
     assert c.lower()[0]["n_live_ops"] == 2
+
+
+def test_division_by_a_scalar_lowers_to_derived_constants():
+    """x / s with a tensor x and a scalar s uses constants derived from s at
+    launch (two scalar slots for floats, three for ints, shared by every
+    division by the same scalar); s / x and x / y take the general form;
+    with the scalar table full the general form is used too."""
+    c = T.Command()
+    x = c.load_tensor("f32", 1)
+    i = c.load_tensor("i32", 1)
+    s = c.load_scalar("f32")
+    k = c.load_scalar("i32")
+    t = c.execute([("div", x, s), ("div", T.CMD_LOCAL(0), s), ("div", i, k), ("div", s, x), ("div", x, x)])
+    for j, dt in enumerate(("f32", "f32", "i32", "f32", "f32")):
+        c.store(t[j], dt, 1)
+    dump = c.lower_kernel().dump()
+    assert dump.count("fdivs") == 2 and dump.count("idivs") == 1
+    assert dump.count("fdivs   r2, s0  ; through s2..s3, derived from s0") == 2  # one shared pair
+    assert "idivs   r1, s1  ; through s4..s6, derived from s1" in dump           # the int triple
+    assert "frdiv   r1, s0" in dump and "fdiv    r0, r0" in dump                 # s / x, x / x: general
+    # 16 scalars in the table: no room for derived constants
+    c = T.Command()
+    x = c.load_tensor("f32", 1)
+    ss = [c.load_scalar("f32") for _ in range(16)]
+    ops = [("add", x, ss[0])] + [("add", T.CMD_LOCAL(j), ss[j + 1]) for j in range(15)] + [("div", T.CMD_LOCAL(15), ss[0])]
+    t = c.execute(ops)
+    c.store(t[-1], "f32", 1)
+    dump = c.lower_kernel().dump()
+    assert "fdivs" not in dump and "fdiv" in dump
