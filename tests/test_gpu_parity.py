@@ -964,3 +964,44 @@ def test_back_to_back_dependent_launches(n, path):
     # every physical element of x follows the same recurrence (a view is a
     # permutation of its buffer), so the buffers compare directly
     assert (x.cpu().numpy() == host.astype(np.int32)).all()
+
+
+def test_concurrent_compile_launch_destroy_from_threads():
+    """Eight host threads, each on its own stream, repeatedly compile a
+    distinct Command, launch it, check it against the oracle and destroy it
+    (slots are reused), with no locking on the caller's side."""
+    import threading
+    errors = []
+    specs = [W.chain_f32(3000 + 17 * t) if t % 3 == 0 else
+             W.wrap_i32(2000 + 5 * t) if t % 3 == 1 else
+             W.threshold_bits(4000 + 33 * t) for t in range(8)]
+    refs = []
+    for spec in specs:
+        bufs = specutil.host_buffers(spec)
+        ref = {k: v.copy() for k, v in bufs.items()}
+        oracle.OracleCommand(spec, ref).eval_range()
+        refs.append((bufs, ref))
+
+    def worker(t):
+        try:
+            spec = specs[t]
+            bufs, ref = refs[t]
+            s = torch.cuda.Stream()
+            dts = W.tensor_dtypes(spec)
+            for _ in range(6):
+                with torch.cuda.stream(s):
+                    c, _ = T.command_from_spec(spec)
+                    k = c.compile()
+                    got, _ = gpuutil.run_cuda(spec, bufs, stream=s.cuda_stream, kernel=k)
+                for name in W.store_names(spec):
+                    gpuutil.compare(got[name], ref[name], dts[name], f"thread {t}: {name}")
+                del k, c
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append((t, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(8)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(300)
+    assert not errors, errors[:3]
