@@ -159,6 +159,7 @@ __device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) { return __ldcs
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint2* p, uint2 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint32_t* p, uint32_t v) { __stcs(reinterpret_cast<unsigned int*>(p), v); }
+__device__ __forceinline__ void st_stream(uint16_t* p, uint16_t v) { __stcs(reinterpret_cast<unsigned short*>(p), v); }
 
 // Load/store one raw element of type dt at element offset off.
 __device__ __forceinline__ uint32_t ld_elem(const void* base, int dt, int64_t off) {

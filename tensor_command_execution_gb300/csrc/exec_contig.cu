@@ -61,22 +61,46 @@ struct ContigStore {
     using M = LaneMap<V>;
     void* base = p.out[o];
     if constexpr (T == kStB1) {
-      // one bit per element: a lane's G bits of group h go to bits
-      // G * (lane % L) .. of word (group start) / 32 + lane / L, L = 32 / G
-      // lanes sharing a word; an xor-shuffle tree ORs them together
+      // one bit per element (min(x, 1) is 1 exactly when x != 0)
       constexpr int G = M::G, L = 32 / G;
       const int lane = threadIdx.x & 31;
       const int64_t chunk = e0 - (int64_t)lane * G;  // a multiple of 32 * V
+      if constexpr (G == 4 && M::NG == 4) {
+        // The lane's 16 bits, element 4h + j at bit 4h + j. The 32 elements
+        // of word h of an 8-lane group are nibble h of its lanes: two
+        // xor-butterflies exchange the lane index bits 0 and 1 with the
+        // nibble index bits, and one shuffle then gives lane 2h + k of the
+        // group bits 16k .. 16k + 15 of its word h, stored as a halfword (a
+        // warp writes its 64 bytes with one store).
+        uint32_t v = min(x[0], 1u);
 #pragma unroll
-      for (int h = 0; h < M::NG; ++h) {
-        uint32_t bits = 0;
+        for (int k = 1; k < 16; ++k) v += min(x[k], 1u) << k;
+        const bool b0 = lane & 1, b1 = lane & 2;
+        const uint32_t k0 = b0 ? 0xF0F0u : 0x0F0Fu, k1 = b1 ? 0xFF00u : 0x00FFu;
+        uint32_t t = __shfl_xor_sync(0xffffffffu, v, 1) & k0;
+        v = (v & k0) | __funnelshift_r(t, t, b0 ? 4 : 28);
+        t = __shfl_xor_sync(0xffffffffu, v, 2) & k1;
+        v = (v & k1) | __funnelshift_r(t, t, b1 ? 8 : 24);
+        const int q = lane & 7;
+        v = __shfl_sync(0xffffffffu, v, (lane & ~7) | ((q & 1) << 2) | (q >> 1));
+        st_stream(reinterpret_cast<uint16_t*>(static_cast<uint32_t*>(base) + chunk / 32) + 8 * (q >> 1) +
+                      2 * (lane >> 3) + (q & 1),
+                  (uint16_t)v);
+      } else {
+        // a lane's G bits of group h go to bits G * (lane % L) .. of word
+        // (group start) / 32 + lane / L, L = 32 / G lanes sharing a word; an
+        // xor-shuffle tree ORs them together
 #pragma unroll
-        for (int j = 0; j < G; ++j) bits |= (x[h * G + j] != 0u ? 1u : 0u) << j;
-        bits <<= G * (lane % L);
+        for (int h = 0; h < M::NG; ++h) {
+          uint32_t bits = min(x[h * G], 1u);
 #pragma unroll
-        for (int m = 1; m < L; m <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, m);
-        if (lane % L == 0)
-          st_stream(static_cast<uint32_t*>(base) + (chunk + (int64_t)h * 32 * G) / 32 + lane / L, bits);
+          for (int j = 1; j < G; ++j) bits += min(x[h * G + j], 1u) << j;
+          bits <<= G * (lane % L);
+#pragma unroll
+          for (int m = 1; m < L; m <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, m);
+          if (lane % L == 0)
+            st_stream(static_cast<uint32_t*>(base) + (chunk + (int64_t)h * 32 * G) / 32 + lane / L, bits);
+        }
       }
     } else {
 #pragma unroll
