@@ -380,6 +380,26 @@ class E2EPipeline:
         self.started = True
 
 
+def per_launch_times(wl, stream, n: int) -> dict:
+    """Median and best of n launches, each between its own pair of events
+    (a pass of its own after the headline region: an event recorded between
+    two launches keeps the second from starting early, so the headline
+    times the launches back to back)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        wl.launch(stream.cuda_stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    if not us:
+        return {"n": 0}
+    med = statistics.median(us)
+    return {"n": n, "median_us": round(med, 2), "best_us": round(us[0], 2),
+            "median_gbs": round(wl.bytes / (med * 1e-6) / 1e9, 1), "best_gbs": round(wl.bytes / (us[0] * 1e-6) / 1e9, 1)}
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest value of x over all ranks (the job's time is its slowest
     rank's); x itself on one rank. Uses the default process group (NCCL on
@@ -448,6 +468,7 @@ def run_ours(args):
     ms = max_over_ranks(start.elapsed_time(stop) / args.steps, world, device)
     gbs = wl.bytes / (ms * 1e-3) / 1e9
     value = whole_job_gbs(wl.bytes, world, ms)
+    per_launch = per_launch_times(wl, stream, min(args.steps, 200))
 
     if args.no_extras:
         if rank == 0:
@@ -536,6 +557,7 @@ def run_ours(args):
                          "kernel": kernel_name,
                          "traffic": profiled_traffic(kernel_name, args.workload),
                          "algorithmic_bytes_per_launch": wl.bytes},
+            "per_launch": per_launch,
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": args.steps * wl.launches_per_step,
@@ -582,6 +604,31 @@ def cpu_baseline(spec, seconds):
     bpe = W.algorithmic_bytes(spec) / n_total
     return {"value": round(m * bpe / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {m} of {n_total} logical elements of the same workload, single thread, "
+                      f"{dt:.1f} s", "elements_per_s": round(m / dt, 1),
+            "multicore": oracle_threads(oc, n_total, bpe, m / dt, seconds)}
+
+
+def split_ranges(m: int, parts: int, align: int = 32) -> list:
+    """[0, m) cut into `parts` contiguous ranges whose inner boundaries are
+    multiples of `align` (so no two ranges write the same packed-bit word)."""
+    step = -(-max(1, m // max(1, parts)) // align) * align
+    cuts = list(range(0, m, step)) + [m]
+    return [(a, b) for a, b in zip(cuts, cuts[1:]) if a < b]
+
+
+def oracle_threads(oc, n_total: int, bpe: float, rate1: float, seconds: float) -> dict:
+    """The same oracle split over the host cores by element ranges (one
+    thread per core; the C walk runs without the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    m = int(min(n_total, max(1 << 16, rate1 * cores * seconds / 2)))
+    ranges = split_ranges(m, cores)
+    t = time.perf_counter()
+    with ThreadPoolExecutor(cores) as ex:
+        list(ex.map(lambda r: oc.eval_range(*r), ranges))
+    dt = time.perf_counter() - t
+    return {"value": round(m * bpe / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "sample": f"first {m} of {n_total} logical elements, {len(ranges)} element ranges on {cores} threads, "
                       f"{dt:.1f} s", "elements_per_s": round(m / dt, 1)}
 
 

@@ -80,3 +80,35 @@ def test_reference_arm_under_torchrun_prints_on_rank_0_only():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["metric"].startswith("fused Command throughput")
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_range_split_keeps_packed_words_apart():
+    sys.path.insert(0, ROOT)
+    import bench
+    for m, parts in [(0, 4), (1, 8), (31, 3), (1000, 8), (4097, 7), (10**6 + 3, 16)]:
+        r = bench.split_ranges(m, parts)
+        assert [a for a, _ in r[1:]] == [b for _, b in r[:-1]]          # contiguous
+        assert (r[0][0] if r else 0) == 0 and (r[-1][1] if r else m) == m
+        assert all(a % 32 == 0 for a, _ in r) and len(r) <= max(1, parts)
+
+
+@pytest.mark.parametrize("name,n", [("threshold_bits", 5003), ("chain_f32", 4099), ("strided_bf16", 0)])
+def test_threaded_oracle_leg_matches_one_thread(name, n):
+    """The multi-core oracle timing writes what one thread writes, packed-bit
+    tail included."""
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np
+
+    import bench
+    import oracle
+    import specutil
+    from inputgen import workloads as W
+    spec = W.FULL[name](*(() if n == 0 else (n,))) if name != "strided_bf16" else W.strided_bf16(40, 72, 80)
+    total = W.numel(spec)
+    one, many = specutil.host_buffers(spec), specutil.host_buffers(spec)
+    oracle.OracleCommand(spec, one).eval_range(0, total)
+    res = bench.oracle_threads(oracle.OracleCommand(spec, many), total, 1.0, 1e12, 1.0)
+    assert res["cores"] >= 1 and res["value"] > 0
+    for s in W.store_names(spec):
+        assert np.array_equal(one[s].view(np.uint8), many[s].view(np.uint8)), s
