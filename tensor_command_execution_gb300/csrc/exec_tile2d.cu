@@ -122,6 +122,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
 }
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -420,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
   const uint32_t full_bar = base;                    // kMaxStages x 8 bytes
   const uint32_t empty_bar = base + 8 * kMaxStages;  // kMaxStages x 8 bytes
   const uint32_t debug_bar = base + 16 * kMaxStages;
+  const uint32_t coords = base + 32 * kMaxStages;    // kMaxStages x 16 bytes: the stage's tile
   const uint32_t stages = base + kBarrierBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ns = p.n_stages;
@@ -467,6 +471,9 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
       }
       const int32_t i0 = (int32_t)(tr * kTileRows), j0 = (int32_t)(tc * kTileCols);
       const uint32_t fb = full_bar + 8 * s;
+      // the tile's coordinates for the consumers (published by the arrive
+      // below, whose release orders this store before the phase completes)
+      sts128(coords + 16 * s, make_uint4(tr, tc, (uint32_t)bc[1], (uint32_t)bc[2]));
       mbar_arrive_expect_tx(fb, p.tx_bytes);
       const uint32_t st = stages + s * p.stage_bytes;
       for (uint32_t j = 0; j < p.n_loads; ++j) {
@@ -521,9 +528,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
       if (lane == 0) atomicOr(p.err, kErrConsumerWait);
       return;
     }
-    const uint32_t tc = t % p.tiles_c, t1 = t / p.tiles_c;
-    const uint32_t tr = ND ? t1 % p.tiles_r : t1, t2 = ND ? t1 / p.tiles_r : 0;
-    const uint32_t b0 = ND ? t2 / p.nb1 : 0, b1 = ND ? t2 % p.nb1 : 0;
+    const uint4 tcrd = lds128(coords + 16 * s);  // written by the producer with this stage
+    const uint32_t tr = tcrd.x, tc = tcrd.y, b0 = tcrd.z, b1 = tcrd.w;
     const int64_t i0 = (int64_t)tr * kTileRows, j0 = (int64_t)tc * kTileCols;
     const uint32_t st = stages + s * p.stage_bytes;
 #pragma unroll 1
