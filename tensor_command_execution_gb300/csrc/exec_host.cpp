@@ -152,7 +152,11 @@ cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_
   if (off == 0 || off > (uint32_t)kTileStageLimit) return cudaErrorInvalidValue;
   p.stage_bytes = off;
   p.tx_bytes = tx;
-  const uint32_t stages_fit = (uint32_t)(2 * kTileStageLimit / off);
+  // stages within 48 KB for the 2-slot tier (its kernel is built for four
+  // CTAs per SM: 3 stages of two 2-byte loads; measured against 4 stages at
+  // three CTAs, strided_bf16 +4%, and two 4-byte loads 2 stages at three
+  // CTAs against 3 at two, batched_transpose +8%), 96 KB for the others
+  const uint32_t stages_fit = (uint32_t)((tier == kTier2 ? 1 : 2) * kTileStageLimit / off);
   p.n_stages = stages_fit < 2 ? 2 : stages_fit > kMaxStages ? kMaxStages : stages_fit;
   for (int j = 0; j < kMaxStores; ++j) {
     p.out[j] = L.out[j];

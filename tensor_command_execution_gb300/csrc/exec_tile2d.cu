@@ -407,8 +407,9 @@ struct TileStore2 {
   }
 };
 
-// Resident CTAs per SM the register budget is sized for.
-CMDX_HD constexpr int tile_min_blocks(int tier) { return tier == kTier2 ? 3 : 2; }
+// Resident CTAs per SM the register budget is sized for (the 2-slot tier
+// fits four in 56 registers; shared memory then allows 3 stages of 16 KB).
+CMDX_HD constexpr int tile_min_blocks(int tier) { return tier == kTier2 ? 4 : 2; }
 // Rows each consumer thread handles per tile pass: 2 in the 2- and 4-slot tiers.
 CMDX_HD constexpr int tile_rows_per_thread(int tier) { return tier == kTier8 ? 1 : 2; }
 
