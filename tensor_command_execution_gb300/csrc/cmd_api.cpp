@@ -1432,7 +1432,9 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n = n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
-      e = cmdx::contig_launch(P.tier, P.extended, p, stream);
+      bool bits_only = !pl.stores.empty();
+      for (const auto& v : pl.stores) bits_only = bits_only && v.dtype == CMD_B1;
+      e = cmdx::contig_launch(P.tier, P.extended, p, stream, bits_only);
     }
     if (e == cudaSuccess && pl.n > n_main) {
       cmdx::GenericParams p;

@@ -225,12 +225,19 @@ struct GenericParams {
 CMDX_DECL_OBJ(0, 0) CMDX_DECL_OBJ(1, 0) CMDX_DECL_OBJ(2, 0) CMDX_DECL_OBJ(3, 0)
 CMDX_DECL_OBJ(0, 1) CMDX_DECL_OBJ(1, 1) CMDX_DECL_OBJ(2, 1) CMDX_DECL_OBJ(3, 1)
 #undef CMDX_DECL_OBJ
+// the extended 2-slot contiguous kernel built for four CTAs per SM
+cudaError_t contig_upload_t0e1o4(int slot, const uint32_t* words, int n);
+cudaError_t contig_launch_t0e1o4(const ContigParams& p, cudaStream_t stream);
 
 // Write a compiled program into slot `slot` of every executor object of its
 // tier and variant (ext: the program uses an extended op or store).
 cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, int n);
 // n must be a multiple of contig_chunk(tier, ext) elements.
-cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream);
+// bits_only: every store of the program is packed bits (such programs read
+// far more than they write, and the extended 2-slot tier runs them on its
+// four-CTA build: measured, threshold_bits +12%, while one-word-per-element
+// stores ran 1-6% slower there).
+cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream, bool bits_only = false);
 int contig_chunk(int tier, bool ext);
 cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int tier, bool ext, const GenericParams& p, cudaStream_t stream);

@@ -28,7 +28,16 @@
 // with division, comparisons, select and packed-bit stores).
 #define CMDX_TIER_CAT2(a, b) a##b
 #define CMDX_TIER_CAT(a, b) CMDX_TIER_CAT2(a, b)
+// An object built with CMDX_OCC4=1 (a contiguous kernel sized for four
+// resident CTAs per SM) appends o4.
+#ifndef CMDX_OCC4
+#define CMDX_OCC4 0
+#endif
+#if CMDX_OCC4
+#define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), e), CMDX_EXT), o4)
+#else
 #define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), e), CMDX_EXT)
+#endif
 
 namespace cmdx {
 

@@ -128,8 +128,10 @@ struct ContigStore {
   }
 };
 
-template <int TIER, bool EXT>
-__global__ void __launch_bounds__(256, tier_min_blocks(TIER)) contig_kernel(const __grid_constant__ ContigParams p) {
+// MINB: resident CTAs per SM the registers are sized for (one object of the
+// extended 2-slot tier is built for 4 instead of 3, for packed-bit programs)
+template <int TIER, bool EXT, int MINB>
+__global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant__ ContigParams p) {
   constexpr int S = tier_slots(TIER);
   constexpr int V = tier_vec(TIER, EXT);
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
@@ -185,6 +187,7 @@ cudaError_t CMDX_TIER_NAME(contig_upload_t)(int slot, const uint32_t* words, int
 
 template <int TIER, bool EXT>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
+  constexpr int MINB = CMDX_OCC4 ? 4 : tier_min_blocks(TIER);
   constexpr int V = tier_vec(TIER, EXT);
   constexpr int kBlock = 256;
   static int grid_cache[64] = {0};
@@ -193,11 +196,11 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
   if (full_grid == 0) {
-    full_grid = persistent_grid(contig_kernel<TIER, EXT>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(contig_kernel<TIER, EXT, MINB>, kBlock, 0, INT64_MAX);
     if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  return launch_pdl(contig_kernel<TIER, EXT>, grid, kBlock, 0, stream, p);
+  return launch_pdl(contig_kernel<TIER, EXT, MINB>, grid, kBlock, 0, stream, p);
 }
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {

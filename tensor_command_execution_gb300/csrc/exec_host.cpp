@@ -50,13 +50,15 @@ bool tier_ok(int tier) { return tier >= kTier2 && tier <= kTier32; }
 cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, int n) {
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
   cudaError_t e = kContigUpload[ext][tier](slot, words, n);
+  if (e == cudaSuccess && ext && tier == kTier2) e = contig_upload_t0e1o4(slot, words, n);
   if (e == cudaSuccess) e = kGenericUpload[ext][tier](slot, words, n);
   for (int nd = 0; nd < 2 && e == cudaSuccess && tier != kTier32; ++nd) e = kTileUpload[ext][nd][tier](slot, words, n);
   return e;
 }
 
-cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream) {
+cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream, bool bits_only) {
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
+  if (ext && tier == kTier2 && bits_only) return contig_launch_t0e1o4(p, stream);
   return kContigLaunch[ext][tier](p, stream);
 }
 
