@@ -10,8 +10,9 @@
 // it. Eight consumer warps read the stage, run the program and store straight
 // to global memory with 16-byte vector stores. A transposed view arrives in
 // its physical layout (one box row per logical column) and is read across box
-// rows; each lane starts that walk at a different box row so that the eight
-// lanes of a tile row hit distinct banks, then rotates its registers back.
+// rows; each lane walks them in an order of its own (step k, box row k ^ cj
+// of its group) so that the eight lanes of a tile row hit distinct banks,
+// then permutes its registers back.
 //
 // Every wait on an mbarrier is bounded by a time limit; a wait that runs out
 // records a code in the kernel's device error word and the CTA stops (after
@@ -136,7 +137,23 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   return v;
 }
 
-__device__ __forceinline__ void rotate8(uint32_t (&y)[8], int c);
+__device__ __forceinline__ void xor_perm8(uint32_t (&y)[8], int c);
+
+// Transposed reads: logical (li, 8 cj + m) is element li of box row
+// q = 8 cj + m. Step k of a lane reads m = k ^ cj, so the lanes of a tile row
+// (cj = 0..7) see eight different q % 8 and, under the swizzle, eight
+// different chunks. Its address is then one per-thread base XOR k * 0x90:
+// bits 7..9 (q % 8 = k ^ cj) and bits 4..6 (the chunk, (li / 8) ^ k ^ cj)
+// both flip with k, and the base's own bits 4..9 start at cj and li / 8 ^ cj.
+__device__ __forceinline__ uint32_t trans_base(uint32_t stage, bool half, int li, int cj) {
+  const uint32_t c = (uint32_t)cj;
+  if (half) {
+    const uint32_t ch = (uint32_t)li >> 3;
+    return (stage + c * 1024 + (li & 7) * 2) | (c << 7) | ((ch ^ c) << 4);
+  }
+  const uint32_t lr = li & 31;
+  return (stage + (li >> 5) * kBoxBytes + c * 1024 + (lr & 3) * 4) | (c << 7) | (((lr >> 2) ^ c) << 4);
+}
 
 // Row-direct: logical (li, 8 cj .. 8 cj + 7).
 __device__ __forceinline__ void read_row(uint32_t (&x)[8], uint32_t stage, int dt, int li, int cj) {
@@ -165,32 +182,21 @@ __device__ __forceinline__ void read_row(uint32_t (&x)[8], uint32_t stage, int d
   }
 }
 
-// Transposed: logical (li, 8 cj + m) is box row q = 8 cj + m, element li.
-// Step k reads m = (k + cj) % 8, so q % 8 differs across a tile row's lanes;
-// the values are then rotated back into column order.
+// Transposed, one row: x[m] = logical (li, 8 cj + m).
 __device__ __forceinline__ void read_trans(uint32_t (&x)[8], uint32_t stage, int dt, int li, int cj) {
   uint32_t y[8];
-  if (dt == 1 || dt == 2) {
-    const uint32_t within = (li & 7) * 2;
-    const uint32_t ch = li >> 3;
+  const bool half = dt == 1 || dt == 2;
+  const uint32_t a = trans_base(stage, half, li, cj);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t q = 8 * cj + ((k + cj) & 7);
-      const uint32_t h = lds16(stage + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+  for (int k = 0; k < 8; ++k) {
+    if (half) {
+      const uint32_t h = lds16(a ^ (uint32_t)(k * 0x90));
       y[k] = dt == 1 ? widen_f16((uint16_t)h) : widen_bf16((uint16_t)h);
-    }
-  } else {
-    const uint32_t box = stage + (li >> 5) * kBoxBytes;
-    const uint32_t lr = li & 31;
-    const uint32_t within = (lr & 3) * 4;
-    const uint32_t ch = lr >> 2;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t q = 8 * cj + ((k + cj) & 7);
-      y[k] = lds32(box + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+    } else {
+      y[k] = lds32(a ^ (uint32_t)(k * 0x90));
     }
   }
-  rotate8(y, cj);
+  xor_perm8(y, cj);
 #pragma unroll
   for (int m = 0; m < 8; ++m) x[m] = y[m];
 }
@@ -201,17 +207,20 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
   return v;
 }
 
-// x[m] = y[(m - c) % 8] for a thread-constant c: rotations by 1, 2 and 4.
-__device__ __forceinline__ void rotate8(uint32_t (&y)[8], int c) {
-  uint32_t z[8];
+// y[m] = y[m ^ c] for a thread-constant c: conditional swaps of the pairs
+// that differ in bit 1, 2 and 4 of the index.
+__device__ __forceinline__ void xor_perm8(uint32_t (&y)[8], int c) {
 #pragma unroll
-  for (int m = 0; m < 8; ++m) z[m] = (c & 1) ? y[(m + 7) & 7] : y[m];
+  for (int b = 1; b < 8; b <<= 1) {
+    const bool f = (c & b) != 0;
 #pragma unroll
-  for (int m = 0; m < 8; ++m) y[m] = (c & 2) ? z[(m + 6) & 7] : z[m];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) z[m] = (c & 4) ? y[(m + 4) & 7] : y[m];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) y[m] = z[m];
+    for (int m = 0; m < 8; ++m)
+      if ((m & b) == 0) {
+        const uint32_t u = y[m], v = y[m | b];
+        y[m] = f ? v : u;
+        y[m | b] = f ? u : v;
+      }
+  }
 }
 
 // Two rows per thread: x[0..7] is box row la, x[8..15] box row lb.
@@ -230,15 +239,12 @@ __device__ __forceinline__ void read_row2(uint32_t (&x)[16], uint32_t stage, int
 // 32-bit (2-byte types) or 64-bit (4-byte types) load fetches both.
 __device__ __forceinline__ void read_trans2(uint32_t (&x)[16], uint32_t stage, int dt, int li, int cj) {
   uint32_t y0[8], y1[8];
-  if (dt == 1 || dt == 2) {
-    const uint32_t within = (li & 7) * 2;
-    const uint32_t ch = li >> 3;
+  const bool half = dt == 1 || dt == 2;
+  const uint32_t a = trans_base(stage, half, li, cj);
+  if (half) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t q = 8 * cj + ((k + cj) & 7);
-      y0[k] = lds32(stage + q * 128 + ((ch ^ (q & 7)) << 4) + within);
-    }
-    rotate8(y0, cj);
+    for (int k = 0; k < 8; ++k) y0[k] = lds32(a ^ (uint32_t)(k * 0x90));
+    xor_perm8(y0, cj);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       if (dt == 1) {
@@ -248,19 +254,14 @@ __device__ __forceinline__ void read_trans2(uint32_t (&x)[16], uint32_t stage, i
       }
     }
   } else {
-    const uint32_t box = stage + (li >> 5) * kBoxBytes;
-    const uint32_t lr = li & 31;
-    const uint32_t within = (lr & 3) * 4;
-    const uint32_t ch = lr >> 2;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t q = 8 * cj + ((k + cj) & 7);
-      const uint2 v = lds64(box + q * 128 + ((ch ^ (q & 7)) << 4) + within);
+      const uint2 v = lds64(a ^ (uint32_t)(k * 0x90));
       y0[k] = v.x;
       y1[k] = v.y;
     }
-    rotate8(y0, cj);
-    rotate8(y1, cj);
+    xor_perm8(y0, cj);
+    xor_perm8(y1, cj);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       x[m] = y0[m];
