@@ -100,11 +100,12 @@ cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_
     // A transposed load whose column count is a multiple of 8 has its column
     // dim split in two, (column / 8, stride 8 ld) then (column % 8, stride
     // ld), each a box of 8: column 8 g + k then lands in box row g + 8 k,
-    // which the consumers read without bank conflicts or register rotation.
+    // which the consumers read without bank conflicts or register permutes.
     // Measured on GB300 it pays for 4-byte loads in batched launches of the
-    // 2-slot tier (+5%); a 2-byte load with 16 KB rows ran 15% slower split
-    // (the box then walks rows eight apart), and the extra read path cost
-    // the plain 2-D kernel 3%, so only that case splits.
+    // 2-slot tier (+5% against rotated reads, +1.2% against XOR-order ones);
+    // a 2-byte load with 16 KB rows ran 15% slower split (the box then walks
+    // rows eight apart), and the extra read path cost the plain 2-D kernel
+    // 3%, so only that case splits.
     struct D { int64_t stride, size; int src; uint32_t box; };
     auto encode_load = [&](bool split) -> CUresult {
       D d[4];

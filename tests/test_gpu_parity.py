@@ -96,6 +96,54 @@ def test_tile_paths(dt, rows, cols):
     assert plan["path"] == "tile2d" and plan["n_transposed"] == 2
 
 
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16", "i32"])
+@pytest.mark.parametrize("n_trans,n_live,tier", [(1, 0, 0), (2, 0, 1), (2, 4, 2)])
+def test_tile_transposed_reads_in_every_tier(dt, n_trans, n_live, tier):
+    """One row-direct and n_trans transposed loads, plus n_live values kept
+    live together, put the program in the 2-, 4- or 8-slot tier of the tile
+    executor: the two-row readers (2- and 4-slot) and the one-row reader
+    (8-slot) over a ragged 130 x 72 index space, every element against the
+    oracle. (At most three loads: a stage of the tile executor holds 48 KB.)"""
+    rows, cols = 130, 72
+    es = 2 if dt in ("f16", "bf16") else 4
+    al = 16 // es
+    ldA = (cols + al - 1) // al * al + al
+    ldB = (rows + al - 1) // al * al + al
+    rng = np.random.default_rng(n_trans * 10 + n_live + len(dt))
+    bs = [f"B{i}" for i in range(n_trans)]
+    ops3 = ("add", "mul", "sub")
+    block, acc = [], "A"
+    for i, b in enumerate(bs):
+        block.append((ops3[i % 3], f"t{i}", acc, b))
+        acc = f"t{i}"
+    qs = [f"q{k}" for k in range(n_live)]
+    for k, q in enumerate(qs):   # all computed before any is consumed
+        block.append((ops3[(k + 1) % 3], q, "A", bs[k % n_trans]))
+    for k, q in enumerate(qs):
+        block.append((ops3[k % 3], f"u{k}", acc, q))
+        acc = f"u{k}"
+    spec = dict(name=f"tile_t{tier}_{dt}", seed=0, sizes=(rows, cols),
+                ops=[("load", "A", dt)] + [("load", b, dt) for b in bs] + [("exec", block), ("store", "out", acc, dt)],
+                views=dict({"A": dict(strides=(ldA, 1), alloc=(rows - 1) * ldA + cols),
+                            "out": dict(strides=(cols, 1), alloc=rows * cols)},
+                           **{b: dict(strides=(1, ldB), alloc=(cols - 1) * ldB + rows) for b in bs}),
+                inputs={})
+    bufs = {}
+    for name in ["A"] + bs:
+        n = spec["views"][name]["alloc"]
+        if dt == "i32":
+            bufs[name] = rng.integers(-2**31, 2**31, size=n).astype(np.int32)
+        else:
+            f = (rng.standard_normal(n) * 2).astype(np.float32)
+            bufs[name] = f if dt == "f32" else f.astype(np.float16) if dt == "f16" else \
+                (f.view(np.uint32) >> 16).astype(np.uint16)
+    bufs["out"] = specutil.sentinel_array(dt, rows * cols)
+    c, _ = T.command_from_spec(spec)
+    assert c.lower()[0]["tier"] == tier
+    plan = gpuutil.parity(spec, bufs)
+    assert plan["path"] == "tile2d" and plan["n_transposed"] == n_trans
+
+
 # ---- randomized Commands ---------------------------------------------------------------
 
 def _dense_strides(shape):
