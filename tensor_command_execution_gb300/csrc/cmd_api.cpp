@@ -1452,6 +1452,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       }
       for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(1);
       p.div[cmdx::kMaxRank - 1] = make_fastdiv(pl.n - n_main);
+      p.top = cmdx::kMaxRank - 1;
       std::memcpy(p.scal, pl.scal, sizeof p.scal);
       p.n = pl.n - n_main;
       p.prog = (uint32_t)k->slot;
@@ -1505,6 +1506,9 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       for (int d = 0; d < cmdx::kMaxRank; ++d) p.out_st[j][d] = pl.ms[j][d];
     }
     for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(pl.msizes[d]);
+    p.top = cmdx::kMaxRank - 1;
+    for (int d = cmdx::kMaxRank - 1; d >= 0; --d)
+      if (pl.msizes[d] > 1) p.top = (uint32_t)d;
     std::memcpy(p.scal, pl.scal, sizeof p.scal);
     p.n = pl.n;
     p.prog = (uint32_t)k->slot;

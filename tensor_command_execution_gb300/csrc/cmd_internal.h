@@ -206,6 +206,7 @@ struct GenericParams {
   int64_t n;
   uint32_t prog;
   uint32_t n_loads;
+  uint32_t top;                         // outermost dim of size > 1 (kMaxRank - 1 if none)
   uint8_t in_dt[kMaxLoads];
 };
 

@@ -27,12 +27,15 @@ __device__ __forceinline__ uint64_t fast_div(const FastDiv& f, uint64_t e) {
 }
 
 // Offset of linear element e in a view with right-aligned strides st: the
-// row-major multi-index of e dotted with the strides.
+// row-major multi-index of e dotted with the strides. The outermost dim of
+// size > 1 takes what remains without a division (e < n bounds it), so a
+// rank-1 view costs one multiply.
 __device__ __forceinline__ int64_t gen_offset(const GenericParams& p, const int64_t* st, int64_t e) {
   int64_t off = 0;
   uint64_t rem = (uint64_t)e;
 #pragma unroll
   for (int k = kMaxRank - 1; k > 0; --k) {
+    if (k == (int)p.top) return off + (int64_t)rem * st[k];
     if (p.div[k].l == 0) continue;  // size-1 dim
     const uint64_t q = fast_div(p.div[k], rem);
     off += (int64_t)(rem - q * (uint64_t)p.div[k].d) * st[k];
@@ -83,14 +86,25 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(con
   for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w * 32 * V < p.n; w += nwarps) {
     const int64_t base = w * 32 * V;
     uint32_t r[S][V];
+    // every load of every view is issued before any is widened, so they are
+    // all in flight at once (a widening right after each load would wait for
+    // it before the next load issues)
 #pragma unroll
     for (int j = 0; j < NL; ++j) {
       if (j < (int)p.n_loads) {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
           const int64_t e = base + 32 * v + lane;
-          r[j][v] = e < p.n ? widen_any(p.in_dt[j], ld_elem(p.in[j], p.in_dt[j], gen_offset(p, p.in_st[j], e))) : 0u;
+          r[j][v] = 0u;
+          if (e < p.n) r[j][v] = ld_elem(p.in[j], p.in_dt[j], gen_offset(p, p.in_st[j], e));
         }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NL; ++j) {
+      if (j < (int)p.n_loads && (p.in_dt[j] == 1 || p.in_dt[j] == 2)) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) r[j][v] = widen_any(p.in_dt[j], r[j][v]);
       }
     }
     GenericStore<V> st{p, base, lane};
