@@ -200,7 +200,9 @@ typedef struct cmd_program_info {
 /* Which executor a launch would use (cmd_plan_launch). */
 typedef enum cmd_path {
   CMD_PATH_NONE = 0,    /* nothing to do (no elements or no stores) */
-  CMD_PATH_CONTIG = 1,  /* every view dense row-major and aligned: vector loads/stores */
+  CMD_PATH_CONTIG = 1,  /* every view dense row-major and aligned, or all off the vector
+                           alignment by one number of elements (the few elements before
+                           they align run per element): vector loads/stores */
   CMD_PATH_TILE2D = 2,  /* 2-D views, row-direct or transposed, staged through shared memory */
   CMD_PATH_GENERIC = 3  /* any other sizes/strides: per-element offsets */
 } cmd_path;

@@ -587,6 +587,9 @@ struct View {
 struct Plan {
   int path = CMD_PATH_NONE;
   int64_t n = 0;
+  // contiguous path: elements before the first one at which every pointer is
+  // aligned for the vector width (they run on the generic executor)
+  int64_t head = 0;
   int mrank = 0;
   int64_t msizes[cmdx::kMaxRank] = {1, 1, 1, 1};
   std::vector<View> loads, stores;       // in slot / output order
@@ -846,6 +849,27 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   if (contig) {
     pl->path = CMD_PATH_CONTIG;
     return CMD_OK;
+  }
+  // One merged unit-stride dim whose pointers are all off the vector
+  // alignment by the same number of elements (every tensor sliced at one
+  // offset, say): after h = 4 - that number elements all of them are aligned,
+  // so the first h run on the generic executor and the rest as above.
+  // (Not with packed bits, whose words must start where the view does.)
+  if (m <= 1 && !any_b1) {
+    bool same = true;
+    int64_t phase = -1;
+    for (size_t i = 0; i < all.size() && same; ++i) {
+      if (m == 1 && wst[i][0] != 1) same = false;
+      const int64_t es = elem_size(all[i]->dtype);
+      const int64_t ph = (int64_t)((reinterpret_cast<uintptr_t>(all[i]->ptr) / (uintptr_t)es) % 4);
+      if (phase < 0) phase = ph;
+      else if (ph != phase) same = false;
+    }
+    if (same && phase > 0 && pl->n > 4 - phase) {
+      pl->path = CMD_PATH_CONTIG;
+      pl->head = 4 - phase;
+      return CMD_OK;
+    }
   }
   // tile: two of the merged dims form the tile, the rest (at most two) are
   // batch dims. The column dim is the first store's unit-stride dim; the row
@@ -1415,19 +1439,50 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
   const Program& P = k->prog;
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   if (pl.path == CMD_PATH_CONTIG) {
-    // whole warp chunks on the contiguous executor, a ragged tail (fewer than
+    // whole warp chunks on the contiguous executor; a head (the elements
+    // before every pointer is vector-aligned) and a ragged tail (fewer than
     // one chunk of elements) on the generic one
     const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended);
-    const int64_t n_main = pl.n - pl.n % chunk;
+    const int64_t head = pl.head;
+    const int64_t n_main = (pl.n - head) - (pl.n - head) % chunk;
+    // the generic executor over the 1-D elements [start, start + count),
+    // skipping [start + gap_at, start + gap_at + gap)
+    auto generic_range = [&](int64_t start, int64_t count, int64_t gap_at, int64_t gap) -> cudaError_t {
+      cmdx::GenericParams p;
+      std::memset(&p, 0, sizeof p);
+      for (size_t j = 0; j < pl.loads.size(); ++j) {
+        p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + start * elem_size(pl.loads[j].dtype);
+        p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+        p.in_st[j][cmdx::kMaxRank - 1] = 1;
+      }
+      for (size_t j = 0; j < pl.stores.size(); ++j) {
+        // (packed bits have no head, and the tail starts at a multiple of
+        // the chunk, so on a word)
+        const int64_t skip = pl.stores[j].dtype == CMD_B1 ? start / 8 : start * elem_size(pl.stores[j].dtype);
+        p.out[j] = static_cast<char*>(pl.stores[j].ptr) + skip;
+        p.out_st[j][cmdx::kMaxRank - 1] = 1;
+      }
+      for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(1);
+      p.div[cmdx::kMaxRank - 1] = make_fastdiv(count);
+      p.top = cmdx::kMaxRank - 1;
+      p.gap_at = gap_at;
+      p.gap = gap;
+      std::memcpy(p.scal, pl.scal, sizeof p.scal);
+      p.n = count;
+      p.prog = (uint32_t)k->slot;
+      p.n_loads = (uint32_t)pl.loads.size();
+      return cmdx::generic_launch(P.tier, P.extended, p, stream);
+    };
     e = cudaSuccess;
-    if (n_main > 0) {
+    if (e == cudaSuccess && n_main > 0) {
       cmdx::ContigParams p;
       std::memset(&p, 0, sizeof p);
       for (size_t j = 0; j < pl.loads.size(); ++j) {
-        p.in[j] = pl.loads[j].ptr;
+        p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + head * elem_size(pl.loads[j].dtype);
         p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
       }
-      for (size_t j = 0; j < pl.stores.size(); ++j) p.out[j] = pl.stores[j].ptr;
+      for (size_t j = 0; j < pl.stores.size(); ++j)
+        p.out[j] = static_cast<char*>(pl.stores[j].ptr) + head * elem_size(pl.stores[j].dtype);
       std::memcpy(p.scal, pl.scal, sizeof p.scal);
       p.n = n_main;
       p.prog = (uint32_t)k->slot;
@@ -1436,29 +1491,12 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       for (const auto& v : pl.stores) bits_only = bits_only && v.dtype == CMD_B1;
       e = cmdx::contig_launch(P.tier, P.extended, p, stream, bits_only);
     }
-    if (e == cudaSuccess && pl.n > n_main) {
-      cmdx::GenericParams p;
-      std::memset(&p, 0, sizeof p);
-      for (size_t j = 0; j < pl.loads.size(); ++j) {
-        p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + n_main * elem_size(pl.loads[j].dtype);
-        p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
-        p.in_st[j][cmdx::kMaxRank - 1] = 1;
-      }
-      for (size_t j = 0; j < pl.stores.size(); ++j) {
-        // (packed bits: n_main is a multiple of 32, so the tail starts on a word)
-        const int64_t skip = pl.stores[j].dtype == CMD_B1 ? n_main / 8 : n_main * elem_size(pl.stores[j].dtype);
-        p.out[j] = static_cast<char*>(pl.stores[j].ptr) + skip;
-        p.out_st[j][cmdx::kMaxRank - 1] = 1;
-      }
-      for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(1);
-      p.div[cmdx::kMaxRank - 1] = make_fastdiv(pl.n - n_main);
-      p.top = cmdx::kMaxRank - 1;
-      std::memcpy(p.scal, pl.scal, sizeof p.scal);
-      p.n = pl.n - n_main;
-      p.prog = (uint32_t)k->slot;
-      p.n_loads = (uint32_t)pl.loads.size();
-      e = cmdx::generic_launch(P.tier, P.extended, p, stream);
-    }
+    // the tail from where the contiguous launch ends; with a head, head and
+    // tail in one launch whose index space skips the contiguous launch's
+    // elements (there are no packed-bit stores then: those index words by
+    // the launch's own element index)
+    if (e == cudaSuccess && pl.n > n_main)
+      e = head == 0 ? generic_range(n_main, pl.n - n_main, pl.n, 0) : generic_range(0, pl.n - n_main, head, n_main);
   } else if (pl.path == CMD_PATH_TILE2D) {
     cmdx::Tile2dLaunch L;
     std::memset(&L, 0, sizeof L);
@@ -1506,6 +1544,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       for (int d = 0; d < cmdx::kMaxRank; ++d) p.out_st[j][d] = pl.ms[j][d];
     }
     for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(pl.msizes[d]);
+    p.gap_at = pl.n;  // no gap
     p.top = cmdx::kMaxRank - 1;
     for (int d = cmdx::kMaxRank - 1; d >= 0; --d)
       if (pl.msizes[d] > 1) p.top = (uint32_t)d;

@@ -207,6 +207,7 @@ struct GenericParams {
   uint32_t prog;
   uint32_t n_loads;
   uint32_t top;                         // outermost dim of size > 1 (kMaxRank - 1 if none)
+  int64_t gap_at, gap;                  // logical index e >= gap_at stands for e + gap (1-D ranges)
   uint8_t in_dt[kMaxLoads];
 };
 

@@ -56,6 +56,7 @@ struct GenericStore {
     if constexpr (T == kStB1) {
       // one bit per element, at its row-major index (the view is dense):
       // the warp's 32 consecutive elements base + 32 v + lane make one word
+      // (launches with packed bits have no gap)
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int64_t e = base + 32 * v + lane;
@@ -68,7 +69,7 @@ struct GenericStore {
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int64_t e = base + 32 * v + lane;
-      if (e < p.n) st_elem<T>(ptr, gen_offset(p, st, e), x[v]);
+      if (e < p.n) st_elem<T>(ptr, gen_offset(p, st, e < p.gap_at ? e : e + p.gap), x[v]);
     }
   }
 };
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(con
         for (int v = 0; v < V; ++v) {
           const int64_t e = base + 32 * v + lane;
           r[j][v] = 0u;
-          if (e < p.n) r[j][v] = ld_elem(p.in[j], p.in_dt[j], gen_offset(p, p.in_st[j], e));
+          if (e < p.n) r[j][v] = ld_elem(p.in[j], p.in_dt[j], gen_offset(p, p.in_st[j], e < p.gap_at ? e : e + p.gap));
         }
       }
     }
