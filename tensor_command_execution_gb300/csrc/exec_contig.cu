@@ -17,7 +17,11 @@ namespace cmdx {
 
 static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
 
-// Load one slot (V elements per lane) of a dense tensor of type dt.
+// Load one slot (V elements per lane) of a dense tensor of type dt. 2-byte
+// types arrive packed, two to a word, in x[0 .. V/2); contig_widen expands
+// them afterwards, so that every load of a chunk issues before any result is
+// used (widening each group as it came would wait for its load before the
+// next one issued).
 template <int V>
 __device__ __forceinline__ void contig_load(uint32_t (&x)[V], const void* base, int dt, int64_t e0) {
   using M = LaneMap<V>;
@@ -35,18 +39,30 @@ __device__ __forceinline__ void contig_load(uint32_t (&x)[V], const void* base, 
     } else {
       if constexpr (M::G == 4) {
         const uint2 q = ld_stream(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + e));
-        if (dt == 1) {
-          widen_f16x2(q.x, x[4 * h], x[4 * h + 1]);
-          widen_f16x2(q.y, x[4 * h + 2], x[4 * h + 3]);
-        } else {
-          widen_bf16x2(q.x, x[4 * h], x[4 * h + 1]);
-          widen_bf16x2(q.y, x[4 * h + 2], x[4 * h + 3]);
-        }
+        x[2 * h] = q.x; x[2 * h + 1] = q.y;
       } else {
-        const uint32_t q = ld_stream(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + e));
-        if (dt == 1) widen_f16x2(q, x[2 * h], x[2 * h + 1]);
-        else widen_bf16x2(q, x[2 * h], x[2 * h + 1]);
+        x[h] = ld_stream(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + e));
       }
+    }
+  }
+}
+
+// Expand a 2-byte slot loaded by contig_load to one fp32 per register: word
+// k holds elements 2k and 2k + 1 (from the last word down, so that no packed
+// word is overwritten before it is read).
+template <int V>
+__device__ __forceinline__ void contig_widen(uint32_t (&x)[V], int dt) {
+  if (dt == 1) {
+#pragma unroll
+    for (int k = V / 2 - 1; k >= 0; --k) {
+      const uint32_t w = x[k];
+      widen_f16x2(w, x[2 * k], x[2 * k + 1]);
+    }
+  } else if (dt == 2) {
+#pragma unroll
+    for (int k = V / 2 - 1; k >= 0; --k) {
+      const uint32_t w = x[k];
+      widen_bf16x2(w, x[2 * k], x[2 * k + 1]);
     }
   }
 }
@@ -165,6 +181,9 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
         for (int j = 0; j < NL; ++j)
           if (j < (int)p.n_loads) contig_load<V>(nx[j], p.in[j], p.in_dt[j], e0 + nwarps * M::W);
       }
+#pragma unroll
+      for (int j = 0; j < NL; ++j)
+        if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
       ContigStore<V> st{p, e0};
       run_program<TIER, V, EXT>(r, prog, p.scal, st);
     }
@@ -175,6 +194,9 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
 #pragma unroll
       for (int j = 0; j < NL; ++j)
         if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
+#pragma unroll
+      for (int j = 0; j < NL; ++j)
+        if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
       ContigStore<V> st{p, e0};
       run_program<TIER, V, EXT>(r, prog, p.scal, st);
     }
