@@ -421,7 +421,8 @@ def whole_job_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
 
 DTYPE_OF = {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
             "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32", "div_clamp_i32": "f32 (int32 out)",
-            "threshold_u32": "u32 (int32 out)", "threshold_bits": "u32 (packed-bit out)"}
+            "threshold_u32": "u32 (int32 out)", "threshold_bits": "u32 (packed-bit out)",
+            "chain_bf16": "f32 (bf16 io)"}
 
 
 def run_ours(args):

@@ -69,6 +69,25 @@ def chain_f32(n: int = 1 << 26) -> dict:
     )
 
 
+def chain_bf16(n: int = 1 << 27) -> dict:
+    """The chain Command, out = (a*b) - (c + a)*s with s = 0.75, on bf16
+    tensors (computed in fp32, rounded once on the store), a, b, c uniform
+    [-4, 4] truncated to bf16, seed 9: the contiguous path's 2-byte loads."""
+    st, al = _dense((n,))
+    return dict(
+        name="chain_bf16", seed=9, sizes=(n,),
+        ops=[("load", "a", "bf16"), ("load", "b", "bf16"), ("load", "c", "bf16"),
+             ("scalar", "s", "f32", 0.75),
+             ("exec", [("mul", "ab", "a", "b"),
+                       ("add", "ca", "c", "a"),
+                       ("mul", "cas", "ca", "s"),
+                       ("sub", "r", "ab", "cas")]),
+             ("store", "out", "r", "bf16")],
+        views={k: dict(strides=st, alloc=al) for k in ("a", "b", "c", "out")},
+        inputs={k: ("uniform_bf16_trunc", -4.0, 4.0) for k in ("a", "b", "c")},
+    )
+
+
 def wrap_i32(n: int = 1 << 28) -> dict:
     """out = x*y + z - w in int32 with two's-complement wraparound, seed 2."""
     st, al = _dense((n,))
@@ -224,6 +243,7 @@ FULL = {
     "div_clamp_i32": div_clamp_i32,
     "threshold_u32": threshold_u32,
     "threshold_bits": threshold_bits,
+    "chain_bf16": chain_bf16,
 }
 
 

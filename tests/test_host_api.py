@@ -105,6 +105,7 @@ def test_lowering_of_the_workloads():
         "div_clamp_i32": (5, 1, 1, 0, 0),
         "threshold_u32": (1, 1, 1, 0, 0),
         "threshold_bits": (1, 1, 1, 0, 0),
+        "chain_bf16": (4, 3, 3, 1, 0),
     }
     small = {"strided_bf16": (64, 64, 64), "batched_transpose": (2, 64, 64)}
     for name, f in W.FULL.items():
