@@ -1,12 +1,14 @@
 // exec_contig.cu - contiguous executor: every view is dense row-major and
-// 16-byte aligned, so each lane moves whole 16-byte (4-byte types) or 8-byte
-// (2-byte types) vectors, a warp's access is contiguous, and the grid strides
-// over warp-sized chunks of 32*V logical elements. It runs whole chunks only:
-// the host hands a ragged tail (fewer than 32*V elements) to the generic
-// executor, so the hot loop carries no bounds checks.
+// aligned for 4-element vectors, so each lane moves whole 16-byte (4-byte
+// types) or 8-byte (2-byte types) vectors, a warp's access is contiguous, and
+// the grid strides over warp-sized chunks of 32*V logical elements. It runs
+// whole chunks only: the host hands a ragged tail (fewer than 32*V elements),
+// and a head when every base is off the alignment by the same element count,
+// to the generic executor, so the hot loop carries no bounds checks.
 //
 // Compiled once per tier and op-set variant: CMDX_TIER and CMDX_EXT select
-// the kernel this object holds.
+// the kernel this object holds (and CMDX_OCC4 the four-CTA build of the
+// extended 2-slot kernel).
 #include "exec_common.cuh"
 
 #if !defined(CMDX_TIER) || !defined(CMDX_EXT)

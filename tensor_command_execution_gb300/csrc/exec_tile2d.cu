@@ -272,10 +272,10 @@ __device__ __forceinline__ void read_trans2(uint32_t (&x)[16], uint32_t stage, i
 
 // Transposed, split layout (batched launches of the 2-slot tier, 4-byte
 // loads): the host split the load's column dim into (column / 8, column % 8),
-// the group first, so logical (li, 8 cj + k) is box row cj + 8 k. Under the 128-byte swizzle (chunk ^= box row % 8 = cj) a tile
-// row's eight lanes read eight distinct chunks at every step, and step k of
-// a lane is register k: eight loads at fixed offsets from one address, with
-// no rotation afterwards.
+// the group first, so logical (li, 8 cj + k) is box row cj + 8 k. Under the
+// 128-byte swizzle (chunk ^= box row % 8 = cj) a tile row's eight lanes read
+// eight distinct chunks at every step, and step k of a lane is register k:
+// eight loads at fixed offsets from one address, with no permutation after.
 __device__ __forceinline__ uint32_t split_base(uint32_t stage, bool half, int li, int cj) {
   if (half) return stage + cj * 128 + ((((uint32_t)li >> 3) ^ (uint32_t)cj) << 4) + (li & 7) * 2;
   const uint32_t lr = li & 31;
