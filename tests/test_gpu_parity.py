@@ -310,13 +310,15 @@ def test_misaligned_bases_use_the_generic_path(off):
 
 @pytest.mark.parametrize("off", [1, 2, 3])
 @pytest.mark.parametrize("n", [2, 3, 517, 10000, 70001])
-def test_bases_off_by_one_count_peel_a_head(off, n):
+@pytest.mark.parametrize("wl", ["wide_dag", "chain_bf16"])
+def test_bases_off_by_one_count_peel_a_head(wl, off, n):
     """Every view off its vector alignment by the same number of elements
-    (f32 inputs and outputs and an f16 output, all sliced off elements into
-    their allocations): the first 4 - off elements run per element and the
-    rest on the contiguous executor, once there are more than 4 - off; every
-    element and the bytes around the views against the oracle."""
-    spec = W.wide_dag(n)
+    (f32 inputs and outputs with an f16 output, or bf16 throughout, all
+    sliced off elements into their allocations): the first 4 - off elements
+    run per element and the rest on the contiguous executor, once there are
+    more than 4 - off; every element and the bytes around the views against
+    the oracle."""
+    spec = W.FULL[wl](n)
     names = W.load_names(spec) + W.store_names(spec)
     plan = gpuutil.parity(spec, offsets={k: off for k in names})
     assert plan["path"] == ("contig" if n > 4 - off else "generic")
