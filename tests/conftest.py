@@ -18,7 +18,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     """GPU tests skip without a GPU unless CMD_REQUIRE_GPU=1, which turns the
-    skip into a failure (so a GPU machine with a broken driver cannot pass)."""
+    skip into a failure (so a machine whose GPU does not come up cannot pass)."""
     try:
         import torch
         have_gpu = torch.cuda.is_available()
