@@ -294,26 +294,31 @@ cmd_status cmd_lower(cmd_command_t cmd, cmd_program_info* info, uint32_t* words,
 
 /* Lower cmd and place the program in constant memory of the current CUDA
  * device. Synchronises that device (it may reuse the constant slot of a
- * destroyed kernel), so do not call it during stream capture. The Command may
- * be destroyed afterwards. All tensors of the Command must share one rank. */
+ * destroyed kernel), so do not call it during stream capture. Allocates the
+ * kernel's 256-byte device error word (cudaMalloc) and waits until it is
+ * cleared. The Command may be destroyed afterwards. All tensors of the
+ * Command must share one rank. */
 cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out);
 
 /* Like cmd_compile, but allocates no device memory. For callers that cannot
- * call cudaMalloc: code running while a CUDA graph is captured in global
- * capture mode, where the runtime refuses allocations, and programs whose
- * device memory belongs wholly to their own pool. The only device memory a
+ * call cudaMalloc: programs whose device memory belongs wholly to their own
+ * pool or to a framework's allocator (a fixed arena sized at start-up, a
+ * budget that the CUDA allocator must not grow), where an allocation outside
+ * the pool is refused or breaks the accounting. The only device memory a
  * kernel needs beyond its inputs and outputs is one 4-byte error word for the
  * tile executor's bounded waits; kernels from this call keep it in a static
  * 256-byte array of the library (one word per constant-memory program slot,
  * so at most CMD_MAX_KERNELS such words) that every GPU which loads the
- * library holds until the process exits. The first call on a device looks up
- * the array's device address on that device, so make it before any stream
- * capture; the call also synchronises the device when it reuses a program
- * slot, like cmd_compile. The word is cleared here; it then keeps whatever
- * the kernel's launches report until cmd_sync_status reads and clears it, and
+ * library holds until the process exits. Like cmd_compile, the call uploads
+ * the program with synchronous copies, clears the word and waits for the
+ * clear, and synchronises the device when it reuses a program slot: make it
+ * outside any stream capture. The first call on a device also looks up the
+ * array's device address on that device. The word then keeps whatever the
+ * kernel's launches report until cmd_sync_status reads and clears it, and
  * launches of the same kernel that overlap on the GPU share (race on) it.
- * Launch, inspect and destroy the kernel with the usual calls. The pages have
- * no counterpart of this entry point. */
+ * Launch, inspect and destroy the kernel with the usual calls; none of them
+ * allocates device memory for such a kernel. The pages have no counterpart
+ * of this entry point. */
 cmd_status cmd_compile_static_scratch(cmd_command_t cmd, cmd_kernel_t* out);
 
 /* Lower cmd into a kernel handle without touching any GPU. Such a kernel can
@@ -352,7 +357,9 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
  * CMD_ERR_DEVICE_TIMEOUT when a device-side wait of the tile executor (an
  * mbarrier wait on its shared-memory pipeline) ran past the time limit and
  * the kernel stopped instead of hanging. The kernel's device error word is
- * cleared when it is reported. */
+ * cleared when it is reported, on cuda_stream, and the call waits for the
+ * clear; a launch of k on another stream that runs meanwhile may have its
+ * report cleared with it. */
 cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream);
 
 /* Process-wide settings of the device-side waits: the time limit of every
@@ -361,6 +368,14 @@ cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream);
  * the timeout path runs (the launch then writes no output and
  * cmd_sync_status returns CMD_ERR_DEVICE_TIMEOUT). */
 cmd_status cmd_configure_waits(uint64_t timeout_ns, int32_t force_timeout);
+
+/* ---- diagnostics --------------------------------------------------------- */
+
+/* Device allocations (cudaMalloc calls that succeeded) this library has made
+ * in this process, on every device together: one per kernel from cmd_compile
+ * and none from any other call. For tests and for callers that account for
+ * device memory. */
+int64_t cmd_device_allocations(void);
 
 #ifdef __cplusplus
 }

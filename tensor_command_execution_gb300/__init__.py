@@ -114,6 +114,7 @@ SIGNATURES = {
     "cmd_launch": (_I, [_P, ctypes.POINTER(cmd_runtime_args), _P]),
     "cmd_sync_status": (_I, [_P, _P]),
     "cmd_configure_waits": (_I, [ctypes.c_uint64, ctypes.c_int32]),
+    "cmd_device_allocations": (ctypes.c_int64, []),
 }
 
 _lib = None
@@ -278,6 +279,10 @@ def cmd_sync_status(k: int, stream: int | None) -> None:
 
 def cmd_configure_waits(timeout_ns: int, force_timeout: bool = False) -> None:
     _check(lib().cmd_configure_waits(int(timeout_ns), 1 if force_timeout else 0), "cmd_configure_waits")
+
+
+def cmd_device_allocations() -> int:
+    return int(lib().cmd_device_allocations())
 
 
 # ---- argument marshalling ----------------------------------------------------

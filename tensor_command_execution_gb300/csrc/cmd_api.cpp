@@ -131,6 +131,18 @@ namespace {
 // ---- device-side wait limit and the test hook that forces a timeout ----------
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int32_t> g_force_timeout{0};
+// successful device allocations made by this library (cmd_device_allocations)
+std::atomic<int64_t> g_device_allocs{0};
+
+// Zero n bytes of device memory at p on the legacy default stream and wait
+// until that is done: a plain cudaMemset of device memory may return before
+// it completes, and a launch on a non-blocking stream made right after would
+// not be ordered after it (its report could then be erased).
+cudaError_t clear_device_now(void* p, size_t n) {
+  cudaError_t e = cudaMemsetAsync(p, 0, n, cudaStreamLegacy);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
+  return e;
+}
 
 // ---- constant-memory program slots, per device -----------------------------
 std::mutex g_slot_mu;
@@ -1017,7 +1029,7 @@ cmd_status compile_with_static_word(cmd_command_t cmd, cmd_kernel_t* out, uint32
   if (reused) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cmdx::upload_program(k->prog.tier, k->prog.extended, slot, k->prog.words.data(), (int)k->prog.words.size());
   // the word keeps whatever the previous kernel in this slot left: clear it
-  if (e == cudaSuccess) e = cudaMemset(words + slot, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = clear_device_now(words + slot, sizeof(uint32_t));
   if (e != cudaSuccess) {
     release_slot(dev, slot);
     delete k;
@@ -1234,8 +1246,11 @@ cmd_status cmd_compile(cmd_command_t cmd, cmd_kernel_t* out) {
     }
   }
   e = cmdx::upload_program(k->prog.tier, k->prog.extended, slot, k->prog.words.data(), (int)k->prog.words.size());
-  if (e == cudaSuccess) e = cudaMalloc(&k->err, 256);
-  if (e == cudaSuccess) e = cudaMemset(k->err, 0, 256);
+  if (e == cudaSuccess) {
+    e = cudaMalloc(&k->err, 256);
+    if (e == cudaSuccess) g_device_allocs.fetch_add(1);
+  }
+  if (e == cudaSuccess) e = clear_device_now(k->err, 256);
   if (e != cudaSuccess) {
     if (k->err) cudaFree(k->err);
     release_slot(dev, slot);
@@ -1566,7 +1581,12 @@ cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream) {
     e = cudaMemcpy(&word, k->err, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     if (word) {
-      cudaMemset(k->err, 0, sizeof word);
+      // cleared on the caller's stream, and waited for, so that a launch
+      // queued there next finds it clear
+      cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+      e = cudaMemsetAsync(k->err, 0, sizeof word, st);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+      if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
       std::string what;
       if (word & 1u) what += " consumer-wait";
       if (word & 2u) what += " producer-wait";
@@ -1582,6 +1602,8 @@ cmd_status cmd_sync_status(cmd_kernel_t k, void* cuda_stream) {
   }
   return CMD_OK;
 }
+
+int64_t cmd_device_allocations(void) { return g_device_allocs.load(); }
 
 cmd_status cmd_configure_waits(uint64_t timeout_ns, int32_t force_timeout) {
   if (timeout_ns == 0) return fail(CMD_ERR_ARG, "timeout_ns must be > 0");

@@ -14,6 +14,7 @@
 // a hand-written kernel instead of being assembled per Command.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -468,6 +469,20 @@ inline cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaSt
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, params);
 }
+
+// A value computed once per device by host code (a grid size, a flag that a
+// kernel attribute is set), read and written from any host thread: relaxed
+// atomics suffice, since every thread that computes it computes the same
+// value and a race only repeats the computation. Zero means "not yet"; a
+// device index outside the table is never cached.
+struct DeviceCache {
+  static constexpr int kDevices = 64;
+  std::atomic<int> v[kDevices];
+  int get(int dev) const { return dev >= 0 && dev < kDevices ? v[dev].load(std::memory_order_relaxed) : 0; }
+  void put(int dev, int x) {
+    if (dev >= 0 && dev < kDevices) v[dev].store(x, std::memory_order_relaxed);
+  }
+};
 
 // Grid size for a persistent grid-stride kernel: enough CTAs to fill the
 // device at the kernel's occupancy, and no more than the work needs.

@@ -121,14 +121,14 @@ template <int TIER, bool EXT>
 static cudaError_t launch_tier(const GenericParams& p, cudaStream_t stream) {
   constexpr int V = tier_vec_strided(TIER);
   constexpr int kBlock = 256;
-  static int grid_cache[64] = {0};
+  static DeviceCache grid_cache;  // (static storage: zero before first use)
   int dev = 0;
   cudaGetDevice(&dev);
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
-  int full_grid = (dev >= 0 && dev < 64) ? grid_cache[dev] : 0;
+  int full_grid = grid_cache.get(dev);
   if (full_grid == 0) {
     full_grid = persistent_grid(generic_kernel<TIER, EXT>, kBlock, 0, INT64_MAX);
-    if (dev >= 0 && dev < 64) grid_cache[dev] = full_grid;
+    grid_cache.put(dev, full_grid);
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
   return launch_pdl(generic_kernel<TIER, EXT>, grid, kBlock, 0, stream, p);

@@ -600,24 +600,22 @@ cudaError_t CMDX_TILE_NAME(tile2d_upload_t)(int slot, const uint32_t* words, int
 template <int TIER, bool ND, bool EXT>
 static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes;
-  static int grid_cache[64][kMaxStages + 1] = {};
-  static bool attr_set[64] = {};
+  static DeviceCache grid_cache[kMaxStages + 1];  // (static storage: zero before first use)
+  static DeviceCache attr_set;
   int dev = 0;
   cudaGetDevice(&dev);
-  const bool cacheable = dev >= 0 && dev < 64;
-  if (!cacheable || !attr_set[dev]) {
+  if (!attr_set.get(dev)) {
     cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBarrierBytes + 2 * kTileStageLimit + 4096);
     if (e != cudaSuccess) return e;
-    if (cacheable) attr_set[dev] = true;
+    attr_set.put(dev, 1);
   }
   // occupancy depends on the stage size; cached for the common size only
-  int full_grid = 0;
-  const bool cache_ok = cacheable && p.stage_bytes == 16384;
-  if (cache_ok) full_grid = grid_cache[dev][p.n_stages];
+  const bool cache_ok = p.stage_bytes == 16384 && p.n_stages <= (uint32_t)kMaxStages;
+  int full_grid = cache_ok ? grid_cache[p.n_stages].get(dev) : 0;
   if (full_grid == 0) {
     full_grid = persistent_grid(tile2d_kernel<TIER, ND, EXT>, kThreads, smem, INT64_MAX);
-    if (cache_ok) grid_cache[dev][p.n_stages] = full_grid;
+    if (cache_ok) grid_cache[p.n_stages].put(dev, full_grid);
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
   return launch_pdl(tile2d_kernel<TIER, ND, EXT>, grid, kThreads, smem, stream, p);

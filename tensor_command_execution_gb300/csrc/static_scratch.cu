@@ -1,14 +1,16 @@
 // static_scratch.cu - compiling a Command without any device allocation.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
-// being captured in global capture mode (where the runtime refuses
-// allocations), and programs whose device memory is owned entirely by their
-// own pool or a framework's allocator. cmd_compile allocates one small device
-// word per kernel (the tile executor reports a device-side wait that ran out
-// of time in it), so such callers use cmd_compile_static_scratch instead: the
-// kernels it returns keep that word in the file-scope array below, which
-// every GPU that loads this library holds until the process exits. Launching,
-// status reporting and destruction are the usual entry points.
+// Some callers cannot call cudaMalloc: programs whose device memory is owned
+// entirely by their own pool or a framework's allocator (an arena sized once
+// at start-up, a memory budget the CUDA allocator must not grow), where an
+// allocation outside the pool is refused or breaks the accounting. cmd_compile
+// allocates one small device word per kernel (the tile executor reports a
+// device-side wait that ran out of time in it), so such callers use
+// cmd_compile_static_scratch instead: the kernels it returns keep that word in
+// the file-scope array below, which every GPU that loads this library holds
+// until the process exits. Launching, status reporting and destruction are the
+// usual entry points. Like cmd_compile, the call makes synchronous copies and
+// may synchronise the device, so it is made outside any stream capture.
 #include <cstdint>
 #include <mutex>
 

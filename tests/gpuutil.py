@@ -2,6 +2,9 @@
 C ABI binding) and through the oracle on the same host bytes, and compare."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -82,6 +85,52 @@ def parity(spec: dict, bufs: dict | None = None, offsets=None):
     for name in W.store_names(spec):
         compare(got[name], ref[name], dts[name], f"{spec['name']}:{name}")
     return plan
+
+
+def host_cores() -> int:
+    """Cores this process may run on."""
+    if hasattr(os, "sched_getaffinity"):
+        return max(1, len(os.sched_getaffinity(0)))
+    return os.cpu_count() or 1
+
+
+def element_ranges(n: int, parts: int, align: int = 32) -> list:
+    """[0, n) cut into at most `parts` contiguous ranges whose inner
+    boundaries are multiples of `align` logical elements (so no two ranges
+    write the same 32-element packed-bit word)."""
+    step = -(-max(1, -(-n // max(1, parts))) // align) * align
+    return [(a, min(n, a + step)) for a in range(0, n, step)]
+
+
+def oracle_every_element(spec: dict, bufs: dict) -> dict:
+    """The oracle over every logical index of spec: fresh copies of the store
+    buffers (their sentinels kept outside the views) written by element
+    ranges split over the host cores. The C walk runs without the
+    interpreter lock, and each range is the plain per-element walk."""
+    ref = {n: bufs[n].copy() for n in W.store_names(spec)}
+    oc = oracle.OracleCommand(spec, {**bufs, **ref})
+    cores = host_cores()
+    ranges = element_ranges(W.numel(spec), 4 * cores)
+    with ThreadPoolExecutor(cores) as ex:
+        list(ex.map(lambda r: oc.eval_range(*r), ranges))
+    return ref
+
+
+def full_parity(spec: dict) -> tuple:
+    """Run spec on the GPU at its own size and compare every element of every
+    store buffer with the oracle (bit-exact; <= 1 ulp for 16-bit floats, and
+    they are in fact exact). Returns (plan, elements compared, max ulp)."""
+    bufs = specutil.host_buffers(spec)
+    got, plan = run_cuda(spec, bufs)
+    ref = oracle_every_element(spec, bufs)
+    dts = W.tensor_dtypes(spec)
+    checked, max_ulp = 0, 0
+    for name in W.store_names(spec):
+        checked += compare(got[name], ref[name], dts[name], f"{spec['name']}:{name} (every element)")
+        if dts[name] in ("f16", "bf16"):
+            max_ulp = max(max_ulp, int(ulp_distance_half(got[name], ref[name]).max(initial=0)))
+        del got[name], ref[name]
+    return plan, checked, max_ulp
 
 
 def sampled_parity(spec: dict, n_samples: int = 1 << 20, seed: int = 0):

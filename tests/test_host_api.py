@@ -325,6 +325,18 @@ def test_lowered_kernel_cannot_launch():
     assert e.value.name == "CMD_ERR_STATE"
 
 
+def test_host_only_calls_allocate_no_device_memory():
+    """Building, lowering, inspecting and planning never allocate device
+    memory (the library's own count stays put)."""
+    before = T.cmd_device_allocations()
+    c, tags = T.command_from_spec(W.strided_bf16(128, 72, 80))
+    k = c.lower_kernel()
+    k.info()
+    k.dump()
+    del k
+    assert T.cmd_device_allocations() == before
+
+
 def test_configure_waits_validates():
     with pytest.raises(T.CmdError) as e:
         T.cmd_configure_waits(0)
