@@ -1531,7 +1531,6 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     }
     for (size_t j = 0; j < pl.stores.size(); ++j) {
       L.out[j] = pl.stores[j].ptr;
-      L.out_dt[j] = (uint8_t)pl.stores[j].dtype;
       L.out_ld[j] = pl.ms[j][row];
       L.out_bst[j][0] = b0 >= 0 ? pl.ms[j][b0] : 0;
       L.out_bst[j][1] = b1 >= 0 ? pl.ms[j][b1] : 0;

@@ -168,7 +168,6 @@ struct Tile2dLaunch {
   uint8_t in_dt[kMaxLoads];
   uint8_t in_trans[kMaxLoads];
   void* out[kMaxStores];
-  uint8_t out_dt[kMaxStores];     // element type of each store (cmd_dtype numbering)
   int64_t out_ld[kMaxStores];     // row stride of each store
   int64_t out_bst[kMaxStores][2]; // batch strides of each store
   uint32_t scal[kMaxScalars];

@@ -43,13 +43,12 @@ constexpr TileLaunch kTileLaunch[2][2][3] = {
     {{tile2d_launch_t0n0e1, tile2d_launch_t1n0e1, tile2d_launch_t2n0e1},
      {tile2d_launch_t0n1e1, tile2d_launch_t1n1e1, tile2d_launch_t2n1e1}}};
 
-// the fragment-layout tile kernel, [op-set variant][tier 0..1]
-constexpr Upload kTileFragUpload[2][2] = {{tile2d_upload_t0n2e0, tile2d_upload_t1n2e0},
-                                          {tile2d_upload_t0n2e1, tile2d_upload_t1n2e1}};
-constexpr TileLaunch kTileFragLaunch[2][2] = {{tile2d_launch_t0n2e0, tile2d_launch_t1n2e0},
-                                              {tile2d_launch_t0n2e1, tile2d_launch_t1n2e1}};
-
 bool tier_ok(int tier) { return tier >= kTier2 && tier <= kTier32; }
+
+// Tile rows the producer of a plain 2-D launch walks together (measured on
+// GB300, strided_bf16 A/B on one box: 1 -> 5982 GB/s, 8 -> 6076; 4 and 16
+// less than 8, 32 below 1).
+constexpr uint32_t kTileGroupRows = 8;
 
 }  // namespace
 
@@ -59,7 +58,6 @@ cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, 
   if (e == cudaSuccess && ext && tier == kTier2) e = contig_upload_t0e1o4(slot, words, n);
   if (e == cudaSuccess) e = kGenericUpload[ext][tier](slot, words, n);
   for (int nd = 0; nd < 2 && e == cudaSuccess && tier != kTier32; ++nd) e = kTileUpload[ext][nd][tier](slot, words, n);
-  if (e == cudaSuccess && tier <= kTier4) e = kTileFragUpload[ext][tier](slot, words, n);
   return e;
 }
 
@@ -162,33 +160,11 @@ cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_
   if (off == 0 || off > (uint32_t)kTileStageLimit) return cudaErrorInvalidValue;
   p.stage_bytes = off;
   p.tx_bytes = tx;
-  bool nd = L.nb[0] > 1 || L.nb[1] > 1;
-  for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
-  // Plain 2-D launches whose loads are all 2-byte run the fragment-layout
-  // kernel in the 2- and 4-slot tiers: ldmatrix reads of the staged boxes,
-  // 2-byte stores through shared memory and one TMA store per warp and tile
-  // (its descriptors: a 64 x 8 box of each such store, 128-byte swizzle).
-  bool frag = !nd && tier <= kTier4;
-  for (uint32_t j = 0; j < L.n_loads && frag; ++j) frag = L.in_dt[j] == 1 || L.in_dt[j] == 2;
-  for (int j = 0; j < kMaxStores && frag; ++j) {
-    if (!L.out[j] || !(L.out_dt[j] == 1 || L.out_dt[j] == 2)) continue;
-    cuuint64_t dims[2] = {(cuuint64_t)L.cols, (cuuint64_t)L.rows};
-    cuuint64_t strides[1] = {(cuuint64_t)L.out_ld[j] * 2};
-    cuuint32_t box[2] = {64, 8};
-    cuuint32_t estr[2] = {1, 1};
-    frag = encode(&p.out_maps[j], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, L.out[j], dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-  }
   // stages within 48 KB for the 2-slot tier (its kernel is built for four
   // CTAs per SM: 3 stages of two 2-byte loads; measured against 4 stages at
   // three CTAs, strided_bf16 +4%, and two 4-byte loads 2 stages at three
   // CTAs against 3 at two, batched_transpose +8%), 96 KB for the others
-  // (the fragment-layout kernel is built for three CTAs per SM in the 2-slot
-  // tier and two in the 4-slot one, each with 16 KB of staging boxes: about
-  // 72 KB and 110 KB of shared memory per CTA)
-  const uint32_t stages_fit = frag ? (uint32_t)(((tier == kTier2 ? 72 : 110) * 1024 - kBarrierBytes - kFragStagingBytes) / off)
-                                   : (uint32_t)((tier == kTier2 ? 1 : 2) * kTileStageLimit / off);
+  const uint32_t stages_fit = (uint32_t)((tier == kTier2 ? 1 : 2) * kTileStageLimit / off);
   p.n_stages = stages_fit < 2 ? 2 : stages_fit > kMaxStages ? kMaxStages : stages_fit;
   for (int j = 0; j < kMaxStores; ++j) {
     p.out[j] = L.out[j];
@@ -204,12 +180,14 @@ cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_
   p.tiles_r = (uint32_t)((L.rows + kTileRows - 1) / kTileRows);
   p.nb1 = (uint32_t)L.nb[1];
   p.n_tiles = (uint32_t)((int64_t)p.tiles_c * p.tiles_r * L.nb[0] * L.nb[1]);
+  p.group_rows = kTileGroupRows < p.tiles_r ? kTileGroupRows : (p.tiles_r > 0 ? p.tiles_r : 1);
   p.timeout_ns = L.timeout_ns;
   p.prog = L.prog;
   p.n_loads = L.n_loads;
   p.debug = L.debug;
+  bool nd = L.nb[0] > 1 || L.nb[1] > 1;
+  for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
   if (tier < kTier2 || tier > kTier8) return cudaErrorInvalidValue;  // no 32-slot tile kernel
-  if (frag) return kTileFragLaunch[ext][tier](p, stream);
   return kTileLaunch[ext][nd][tier](p, stream);
 }
 

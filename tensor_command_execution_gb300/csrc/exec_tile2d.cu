@@ -26,19 +26,14 @@
 // through LDS on AMD hardware).
 //
 // Compiled once per tier (CMDX_TIER 0..2), view variant (CMDX_ND 0: plain
-// 2-D views; 1: batch dims, broadcast loads or descriptors of another rank;
-// 2: the fragment-layout kernel for plain 2-D views whose loads are all
-// 2-byte, tiers 0 and 1 only) and op-set variant (CMDX_EXT): each object
-// holds one kernel. The TMA descriptors are encoded on the host
-// (exec_host.cpp).
+// 2-D views; 1: batch dims, broadcast loads or descriptors of another rank)
+// and op-set variant (CMDX_EXT): each object holds one kernel. The TMA
+// descriptors are encoded on the host (exec_host.cpp).
 #include "exec_common.cuh"
 #include "exec_tile2d.h"
 
 #if !defined(CMDX_TIER) || !defined(CMDX_ND) || !defined(CMDX_EXT)
-#error "exec_tile2d.cu is compiled per variant, with -DCMDX_TIER=<0..2> -DCMDX_ND=<0|1|2> -DCMDX_EXT=<0|1>"
-#endif
-#if CMDX_ND == 2 && CMDX_TIER > 1
-#error "the fragment-layout kernel (CMDX_ND=2) is built for the 2- and 4-slot tiers only"
+#error "exec_tile2d.cu is compiled per variant, with -DCMDX_TIER=<0..2> -DCMDX_ND=<0|1> -DCMDX_EXT=<0|1>"
 #endif
 // tile2d_<f>_t<tier>n<nd>e<ext>: this object's entry points
 #define CMDX_TILE_NAME(f) \
@@ -394,10 +389,12 @@ struct TileStore {
   }
 };
 
-// Two rows per thread: x[0..7] to row i, x[8..15] to row i + 1 (if it exists).
+// Two rows per thread: x[0..7] to row i, x[8..15] to row i + 1 (if it
+// exists); the second row's state is derived from the first when it is
+// stored (the consumers are short of registers).
 template <bool ND>
 struct TileStore2 {
-  TileStore<ND> lo, hi;
+  TileStore<ND> lo;
   bool second;
 
   template <int T>
@@ -409,7 +406,23 @@ struct TileStore2 {
       b[m] = x[8 + m];
     }
     lo.template store<T>(a, o);
-    if (second) hi.template store<T>(b, o);
+    if (second) {
+      TileStore<ND> hi = lo;
+      hi.i += 1;
+      hi.template store<T>(b, o);
+    }
+  }
+};
+
+// Stage index and phase parity of a pipeline ring of ns stages, stepped once
+// per tile (no division per tile).
+struct StageRing {
+  uint32_t s = 0, ph = 0;
+  __device__ __forceinline__ void next(uint32_t ns) {
+    if (++s == ns) {
+      s = 0;
+      ph ^= 1u;
+    }
   }
 };
 
@@ -425,8 +438,9 @@ __device__ __forceinline__ void tile_produce(const Tile2dParams& p, uint32_t ful
   bool ok = true;
   TileWalk tw;  // (batched launches: it replaces three divisions a tile)
   if (ND) tw.init(p, true, blockIdx.x, gridDim.x);
-  for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
-    const uint32_t s = n % ns, ph = (n / ns) & 1;
+  StageRing ring;
+  for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n, ring.next(ns)) {
+    const uint32_t s = ring.s, ph = ring.ph;
     if (!mbar_wait(empty_bar + 8 * s, ph ^ 1, p.timeout_ns)) {
       atomicOr(p.err, kErrProducerWait);
       ok = false;
@@ -434,22 +448,30 @@ __device__ __forceinline__ void tile_produce(const Tile2dParams& p, uint32_t ful
     }
     // t = ((b0 * nb1 + b1) * tiles_r + tile row) * tiles_c + tile column
     uint32_t tc, tr;
-    int32_t bc[3] = {0, 0, 0};
+    int32_t bc1 = 0, bc2 = 0;  // batch coordinates b0, b1
     if (ND) {
       tc = tw.tc;
       tr = tw.tr;
-      bc[1] = (int32_t)tw.b0;
-      bc[2] = (int32_t)tw.b1;
+      bc1 = (int32_t)tw.b0;
+      bc2 = (int32_t)tw.b1;
       tw.next(p, true);
     } else {
-      tc = t % p.tiles_c;
-      tr = t / p.tiles_c;
+      // tiles in groups of group_rows tile rows, column by column within a
+      // group: the tiles in flight at once then cover a block of tile rows
+      // and columns, so a transposed operand is read in runs of
+      // 128 B x group_rows from each of its rows, not 128 B
+      const uint32_t per_group = p.group_rows * p.tiles_c;
+      const uint32_t g = t / per_group, rem = t - g * per_group;
+      const uint32_t g0 = g * p.group_rows;
+      const uint32_t h = p.tiles_r - g0 < p.group_rows ? p.tiles_r - g0 : p.group_rows;
+      tc = rem / h;
+      tr = g0 + (rem - tc * h);
     }
     const int32_t i0 = (int32_t)(tr * kTileRows), j0 = (int32_t)(tc * kTileCols);
     const uint32_t fb = full_bar + 8 * s;
     // the tile's coordinates for the consumers (published by the arrive
     // below, whose release orders this store before the phase completes)
-    sts128(coords + 16 * s, make_uint4(tr, tc, (uint32_t)bc[1], (uint32_t)bc[2]));
+    sts128(coords + 16 * s, make_uint4(tr, tc, (uint32_t)bc1, (uint32_t)bc2));
     mbar_arrive_expect_tx(fb, p.tx_bytes);
     const uint32_t st = stages + s * p.stage_bytes;
     for (uint32_t j = 0; j < p.n_loads; ++j) {
@@ -466,7 +488,7 @@ __device__ __forceinline__ void tile_produce(const Tile2dParams& p, uint32_t ful
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t src = p.in_src[j][k];
-          c[k + 1] = src == 0 ? outer : src == 3 ? outer / 8 : src == 4 ? 0 : bc[src];
+          c[k + 1] = src == 0 ? outer : src == 1 ? bc1 : src == 2 ? bc2 : src == 3 ? outer / 8 : 0;
         }
       }
       const int rank = ND ? p.in_rank[j] : 2;
@@ -539,9 +561,9 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
     if (!mbar_wait(debug_bar, 0, p.timeout_ns) && lane == 0) atomicOr(p.err, kErrDebugWait);
     return;
   }
-  uint32_t n = 0;
-  for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
-    const uint32_t s = n % ns, ph = (n / ns) & 1;
+  StageRing ring;
+  for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ring.next(ns)) {
+    const uint32_t s = ring.s, ph = ring.ph;
     if (!mbar_wait(full_bar + 8 * s, ph, p.timeout_ns)) {
       if (lane == 0) atomicOr(p.err, kErrConsumerWait);
       return;
@@ -594,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
           }
         }
         if constexpr (RPT == 2) {
-          TileStore2<ND> sto{{p, i, jc, fullc, nleft, b0, b1}, {p, i + 1, jc, fullc, nleft, b0, b1}, i + 1 < p.rows};
+          TileStore2<ND> sto{{p, i, jc, fullc, nleft, b0, b1}, i + 1 < p.rows};
           run_program<TIER, V, EXT>(r, prog, p.scal, sto);
         } else {
           TileStore<ND> sto{p, i, jc, fullc, nleft, b0, b1};
@@ -607,252 +629,22 @@ __global__ void __launch_bounds__(kThreads, tile_min_blocks(TIER)) tile2d_kernel
   }
 }
 
-// ---- fragment-layout kernel: every load 2-byte, plain 2-D views ----------------
-// Consumer warp w owns rows 8w .. 8w + 7 of the tile, all 64 columns. Lane t
-// holds, per slot, row 8w + t/4 at columns 8g + 2(t%4) and 8g + 2(t%4) + 1
-// (elements 2g and 2g + 1 of the slot, g = 0..7): the layout in which
-// ldmatrix hands out an 8 x 8 matrix of 16-bit elements. A row-direct box
-// (box row = tile row) is read with ldmatrix, four column groups per
-// instruction; a transposed box (box row = tile column) with ldmatrix.trans,
-// which transposes each 8 x 8 block on the way: one instruction gives the
-// lane 8 elements of either kind, where the row-at-a-time readers above take
-// one shared load per column and register permutes. Under the 128-byte
-// swizzle the 8 row addresses of each matrix fall in 8 distinct 16-byte bank
-// groups, so no access conflicts. Stores of 2-byte types go back through
-// shared memory the same way (stmatrix into a swizzled 8 x 64 staging box of
-// the warp) and out with one TMA store per warp and tile; 4-byte stores are
-// 8-byte vectors from the registers. The stage is released to the producer
-// as soon as its boxes are in registers, before the program runs.
-__device__ __forceinline__ void ldsm4(uint32_t (&d)[4], uint32_t a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-               : "r"(a)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm4t(uint32_t (&d)[4], uint32_t a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-               : "r"(a)
-               : "memory");
-}
-__device__ __forceinline__ void stsm4(uint32_t a, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v0), "r"(v1),
-               "r"(v2), "r"(v3)
-               : "memory");
-}
-// One 2-D box from shared memory to global memory (this CTA's bulk group).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// all but the newest bulk group of this thread have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read_all_but_one() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-// every bulk group of this thread has completed (its writes are done)
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// order this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) reads of them
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Stores of the fragment-layout kernel for one warp and tile.
-struct FragStore {
-  const Tile2dParams& p;
-  uint32_t stg;        // the warp's two 1 KB staging boxes (1024-byte aligned)
-  uint32_t soff0, soff1;  // this lane's stmatrix row addresses in a box: column groups 0-3, 4-7
-  int32_t i0w, j0;     // the warp's first row and the tile's first column
-  uint32_t& nbuf;      // staging box to use next (alternates)
-  bool full;           // the warp's 8 x 64 band lies inside the view
-
-  template <int T>
-  __device__ __forceinline__ void store(const uint32_t (&x)[16], uint32_t o) const {
-    // packed-bit stores never come here: the host plans programs that have
-    // them onto the contiguous or generic executor
-    if constexpr (T == kStB1) {
-      return;
-    } else if constexpr (T == kStF16 || T == kStBF16) {
-      uint32_t h[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        h[g] = T == kStF16 ? narrow_f16x2(x[2 * g], x[2 * g + 1]) : narrow_bf16x2(x[2 * g], x[2 * g + 1]);
-      const int lane = threadIdx.x & 31;
-      const uint32_t box = stg + (nbuf & 1u) * 1024u;
-      nbuf ^= 1u;
-      // the store issued from this box two stores ago has read it
-      if (lane == 0) bulk_wait_read_all_but_one();
-      __syncwarp();
-      stsm4(box + soff0, h[0], h[1], h[2], h[3]);
-      stsm4(box + soff1, h[4], h[5], h[6], h[7]);
-      fence_async_smem();
-      __syncwarp();
-      // rows and columns past the view are clipped by the TMA unit
-      if (lane == 0) {
-        tma_store_2d(&p.out_maps[o], j0, i0w, box);
-        bulk_commit();
-      }
-    } else {
-      const int lane = threadIdx.x & 31;
-      const int64_t i = (int64_t)i0w + (lane >> 2);
-      const int64_t j = (int64_t)j0 + 2 * (lane & 3);
-      uint32_t* base = static_cast<uint32_t*>(p.out[o]) + i * p.out_ld[o] + j;
-      if (full) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) st_stream(reinterpret_cast<uint2*>(base + 8 * g), make_uint2(x[2 * g], x[2 * g + 1]));
-      } else if (i < p.rows) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (j + 8 * g + e < p.cols) st_elem<T>(base, 8 * g + e, x[2 * g + e]);
-      }
-    }
-  }
-};
-
-// Resident CTAs per SM the fragment-layout kernel's registers are sized for.
-CMDX_HD constexpr int tile_frag_min_blocks(int tier) { return tier == kTier2 ? 3 : 2; }
-
-template <int TIER, bool EXT>
-__global__ void __launch_bounds__(kThreads, tile_frag_min_blocks(TIER))
-    tile2d_frag_kernel(const __grid_constant__ Tile2dParams p) {
-  extern __shared__ __align__(1024) unsigned char smem[];
-  constexpr int S = tier_slots(TIER);
-  constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
-  static_assert(S == 2 || S == 4, "the fragment-layout kernel serves the 2- and 4-slot tiers");
-  const uint32_t base = smem_u32(smem);
-  const uint32_t full_bar = base;
-  const uint32_t empty_bar = base + 8 * kMaxStages;
-  const uint32_t debug_bar = base + 16 * kMaxStages;
-  const uint32_t coords = base + 32 * kMaxStages;
-  const uint32_t stages = base + kBarrierBytes;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ns = p.n_stages;
-
-  if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < ns; ++s) {
-      mbar_init(full_bar + 8 * s, 1);
-      mbar_init(empty_bar + 8 * s, kConsumerWarps);
-    }
-    mbar_init(debug_bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-
-  if (warp == kConsumerWarps) {
-    if (lane != 0 || p.debug) return;
-    tile_produce<false>(p, full_bar, empty_bar, coords, stages, ns);
-    return;
-  }
-
-  if (p.debug) {
-    // test hook: a wait that nothing satisfies must give up and report
-    if (!mbar_wait(debug_bar, 0, p.timeout_ns) && lane == 0) atomicOr(p.err, kErrDebugWait);
-    return;
-  }
-  const uint32_t* prog = c_prog[p.prog];
-  // this lane's row addresses for ldmatrix / stmatrix: matrix m = lane / 8,
-  // row r = lane % 8 of it; column groups 4h + m (h = 0, 1)
-  const uint32_t m8 = (uint32_t)lane >> 3, r8 = (uint32_t)lane & 7u;
-  const uint32_t soff0 = r8 * 128u + ((m8 ^ r8) << 4), soff1 = r8 * 128u + (((4u + m8) ^ r8) << 4);
-  // row-direct box: rows 8w + r, chunk (4h + m) ^ r
-  const uint32_t roff0 = (uint32_t)warp * 1024u + soff0, roff1 = (uint32_t)warp * 1024u + soff1;
-  // transposed box: box rows 8(4h + m) + r (tile columns), chunk w ^ r (tile rows 8w ..)
-  const uint32_t toff0 = (8u * m8 + r8) * 128u + (((uint32_t)warp ^ r8) << 4), toff1 = toff0 + 32u * 128u;
-  const uint32_t stg = stages + ns * p.stage_bytes + (uint32_t)warp * 2048u;
-  uint32_t nbuf = 0;
-  uint32_t n = 0;
-  for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++n) {
-    const uint32_t s = n % ns, ph = (n / ns) & 1;
-    if (!mbar_wait(full_bar + 8 * s, ph, p.timeout_ns)) {
-      if (lane == 0) atomicOr(p.err, kErrConsumerWait);
-      break;
-    }
-    const uint4 tcrd = lds128(coords + 16 * s);  // written by the producer with this stage
-    const int32_t i0w = (int32_t)(tcrd.x * kTileRows) + 8 * warp, j0 = (int32_t)(tcrd.y * kTileCols);
-    const uint32_t st = stages + s * p.stage_bytes;
-    uint32_t r[S][16];
-#pragma unroll
-    for (int j = 0; j < NL; ++j) {
-      if (j < (int)p.n_loads) {
-        const uint32_t at = st + p.load_off[j];
-        uint32_t a[4], b[4];
-        if (p.in_trans[j]) {
-          ldsm4t(a, at + toff0);
-          ldsm4t(b, at + toff1);
-        } else {
-          ldsm4(a, at + roff0);
-          ldsm4(b, at + roff1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          r[j][q] = a[q];
-          r[j][4 + q] = b[q];
-        }
-      }
-    }
-    // every box of the stage is in registers: hand the stage back
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar + 8 * s);
-    if (i0w >= p.rows) continue;  // (a ragged last tile row: this warp's band is empty)
-#pragma unroll
-    for (int j = 0; j < NL; ++j) {
-      if (j < (int)p.n_loads) {
-        // pair g (two 16-bit elements) becomes elements 2g, 2g + 1, from the
-        // last pair down so that no pair is overwritten before it is read
-        if (p.in_dt[j] == 1) {
-#pragma unroll
-          for (int g = 7; g >= 0; --g) {
-            const uint32_t w2 = r[j][g];
-            widen_f16x2(w2, r[j][2 * g], r[j][2 * g + 1]);
-          }
-        } else {
-#pragma unroll
-          for (int g = 7; g >= 0; --g) {
-            const uint32_t w2 = r[j][g];
-            widen_bf16x2(w2, r[j][2 * g], r[j][2 * g + 1]);
-          }
-        }
-      }
-    }
-    const bool full = i0w + 8 <= p.rows && (int64_t)j0 + kTileCols <= p.cols;
-    FragStore sto{p, stg, soff0, soff1, i0w, j0, nbuf, full};
-    run_program<TIER, 16, EXT>(r, prog, p.scal, sto);
-  }
-  // the TMA stores read their staging boxes and write global memory
-  // asynchronously: let them finish before the CTA's shared memory goes
-  if (lane == 0) bulk_wait_all();
-}
-
 cudaError_t CMDX_TILE_NAME(tile2d_upload_t)(int slot, const uint32_t* words, int n) {
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
 // ---- host side ----------------------------------------------------------------
 
-// CMDX_ND 2 objects hold the fragment-layout kernel; 0 and 1 the row-pair
-// kernel without and with the batch / broadcast bookkeeping.
-template <int TIER, int NDV, bool EXT>
-static auto tile_kernel_of() {
-  if constexpr (NDV == 2) return tile2d_frag_kernel<TIER, EXT>;
-  else return tile2d_kernel<TIER, NDV == 1, EXT>;
-}
-
-template <int TIER, int NDV, bool EXT>
+template <int TIER, bool ND, bool EXT>
 static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
-  const auto kernel = tile_kernel_of<TIER, NDV, EXT>();
-  const size_t extra = NDV == 2 ? (size_t)kFragStagingBytes : 0;
-  const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes + extra;
+  const size_t smem = (size_t)kBarrierBytes + (size_t)p.n_stages * p.stage_bytes;
   static DeviceCache grid_cache[kMaxStages + 1];  // (static storage: zero before first use)
   static DeviceCache attr_set;
   int dev = 0;
   cudaGetDevice(&dev);
   if (!attr_set.get(dev)) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kBarrierBytes + 2 * kTileStageLimit + 4096 + extra));
+    cudaError_t e = cudaFuncSetAttribute(tile2d_kernel<TIER, ND, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kBarrierBytes + 2 * kTileStageLimit + 4096);
     if (e != cudaSuccess) return e;
     attr_set.put(dev, 1);
   }
@@ -860,15 +652,15 @@ static cudaError_t launch_tier(const Tile2dParams& p, cudaStream_t stream) {
   const bool cache_ok = p.stage_bytes == 16384 && p.n_stages <= (uint32_t)kMaxStages;
   int full_grid = cache_ok ? grid_cache[p.n_stages].get(dev) : 0;
   if (full_grid == 0) {
-    full_grid = persistent_grid(kernel, kThreads, smem, INT64_MAX);
+    full_grid = persistent_grid(tile2d_kernel<TIER, ND, EXT>, kThreads, smem, INT64_MAX);
     if (cache_ok) grid_cache[p.n_stages].put(dev, full_grid);
   }
   const int grid = (int)(p.n_tiles < full_grid ? p.n_tiles : full_grid);
-  return launch_pdl(kernel, grid, kThreads, smem, stream, p);
+  return launch_pdl(tile2d_kernel<TIER, ND, EXT>, grid, kThreads, smem, stream, p);
 }
 
 cudaError_t CMDX_TILE_NAME(tile2d_launch_t)(const Tile2dParams& p, cudaStream_t stream) {
-  return launch_tier<CMDX_TIER, CMDX_ND, CMDX_EXT != 0>(p, stream);
+  return launch_tier<CMDX_TIER, CMDX_ND != 0, CMDX_EXT != 0>(p, stream);
 }
 
 }  // namespace cmdx

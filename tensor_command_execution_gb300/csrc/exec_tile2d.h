@@ -14,9 +14,6 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 4;
 constexpr int kBarrierBytes = 1024;   // barriers; stages start 1024-byte aligned
 constexpr int kBoxBytes = 8192;       // one 64-row box of 128-byte rows
-// the fragment-layout kernel's staging boxes for 2-byte stores: two 8 x 64
-// boxes (1 KB each) per consumer warp, after the stages
-constexpr int kFragStagingBytes = kConsumerWarps * 2 * 1024;
 
 // error codes (bits of the error word)
 constexpr uint32_t kErrConsumerWait = 1u << 0;
@@ -26,8 +23,6 @@ constexpr uint32_t kErrDebugWait = 1u << 3;
 
 struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap maps[kMaxLoads];
-  // the fragment-layout kernel's 2-byte stores: 64-column x 8-row boxes, 128-byte swizzle
-  CUtensorMap out_maps[kMaxStores];
   void* out[kMaxStores];
   int64_t out_ld[kMaxStores];
   int64_t out_bst[kMaxStores][2];
@@ -36,6 +31,7 @@ struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
   int64_t rows, cols;
   uint64_t timeout_ns;
   uint32_t tiles_r, tiles_c, nb1, n_tiles;
+  uint32_t group_rows;  // plain 2-D launches: tile rows walked together (>= 1)
   uint32_t prog, n_loads, n_stages, stage_bytes, tx_bytes, debug;
   uint32_t load_off[kMaxLoads];  // byte offset of load j in a stage
   uint8_t in_dt[kMaxLoads];
@@ -50,9 +46,7 @@ struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
 
 // Entry points of the objects built from exec_tile2d.cu, one per tier t
 // (0..2), view variant x (0 for plain 2-D views, 1 for batch dims, broadcast
-// loads or descriptors of rank other than 2, 2 for the fragment-layout
-// kernel of plain 2-D views with 2-byte loads, tiers 0 and 1) and op-set
-// variant v.
+// loads or descriptors of rank other than 2) and division variant v.
 #define CMDX_DECL_TILE(t, x, v)                                                         \
   cudaError_t tile2d_upload_t##t##n##x##e##v(int slot, const uint32_t* words, int n_words); \
   cudaError_t tile2d_launch_t##t##n##x##e##v(const Tile2dParams& p, cudaStream_t stream);
@@ -60,7 +54,6 @@ CMDX_DECL_TILE(0, 0, 0) CMDX_DECL_TILE(0, 1, 0) CMDX_DECL_TILE(1, 0, 0)
 CMDX_DECL_TILE(1, 1, 0) CMDX_DECL_TILE(2, 0, 0) CMDX_DECL_TILE(2, 1, 0)
 CMDX_DECL_TILE(0, 0, 1) CMDX_DECL_TILE(0, 1, 1) CMDX_DECL_TILE(1, 0, 1)
 CMDX_DECL_TILE(1, 1, 1) CMDX_DECL_TILE(2, 0, 1) CMDX_DECL_TILE(2, 1, 1)
-CMDX_DECL_TILE(0, 2, 0) CMDX_DECL_TILE(1, 2, 0) CMDX_DECL_TILE(0, 2, 1) CMDX_DECL_TILE(1, 2, 1)
 #undef CMDX_DECL_TILE
 
 }  // namespace cmdx
