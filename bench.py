@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=list(W.FULL))
+    ap.add_argument("--workload", default=HEADLINE, choices=list(W.FULL) + list(W.PROFILE))
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -63,11 +63,13 @@ def parse():
 
 
 def make_spec(name, size):
-    f = W.FULL[name]
+    f = W.FULL.get(name) or W.PROFILE[name]
     if not size:
         return f()
     if name == "strided_bf16":
         return f(size, size, size + 128)
+    if name == "tile4_f32":
+        return f(size, size)
     if name == "batched_transpose":
         return f(max(1, size // (1 << 20)))
     return f(size)
@@ -421,6 +423,7 @@ def whole_job_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
 
 
 DTYPE_OF = {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_bf16": "f32 (bf16 io)",
+            "tile4_f32": "f32", "wide32_f32": "f32",
             "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32", "div_clamp_i32": "f32 (int32 out)",
             "threshold_u32": "u32 (int32 out)", "threshold_bits": "u32 (packed-bit out)",
             "chain_bf16": "f32 (bf16 io)"}
@@ -643,7 +646,7 @@ def run_reference(args):
         return
     import inputgen
     import oracle
-    spec = W.FULL[args.workload]()
+    spec = make_spec(args.workload, 0)
     dts = W.tensor_dtypes(spec)
     bufs = {}
     for k, name in enumerate(W.load_names(spec)):

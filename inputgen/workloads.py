@@ -232,6 +232,45 @@ def threshold_bits(n: int = 1 << 28) -> dict:
     )
 
 
+def tile4_f32(m: int = 4096, n: int = 4096) -> dict:
+    """out = A*B^T + C^T*s - A, fp32, with A row-direct (leading dimension
+    n + 32) and B, C read through their transposes: three staged loads and
+    a value kept live beside them put the program in the 4-slot tier of the
+    tile executor, normal(0,1), seed 10 (a profiling case, not a headline)."""
+    ld = n + 32
+    return dict(
+        name="tile4_f32", seed=10, sizes=(m, n),
+        ops=[("load", "A", "f32"), ("load", "B", "f32"), ("load", "C", "f32"),
+             ("scalar", "s", "f32", 0.5),
+             ("exec", [("mul", "AB", "A", "B"), ("mul", "Cs", "C", "s"), ("add", "t", "AB", "Cs"),
+                       ("sub", "r", "t", "A")]),
+             ("store", "out", "r", "f32")],
+        views={"A": dict(strides=(ld, 1), alloc=(m - 1) * ld + n),
+               "B": dict(strides=(1, m), alloc=n * m),
+               "C": dict(strides=(1, m), alloc=n * m),
+               "out": dict(strides=(n, 1), alloc=m * n)},
+        inputs={k: ("normal_f32", 0.0, 0.0) for k in ("A", "B", "C")},
+    )
+
+
+def wide32_f32(n: int = 1 << 24) -> dict:
+    """A sum of products over nine fp32 inputs, x0*x1 + x2*x3 + ... + x8:
+    nine loads live at once put the program past eight slots, in the 32-slot
+    tier of the contiguous executor, normal(0,1), seed 11 (a profiling case,
+    not a headline)."""
+    st, al = _dense((n,))
+    names = tuple(f"x{k}" for k in range(9))
+    body = [("mul", "p0", "x0", "x1"), ("mul", "p1", "x2", "x3"), ("mul", "p2", "x4", "x5"),
+            ("mul", "p3", "x6", "x7"), ("add", "q0", "p0", "p1"), ("add", "q1", "p2", "p3"),
+            ("add", "q2", "q0", "q1"), ("add", "r", "q2", "x8")]
+    return dict(
+        name="wide32_f32", seed=11, sizes=(n,),
+        ops=[("load", k, "f32") for k in names] + [("exec", body), ("store", "out", "r", "f32")],
+        views={k: dict(strides=st, alloc=al) for k in names + ("out",)},
+        inputs={k: ("normal_f32", 0.0, 0.0) for k in names},
+    )
+
+
 # Full-size workloads, in the order they are listed for this path.
 FULL = {
     "add_f32": add_f32,
@@ -244,6 +283,14 @@ FULL = {
     "threshold_u32": threshold_u32,
     "threshold_bits": threshold_bits,
     "chain_bf16": chain_bf16,
+}
+
+# Cases that run the executor objects the workloads above do not reach (the
+# 4-slot tile tier, the 32-slot tier), for profiling; bench.py accepts them
+# by name but they are not part of its per-workload table.
+PROFILE = {
+    "tile4_f32": tile4_f32,
+    "wide32_f32": wide32_f32,
 }
 
 

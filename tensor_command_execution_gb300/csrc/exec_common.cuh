@@ -264,21 +264,18 @@ __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* _
   case s_: {                 \
     CMDX_UNROLL for (int v = 0; v < V; ++v) r[s_][v] = y[v]; \
   } break;
-#define CMDX_W_BIN(d_, op_) \
-  case (kWBin0 + op_) * 32 + d_: { \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = bin<op_>(r[d_][v], x[v]); \
-  } break;
-#define CMDX_W_UN(d_, op_) \
-  case (kWUn0 + op_) * 32 + d_: { \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) r[d_][v] = un<op_>(x[v]); \
-  } break;
 
+// The 32-slot tier: the arithmetic, min/max and unary words run in the
+// inline-PTX loop of AsmWide (a jump on the source slot, then one on the op
+// and destination); each word it returns (a store, the end, a division,
+// comparison or select) is performed here and the loop re-entered.
 template <int V, bool EXT, class Pol>
 __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* __restrict__ prog,
                                          const uint32_t* __restrict__ scal, Pol& pol) {
+  uint32_t pc = 0;
 #pragma unroll 1
-  for (int pc = 0;; ++pc) {
-    const uint32_t w = prog[pc];
+  for (;;) {
+    const uint32_t w = AsmWide<V>::run(r, pc, prog, scal);
     const uint32_t kind = w >> 24;
     const uint32_t aux = w & 0xffu;
     const uint32_t base = kind & 0x3fu;
@@ -410,17 +407,7 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
       }
       continue;
     }
-    switch (base * 32 + ((w >> 16) & 0xffu)) {
-      CMDX_SA32(CMDX_W_BIN, kFAdd) CMDX_SA32(CMDX_W_BIN, kFSub) CMDX_SA32(CMDX_W_BIN, kFRsub)
-      CMDX_SA32(CMDX_W_BIN, kFMul) CMDX_SA32(CMDX_W_BIN, kIAdd) CMDX_SA32(CMDX_W_BIN, kISub)
-      CMDX_SA32(CMDX_W_BIN, kIRsub) CMDX_SA32(CMDX_W_BIN, kIMul)
-      CMDX_SA32(CMDX_W_BIN, kFMin) CMDX_SA32(CMDX_W_BIN, kFMax)
-      CMDX_SA32(CMDX_W_BIN, kIMin) CMDX_SA32(CMDX_W_BIN, kIMax)
-      CMDX_SA32(CMDX_W_UN, kFNeg) CMDX_SA32(CMDX_W_UN, kINeg) CMDX_SA32(CMDX_W_UN, kMov)
-      CMDX_SA32(CMDX_W_UN, kFAbs) CMDX_SA32(CMDX_W_UN, kIAbs) CMDX_SA32(CMDX_W_UN, kI2F)
-      CMDX_SA32(CMDX_W_UN, kF2I)
-      default: break;
-    }
+    return;  // (not reached: AsmWide runs every other kind)
   }
 }
 

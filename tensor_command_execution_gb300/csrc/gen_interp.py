@@ -341,6 +341,120 @@ struct AsmInterp<{S}, {V}, {"true" if ext else "false"}> {{
 """
 
 
+# Kinds of the wide encoding (cmd_internal.h WideKind): binary ops at
+# 0 .. N_BIN - 1, unary ops at N_BIN .. N_BIN + N_UN - 1; everything from
+# N_BIN + N_UN on (stores, end, comparisons, select, division by a scalar)
+# and the staged binary ops leave the loop.
+W_SLOTS = 32
+W_BASE_KINDS = N_BIN + N_UN
+W_SCALAR = 0x40
+
+
+def gen_wide(V: int) -> str:
+    """The 32-slot tier: word = kind << 24 | d << 16 | s << 8 | aux. The
+    source operand (slot s, or scalar aux when the kind has the scalar flag)
+    is copied into V staging registers by a first jump table on s; a second
+    table on (kind, d) applies the op to the destination's registers. Words
+    this loop does not run leave it and are returned to the caller."""
+    S = W_SLOTS
+
+    def reg(i, v):
+        return f"%{i * V + v}"
+
+    slot_ops = S * V
+    o_idx, o_word, o_prog, o_scal = slot_ops, slot_ops + 1, slot_ops + 2, slot_ops + 3
+    xs = [f"%%x{v}" for v in range(V)]
+    fetch_labels, fetch_bodies = [], []
+    for s in range(S):
+        lab = f"$LF{s}"
+        fetch_labels.append(lab)
+        fetch_bodies.append(f"{lab}: " + " ".join(f"mov.b32 {xs[v]}, {reg(s, v)};" for v in range(V)) +
+                            " bra.uni $Lop;")
+    op_labels, op_bodies = [], []
+    for kind in range(W_BASE_KINDS):
+        for d in range(S):
+            if kind < N_BIN:
+                op = BIN[kind]
+                if isinstance(op, tuple):
+                    op_labels.append("$Lexit")
+                    continue
+                body = " ".join(op.format(d=reg(d, v), x=xs[v]) for v in range(V))
+            else:
+                u = kind - N_BIN
+                body = " ".join(UN[u].format(d=reg(d, v), x=xs[v]) for v in range(V))
+            lab = f"$LO{kind}_{d}"
+            op_labels.append(lab)
+            op_bodies.append(f"{lab}: {body} bra.uni $Lloop;")
+
+    def table(name, labels):
+        return f"{name}: .branchtargets " + ",\n".join(
+            ", ".join(labels[i:i + 16]) for i in range(0, len(labels), 16)) + ";"
+
+    lines = ["{"]
+    lines.append(".reg .b32 %%w, %%wc, %%c, %%kd, %%aux, %%k, %%t, " + ", ".join(xs) + ";")
+    lines.append(".reg .b64 %%cbase, %%ca, %%sa;")
+    lines.append(".reg .pred %%p0;")
+    lines.append(table("$Lfetch", fetch_labels))
+    lines.append(table("$Lops", op_labels))
+    lines.append(f"cvta.to.const.u64 %%cbase, %{o_prog};")
+    lines.append(f"mad.wide.u32 %%ca, %{o_idx}, 4, %%cbase;")
+    lines.append("ld.const.u32 %%w, [%%ca];")
+    lines.append("$Lloop:")
+    lines.append("mov.b32 %%wc, %%w;")
+    lines.append("add.u64 %%ca, %%ca, 4;")
+    lines.append("ld.const.u32 %%w, [%%ca];")
+    # kind without the scalar flag; kinds past the unary ops leave the loop
+    lines.append("shr.u32 %%kd, %%wc, 24;")
+    lines.append(f"and.b32 %%c, %%kd, {W_SCALAR - 1};")
+    lines.append(f"setp.ge.u32 %%p0, %%c, {W_BASE_KINDS};")
+    lines.append("@%%p0 bra.uni $Lexit;")
+    lines.append(f"and.b32 %%t, %%kd, {W_SCALAR};")
+    lines.append("setp.ne.u32 %%p0, %%t, 0;")
+    lines.append("@%%p0 bra.uni $Lscalar;")
+    lines.append("bfe.u32 %%t, %%wc, 8, 8;")
+    lines.append("brx.idx.uni %%t, $Lfetch;")
+    lines += fetch_bodies
+    lines.append(f"$Lscalar: and.b32 %%aux, %%wc, 255; mad.wide.u32 %%sa, %%aux, 4, %{o_scal}; ld.u32 %%k, [%%sa]; " +
+                 " ".join(f"mov.b32 {xs[v]}, %%k;" for v in range(V)))
+    lines.append("$Lop:")
+    lines.append("bfe.u32 %%t, %%wc, 16, 8;")
+    lines.append(f"mad.lo.u32 %%t, %%c, {S}, %%t;")
+    lines.append("brx.idx.uni %%t, $Lops;")
+    lines += op_bodies
+    lines.append("$Lexit:")
+    lines.append(f"mov.b32 %{o_word}, %%wc;")
+    lines.append("sub.u64 %%ca, %%ca, %%cbase;")
+    lines.append(f"cvt.u32.u64 %{o_idx}, %%ca;")
+    lines.append(f"shr.u32 %{o_idx}, %{o_idx}, 2;")
+    lines.append("}")
+    asm = "\n".join(lines)
+    out_lines = []
+    for ln in asm.split("\n"):
+        out_lines.append('    "' + ln.replace("\\", "\\\\").replace('"', '\\"') + '\\n"')
+    outs = ", ".join(f'"+r"(r[{i}][{v}])' for i in range(S) for v in range(V))
+    return f"""
+template <>
+struct AsmWide<{V}> {{
+  // Run the arithmetic, min/max and unary words from prog[idx] on; return
+  // the first other word (a store, the end, a division, comparison or
+  // select), with idx pointing past it.
+  static __device__ __forceinline__ uint32_t run(uint32_t (&r)[{S}][{V}], uint32_t& idx, const uint32_t* prog,
+                                                 const uint32_t* scal) {{
+    uint32_t word;
+    asm volatile(
+{chr(10).join(out_lines)}
+        : {outs}, "+r"(idx), "=r"(word)
+        : "l"(prog), "l"(scal)
+        : "memory");
+    return word;
+  }}
+}};
+"""
+
+
+WIDE_V = [2]
+
+
 def main():
     parts = [
         "// interp_asm.cuh - GENERATED by gen_interp.py; do not edit by hand.\n"
@@ -354,6 +468,10 @@ def main():
     for S, V in TIERS:
         for ext in (False, True):
             parts.append(gen_tier(S, V, ext))
+    parts.append("\n// The 32-slot tier's loop for V elements per slot.\n"
+                 "template <int V>\nstruct AsmWide;\n")
+    for V in WIDE_V:
+        parts.append(gen_wide(V))
     parts.append("\n}  // namespace cmdx\n")
     with open(OUT, "w") as f:
         f.write("".join(parts))

@@ -19,6 +19,8 @@ import specutil
     W.strided_bf16(130, 72, 80),
     W.threshold_bits((1 << 12) + 17),
     W.batched_transpose(3, 40, 24),
+    W.tile4_f32(68, 40),
+    W.wide32_f32(1000),
 ], ids=lambda s: s["name"])
 def test_split_oracle_equals_single_walk(spec):
     bufs = specutil.host_buffers(spec)
