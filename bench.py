@@ -235,7 +235,8 @@ class Workload:
         self.bytes = self.plan["bytes"]
         self.elements = self.plan["n_elements"]
         info = self.kernel.info()
-        chunk = 32 * (2 if info["tier"] == 3 else 16 if (info["tier"] == 0 and info["extended"]) else 8)
+        # elements per warp chunk of the contiguous executor: 32 x (elements per slot per thread)
+        chunk = 32 * {3: 2, 4: 4}.get(info["tier"], 16 if (info["tier"] == 0 and info["extended"]) else 8)
         self.launches_per_step = 1 + (1 if (self.plan["path"] == "contig" and self.elements % chunk != 0) else 0)
 
     def units(self, name, a, b):

@@ -189,7 +189,7 @@ typedef struct cmd_program_info {
   int32_t n_stores;
   int32_t n_slots;      /* register slots the program needs */
   int32_t n_words;      /* program words, including the end marker */
-  int32_t tier;         /* executor family: 0 = 2 slots, 1 = 4, 2 = 8, 3 = 32 */
+  int32_t tier;         /* executor family: 0 = 2 slots, 1 = 4, 2 = 8, 3 = 32, 4 = 16 */
   int32_t n_moves;      /* copies the two-address form needed */
   int32_t extended;     /* 1 if the program has a live division, comparison or
                            select, or a packed-bit store: it runs the

@@ -39,7 +39,7 @@ def _objs(tiers, nds=(None,)):
 CU_SOURCES = [("exec_tile2d.cu", _objs((2,), (0, 1))), ("exec_generic.cu", _objs((2,))),
               ("exec_contig.cu", _objs((2,))), ("exec_contig.cu", [dict(CMDX_TIER=0, CMDX_EXT=1, CMDX_OCC4=1)]),
               ("exec_tile2d.cu", _objs((1, 0), (0, 1))),
-              ("exec_generic.cu", _objs((3, 1, 0))), ("exec_contig.cu", _objs((3, 1, 0))),
+              ("exec_generic.cu", _objs((4, 3, 1, 0))), ("exec_contig.cu", _objs((4, 3, 1, 0))),
               ("static_scratch.cu", [{}])]
 CPP_SOURCES = ["cmd_api.cpp", "cmd_yaml.cpp", "exec_host.cpp"]
 HEADERS = ["cmd_internal.h", "exec_common.cuh", "exec_tile2d.h", "interp_asm.cuh", "gen_interp.py"]

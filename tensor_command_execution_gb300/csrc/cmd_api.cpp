@@ -509,10 +509,11 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
   if (P->n_slots > cmdx::kMaxSlots)
     return fail(CMD_ERR_LIMIT, "the program needs more than " + std::to_string(cmdx::kMaxSlots - 1) +
                                    " simultaneously live values besides the staging slot of its comparisons");
-  P->tier = P->n_slots <= 2   ? cmdx::kTier2
-            : P->n_slots <= 4 ? cmdx::kTier4
-            : P->n_slots <= 8 ? cmdx::kTier8
-                              : cmdx::kTier32;
+  P->tier = P->n_slots <= 2    ? cmdx::kTier2
+            : P->n_slots <= 4  ? cmdx::kTier4
+            : P->n_slots <= 8  ? cmdx::kTier8
+            : P->n_slots <= 16 ? cmdx::kTier16
+                               : cmdx::kTier32;
 
   // encode
   P->words.clear();
@@ -539,7 +540,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
   }
   for (const Instr& in : P->code) {
     uint32_t w = 0;
-    if (P->tier != cmdx::kTier32) {
+    if (!cmdx::tier_wide(P->tier)) {
       switch (in.kind) {
         case Instr::kBin: w = cmdx::fz_bin(S, in.op, in.d, in.s); break;
         case Instr::kUn: w = cmdx::fz_un(S, in.op, in.d, in.s); break;
@@ -568,7 +569,7 @@ cmd_status lower(const std::vector<Op>& ops, Program* P) {
     }
     P->words.push_back(w);
   }
-  P->words.push_back(P->tier != cmdx::kTier32 ? cmdx::fz_end(S) : cmdx::wd_word(cmdx::kWEnd, 0, 0, 0));
+  P->words.push_back(!cmdx::tier_wide(P->tier) ? cmdx::fz_end(S) : cmdx::wd_word(cmdx::kWEnd, 0, 0, 0));
   if ((int)P->words.size() > cmdx::kMaxProgramWords)
     return fail(CMD_ERR_LIMIT, "the lowered program has " + std::to_string(P->words.size()) +
                                    " words; the limit is " + std::to_string(cmdx::kMaxProgramWords));
@@ -888,7 +889,7 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   // dim is the unit-stride dim of the loads that are not unit-stride along
   // the column dim (or, without such loads, the store's next smallest stride).
   // (not with packed-bit stores: those take the generic executor)
-  if (m >= 2 && P.tier != cmdx::kTier32 && !pl->loads.empty() && !any_b1) {
+  if (m >= 2 && !cmdx::tier_wide(P.tier) && !pl->loads.empty() && !any_b1) {
     const size_t nl = pl->loads.size();
     int col = -1, row = -1;
     for (int q = 0; q < m; ++q)

@@ -22,13 +22,17 @@ constexpr int kMaxSlots = 32;
 constexpr int kMaxPrograms = 48;
 constexpr int kMaxWords = 256;
 
-// Executor families by register-slot count. The two small tiers dispatch on
-// one fused (opcode, dst, src) case; the wide tier fetches the source operand
-// and then dispatches on (opcode, dst).
-enum Tier { kTier2 = 0, kTier4 = 1, kTier8 = 2, kTier32 = 3 };
+// Executor families by register-slot count. The 2-, 4- and 8-slot tiers
+// dispatch on one fused (opcode, dst, src) case; the wide tiers (16 and 32
+// slots) fetch the source operand and then dispatch on (opcode, dst). (The
+// 16-slot tier is numbered after the 32-slot one, which kept its number.)
+enum Tier { kTier2 = 0, kTier4 = 1, kTier8 = 2, kTier32 = 3, kTier16 = 4 };
+constexpr int kNumTiers = 5;
 CMDX_HD constexpr int tier_slots(int tier) {
-  return tier == kTier2 ? 2 : tier == kTier4 ? 4 : tier == kTier8 ? 8 : 32;
+  return tier == kTier2 ? 2 : tier == kTier4 ? 4 : tier == kTier8 ? 8 : tier == kTier16 ? 16 : 32;
 }
+// The wide encoding (wd_word) and the two-level dispatch serve these tiers.
+CMDX_HD constexpr bool tier_wide(int tier) { return tier == kTier16 || tier == kTier32; }
 // Elements each thread keeps per slot in the contiguous executor: 8 in the
 // fused tiers and 2 in the 32-slot one, except 16 in the extended variant of
 // the 2-slot tier, whose programs (divisions, comparisons, packed-bit stores)
@@ -36,7 +40,7 @@ CMDX_HD constexpr int tier_slots(int tier) {
 // dispatch over more elements (measured: packed-bit threshold +22 %), while
 // plain 2-slot programs run faster at the higher occupancy of 8.
 CMDX_HD constexpr int tier_vec(int tier, bool ext) {
-  return tier == kTier32 ? 2 : (tier == kTier2 && ext) ? 16 : 8;
+  return tier == kTier32 ? 2 : tier == kTier16 ? 4 : (tier == kTier2 && ext) ? 16 : 8;
 }
 // Whether the contiguous executor prefetches the next chunk's loads while
 // the program runs on the current one: in the base variant of the 2-slot
@@ -46,9 +50,11 @@ CMDX_HD constexpr int tier_vec(int tier, bool ext) {
 CMDX_HD constexpr bool contig_prefetch(int tier, bool ext) { return tier == kTier2 && !ext; }
 // ... and in the generic executor, whose addressing needs more registers:
 // 8, and 4 in the 8-slot tier.
-CMDX_HD constexpr int tier_vec_strided(int tier) { return tier == kTier8 ? 4 : tier == kTier32 ? 2 : 8; }
+CMDX_HD constexpr int tier_vec_strided(int tier) {
+  return tier == kTier8 || tier == kTier16 ? 4 : tier == kTier32 ? 2 : 8;
+}
 // Resident 256-thread CTAs per SM each executor is compiled for (caps registers).
-CMDX_HD constexpr int tier_min_blocks(int tier) { return tier == kTier32 ? 2 : 3; }
+CMDX_HD constexpr int tier_min_blocks(int tier) { return tier_wide(tier) ? 2 : 3; }
 // Program words a program may have: one less than its constant-memory row,
 // so the interpreter's read-ahead of the word after the last stays in the row.
 constexpr int kMaxProgramWords = kMaxWords - 1;
@@ -125,10 +131,10 @@ enum DerivedKind {
 };
 constexpr uint32_t kSDivSlow = 0x80000000u;
 
-// ---- wide encoding (tier 32) -------------------------------------------------
+// ---- wide encoding (tiers 16 and 32) ---------------------------------------
 // word = kind << 24 | d << 16 | s << 8 | aux. The source operand x is slot s,
 // or scalar aux when the kind has kWScalar set. Selects read the staging
-// slot X = 31 as their condition.
+// slot X (the tier's last slot, 15 or 31) as their condition.
 enum WideKind {
   kWBin0 = 0,    // + BinOp
   kWUn0 = 16,    // + UnOp
@@ -224,8 +230,8 @@ struct GenericParams {
   cudaError_t contig_launch_t##t##e##v(const ContigParams& p, cudaStream_t stream); \
   cudaError_t generic_upload_t##t##e##v(int slot, const uint32_t* words, int n);    \
   cudaError_t generic_launch_t##t##e##v(const GenericParams& p, cudaStream_t stream);
-CMDX_DECL_OBJ(0, 0) CMDX_DECL_OBJ(1, 0) CMDX_DECL_OBJ(2, 0) CMDX_DECL_OBJ(3, 0)
-CMDX_DECL_OBJ(0, 1) CMDX_DECL_OBJ(1, 1) CMDX_DECL_OBJ(2, 1) CMDX_DECL_OBJ(3, 1)
+CMDX_DECL_OBJ(0, 0) CMDX_DECL_OBJ(1, 0) CMDX_DECL_OBJ(2, 0) CMDX_DECL_OBJ(3, 0) CMDX_DECL_OBJ(4, 0)
+CMDX_DECL_OBJ(0, 1) CMDX_DECL_OBJ(1, 1) CMDX_DECL_OBJ(2, 1) CMDX_DECL_OBJ(3, 1) CMDX_DECL_OBJ(4, 1)
 #undef CMDX_DECL_OBJ
 // the extended 2-slot contiguous kernel built for four CTAs per SM
 cudaError_t contig_upload_t0e1o4(int slot, const uint32_t* words, int n);

@@ -243,39 +243,68 @@ __device__ __forceinline__ void run_fused(uint32_t (&r)[S][V], const uint32_t* _
   }
 }
 
-// ---- wide dispatch (32 slots): fetch the source, then (op, dst) -------------
-#define CMDX_SA32(M, ...)                                                                 \
+// ---- wide dispatch (16 and 32 slots): fetch the source, then (op, dst) ------
+#define CMDX_SA16(M, ...)                                                                 \
   CMDX_SA8(M, __VA_ARGS__) M(8, __VA_ARGS__) M(9, __VA_ARGS__) M(10, __VA_ARGS__)         \
-  M(11, __VA_ARGS__) M(12, __VA_ARGS__) M(13, __VA_ARGS__) M(14, __VA_ARGS__)             \
-  M(15, __VA_ARGS__) M(16, __VA_ARGS__) M(17, __VA_ARGS__) M(18, __VA_ARGS__)             \
+  M(11, __VA_ARGS__) M(12, __VA_ARGS__) M(13, __VA_ARGS__) M(14, __VA_ARGS__) M(15, __VA_ARGS__)
+#define CMDX_SA32(M, ...)                                                                 \
+  CMDX_SA16(M, __VA_ARGS__) M(16, __VA_ARGS__) M(17, __VA_ARGS__) M(18, __VA_ARGS__)      \
   M(19, __VA_ARGS__) M(20, __VA_ARGS__) M(21, __VA_ARGS__) M(22, __VA_ARGS__)             \
   M(23, __VA_ARGS__) M(24, __VA_ARGS__) M(25, __VA_ARGS__) M(26, __VA_ARGS__)             \
   M(27, __VA_ARGS__) M(28, __VA_ARGS__) M(29, __VA_ARGS__) M(30, __VA_ARGS__) M(31, __VA_ARGS__)
 
-#define CMDX_W_FETCH(s_, x_) \
-  case s_: {                 \
-    CMDX_UNROLL for (int v = 0; v < V; ++v) x[v] = r[s_][v]; \
-  } break;
-#define CMDX_W_FETCH_Y(s_, x_) \
-  case s_: {                   \
+#define CMDX_W_GET(s_, x_) \
+  case s_: {               \
     CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = r[s_][v]; \
   } break;
-#define CMDX_W_PUT_Y(s_, x_) \
-  case s_: {                 \
+#define CMDX_W_PUT(s_, x_) \
+  case s_: {               \
     CMDX_UNROLL for (int v = 0; v < V; ++v) r[s_][v] = y[v]; \
   } break;
 
-// The 32-slot tier: the arithmetic, min/max and unary words run in the
-// inline-PTX loop of AsmWide (a jump on the source slot, then one on the op
-// and destination); each word it returns (a store, the end, a division,
-// comparison or select) is performed here and the loop re-entered.
-template <int V, bool EXT, class Pol>
-__device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* __restrict__ prog,
+// y = slot s, and slot s = y, for a slot number known only at run time (a
+// switch over the tier's slots, so the slots stay in registers).
+template <int S, int V>
+__device__ __forceinline__ void slot_get(const uint32_t (&r)[S][V], uint32_t s, uint32_t (&y)[V]) {
+  if constexpr (S == 32) {
+    switch (s) {
+      CMDX_SA32(CMDX_W_GET, 0)
+      default: break;
+    }
+  } else {
+    switch (s) {
+      CMDX_SA16(CMDX_W_GET, 0)
+      default: break;
+    }
+  }
+}
+template <int S, int V>
+__device__ __forceinline__ void slot_put(uint32_t (&r)[S][V], uint32_t s, const uint32_t (&y)[V]) {
+  if constexpr (S == 32) {
+    switch (s) {
+      CMDX_SA32(CMDX_W_PUT, 0)
+      default: break;
+    }
+  } else {
+    switch (s) {
+      CMDX_SA16(CMDX_W_PUT, 0)
+      default: break;
+    }
+  }
+}
+
+// A wide tier (S = 16 or 32 slots): the arithmetic, min/max and unary words
+// run in the inline-PTX loop of AsmWide (a jump on the source slot, then one
+// on the op and destination); each word it returns (a store, the end, a
+// division, comparison or select) is performed here and the loop re-entered.
+template <int S, int V, bool EXT, class Pol>
+__device__ __forceinline__ void run_wide(uint32_t (&r)[S][V], const uint32_t* __restrict__ prog,
                                          const uint32_t* __restrict__ scal, Pol& pol) {
+  static_assert(S == 16 || S == 32, "the wide dispatch is generated for 16 and 32 slots");
   uint32_t pc = 0;
 #pragma unroll 1
   for (;;) {
-    const uint32_t w = AsmWide<V>::run(r, pc, prog, scal);
+    const uint32_t w = AsmWide<S, V>::run(r, pc, prog, scal);
     const uint32_t kind = w >> 24;
     const uint32_t aux = w & 0xffu;
     const uint32_t base = kind & 0x3fu;
@@ -285,48 +314,32 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
       const uint32_t k = scal[aux];
       CMDX_UNROLL for (int v = 0; v < V; ++v) x[v] = k;
     } else {
-      switch ((w >> 8) & 0xffu) {
-        CMDX_SA32(CMDX_W_FETCH, 0)
-        default: break;
-      }
+      slot_get<S, V>(r, (w >> 8) & 0xffu, x);
     }
+    const uint32_t d = (w >> 16) & 0xffu;
     if (base >= kWBin0 + kFDiv && base <= kWBin0 + kIRdiv) {
       // the division ops (kFDiv, kFRdiv, kIDiv, kIRdiv are consecutive): one
       // body for every destination, fetch, divide, write back; the base
       // variant ends the program (the host never launches that pairing)
       if constexpr (!EXT) return;
-      const uint32_t d = (w >> 16) & 0xffu;
       uint32_t y[V];
-      switch (d) {
-        CMDX_SA32(CMDX_W_FETCH_Y, 0)
-        default: break;
-      }
+      slot_get<S, V>(r, d, y);
       const uint32_t op = base - kWBin0;
       CMDX_UNROLL for (int v = 0; v < V; ++v) {
         const bool rev = op == kFRdiv || op == kIRdiv;
         const uint32_t a = rev ? x[v] : y[v], b = rev ? y[v] : x[v];
         y[v] = op >= kIDiv ? idiv(a, b) : bin<kFDiv>(a, b);
       }
-      switch (d) {
-        CMDX_SA32(CMDX_W_PUT_Y, 0)
-        default: break;
-      }
+      slot_put<S, V>(r, d, y);
       continue;
     }
     if (base >= kWCmp0 && base < kWCmp0 + kNumCmp) {
       // comparisons: one body for every destination, like the divisions
       if constexpr (!EXT) return;
-      const uint32_t d = (w >> 16) & 0xffu;
       uint32_t y[V];
-      switch (d) {
-        CMDX_SA32(CMDX_W_FETCH_Y, 0)
-        default: break;
-      }
+      slot_get<S, V>(r, d, y);
       CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = cmp_rel((int)(base - kWCmp0), y[v], x[v]);
-      switch (d) {
-        CMDX_SA32(CMDX_W_PUT_Y, 0)
-        default: break;
-      }
+      slot_put<S, V>(r, d, y);
       continue;
     }
     if (base == kWSDiv0 || base == kWSDiv0 + 1) {
@@ -334,12 +347,8 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
       // sequence when every element of the warp is in range, else the
       // general division (the same arithmetic as the fused cases)
       if constexpr (!EXT) return;
-      const uint32_t d = (w >> 16) & 0xffu;
       uint32_t y[V];
-      switch (d) {
-        CMDX_SA32(CMDX_W_FETCH_Y, 0)
-        default: break;
-      }
+      slot_get<S, V>(r, d, y);
       if (base == kWSDiv0) {
         const float sv = __uint_as_float(scal[aux]), rv = __uint_as_float(scal[aux + 1]);
         bool ok = rv != 0.0f;
@@ -372,26 +381,16 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
           }
         }
       }
-      switch (d) {
-        CMDX_SA32(CMDX_W_PUT_Y, 0)
-        default: break;
-      }
+      slot_put<S, V>(r, d, y);
       continue;
     }
     if (base == kWSel) {
-      // d = X != 0 ? d : x, X the staging slot 31
+      // d = X != 0 ? d : x, X the staging slot S - 1
       if constexpr (!EXT) return;
-      const uint32_t d = (w >> 16) & 0xffu;
       uint32_t y[V];
-      switch (d) {
-        CMDX_SA32(CMDX_W_FETCH_Y, 0)
-        default: break;
-      }
-      CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = r[31][v] != 0u ? y[v] : x[v];
-      switch (d) {
-        CMDX_SA32(CMDX_W_PUT_Y, 0)
-        default: break;
-      }
+      slot_get<S, V>(r, d, y);
+      CMDX_UNROLL for (int v = 0; v < V; ++v) y[v] = r[S - 1][v] != 0u ? y[v] : x[v];
+      slot_put<S, V>(r, d, y);
       continue;
     }
     if (base >= kWStore0 && base < kWStore0 + kNumSt) {
@@ -414,7 +413,7 @@ __device__ __forceinline__ void run_wide(uint32_t (&r)[32][V], const uint32_t* _
 template <int TIER, int V, bool EXT, class Pol>
 __device__ __forceinline__ void run_program(uint32_t (&r)[tier_slots(TIER)][V], const uint32_t* prog,
                                             const uint32_t* scal, Pol& pol) {
-  if constexpr (TIER == kTier32) run_wide<V, EXT>(r, prog, scal, pol);
+  if constexpr (tier_wide(TIER)) run_wide<tier_slots(TIER), V, EXT>(r, prog, scal, pol);
   else run_fused<tier_slots(TIER), V, EXT>(r, prog, scal, pol);
 }
 

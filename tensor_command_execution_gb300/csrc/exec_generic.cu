@@ -13,7 +13,7 @@
 #include "exec_common.cuh"
 
 #if !defined(CMDX_TIER) || !defined(CMDX_EXT)
-#error "exec_generic.cu is compiled per tier and variant, with -DCMDX_TIER=<0..3> -DCMDX_EXT=<0|1>"
+#error "exec_generic.cu is compiled per tier and variant, with -DCMDX_TIER=<0..4> -DCMDX_EXT=<0|1>"
 #endif
 
 namespace cmdx {

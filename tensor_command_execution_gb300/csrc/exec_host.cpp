@@ -19,19 +19,19 @@ using GenericLaunch = cudaError_t (*)(const GenericParams&, cudaStream_t);
 using TileLaunch = cudaError_t (*)(const Tile2dParams&, cudaStream_t);
 
 // [op-set variant][tier]
-constexpr Upload kContigUpload[2][4] = {
-    {contig_upload_t0e0, contig_upload_t1e0, contig_upload_t2e0, contig_upload_t3e0},
-    {contig_upload_t0e1, contig_upload_t1e1, contig_upload_t2e1, contig_upload_t3e1}};
-constexpr Upload kGenericUpload[2][4] = {
-    {generic_upload_t0e0, generic_upload_t1e0, generic_upload_t2e0, generic_upload_t3e0},
-    {generic_upload_t0e1, generic_upload_t1e1, generic_upload_t2e1, generic_upload_t3e1}};
-constexpr ContigLaunch kContigLaunch[2][4] = {
-    {contig_launch_t0e0, contig_launch_t1e0, contig_launch_t2e0, contig_launch_t3e0},
-    {contig_launch_t0e1, contig_launch_t1e1, contig_launch_t2e1, contig_launch_t3e1}};
-constexpr GenericLaunch kGenericLaunch[2][4] = {
-    {generic_launch_t0e0, generic_launch_t1e0, generic_launch_t2e0, generic_launch_t3e0},
-    {generic_launch_t0e1, generic_launch_t1e1, generic_launch_t2e1, generic_launch_t3e1}};
-// [op-set variant][view variant][tier]; the 32-slot tier has no tile kernel
+constexpr Upload kContigUpload[2][kNumTiers] = {
+    {contig_upload_t0e0, contig_upload_t1e0, contig_upload_t2e0, contig_upload_t3e0, contig_upload_t4e0},
+    {contig_upload_t0e1, contig_upload_t1e1, contig_upload_t2e1, contig_upload_t3e1, contig_upload_t4e1}};
+constexpr Upload kGenericUpload[2][kNumTiers] = {
+    {generic_upload_t0e0, generic_upload_t1e0, generic_upload_t2e0, generic_upload_t3e0, generic_upload_t4e0},
+    {generic_upload_t0e1, generic_upload_t1e1, generic_upload_t2e1, generic_upload_t3e1, generic_upload_t4e1}};
+constexpr ContigLaunch kContigLaunch[2][kNumTiers] = {
+    {contig_launch_t0e0, contig_launch_t1e0, contig_launch_t2e0, contig_launch_t3e0, contig_launch_t4e0},
+    {contig_launch_t0e1, contig_launch_t1e1, contig_launch_t2e1, contig_launch_t3e1, contig_launch_t4e1}};
+constexpr GenericLaunch kGenericLaunch[2][kNumTiers] = {
+    {generic_launch_t0e0, generic_launch_t1e0, generic_launch_t2e0, generic_launch_t3e0, generic_launch_t4e0},
+    {generic_launch_t0e1, generic_launch_t1e1, generic_launch_t2e1, generic_launch_t3e1, generic_launch_t4e1}};
+// [op-set variant][view variant][tier]; the wide tiers have no tile kernel
 constexpr Upload kTileUpload[2][2][3] = {
     {{tile2d_upload_t0n0e0, tile2d_upload_t1n0e0, tile2d_upload_t2n0e0},
      {tile2d_upload_t0n1e0, tile2d_upload_t1n1e0, tile2d_upload_t2n1e0}},
@@ -43,7 +43,7 @@ constexpr TileLaunch kTileLaunch[2][2][3] = {
     {{tile2d_launch_t0n0e1, tile2d_launch_t1n0e1, tile2d_launch_t2n0e1},
      {tile2d_launch_t0n1e1, tile2d_launch_t1n1e1, tile2d_launch_t2n1e1}}};
 
-bool tier_ok(int tier) { return tier >= kTier2 && tier <= kTier32; }
+bool tier_ok(int tier) { return tier >= 0 && tier < kNumTiers; }
 
 // Tile rows the producer of a plain 2-D launch walks together (measured on
 // GB300, strided_bf16 A/B on one box: 1 -> 5982 GB/s, 8 -> 6076; 4 and 16
@@ -57,7 +57,7 @@ cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, 
   cudaError_t e = kContigUpload[ext][tier](slot, words, n);
   if (e == cudaSuccess && ext && tier == kTier2) e = contig_upload_t0e1o4(slot, words, n);
   if (e == cudaSuccess) e = kGenericUpload[ext][tier](slot, words, n);
-  for (int nd = 0; nd < 2 && e == cudaSuccess && tier != kTier32; ++nd) e = kTileUpload[ext][nd][tier](slot, words, n);
+  for (int nd = 0; nd < 2 && e == cudaSuccess && !tier_wide(tier); ++nd) e = kTileUpload[ext][nd][tier](slot, words, n);
   return e;
 }
 
@@ -187,7 +187,7 @@ cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_
   p.debug = L.debug;
   bool nd = L.nb[0] > 1 || L.nb[1] > 1;
   for (uint32_t j = 0; j < L.n_loads; ++j) nd = nd || p.in_bcast[j] || p.in_rank[j] != 2;
-  if (tier < kTier2 || tier > kTier8) return cudaErrorInvalidValue;  // no 32-slot tile kernel
+  if (tier < kTier2 || tier > kTier8) return cudaErrorInvalidValue;  // no wide-tier tile kernel
   return kTileLaunch[ext][nd][tier](p, stream);
 }
 

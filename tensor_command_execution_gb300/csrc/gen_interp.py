@@ -345,18 +345,17 @@ struct AsmInterp<{S}, {V}, {"true" if ext else "false"}> {{
 # 0 .. N_BIN - 1, unary ops at N_BIN .. N_BIN + N_UN - 1; everything from
 # N_BIN + N_UN on (stores, end, comparisons, select, division by a scalar)
 # and the staged binary ops leave the loop.
-W_SLOTS = 32
 W_BASE_KINDS = N_BIN + N_UN
 W_SCALAR = 0x40
 
 
-def gen_wide(V: int) -> str:
-    """The 32-slot tier: word = kind << 24 | d << 16 | s << 8 | aux. The
-    source operand (slot s, or scalar aux when the kind has the scalar flag)
-    is copied into V staging registers by a first jump table on s; a second
-    table on (kind, d) applies the op to the destination's registers. Words
-    this loop does not run leave it and are returned to the caller."""
-    S = W_SLOTS
+def gen_wide(S: int, V: int) -> str:
+    """A wide tier (16 or 32 slots): word = kind << 24 | d << 16 | s << 8 |
+    aux. The source operand (slot s, or scalar aux when the kind has the
+    scalar flag) is copied into V staging registers by a first jump table on
+    s; a second table on (kind, d) applies the op to the destination's
+    registers. Words this loop does not run leave it and are returned to the
+    caller."""
 
     def reg(i, v):
         return f"%{i * V + v}"
@@ -434,7 +433,7 @@ def gen_wide(V: int) -> str:
     outs = ", ".join(f'"+r"(r[{i}][{v}])' for i in range(S) for v in range(V))
     return f"""
 template <>
-struct AsmWide<{V}> {{
+struct AsmWide<{S}, {V}> {{
   // Run the arithmetic, min/max and unary words from prog[idx] on; return
   // the first other word (a store, the end, a division, comparison or
   // select), with idx pointing past it.
@@ -452,7 +451,7 @@ struct AsmWide<{V}> {{
 """
 
 
-WIDE_V = [2]
+WIDE = [(32, 2), (16, 4)]
 
 
 def main():
@@ -468,10 +467,10 @@ def main():
     for S, V in TIERS:
         for ext in (False, True):
             parts.append(gen_tier(S, V, ext))
-    parts.append("\n// The 32-slot tier's loop for V elements per slot.\n"
-                 "template <int V>\nstruct AsmWide;\n")
-    for V in WIDE_V:
-        parts.append(gen_wide(V))
+    parts.append("\n// The loop of a wide tier of S slots, V elements per slot.\n"
+                 "template <int S, int V>\nstruct AsmWide;\n")
+    for S, V in WIDE:
+        parts.append(gen_wide(S, V))
     parts.append("\n}  // namespace cmdx\n")
     with open(OUT, "w") as f:
         f.write("".join(parts))

@@ -351,8 +351,37 @@ def test_wide_tier_program():
     bufs["out"] = specutil.sentinel_array("f32", n)
     bufs["out2"] = specutil.sentinel_array("bf16", n)
     c, _ = T.command_from_spec(spec)
-    assert c.lower()[0]["tier"] == 3
+    info = c.lower()[0]
+    assert info["tier"] == 3 and info["n_slots"] > 16
     assert gpuutil.parity(spec, bufs)["path"] == "contig"
+
+
+@pytest.mark.parametrize("strided", [False, True])
+@pytest.mark.parametrize("n_loads", [9, 12, 15])
+def test_sixteen_slot_tier_program(n_loads, strided):
+    """Programs with 9 to 16 live values run the 16-slot tier (two-level
+    dispatch, 4 elements per slot): every load live until the end, sums and
+    products chained over them, an f32 and a bf16 store; dense views on the
+    contiguous executor, stride-2 views on the generic one."""
+    rng = np.random.default_rng(n_loads)
+    n = 4099
+    st = 2 if strided else 1
+    names = [f"x{i}" for i in range(n_loads)]
+    block = [("add", "c0", "x0", names[-1])] + [("mul" if i % 2 else "sub", f"c{i}", f"c{i-1}", names[i])
+                                                 for i in range(1, n_loads)]
+    block += [("mul", "m", names[0], names[1]), ("add", "r", f"c{n_loads - 1}", "m"), ("neg", "q", "r", None)]
+    spec = dict(name=f"tier16_{n_loads}", seed=0, sizes=(n,),
+                ops=[("load", k, "f32") for k in names] + [("exec", block), ("store", "out", "r", "f32"),
+                                                            ("store", "out2", "q", "bf16")],
+                views={k: dict(strides=(st,), alloc=st * (n - 1) + 1) for k in names + ["out", "out2"]},
+                inputs={})
+    bufs = {k: (rng.standard_normal(spec["views"][k]["alloc"]) * 1.5).astype(np.float32) for k in names}
+    bufs["out"] = specutil.sentinel_array("f32", spec["views"]["out"]["alloc"])
+    bufs["out2"] = specutil.sentinel_array("bf16", spec["views"]["out2"]["alloc"])
+    c, _ = T.command_from_spec(spec)
+    info = c.lower()[0]
+    assert info["tier"] == 4 and 8 < info["n_slots"] <= 16, info
+    assert gpuutil.parity(spec, bufs)["path"] == ("generic" if strided else "contig")
 
 
 def test_special_values():
@@ -644,7 +673,7 @@ def _pairs(vals):
     return np.repeat(vals, vals.size), np.tile(vals, vals.size)
 
 
-@pytest.mark.parametrize("tier_pad", [0, 9])
+@pytest.mark.parametrize("tier_pad", [0, 9, 14])
 def test_new_float_ops_on_special_values(tier_pad):
     """Every pair of special floats through div / min / max (both operand
     orders reach the reversed forms), abs and to_i32; tier_pad extra live
@@ -677,11 +706,12 @@ def test_new_float_ops_on_special_values(tier_pad):
         bufs[o] = specutil.sentinel_array(dt, n)
     if tier_pad:
         c, _ = T.command_from_spec(spec)
-        assert c.lower()[0]["tier"] == 3
+        # (9 pads: 13-14 slots, the 16-slot tier; 14 pads: 18-19, the 32-slot tier)
+        assert c.lower()[0]["tier"] == (4 if tier_pad < 14 else 3)
     gpuutil.parity(spec, bufs)
 
 
-@pytest.mark.parametrize("tier_pad", [0, 9])
+@pytest.mark.parametrize("tier_pad", [0, 9, 14])
 def test_new_int_ops_on_edge_values(tier_pad):
     """Every pair of int32 edge values through division (zero and -1
     divisors, INT_MIN / -1, both operand orders), min / max, abs and
@@ -714,7 +744,8 @@ def test_new_int_ops_on_edge_values(tier_pad):
         bufs[o] = specutil.sentinel_array(dt, n)
     if tier_pad:
         c, _ = T.command_from_spec(spec)
-        assert c.lower()[0]["tier"] == 3
+        # (9 pads: 13-14 slots, the 16-slot tier; 14 pads: 18-19, the 32-slot tier)
+        assert c.lower()[0]["tier"] == (4 if tier_pad < 14 else 3)
     gpuutil.parity(spec, bufs)
 
 
@@ -891,9 +922,10 @@ def test_comparisons_and_select_on_special_values(pad):
             views[o] = dict(strides=(1,), alloc=(n + 31) // 32 if dt == "b1" else n)
             bufs[o] = specutil.sentinel_array(dt, views[o]["alloc"])
         spec = dict(name=f"cmpspecials{gi}", seed=0, sizes=(n,), ops=ops, views=views, inputs={})
-        if pad == 9 and any(src == acc for _, src, _ in group):
+        if pad >= 4 and any(src == acc for _, src, _ in group):
+            # (4 pads: 13 slots, the 16-slot tier; 9 pads: 18 slots, the 32-slot tier)
             c, _ = T.command_from_spec(spec)
-            assert c.lower()[0]["tier"] == 3
+            assert c.lower()[0]["tier"] == (4 if pad < 9 else 3)
         gpuutil.parity(spec, bufs)
 
 

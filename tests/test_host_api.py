@@ -179,18 +179,23 @@ def test_mixed_classes_rejected():
         c.execute([("min", a, i)])
 
 
-def test_wide_program_uses_the_32_slot_tier():
-    # 12 loads all live until the end: needs more than 8 slots
+@pytest.mark.parametrize("n_loads,tier", [(12, 4), (16, 3)])
+def test_wide_programs_use_the_16_and_32_slot_tiers(n_loads, tier):
+    # n loads all live until the end: 9 to 16 slots run the 16-slot tier
+    # (tier number 4), more the 32-slot one (tier number 3)
     c = T.Command()
-    xs = [c.load_tensor("f32", 1) for _ in range(12)]
-    ops = [("add", xs[0], xs[11])] + [("add", T.CMD_LOCAL(i), xs[(i + 1) % 12]) for i in range(11)]
-    ops += [("mul", xs[k], xs[k]) for k in range(12)]
+    xs = [c.load_tensor("f32", 1) for _ in range(n_loads)]
+    ops = [("add", xs[0], xs[-1])] + [("add", T.CMD_LOCAL(i), xs[(i + 1) % n_loads]) for i in range(n_loads - 1)]
+    ops += [("mul", xs[k], xs[k]) for k in range(n_loads)]
     t = c.execute(ops)
-    c.store(t[11], "f32", 1)
-    for k in range(12, 19):
+    c.store(t[n_loads - 1], "f32", 1)
+    for k in range(n_loads, n_loads + 7):
         c.store(t[k], "f32", 1)
-    info, _ = c.lower()
-    assert info["tier"] == 3 and info["n_slots"] > 8
+    info, words = c.lower()
+    assert info["tier"] == tier and info["n_slots"] > 8
+    assert (info["n_slots"] <= 16) == (tier == 4)
+    # the wide encoding: the end word is kind 31 in the top byte
+    assert words[-1] >> 24 == 31
 
 
 def test_store_of_loads_and_scalars_only():
