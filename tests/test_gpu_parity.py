@@ -876,6 +876,110 @@ def test_random_compare_select_commands(seed):
     gpuutil.parity(spec, bufs)
 
 
+def random_wide_case(seed):
+    """A random Command whose lowered program needs more than 8 slots (the
+    16- and 32-slot tiers): 9 to 16 loads of mixed types, operands drawn
+    from the whole history so that early values stay live, 2 to 6 stores
+    (int results sometimes as packed bits). By seed % 3: every E op including
+    division, comparisons and select (the extended variant); only the base
+    ops (add, sub, mul, min, max, neg, abs, conversions); or the base ops
+    with a closing sum over 20 independent products, which keeps more than
+    16 values live (the 32-slot tier). Drawn again (from the same seed's
+    stream) until the program is past 8 slots (past 16 for the third kind)."""
+    rng = np.random.default_rng(40_000 + seed)
+    mode = seed % 3
+    bin_ops = BIN_OPS if mode == 0 else [o for o in BIN_OPS if o != "div"]
+    kinds, kp = (["bin", "un", "cmp", "sel"], [0.55, 0.15, 0.2, 0.1]) if mode == 0 else (["bin", "un"], [0.8, 0.2])
+    while True:
+        rank = int(rng.integers(1, 3))
+        sizes = tuple(int(x) for x in rng.integers(2, 40, size=rank))
+        if rng.random() < 0.5:
+            sizes = sizes[:-1] + (int(rng.integers(300, 3000)),)
+        ops, views, bufs = [], {}, {}
+        vals = {"f": [], "i": []}
+        for i in range(int(rng.integers(9, 17))):
+            dt = str(rng.choice(["f32", "f16", "bf16", "i32"], p=[0.4, 0.15, 0.15, 0.3]))
+            name = f"L{i}"
+            ops.append(("load", name, dt))
+            st, n = _random_view(rng, sizes, allow_broadcast=True) if rng.random() < 0.4 else _dense_strides(sizes)
+            views[name] = dict(strides=st, alloc=n)
+            bufs[name] = _random_values(rng, dt, n)
+            if dt == "i32" and rng.random() < 0.5:
+                bufs[name] = rng.integers(-5, 6, size=n).astype(np.int32)
+            vals["i" if dt == "i32" else "f"].append(name)
+        for i in range(int(rng.integers(0, 4))):
+            name = f"S{i}"
+            if rng.random() < 0.5:
+                ops.append(("scalar", name, "i32", int(rng.choice([0, -1, 3, int(rng.integers(-2**31, 2**31))]))))
+                vals["i"].append(name)
+            else:
+                ops.append(("scalar", name, "f32", float(np.float32(rng.choice([0.0, -0.0, 1.5, rng.standard_normal()])))))
+                vals["f"].append(name)
+        block, last = [], []
+        for i in range(int(rng.integers(10, 40))):
+            name = f"E{i}"
+            kind = rng.choice(kinds, p=kp)
+            cls = str(rng.choice([c for c in ("f", "i") if vals[c]]))
+            a = str(rng.choice(vals[cls]))
+            if kind == "bin":
+                block.append((str(rng.choice(bin_ops)), name, a, str(rng.choice(vals[cls]))))
+                out = cls
+            elif kind == "un":
+                eop = str(rng.choice(UN_OPS))
+                out = {"to_f32": "f", "to_i32": "i"}.get(eop, cls)
+                block.append((eop, name, a, None))
+            elif kind == "cmp":
+                block.append((str(rng.choice(CMP_OPS)), name, a, str(rng.choice(vals[cls]))))
+                out = "i"
+            else:
+                if not vals["i"]:
+                    continue
+                block.append(("select", name, a, str(rng.choice(vals[cls])), str(rng.choice(vals["i"]))))
+                out = cls
+            vals[out].append(name)
+            last.append((name, out))
+        if mode == 2:
+            # 20 products of loads, all live until the closing sum
+            cls = "f" if len(vals["f"]) >= 2 else "i"
+            pool = [v for v in vals[cls] if v.startswith("L")] or vals[cls]
+            prods = []
+            for k in range(20):
+                name = f"P{k}"
+                block.append(("mul", name, str(rng.choice(pool)), str(rng.choice(pool))))
+                prods.append(name)
+            acc = prods[0]
+            for k in range(1, 20):
+                block.append(("add", f"Q{k}", acc, prods[k]))
+                acc = f"Q{k}"
+            last.append((acc, cls))
+        ops.append(("exec", block))
+        n_el = int(np.prod(sizes))
+        for i in range(int(rng.integers(2, 7))):
+            src, cls = last[-1 - int(rng.integers(0, min(12, len(last))))]
+            dt = ("b1" if rng.random() < 0.3 else "i32") if cls == "i" else str(rng.choice(["f32", "f16", "bf16"]))
+            name = f"O{i}"
+            ops.append(("store", name, src, dt))
+            if dt == "b1":
+                st, _ = _dense_strides(sizes)
+                views[name] = dict(strides=st, alloc=(n_el + 31) // 32)
+            else:
+                st, n = _random_view(rng, sizes, allow_broadcast=False) if rng.random() < 0.3 else _dense_strides(sizes)
+                views[name] = dict(strides=st, alloc=n)
+            bufs[name] = specutil.sentinel_array(dt, views[name]["alloc"])
+        spec = dict(name=f"wide{seed}", seed=seed, sizes=sizes, ops=ops, views=views, inputs={})
+        c, _ = T.command_from_spec(spec)
+        if c.lower()[0]["n_slots"] > (16 if mode == 2 else 8):
+            return spec, bufs
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_wide_commands(seed):
+    spec, bufs = random_wide_case(seed)
+    c, _ = T.command_from_spec(spec)
+    assert c.lower()[0]["tier"] in (3, 4)
+    gpuutil.parity(spec, bufs)
+
+
 @pytest.mark.parametrize("pad", [0, 4, 9])
 def test_comparisons_and_select_on_special_values(pad):
     """Every pair of special floats and of int edge values through every
