@@ -87,7 +87,8 @@ def measured_peak():
 
 KERNEL_SOURCES = {
     "exec_contig": ["exec_contig.cu", "exec_common.cuh", "interp_asm.cuh", "cmd_internal.h"],
-    "exec_tile2d": ["exec_tile2d.cu", "exec_tile2d.h", "exec_common.cuh", "interp_asm.cuh", "cmd_internal.h"],
+    "exec_tile2d": ["exec_tile2d.cu", "exec_tile2d.h", "exec_common.cuh", "exec_pipe.cuh", "interp_asm.cuh",
+                    "cmd_internal.h"],
     "exec_generic": ["exec_generic.cu", "exec_common.cuh", "interp_asm.cuh", "cmd_internal.h"],
 }
 

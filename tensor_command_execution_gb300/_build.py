@@ -42,7 +42,7 @@ CU_SOURCES = [("exec_tile2d.cu", _objs((2,), (0, 1))), ("exec_generic.cu", _objs
               ("exec_generic.cu", _objs((4, 3, 1, 0))), ("exec_contig.cu", _objs((4, 3, 1, 0))),
               ("static_scratch.cu", [{}])]
 CPP_SOURCES = ["cmd_api.cpp", "cmd_yaml.cpp", "exec_host.cpp"]
-HEADERS = ["cmd_internal.h", "exec_common.cuh", "exec_tile2d.h", "interp_asm.cuh", "gen_interp.py"]
+HEADERS = ["cmd_internal.h", "exec_common.cuh", "exec_pipe.cuh", "exec_tile2d.h", "interp_asm.cuh", "gen_interp.py"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -150,6 +150,12 @@ CMDX_HD constexpr uint32_t wd_word(int kind, int d, int s, int aux) {
 }
 
 // ---- launch parameters (passed by value as __grid_constant__) ---------------
+// Bits of a kernel's device error word: a bounded wait that gave up.
+constexpr uint32_t kErrConsumerWait = 1u << 0;  // data for a stage never arrived
+constexpr uint32_t kErrProducerWait = 1u << 1;  // a stage was never freed
+constexpr uint32_t kErrDrainWait = 1u << 2;     // copies still in flight at the stop never landed
+constexpr uint32_t kErrDebugWait = 1u << 3;     // the test hook's wait (nothing completes it)
+
 struct ContigParams {
   const void* in[kMaxLoads];
   void* out[kMaxStores];

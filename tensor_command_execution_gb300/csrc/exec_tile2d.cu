@@ -30,6 +30,7 @@
 // and op-set variant (CMDX_EXT): each object holds one kernel. The TMA
 // descriptors are encoded on the host (exec_host.cpp).
 #include "exec_common.cuh"
+#include "exec_pipe.cuh"
 #include "exec_tile2d.h"
 
 #if !defined(CMDX_TIER) || !defined(CMDX_ND) || !defined(CMDX_EXT)
@@ -43,42 +44,6 @@ namespace cmdx {
 
 static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
 
-// ---- mbarrier / TMA primitives (inline PTX) ----------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase of parity `parity` to complete, for at most timeout_ns.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > timeout_ns) return false;
-  }
-}
 // One box of a descriptor of rank 1..5 at coordinates c[0..rank).
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int rank, const int32_t (&c)[5],
                                          uint32_t bar) {
@@ -118,25 +83,6 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
 // A 64 x 64 box with 128-byte rows and the 128-byte swizzle keeps 16-byte
 // chunk c of row q at q*128 + ((c ^ (q % 8)) * 16); 4-byte views use two boxes
 // of 32 elements per row, the second 8 KB after the first.
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds16(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-
 __device__ __forceinline__ void xor_perm8(uint32_t (&y)[8], int c);
 
 // Transposed reads: logical (li, 8 cj + m) is element li of box row
@@ -201,11 +147,6 @@ __device__ __forceinline__ void read_trans(uint32_t (&x)[8], uint32_t stage, int
   for (int m = 0; m < 8; ++m) x[m] = y[m];
 }
 
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
 
 // y[m] = y[m ^ c] for a thread-constant c: conditional swaps of the pairs
 // that differ in bit 1, 2 and 4 of the index.

@@ -15,11 +15,6 @@ constexpr int kMaxStages = 4;
 constexpr int kBarrierBytes = 1024;   // barriers; stages start 1024-byte aligned
 constexpr int kBoxBytes = 8192;       // one 64-row box of 128-byte rows
 
-// error codes (bits of the error word)
-constexpr uint32_t kErrConsumerWait = 1u << 0;
-constexpr uint32_t kErrProducerWait = 1u << 1;
-constexpr uint32_t kErrDrainWait = 1u << 2;
-constexpr uint32_t kErrDebugWait = 1u << 3;
 
 struct Tile2dParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap maps[kMaxLoads];
