@@ -38,6 +38,7 @@ def _objs(tiers, nds=(None,)):
 
 CU_SOURCES = [("exec_tile2d.cu", _objs((2,), (0, 1))), ("exec_generic.cu", _objs((2,))),
               ("exec_contig.cu", _objs((2,))), ("exec_contig.cu", [dict(CMDX_TIER=0, CMDX_EXT=1, CMDX_OCC4=1)]),
+              ("exec_contig.cu", [dict(CMDX_TIER=1, CMDX_EXT=0, CMDX_HALF16=1)]),
               ("exec_tile2d.cu", _objs((1, 0), (0, 1))),
               ("exec_generic.cu", _objs((4, 3, 1, 0))), ("exec_contig.cu", _objs((4, 3, 1, 0))),
               ("static_scratch.cu", [{}])]

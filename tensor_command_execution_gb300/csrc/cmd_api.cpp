@@ -1458,7 +1458,9 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     // whole warp chunks on the contiguous executor; a head (the elements
     // before every pointer is vector-aligned) and a ragged tail (fewer than
     // one chunk of elements) on the generic one
-    const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended);
+    bool half2 = !pl.loads.empty();
+    for (const auto& v : pl.loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
+    const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended, half2);
     const int64_t head = pl.head;
     const int64_t n_main = (pl.n - head) - (pl.n - head) % chunk;
     // the generic executor over the 1-D elements [start, start + count),
@@ -1505,7 +1507,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n_loads = (uint32_t)pl.loads.size();
       bool bits_only = !pl.stores.empty();
       for (const auto& v : pl.stores) bits_only = bits_only && v.dtype == CMD_B1;
-      e = cmdx::contig_launch(P.tier, P.extended, p, stream, bits_only);
+      e = cmdx::contig_launch(P.tier, P.extended, p, stream, bits_only, half2);
     }
     // the tail from where the contiguous launch ends; with a head, head and
     // tail in one launch whose index space skips the contiguous launch's

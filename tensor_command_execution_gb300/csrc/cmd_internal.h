@@ -242,6 +242,9 @@ CMDX_DECL_OBJ(0, 1) CMDX_DECL_OBJ(1, 1) CMDX_DECL_OBJ(2, 1) CMDX_DECL_OBJ(3, 1) 
 // the extended 2-slot contiguous kernel built for four CTAs per SM
 cudaError_t contig_upload_t0e1o4(int slot, const uint32_t* words, int n);
 cudaError_t contig_launch_t0e1o4(const ContigParams& p, cudaStream_t stream);
+// the base 4-slot contiguous kernel at 16 elements per slot (2-byte loads)
+cudaError_t contig_upload_t1e0h16(int slot, const uint32_t* words, int n);
+cudaError_t contig_launch_t1e0h16(const ContigParams& p, cudaStream_t stream);
 
 // Write a compiled program into slot `slot` of every executor object of its
 // tier and variant (ext: the program uses an extended op or store).
@@ -251,8 +254,11 @@ cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, 
 // far more than they write, and the extended 2-slot tier runs them on its
 // four-CTA build: measured, threshold_bits +12%, while one-word-per-element
 // stores ran 1-6% slower there).
-cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream, bool bits_only = false);
-int contig_chunk(int tier, bool ext);
+// half2: every load of the program is 2-byte (f16 or bf16); the base 4-slot
+// tier then runs its 16-element build (its chunk is 512 elements).
+cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream, bool bits_only = false,
+                          bool half2 = false);
+int contig_chunk(int tier, bool ext, bool half2 = false);
 cudaError_t tile2d_launch(int tier, bool ext, const Tile2dLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int tier, bool ext, const GenericParams& p, cudaStream_t stream);
 

@@ -30,12 +30,19 @@
 #define CMDX_TIER_CAT2(a, b) a##b
 #define CMDX_TIER_CAT(a, b) CMDX_TIER_CAT2(a, b)
 // An object built with CMDX_OCC4=1 (a contiguous kernel sized for four
-// resident CTAs per SM) appends o4.
+// resident CTAs per SM) appends o4; one built with CMDX_HALF16=1 (the
+// contiguous 4-slot kernel at 16 elements per slot, for programs whose loads
+// are all 2-byte) appends h16.
 #ifndef CMDX_OCC4
 #define CMDX_OCC4 0
 #endif
+#ifndef CMDX_HALF16
+#define CMDX_HALF16 0
+#endif
 #if CMDX_OCC4
 #define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), e), CMDX_EXT), o4)
+#elif CMDX_HALF16
+#define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), e), CMDX_EXT), h16)
 #else
 #define CMDX_TIER_NAME(f) CMDX_TIER_CAT(CMDX_TIER_CAT(CMDX_TIER_CAT(f, CMDX_TIER), e), CMDX_EXT)
 #endif

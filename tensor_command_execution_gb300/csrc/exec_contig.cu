@@ -14,10 +14,20 @@
 #if !defined(CMDX_TIER) || !defined(CMDX_EXT)
 #error "exec_contig.cu is compiled per tier and variant, with -DCMDX_TIER=<0..4> -DCMDX_EXT=<0|1>"
 #endif
+#if CMDX_HALF16 && (CMDX_TIER != 1 || CMDX_EXT != 0)
+#error "the 16-element build (CMDX_HALF16) is of the base 4-slot tier only"
+#endif
 
 namespace cmdx {
 
 static __constant__ uint32_t c_prog[kMaxPrograms][kMaxWords];
+
+// Elements per slot per thread of this object's kernel: the tier's, or 16
+// in the CMDX_HALF16 build of the 4-slot tier (2-byte values carry half the
+// bytes per element, so the interpreter's per-chunk cost is spread over
+// twice the elements; measured, the bf16 chain Command +8%, while the fp32
+// one loses 3% at 16).
+CMDX_HD constexpr int contig_vec(int tier, bool ext) { return CMDX_HALF16 ? 16 : tier_vec(tier, ext); }
 
 // Load one slot (V elements per lane) of a dense tensor of type dt. 2-byte
 // types arrive packed, two to a word, in x[0 .. V/2); contig_widen expands
@@ -151,7 +161,7 @@ struct ContigStore {
 template <int TIER, bool EXT, int MINB>
 __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant__ ContigParams p) {
   constexpr int S = tier_slots(TIER);
-  constexpr int V = tier_vec(TIER, EXT);
+  constexpr int V = contig_vec(TIER, EXT);
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
   using M = LaneMap<V>;
   const int lane = threadIdx.x & 31;
@@ -212,7 +222,7 @@ cudaError_t CMDX_TIER_NAME(contig_upload_t)(int slot, const uint32_t* words, int
 template <int TIER, bool EXT>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   constexpr int MINB = CMDX_OCC4 ? 4 : tier_min_blocks(TIER);
-  constexpr int V = tier_vec(TIER, EXT);
+  constexpr int V = contig_vec(TIER, EXT);
   constexpr int kBlock = 256;
   static DeviceCache grid_cache;  // (static storage: zero before first use)
   int dev = 0;

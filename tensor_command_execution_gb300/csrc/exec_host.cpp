@@ -9,7 +9,10 @@
 
 namespace cmdx {
 
-int contig_chunk(int tier, bool ext) { return 32 * tier_vec(tier, ext); }
+// the base 4-slot tier's 16-element build serves programs whose loads are all 2-byte
+static bool half16(int tier, bool ext, bool half2) { return half2 && tier == kTier4 && !ext; }
+
+int contig_chunk(int tier, bool ext, bool half2) { return 32 * (half16(tier, ext, half2) ? 16 : tier_vec(tier, ext)); }
 
 namespace {
 
@@ -56,13 +59,16 @@ cudaError_t upload_program(int tier, bool ext, int slot, const uint32_t* words, 
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
   cudaError_t e = kContigUpload[ext][tier](slot, words, n);
   if (e == cudaSuccess && ext && tier == kTier2) e = contig_upload_t0e1o4(slot, words, n);
+  if (e == cudaSuccess && !ext && tier == kTier4) e = contig_upload_t1e0h16(slot, words, n);
   if (e == cudaSuccess) e = kGenericUpload[ext][tier](slot, words, n);
   for (int nd = 0; nd < 2 && e == cudaSuccess && !tier_wide(tier); ++nd) e = kTileUpload[ext][nd][tier](slot, words, n);
   return e;
 }
 
-cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream, bool bits_only) {
+cudaError_t contig_launch(int tier, bool ext, const ContigParams& p, cudaStream_t stream, bool bits_only,
+                          bool half2) {
   if (!tier_ok(tier)) return cudaErrorInvalidValue;
+  if (half16(tier, ext, half2)) return contig_launch_t1e0h16(p, stream);
   if (ext && tier == kTier2 && bits_only) return contig_launch_t0e1o4(p, stream);
   return kContigLaunch[ext][tier](p, stream);
 }

@@ -34,6 +34,8 @@ pytestmark = pytest.mark.gpu
     (W.threshold_u32((1 << 18) + 13), "contig"),
     (W.threshold_bits((1 << 18) + 13), "contig"),
     (W.threshold_bits(77), "contig"),
+    (W.chain_bf16((1 << 18) + 7), "contig"),
+    (W.chain_bf16(511), "contig"),
     (W.tile4_f32(132, 72), "tile2d"),
     (W.wide32_f32((1 << 16) + 7), "contig"),
 ], ids=lambda x: x["name"] + str(x["sizes"]) if isinstance(x, dict) else x)
