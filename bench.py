@@ -238,8 +238,8 @@ class Workload:
         info = self.kernel.info()
         # elements per warp chunk of the contiguous executor: 32 x (elements per slot per thread)
         half2 = all(self.dts[n] in ("f16", "bf16") for n in W.load_names(spec))
-        per_slot = {3: 2, 4: 4}.get(info["tier"], 16 if ((info["tier"] == 0 and info["extended"]) or
-                                                         (info["tier"] == 1 and not info["extended"] and half2)) else 8)
+        per_slot = {0: 16, 3: 2, 4: 4}.get(info["tier"], 16 if (info["tier"] == 1 and not info["extended"] and half2)
+                                           else 8)
         chunk = 32 * per_slot
         self.launches_per_step = 1 + (1 if (self.plan["path"] == "contig" and self.elements % chunk != 0) else 0)
 

@@ -33,21 +33,18 @@ CMDX_HD constexpr int tier_slots(int tier) {
 }
 // The wide encoding (wd_word) and the two-level dispatch serve these tiers.
 CMDX_HD constexpr bool tier_wide(int tier) { return tier == kTier16 || tier == kTier32; }
-// Elements each thread keeps per slot in the contiguous executor: 8 in the
-// fused tiers and 2 in the 32-slot one, except 16 in the extended variant of
-// the 2-slot tier, whose programs (divisions, comparisons, packed-bit stores)
-// do more work per program word: the wider vector spreads each word's
-// dispatch over more elements (measured: packed-bit threshold +22 %), while
-// plain 2-slot programs run faster at the higher occupancy of 8.
+// Elements each thread keeps per slot in the contiguous executor: 16 in the
+// 2-slot tier, 8 in the 4- and 8-slot tiers (16 in a second build of the
+// base 4-slot tier, for programs whose loads are all 2-byte), 4 in the
+// 16-slot tier and 2 in the 32-slot one. More elements per slot spread each
+// program word's dispatch over more elements; fewer keep more CTAs
+// resident. Measured for the 2-slot tier (A/B on one box, against 8 elements
+// with the next chunk's loads prefetched in registers): bf16 add +8.7%,
+// bf16 scale +17%, the 2^20-element fp32 add +16%, fp32 at 2^26-2^27
+// within 1%; for its extended programs: packed-bit threshold +22%.
 CMDX_HD constexpr int tier_vec(int tier, bool ext) {
-  return tier == kTier32 ? 2 : tier == kTier16 ? 4 : (tier == kTier2 && ext) ? 16 : 8;
+  return tier == kTier2 ? 16 : tier == kTier32 ? 2 : tier == kTier16 ? 4 : 8;
 }
-// Whether the contiguous executor prefetches the next chunk's loads while
-// the program runs on the current one: in the base variant of the 2-slot
-// tier, whose one or two loads leave few bytes in flight per thread
-// otherwise (measured: two-load add +4.6 %; the extended variant's wider
-// vector serves it better, and its registers leave no room for both).
-CMDX_HD constexpr bool contig_prefetch(int tier, bool ext) { return tier == kTier2 && !ext; }
 // ... and in the generic executor, whose addressing needs more registers:
 // 8, and 4 in the 8-slot tier.
 CMDX_HD constexpr int tier_vec_strided(int tier) {

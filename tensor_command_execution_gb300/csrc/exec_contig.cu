@@ -171,47 +171,17 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
   int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   pdl_wait();
   pdl_trigger();
-  if constexpr (contig_prefetch(TIER, EXT)) {
-    // software pipeline: the next chunk's loads are issued before the
-    // program runs on this one, so their latency overlaps its work and
-    // stores (the base 2-slot tier has the registers for a second set)
-    uint32_t nx[NL][V];
-    if (w < n_chunks) {
+  for (; w < n_chunks; w += nwarps) {
+    const int64_t e0 = w * M::W + (int64_t)lane * M::G;
+    uint32_t r[S][V];
 #pragma unroll
-      for (int j = 0; j < NL; ++j)
-        if (j < (int)p.n_loads) contig_load<V>(nx[j], p.in[j], p.in_dt[j], w * M::W + (int64_t)lane * M::G);
-    }
-    for (; w < n_chunks; w += nwarps) {
-      const int64_t e0 = w * M::W + (int64_t)lane * M::G;
-      uint32_t r[S][V];
+    for (int j = 0; j < NL; ++j)
+      if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
 #pragma unroll
-      for (int j = 0; j < NL; ++j)
-#pragma unroll
-        for (int v = 0; v < V; ++v) r[j][v] = nx[j][v];
-      if (w + nwarps < n_chunks) {
-#pragma unroll
-        for (int j = 0; j < NL; ++j)
-          if (j < (int)p.n_loads) contig_load<V>(nx[j], p.in[j], p.in_dt[j], e0 + nwarps * M::W);
-      }
-#pragma unroll
-      for (int j = 0; j < NL; ++j)
-        if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
-      ContigStore<V> st{p, e0};
-      run_program<TIER, V, EXT>(r, prog, p.scal, st);
-    }
-  } else {
-    for (; w < n_chunks; w += nwarps) {
-      const int64_t e0 = w * M::W + (int64_t)lane * M::G;
-      uint32_t r[S][V];
-#pragma unroll
-      for (int j = 0; j < NL; ++j)
-        if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
-#pragma unroll
-      for (int j = 0; j < NL; ++j)
-        if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
-      ContigStore<V> st{p, e0};
-      run_program<TIER, V, EXT>(r, prog, p.scal, st);
-    }
+    for (int j = 0; j < NL; ++j)
+      if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
+    ContigStore<V> st{p, e0};
+    run_program<TIER, V, EXT>(r, prog, p.scal, st);
   }
 }
 
