@@ -4,9 +4,12 @@
 // A program word selects one case of a jump table whose slot numbers are
 // fixed in the code, so slots never need run-time register indexing (which
 // would spill them to local memory). All threads of a launch run the same
-// program, so the dispatch branch is warp-uniform. In the 4- and 8-slot
-// tiers the loop is inline PTX (interp_asm.cuh, generated): each case updates
-// its destination registers in place and the dispatch moves no data.
+// program, so the dispatch branch is warp-uniform. The loop is inline PTX
+// (interp_asm.cuh, generated): in the 2-, 4- and 8-slot tiers one jump per
+// word on (op, destination, source), each case updating its destination's
+// registers in place, so the dispatch moves no data; in the 16- and 32-slot
+// tiers two jumps per word, the first copying the source slot into staging
+// registers, the second applying the op to the destination.
 //
 // rocRoller, "Design Overview": the program plays the part of the scheduled
 // instructions generated from the KernelGraph (sections "Generating

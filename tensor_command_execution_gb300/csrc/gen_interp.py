@@ -30,6 +30,14 @@ comparison and select cases; in the base variant those cases exit like the
 end word, so its loop carries none of their code (the host runs a program
 on the base variant only when it has none of them).
 
+The wide tiers (16 and 32 slots, the wide encoding of cmd_internal.h) are
+emitted once each (gen_wide): a fused table would need S^2 cases per op
+(for 16 slots about 7000, which took minutes to compile), so each word
+takes two jumps, the first on the source slot (copying it, or a broadcast
+scalar, into V staging registers), the second on (op, destination). Only
+the arithmetic, min/max and unary words run there; every other word leaves
+the loop for the caller.
+
 Run: python gen_interp.py  (writes interp_asm.cuh next to this file)
 """
 from __future__ import annotations
