@@ -152,9 +152,14 @@ typedef struct cmd_xop {
   cmd_tag c;
 } cmd_xop;
 
-/* Runtime argument of a Load_Tensor or Store_Tensor tag: a device pointer and
- * the view. sizes are the logical sizes (equal for every tensor of the
- * Command); strides are in elements, >= 0, one per logical dim. */
+/* Runtime argument of a Load_Tensor or Store_Tensor tag: a pointer the GPU
+ * can address and the view. sizes are the logical sizes (equal for every
+ * tensor of the Command); strides are in elements, >= 0, one per logical dim.
+ * The pointer is device memory, or pinned (page-locked) host memory from
+ * cudaHostAlloc / cudaHostRegister, whose address is valid on the device
+ * under unified addressing: the kernel then reads and writes it across the
+ * host link itself, with no separate copy (on a Grace host, the coherent
+ * CPU-GPU link). Pageable host memory is not accepted by this contract. */
 typedef struct cmd_tensor_arg {
   cmd_tag tag;
   int32_t rank;
@@ -339,7 +344,9 @@ cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* nee
 /* ---- launching --------------------------------------------------------- */
 
 /* Validate args against the kernel and report the executor it would use,
- * without touching the GPU. */
+ * without touching the GPU (and so without looking at where the memory lies:
+ * cmd_launch runs a CMD_PATH_TILE2D plan on the generic executor when a load
+ * is in pinned host memory). */
 cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_launch_plan* plan);
 
 /* Validate args and enqueue one fused pass on stream cuda_stream (a
@@ -348,7 +355,10 @@ cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_lau
  * and Load_Scalar tag needs exactly one argument; arguments for dead tags may
  * be omitted. Stores must not overlap any other tensor argument (an identical
  * view of the same element type, used in place, is allowed) and must not
- * overlap themselves. Returns after the launch is enqueued (asynchronous). A
+ * overlap themselves. Tensors may lie in pinned host memory (see
+ * cmd_tensor_arg); views that would take the tile executor then run on the
+ * generic one, since the tile executor's TMA copies are issued on device
+ * memory only. Returns after the launch is enqueued (asynchronous). A
  * launch with zero elements does nothing. Safe to capture in a CUDA graph. */
 cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_stream);
 

@@ -1452,6 +1452,22 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     return fail(CMD_ERR_NOMEM, "out of host memory");
   }
   if (pl.path == CMD_PATH_NONE) return CMD_OK;
+  // A load in pinned host memory never takes the tile executor, whose loads
+  // are TMA copies that this library issues on device memory only; the
+  // generic executor reads the same views with plain loads.
+  if (pl.path == CMD_PATH_TILE2D) {
+    for (const View& v : pl.loads) {
+      cudaPointerAttributes a;
+      if (cudaPointerGetAttributes(&a, v.ptr) != cudaSuccess) {
+        cudaGetLastError();  // (an unknown pointer: left to the launch)
+        continue;
+      }
+      if (a.type == cudaMemoryTypeHost) {
+        pl.path = CMD_PATH_GENERIC;
+        break;
+      }
+    }
+  }
   const Program& P = k->prog;
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   if (pl.path == CMD_PATH_CONTIG) {
