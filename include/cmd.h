@@ -207,7 +207,11 @@ typedef enum cmd_path {
   CMD_PATH_NONE = 0,    /* nothing to do (no elements or no stores) */
   CMD_PATH_CONTIG = 1,  /* every view dense row-major and aligned, or all off the vector
                            alignment by one number of elements (the few elements before
-                           they align run per element): vector loads/stores */
+                           they align run per element): vector loads/stores. With
+                           merged_rank 2: rows, every view unit-stride along the columns,
+                           each row starting on a 4-element boundary (a load's row stride
+                           may be 0) and a whole number of warp chunks long (padded or
+                           sliced row-major tensors) */
   CMD_PATH_TILE2D = 2,  /* 2-D views, row-direct or transposed, staged through shared memory */
   CMD_PATH_GENERIC = 3  /* any other sizes/strides: per-element offsets */
 } cmd_path;

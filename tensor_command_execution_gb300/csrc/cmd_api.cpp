@@ -603,6 +603,9 @@ struct Plan {
   // contiguous path: elements before the first one at which every pointer is
   // aligned for the vector width (they run on the generic executor)
   int64_t head = 0;
+  // contiguous path over rows (two merged dims, each view unit-stride along
+  // the inner one): the row count; 0 for one dense range
+  int64_t rows = 0;
   int mrank = 0;
   int64_t msizes[cmdx::kMaxRank] = {1, 1, 1, 1};
   std::vector<View> loads, stores;       // in slot / output order
@@ -881,6 +884,28 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
     if (same && phase > 0 && pl->n > 4 - phase) {
       pl->path = CMD_PATH_CONTIG;
       pl->head = 4 - phase;
+      return CMD_OK;
+    }
+  }
+  // Rows: two merged dims, every view unit-stride along the inner (column)
+  // one, each row starting on the vector alignment (a base and a row stride
+  // of whole 4-element vectors; a load's row stride may be 0, one row read
+  // for every row), and rows a whole number of the contiguous executor's
+  // warp chunks long, so that no chunk crosses a row: the contiguous kernel
+  // then walks (row, chunk) pairs. Padded and sliced row-major tensors
+  // (x[:, :n] of a wider x) take it. (Not with packed bits.)
+  if (m == 2 && !any_b1) {
+    bool half2 = !pl->loads.empty();
+    for (const auto& v : pl->loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
+    const int64_t W = cmdx::contig_chunk(P.tier, P.extended, half2);
+    bool rows_ok = ms[1] % W == 0 && ms[0] < (int64_t(1) << 30) && ms[1] / W < (int64_t(1) << 30);
+    for (size_t i = 0; i < all.size() && rows_ok; ++i) {
+      const int es = elem_size(all[i]->dtype);
+      if (wst[i][1] != 1 || wst[i][0] % 4 != 0 || !aligned(all[i]->ptr, 4 * es)) rows_ok = false;
+    }
+    if (rows_ok) {
+      pl->path = CMD_PATH_CONTIG;
+      pl->rows = ms[0];
       return CMD_OK;
     }
   }
@@ -1478,7 +1503,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     for (const auto& v : pl.loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
     const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended, half2);
     const int64_t head = pl.head;
-    const int64_t n_main = (pl.n - head) - (pl.n - head) % chunk;
+    const int64_t n_main = (pl.n - head) - (pl.n - head) % chunk;  // (all of it over rows)
     // the generic executor over the 1-D elements [start, start + count),
     // skipping [start + gap_at, start + gap_at + gap)
     auto generic_range = [&](int64_t start, int64_t count, int64_t gap_at, int64_t gap) -> cudaError_t {
@@ -1521,6 +1546,14 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       p.n = n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
+      if (pl.rows > 1) {
+        // merged dims are right-aligned: the row dim is the second to last
+        const int rd = cmdx::kMaxRank - 2;
+        p.rows = (int32_t)pl.rows;
+        p.row_chunks = (int32_t)(pl.msizes[rd + 1] / chunk);
+        for (size_t j = 0; j < pl.loads.size(); ++j) p.in_ld[j] = pl.ml[j][rd];
+        for (size_t j = 0; j < pl.stores.size(); ++j) p.out_ld[j] = pl.ms[j][rd];
+      }
       bool bits_only = !pl.stores.empty();
       for (const auto& v : pl.stores) bits_only = bits_only && v.dtype == CMD_B1;
       e = cmdx::contig_launch(P.tier, P.extended, p, stream, bits_only, half2);

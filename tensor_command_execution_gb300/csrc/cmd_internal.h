@@ -161,6 +161,14 @@ struct ContigParams {
   uint32_t prog;         // program slot in constant memory
   uint32_t n_loads;
   uint8_t in_dt[kMaxLoads];
+  // Row-contiguous launches (rows > 1): the elements are `rows` rows of
+  // row_chunks warp chunks each (n = rows * row_chunks * 32 * V); row r of a
+  // view starts r * ld elements after its base (ld = 0: one row read for
+  // every row). One dense range otherwise (rows = 1, the ld unused).
+  int32_t rows;
+  int32_t row_chunks;
+  int64_t in_ld[kMaxLoads];
+  int64_t out_ld[kMaxStores];
 };
 
 // What the tile executor needs from the host. The logical index space is

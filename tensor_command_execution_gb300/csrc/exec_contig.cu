@@ -79,15 +79,23 @@ __device__ __forceinline__ void contig_widen(uint32_t (&x)[V], int dt) {
   }
 }
 
-template <int V>
+// A view's row `row` (row-contiguous launches; row 0 is the base).
+__device__ __forceinline__ const void* row_start(const void* base, int64_t row, int64_t ld, int dt) {
+  return static_cast<const char*>(base) + row * ld * ((dt == 0 || dt == 3) ? 4 : 2);
+}
+
+template <int V, bool ROWS>
 struct ContigStore {
   const ContigParams& p;
   int64_t e0;
+  int64_t row;  // (row-contiguous launches)
 
   template <int T>
   __device__ __forceinline__ void store(const uint32_t (&x)[V], uint32_t o) const {
     using M = LaneMap<V>;
     void* base = p.out[o];
+    if constexpr (ROWS && T != kStB1)  // (packed-bit stores never take rows)
+      base = static_cast<char*>(base) + row * p.out_ld[o] * ((T == kStF32 || T == kStI32) ? 4 : 2);
     if constexpr (T == kStB1) {
       // one bit per element (min(x, 1) is 1 exactly when x != 0)
       constexpr int G = M::G, L = 32 / G;
@@ -156,32 +164,60 @@ struct ContigStore {
   }
 };
 
-// MINB: resident CTAs per SM the registers are sized for (one object of the
-// extended 2-slot tier is built for 4 instead of 3, for packed-bit programs)
-template <int TIER, bool EXT, int MINB>
-__global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant__ ContigParams p) {
+// One warp chunk: elements e0 .. of each view (of its row `row` when ROWS).
+template <int TIER, bool EXT, bool ROWS>
+__device__ __forceinline__ void contig_run_chunk(const ContigParams& p, const uint32_t* prog, int64_t e0,
+                                                 int64_t row) {
   constexpr int S = tier_slots(TIER);
   constexpr int V = contig_vec(TIER, EXT);
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
+  uint32_t r[S][V];
+#pragma unroll
+  for (int j = 0; j < NL; ++j)
+    if (j < (int)p.n_loads) {
+      const void* b = p.in[j];
+      if constexpr (ROWS) b = row_start(b, row, p.in_ld[j], p.in_dt[j]);
+      contig_load<V>(r[j], b, p.in_dt[j], e0);
+    }
+#pragma unroll
+  for (int j = 0; j < NL; ++j)
+    if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
+  ContigStore<V, ROWS> st{p, e0, row};
+  run_program<TIER, V, EXT>(r, prog, p.scal, st);
+}
+
+// MINB: resident CTAs per SM the registers are sized for (one object of the
+// extended 2-slot tier is built for 4 instead of 3, for packed-bit programs).
+// ROWS: a row-contiguous launch; warp w takes chunk w % row_chunks of row
+// w / row_chunks, the pair stepped by the grid's warp count with a carry
+// instead of dividing per chunk.
+template <int TIER, bool EXT, int MINB, bool ROWS>
+__global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant__ ContigParams p) {
+  constexpr int V = contig_vec(TIER, EXT);
   using M = LaneMap<V>;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t* prog = c_prog[p.prog];
-  const int64_t n_chunks = p.n / M::W;  // the host passes a multiple of W
   int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   pdl_wait();
   pdl_trigger();
-  for (; w < n_chunks; w += nwarps) {
-    const int64_t e0 = w * M::W + (int64_t)lane * M::G;
-    uint32_t r[S][V];
-#pragma unroll
-    for (int j = 0; j < NL; ++j)
-      if (j < (int)p.n_loads) contig_load<V>(r[j], p.in[j], p.in_dt[j], e0);
-#pragma unroll
-    for (int j = 0; j < NL; ++j)
-      if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
-    ContigStore<V> st{p, e0};
-    run_program<TIER, V, EXT>(r, prog, p.scal, st);
+  if constexpr (!ROWS) {
+    const int64_t n_chunks = p.n / M::W;  // the host passes a multiple of W
+    for (; w < n_chunks; w += nwarps) contig_run_chunk<TIER, EXT, false>(p, prog, w * M::W + (int64_t)lane * M::G, 0);
+  } else {
+    // rows and row_chunks are below 2^31, and so is the grid's warp count
+    const int rc = p.row_chunks;
+    int row = (int)(w / rc), c = (int)(w % rc);
+    const int drow = (int)(nwarps / rc), dc = (int)(nwarps % rc);
+    while (row < p.rows) {
+      contig_run_chunk<TIER, EXT, true>(p, prog, (int64_t)c * M::W + (int64_t)lane * M::G, row);
+      c += dc;
+      row += drow;
+      if (c >= rc) {
+        c -= rc;
+        ++row;
+      }
+    }
   }
 }
 
@@ -189,9 +225,11 @@ cudaError_t CMDX_TIER_NAME(contig_upload_t)(int slot, const uint32_t* words, int
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
-template <int TIER, bool EXT>
+template <int TIER, bool EXT, bool ROWS>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
-  constexpr int MINB = CMDX_OCC4 ? 4 : tier_min_blocks(TIER);
+  // (the 2-slot tier's dense-range kernel fits 64 registers and so runs four
+  // CTAs per SM; its row-walking one is held to the same)
+  constexpr int MINB = (CMDX_OCC4 || (ROWS && TIER == kTier2 && !EXT)) ? 4 : tier_min_blocks(TIER);
   constexpr int V = contig_vec(TIER, EXT);
   constexpr int kBlock = 256;
   static DeviceCache grid_cache;  // (static storage: zero before first use)
@@ -200,15 +238,16 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = grid_cache.get(dev);
   if (full_grid == 0) {
-    full_grid = persistent_grid(contig_kernel<TIER, EXT, MINB>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(contig_kernel<TIER, EXT, MINB, ROWS>, kBlock, 0, INT64_MAX);
     grid_cache.put(dev, full_grid);
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  return launch_pdl(contig_kernel<TIER, EXT, MINB>, grid, kBlock, 0, stream, p);
+  return launch_pdl(contig_kernel<TIER, EXT, MINB, ROWS>, grid, kBlock, 0, stream, p);
 }
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
-  return launch_tier<CMDX_TIER, CMDX_EXT != 0>(p, stream);
+  if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);
+  return launch_tier<CMDX_TIER, CMDX_EXT != 0, false>(p, stream);
 }
 
 }  // namespace cmdx

@@ -565,7 +565,11 @@ def test_nd_views_on_the_tile_executor(dt, case, sizes):
     plan = gpuutil.parity(spec, bufs)
     es = 2 if dt == "bf16" else 4
     aligned = all((s * es) % 16 == 0 for s in (B, R, C, R * C))
-    if case in ("batched_transpose", "padded_batched", "batch_broadcast", "row_broadcast", "col_broadcast") \
+    if case == "batch_broadcast" and aligned and (R * C) % 512 == 0:
+        # (row, column) merge into rows of R * C elements, whole warp chunks
+        # of the 2-slot tier: A's rows are one row read for every batch
+        assert plan["path"] == "contig" and plan["merged_rank"] == 2, plan
+    elif case in ("batched_transpose", "padded_batched", "batch_broadcast", "row_broadcast", "col_broadcast") \
             and aligned:
         assert plan["path"] == "tile2d", plan
     if case == "perm_210" and aligned and (B * es) % 16 == 0:

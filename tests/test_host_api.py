@@ -279,6 +279,39 @@ def test_padded_rows_and_permutations_use_the_tile_path():
     assert p["path"] == "generic" and p["merged_rank"] == 3
 
 
+def test_padded_rows_whole_chunks_long_take_the_contiguous_executor():
+    """Two merged dims, every view unit-stride along the columns, row starts
+    on 4-element boundaries, and rows a whole number of warp chunks long
+    (512 elements for the two-input add's 2-slot tier): contiguous, merged
+    rank 2. A row length that is not, a row stride off the boundary, a
+    transposed load or a packed-bit store keep the other paths."""
+    spec = W.add_f32(0)
+    spec["sizes"] = (64, 1024)
+    spec["views"] = {"x": dict(strides=(1032, 1), alloc=64 * 1032), "y": dict(strides=(1024 + 64, 1), alloc=64 * 1088),
+                     "out": dict(strides=(1028, 1), alloc=64 * 1028)}
+    p = _plan(spec)
+    assert p["path"] == "contig" and p["merged_rank"] == 2 and p["merged_sizes"] == [64, 1024]
+    spec["views"]["y"] = dict(strides=(0, 1), alloc=1024)       # one row read for every row
+    assert _plan(spec)["path"] == "contig"
+    spec["sizes"] = (64, 768)                                     # 1.5 chunks per row
+    assert _plan(spec)["path"] == "tile2d"
+    spec["sizes"] = (64, 1024)
+    spec["views"]["x"] = dict(strides=(1030, 1), alloc=64 * 1030)  # rows 8 bytes off the 16-byte boundary
+    assert _plan(spec)["path"] == "generic"
+    spec["views"]["x"] = dict(strides=(1, 64), alloc=64 * 1024)    # transposed
+    assert _plan(spec)["path"] == "tile2d"
+    # the chain Command's 4-slot tier has 256-element chunks
+    ch = W.chain_f32(0)
+    ch["sizes"] = (10, 768)
+    ch["views"] = {k: dict(strides=(800, 1), alloc=10 * 800) for k in ("a", "b", "c", "out")}
+    p = _plan(ch)
+    assert p["path"] == "contig" and p["merged_rank"] == 2
+    bits = W.threshold_bits(0)
+    bits["sizes"] = (8, 1024)
+    bits["views"] = {"x": dict(strides=(1040, 1), alloc=8 * 1040), "bits": dict(strides=(1024, 1), alloc=256)}
+    assert _plan(bits)["path"] != "contig"
+
+
 def test_unaligned_pointer_falls_back_to_generic():
     assert _plan(W.add_f32(4096), ptrs={"x": BASE + (1 << 28) + 4})["path"] == "generic"
 
