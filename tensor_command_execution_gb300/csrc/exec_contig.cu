@@ -199,6 +199,34 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t* prog = c_prog[p.prog];
   int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if constexpr (!EXT) {
+    // A launch of at most one chunk per warp (a small one) cannot pipeline
+    // its loads, so it would take the DRAM latency after the wait for the
+    // previous launch. Its warps ask L2 for their chunk of every load
+    // first: a prefetch returns nothing to the thread, and L2 is where
+    // every SM's accesses meet, so a line that the previous launch writes
+    // afterwards is updated there and never read stale.
+    const int64_t n_chunks = ROWS ? (int64_t)p.rows * p.row_chunks : p.n / M::W;
+    if (n_chunks <= nwarps && w < n_chunks) {
+      int64_t e_first = w * M::W, row0 = 0;
+      if constexpr (ROWS) {
+        row0 = w / p.row_chunks;
+        e_first = (w - row0 * p.row_chunks) * M::W;
+      }
+      e_first += (int64_t)lane * M::G;
+#pragma unroll
+      for (int j = 0; j < kMaxLoads; ++j)
+        if (j < (int)p.n_loads) {
+          const void* b = p.in[j];
+          if constexpr (ROWS) b = row_start(b, row0, p.in_ld[j], p.in_dt[j]);
+          const int es = (p.in_dt[j] == 0 || p.in_dt[j] == 3) ? 4 : 2;
+#pragma unroll
+          for (int h = 0; h < M::NG; ++h)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(b) +
+                                                          (e_first + (int64_t)h * 32 * M::G) * es));
+        }
+    }
+  }
   pdl_wait();
   pdl_trigger();
   if constexpr (!ROWS) {

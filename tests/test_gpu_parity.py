@@ -1136,7 +1136,7 @@ def test_kernel_from_text_form(spec):
 
 
 @pytest.mark.parametrize("n,path", [(1 << 20, "contig"), (5000, "contig"), (3 * 64 * 96, "tile2d"),
-                                    (4099, "generic")])
+                                    (4099, "generic"), (64 * 1024, "rows")])
 def test_back_to_back_dependent_launches(n, path):
     """Launches may begin while the previous kernel on the stream runs
     (programmatic dependent launch), but each waits for it before touching
@@ -1146,6 +1146,8 @@ def test_back_to_back_dependent_launches(n, path):
     rng = np.random.default_rng(n)
     if path == "tile2d":
         sizes, st_x = (3, 64, 96), (64 * 96, 1, 64)  # x read through a transposed view
+    elif path == "rows":
+        sizes, st_x = (64, 1024), (1040, 1)  # x's rows padded: the contiguous executor walks rows
     else:
         sizes, st_x = (n,), (1,)
     dense = W._dense(sizes)[0]
@@ -1154,6 +1156,11 @@ def test_back_to_back_dependent_launches(n, path):
         big = torch.empty(n + 1, dtype=torch.int32, device="cuda")
         big[1:].copy_(x)
         x = big[1:]
+    pad = None
+    if path == "rows":
+        pad = torch.full((64, 1040), -5, dtype=torch.int32, device="cuda")
+        pad[:, :1024].copy_(x.view(64, 1024))
+        x = pad.view(-1)
     y = torch.empty(n, dtype=torch.int32, device="cuda")
     # A: y = x * x + k (reads x, writes y);  B: x = -y (reads y, overwrites x)
     ca = T.Command()
@@ -1170,8 +1177,8 @@ def test_back_to_back_dependent_launches(n, path):
     vy = T.TensorView(y.data_ptr(), sizes, dense)
     args_a = ka_k.args({xa: vx, ya: vy}, {ka: 7})
     args_b = kb_k.args({yb: vy, xb: vx}, {})
-    assert ka_k.plan({xa: vx, ya: vy}, {ka: 7})["path"] == path
-    host = x.cpu().numpy().astype(np.int64)
+    assert ka_k.plan({xa: vx, ya: vy}, {ka: 7})["path"] == ("contig" if path == "rows" else path)
+    host = (pad[:, :1024].reshape(-1) if pad is not None else x).cpu().numpy().astype(np.int64)
     stream = torch.cuda.current_stream().cuda_stream
     for _ in range(12):
         ka_k.launch_args(args_a, stream)
@@ -1179,6 +1186,11 @@ def test_back_to_back_dependent_launches(n, path):
         yv = (host * host + 7) % 2**32                 # A, modulo 2^32
         host = ((-yv) % 2**32 + 2**31) % 2**32 - 2**31  # B, back to int32
     torch.cuda.synchronize()
+    if pad is not None:
+        # the view's elements follow the recurrence; the row padding is untouched
+        assert (pad[:, :1024].cpu().numpy().reshape(-1) == host.astype(np.int32)).all()
+        assert (pad[:, 1024:].cpu().numpy() == -5).all()
+        return
     # every physical element of x follows the same recurrence (a view is a
     # permutation of its buffer), so the buffers compare directly
     assert (x.cpu().numpy() == host.astype(np.int32)).all()
