@@ -606,6 +606,9 @@ struct Plan {
   // contiguous path over rows (two merged dims, each view unit-stride along
   // the inner one): the row count; 0 for one dense range
   int64_t rows = 0;
+  // contiguous path with loads off the stores' vector alignment (1-D): the
+  // head then ends where the stores align, 4 elements further on
+  bool shifted = false;
   int mrank = 0;
   int64_t msizes[cmdx::kMaxRank] = {1, 1, 1, 1};
   std::vector<View> loads, stores;       // in slot / output order
@@ -884,6 +887,33 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
     if (same && phase > 0 && pl->n > 4 - phase) {
       pl->path = CMD_PATH_CONTIG;
       pl->head = 4 - phase;
+      return CMD_OK;
+    }
+  }
+  // Shifted: one merged unit-stride dim whose stores all sit the same number
+  // of elements off the vector alignment while some loads sit off it by
+  // other numbers (x[1:] - x[:-1], say). The head runs up to where the
+  // stores align, plus 4 elements; from there each load is read as aligned
+  // vectors from up to 3 elements before it, each lane taking the end of its
+  // elements from its right neighbour, and a tail of at least 4 elements is
+  // left, so that those vectors stay inside the views. (The 2- and 4-slot
+  // tiers, whose slots leave room for the extra vector; not with packed bits.)
+  if (m == 1 && !any_b1 && !pl->stores.empty() && (P.tier == cmdx::kTier2 || P.tier == cmdx::kTier4)) {
+    bool ok = true;
+    int64_t sp = -1;
+    for (size_t i = 0; i < all.size() && ok; ++i)
+      if (wst[i][0] != 1) ok = false;
+    for (const View& v : pl->stores) {
+      const int64_t ph = (int64_t)((reinterpret_cast<uintptr_t>(v.ptr) / (uintptr_t)elem_size(v.dtype)) % 4);
+      if (sp < 0) sp = ph;
+      else if (ph != sp) ok = false;
+    }
+    const int64_t head = (4 - sp) % 4 + 4;
+    const int64_t W = cmdx::contig_chunk(P.tier, P.extended, false);
+    if (ok && pl->n >= head + W + 4) {
+      pl->path = CMD_PATH_CONTIG;
+      pl->head = head;
+      pl->shifted = true;
       return CMD_OK;
     }
   }
@@ -1499,11 +1529,12 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     // whole warp chunks on the contiguous executor; a head (the elements
     // before every pointer is vector-aligned) and a ragged tail (fewer than
     // one chunk of elements) on the generic one
-    bool half2 = !pl.loads.empty();
+    bool half2 = !pl.shifted && !pl.loads.empty();
     for (const auto& v : pl.loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
     const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended, half2);
     const int64_t head = pl.head;
-    const int64_t n_main = (pl.n - head) - (pl.n - head) % chunk;  // (all of it over rows)
+    // (all of it over rows; a shifted launch leaves at least 4 elements after)
+    const int64_t n_main = pl.shifted ? (pl.n - head - 4) / chunk * chunk : (pl.n - head) - (pl.n - head) % chunk;
     // the generic executor over the 1-D elements [start, start + count),
     // skipping [start + gap_at, start + gap_at + gap)
     auto generic_range = [&](int64_t start, int64_t count, int64_t gap_at, int64_t gap) -> cudaError_t {
@@ -1537,8 +1568,13 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       cmdx::ContigParams p;
       std::memset(&p, 0, sizeof p);
       for (size_t j = 0; j < pl.loads.size(); ++j) {
-        p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + head * elem_size(pl.loads[j].dtype);
+        const int64_t es = elem_size(pl.loads[j].dtype);
+        p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + head * es;
         p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+        if (pl.shifted) {
+          p.in_shift[j] = (uint8_t)((reinterpret_cast<uintptr_t>(p.in[j]) / (uintptr_t)es) % 4);
+          p.shifted = 1;
+        }
       }
       for (size_t j = 0; j < pl.stores.size(); ++j)
         p.out[j] = static_cast<char*>(pl.stores[j].ptr) + head * elem_size(pl.stores[j].dtype);

@@ -169,6 +169,12 @@ struct ContigParams {
   int32_t row_chunks;
   int64_t in_ld[kMaxLoads];
   int64_t out_ld[kMaxStores];
+  // Shifted launches (1-D, the 2- and 4-slot tiers): load j's first element
+  // sits in_shift[j] elements past a vector boundary (0: aligned); every
+  // store is aligned, and each view extends at least 4 elements before and
+  // after the launch's range.
+  uint8_t in_shift[kMaxLoads];
+  uint8_t shifted;
 };
 
 // What the tile executor needs from the host. The logical index space is

@@ -79,6 +79,70 @@ __device__ __forceinline__ void contig_widen(uint32_t (&x)[V], int dt) {
   }
 }
 
+// A slot whose view starts r (1..3) elements past a vector boundary, while
+// the launch's stores are aligned (x[1:] - x[:-1], say): each lane reads the
+// aligned vectors that hold the start of its groups, from r elements before
+// the view, in the same pattern as contig_load (its base is `a`, r elements
+// before the view's); contig_shift then gives each lane its elements from
+// its own vector and its right neighbour's. The last lane takes the next
+// group's first vector, or for the chunk's last group one more vector, which
+// it reads there (the host starts such a launch at least 4 elements into the
+// views and leaves at least 4 after it, so these reads stay inside them).
+// 2-byte values are still packed, two to a word; r is uniform over the launch.
+template <int V>
+__device__ __forceinline__ void contig_shift(uint32_t (&x)[V], const void* a, int dt, int r, int64_t e0, int lane) {
+  using M = LaneMap<V>;
+  static_assert(M::G == 4, "shifted loads take groups of 4 elements");
+  const bool last = lane == 31;
+  // the vector after the chunk (read by the last lane only)
+  const int64_t e_after = e0 + 4 + (int64_t)(M::NG - 1) * 32 * M::G;
+  if (dt == 0 || dt == 3) {
+    uint4 ex = make_uint4(0, 0, 0, 0);
+    if (last) ex = ld_stream(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(a) + e_after));
+    const uint32_t exw[4] = {ex.x, ex.y, ex.z, ex.w};
+#pragma unroll
+    for (int h = 0; h < M::NG; ++h) {
+      uint32_t n[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t dn = __shfl_down_sync(0xffffffffu, x[4 * h + q], 1);
+        const uint32_t wrap = h + 1 < M::NG ? __shfl_sync(0xffffffffu, x[4 * (h + 1) + q], 0) : exw[q];
+        n[q] = last ? wrap : dn;
+      }
+      const uint32_t m1 = x[4 * h + 1], m2 = x[4 * h + 2], m3 = x[4 * h + 3];
+      if (r == 1) {
+        x[4 * h] = m1; x[4 * h + 1] = m2; x[4 * h + 2] = m3; x[4 * h + 3] = n[0];
+      } else if (r == 2) {
+        x[4 * h] = m2; x[4 * h + 1] = m3; x[4 * h + 2] = n[0]; x[4 * h + 3] = n[1];
+      } else {
+        x[4 * h] = m3; x[4 * h + 1] = n[0]; x[4 * h + 2] = n[1]; x[4 * h + 3] = n[2];
+      }
+    }
+  } else {
+    uint2 ex = make_uint2(0, 0);
+    if (last) ex = ld_stream(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a) + e_after));
+    const uint32_t exw[2] = {ex.x, ex.y};
+#pragma unroll
+    for (int h = 0; h < M::NG; ++h) {
+      uint32_t n[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t dn = __shfl_down_sync(0xffffffffu, x[2 * h + q], 1);
+        const uint32_t wrap = h + 1 < M::NG ? __shfl_sync(0xffffffffu, x[2 * (h + 1) + q], 0) : exw[q];
+        n[q] = last ? wrap : dn;
+      }
+      const uint32_t m0 = x[2 * h], m1 = x[2 * h + 1];
+      if (r == 1) {
+        x[2 * h] = __funnelshift_r(m0, m1, 16); x[2 * h + 1] = __funnelshift_r(m1, n[0], 16);
+      } else if (r == 2) {
+        x[2 * h] = m1; x[2 * h + 1] = n[0];
+      } else {
+        x[2 * h] = __funnelshift_r(m1, n[0], 16); x[2 * h + 1] = __funnelshift_r(n[0], n[1], 16);
+      }
+    }
+  }
+}
+
 // A view's row `row` (row-contiguous launches; row 0 is the base).
 __device__ __forceinline__ const void* row_start(const void* base, int64_t row, int64_t ld, int dt) {
   return static_cast<const char*>(base) + row * ld * ((dt == 0 || dt == 3) ? 4 : 2);
@@ -164,21 +228,31 @@ struct ContigStore {
   }
 };
 
-// One warp chunk: elements e0 .. of each view (of its row `row` when ROWS).
-template <int TIER, bool EXT, bool ROWS>
+// One warp chunk: elements e0 .. of each view (of its row `row` when ROWS;
+// with loads off the stores' alignment when SHIFT).
+template <int TIER, bool EXT, bool ROWS, bool SHIFT>
 __device__ __forceinline__ void contig_run_chunk(const ContigParams& p, const uint32_t* prog, int64_t e0,
                                                  int64_t row) {
   constexpr int S = tier_slots(TIER);
   constexpr int V = contig_vec(TIER, EXT);
   constexpr int NL = S < kMaxLoads ? S : kMaxLoads;
   uint32_t r[S][V];
+  // (a shifted load reads from the aligned vector before its first element)
+  auto base_of = [&](int j) -> const void* {
+    const void* b = p.in[j];
+    if constexpr (ROWS) b = row_start(b, row, p.in_ld[j], p.in_dt[j]);
+    if constexpr (SHIFT) b = static_cast<const char*>(b) - (int)p.in_shift[j] * ((p.in_dt[j] == 0 || p.in_dt[j] == 3) ? 4 : 2);
+    return b;
+  };
 #pragma unroll
   for (int j = 0; j < NL; ++j)
-    if (j < (int)p.n_loads) {
-      const void* b = p.in[j];
-      if constexpr (ROWS) b = row_start(b, row, p.in_ld[j], p.in_dt[j]);
-      contig_load<V>(r[j], b, p.in_dt[j], e0);
-    }
+    if (j < (int)p.n_loads) contig_load<V>(r[j], base_of(j), p.in_dt[j], e0);
+  if constexpr (SHIFT) {
+#pragma unroll
+    for (int j = 0; j < NL; ++j)
+      if (j < (int)p.n_loads && p.in_shift[j])
+        contig_shift<V>(r[j], base_of(j), p.in_dt[j], p.in_shift[j], e0, threadIdx.x & 31);
+  }
 #pragma unroll
   for (int j = 0; j < NL; ++j)
     if (j < (int)p.n_loads) contig_widen<V>(r[j], p.in_dt[j]);
@@ -191,7 +265,7 @@ __device__ __forceinline__ void contig_run_chunk(const ContigParams& p, const ui
 // ROWS: a row-contiguous launch; warp w takes chunk w % row_chunks of row
 // w / row_chunks, the pair stepped by the grid's warp count with a carry
 // instead of dividing per chunk.
-template <int TIER, bool EXT, int MINB, bool ROWS>
+template <int TIER, bool EXT, int MINB, bool ROWS, bool SHIFT>
 __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant__ ContigParams p) {
   constexpr int V = contig_vec(TIER, EXT);
   using M = LaneMap<V>;
@@ -231,14 +305,15 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
   pdl_trigger();
   if constexpr (!ROWS) {
     const int64_t n_chunks = p.n / M::W;  // the host passes a multiple of W
-    for (; w < n_chunks; w += nwarps) contig_run_chunk<TIER, EXT, false>(p, prog, w * M::W + (int64_t)lane * M::G, 0);
+    for (; w < n_chunks; w += nwarps)
+      contig_run_chunk<TIER, EXT, false, SHIFT>(p, prog, w * M::W + (int64_t)lane * M::G, 0);
   } else {
     // rows and row_chunks are below 2^31, and so is the grid's warp count
     const int rc = p.row_chunks;
     int row = (int)(w / rc), c = (int)(w % rc);
     const int drow = (int)(nwarps / rc), dc = (int)(nwarps % rc);
     while (row < p.rows) {
-      contig_run_chunk<TIER, EXT, true>(p, prog, (int64_t)c * M::W + (int64_t)lane * M::G, row);
+      contig_run_chunk<TIER, EXT, true, false>(p, prog, (int64_t)c * M::W + (int64_t)lane * M::G, row);
       c += dc;
       row += drow;
       if (c >= rc) {
@@ -253,7 +328,7 @@ cudaError_t CMDX_TIER_NAME(contig_upload_t)(int slot, const uint32_t* words, int
   return cudaMemcpyToSymbol(c_prog, words, sizeof(uint32_t) * n, sizeof(uint32_t) * kMaxWords * slot);
 }
 
-template <int TIER, bool EXT, bool ROWS>
+template <int TIER, bool EXT, bool ROWS, bool SHIFT = false>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   // (the 2-slot tier's dense-range kernel fits 64 registers and so runs four
   // CTAs per SM; its row-walking one is held to the same)
@@ -266,15 +341,24 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   const int64_t work_blocks = (p.n + (int64_t)kBlock * V - 1) / ((int64_t)kBlock * V);
   int full_grid = grid_cache.get(dev);
   if (full_grid == 0) {
-    full_grid = persistent_grid(contig_kernel<TIER, EXT, MINB, ROWS>, kBlock, 0, INT64_MAX);
+    full_grid = persistent_grid(contig_kernel<TIER, EXT, MINB, ROWS, SHIFT>, kBlock, 0, INT64_MAX);
     grid_cache.put(dev, full_grid);
   }
   const int grid = (int)(work_blocks < full_grid ? work_blocks : full_grid);
-  return launch_pdl(contig_kernel<TIER, EXT, MINB, ROWS>, grid, kBlock, 0, stream, p);
+  return launch_pdl(contig_kernel<TIER, EXT, MINB, ROWS, SHIFT>, grid, kBlock, 0, stream, p);
 }
+
+// Objects whose kernels take shifted loads: the 2- and 4-slot tiers (their
+// slots leave room for the extra vector per load), not the 16-element or
+// four-CTA builds.
+constexpr bool kShiftObject = (CMDX_TIER == kTier2 || CMDX_TIER == kTier4) && !CMDX_HALF16 && !CMDX_OCC4;
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
   if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);
+  if (p.shifted) {
+    if constexpr (kShiftObject) return launch_tier<CMDX_TIER, CMDX_EXT != 0, false, true>(p, stream);
+    return cudaErrorInvalidValue;
+  }
   return launch_tier<CMDX_TIER, CMDX_EXT != 0, false>(p, stream);
 }
 

@@ -1136,7 +1136,7 @@ def test_kernel_from_text_form(spec):
 
 
 @pytest.mark.parametrize("n,path", [(1 << 20, "contig"), (5000, "contig"), (3 * 64 * 96, "tile2d"),
-                                    (4099, "generic"), (64 * 1024, "rows")])
+                                    (500, "generic"), (64 * 1024, "rows"), (70_001, "shifted")])
 def test_back_to_back_dependent_launches(n, path):
     """Launches may begin while the previous kernel on the stream runs
     (programmatic dependent launch), but each waits for it before touching
@@ -1152,7 +1152,8 @@ def test_back_to_back_dependent_launches(n, path):
         sizes, st_x = (n,), (1,)
     dense = W._dense(sizes)[0]
     x = torch.from_numpy(rng.integers(-2**31, 2**31, size=n).astype(np.int32)).cuda()
-    if path == "generic":  # a misaligned base forces the generic executor
+    if path in ("generic", "shifted"):  # x one element off the vector alignment, y on it: too short
+        # for one warp chunk, per element; longer, the loads are shifted
         big = torch.empty(n + 1, dtype=torch.int32, device="cuda")
         big[1:].copy_(x)
         x = big[1:]
@@ -1177,7 +1178,7 @@ def test_back_to_back_dependent_launches(n, path):
     vy = T.TensorView(y.data_ptr(), sizes, dense)
     args_a = ka_k.args({xa: vx, ya: vy}, {ka: 7})
     args_b = kb_k.args({yb: vy, xb: vx}, {})
-    assert ka_k.plan({xa: vx, ya: vy}, {ka: 7})["path"] == ("contig" if path == "rows" else path)
+    assert ka_k.plan({xa: vx, ya: vy}, {ka: 7})["path"] == ("contig" if path in ("rows", "shifted") else path)
     host = (pad[:, :1024].reshape(-1) if pad is not None else x).cpu().numpy().astype(np.int64)
     stream = torch.cuda.current_stream().cuda_stream
     for _ in range(12):

@@ -312,8 +312,28 @@ def test_padded_rows_whole_chunks_long_take_the_contiguous_executor():
     assert _plan(bits)["path"] != "contig"
 
 
-def test_unaligned_pointer_falls_back_to_generic():
-    assert _plan(W.add_f32(4096), ptrs={"x": BASE + (1 << 28) + 4})["path"] == "generic"
+def test_loads_off_the_stores_alignment_take_the_shifted_contiguous_path():
+    """1-D unit-stride views whose loads sit off the stores' vector alignment
+    by other element counts run contiguous (shifted loads) in the 2- and
+    4-slot tiers once the launch is longer than its head (up to 7 elements),
+    one warp chunk and 4 more; otherwise, and for wider tiers, two stores at
+    different offsets, packed bits or a non-unit stride, per element."""
+    x_off = {"x": BASE + (1 << 28) + 4}                      # x one element past a 16-byte boundary
+    p = _plan(W.add_f32(4096), ptrs=x_off)
+    assert p["path"] == "contig" and p["merged_rank"] == 1
+    assert _plan(W.add_f32(512 + 11), ptrs=x_off)["path"] == "contig"
+    assert _plan(W.add_f32(512 + 6), ptrs=x_off)["path"] == "generic"   # shorter than head + chunk + 4
+    out_off = {"out": BASE + 2 * (1 << 28) + 8}                # the store two elements in: head 2 + 4
+    assert _plan(W.add_f32(4096), ptrs=out_off)["path"] == "contig"
+    assert _plan(W.wide_dag(4096), ptrs={"a": BASE + 4})["path"] == "generic"    # 8-slot tier
+    two = W.add_f32(4096)
+    two["ops"] = two["ops"] + [("store", "out2", "z", "f32")]
+    two["views"]["out2"] = dict(strides=(1,), alloc=4096)
+    assert _plan(two)["path"] == "contig"
+    assert _plan(two, ptrs={"x": BASE + 4, "out2": BASE + 3 * (1 << 28) + 4})["path"] == "generic"  # stores apart
+    stride2 = W.add_f32(4096)
+    stride2["views"]["x"] = dict(strides=(2,), alloc=8191)
+    assert _plan(stride2)["path"] == "generic"
 
 
 def test_launch_validation_errors():
