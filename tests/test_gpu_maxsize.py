@@ -39,7 +39,9 @@ def _formula(idx: np.ndarray, mul: int, add: int) -> np.ndarray:
     return (idx.astype(object) * mul + add) % 2**32
 
 
-def _int_case(n: int, offset: int, path: str):
+def _int_case(n: int, offset: int, path: str, z2_offset=None):
+    """z = x * y + x with x `offset` elements into its allocation; with
+    z2_offset, a second store of the same value that many elements in."""
     torch.cuda.empty_cache()
     big = torch.empty(n + offset, dtype=torch.int32, device="cuda")
     x = big[offset:]
@@ -51,18 +53,26 @@ def _int_case(n: int, offset: int, path: str):
     tx, ty = c.load_tensor("i32", 1), c.load_tensor("i32", 1)
     t = c.execute([("mul", tx, ty), ("add", T.CMD_LOCAL(0), tx)])
     tz = c.store(t[1], "i32", 1)
+    args = {tx: x, ty: y, tz: z}
+    outs = [z]
+    if z2_offset is not None:
+        big2 = torch.empty(n + z2_offset, dtype=torch.int32, device="cuda")
+        z2 = big2[z2_offset:]
+        args[c.store(t[1], "i32", 1)] = z2
+        outs.append(z2)
     k = c.compile()
-    assert k.plan({tx: x, ty: y, tz: z})["path"] == path
-    k.launch({tx: x, ty: y, tz: z})
+    assert k.plan(args)["path"] == path
+    k.launch(args)
     k.sync()
     torch.cuda.synchronize()
     idx = _sample(n, np.random.default_rng(n))
-    got = z[torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.int64) % 2**32
     xv, yv = _formula(idx, 1, 12345), _formula(idx, 2654435761, 7)
     want = np.array([int(a * b + a) % 2**32 for a, b in zip(xv, yv)], dtype=np.int64)
-    bad = np.flatnonzero(got != want)
-    assert bad.size == 0, (path, int(idx[bad[0]]), int(got[bad[0]]), int(want[bad[0]]))
-    del big, y, z
+    for out in outs:
+        got = out[torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.int64) % 2**32
+        bad = np.flatnonzero(got != want)
+        assert bad.size == 0, (path, int(idx[bad[0]]), int(got[bad[0]]), int(want[bad[0]]))
+    del big, y, z, outs, args
     torch.cuda.empty_cache()
 
 
@@ -70,9 +80,15 @@ def test_contiguous_past_2_32_elements():
     _int_case((1 << 32) + 37, 0, "contig")
 
 
+def test_shifted_loads_past_2_32_elements():
+    # x one element past its allocation's start, y and z aligned: the
+    # contiguous executor with x's loads shifted
+    _int_case((1 << 32) + 5, 1, "contig")
+
+
 def test_generic_past_2_32_elements():
-    # a base one element past an allocation's start is not 16-byte aligned
-    _int_case((1 << 32) + 5, 1, "generic")
+    # two stores at different offsets from the vector alignment: per element
+    _int_case((1 << 32) + 5, 1, "generic", z2_offset=1)
 
 
 def test_tile_past_2_31_elements():
