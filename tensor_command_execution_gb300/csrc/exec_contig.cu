@@ -288,8 +288,9 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
         e_first = (w - row0 * p.row_chunks) * M::W;
       }
       e_first += (int64_t)lane * M::G;
+      constexpr int NL = tier_slots(TIER) < kMaxLoads ? tier_slots(TIER) : kMaxLoads;
 #pragma unroll
-      for (int j = 0; j < kMaxLoads; ++j)
+      for (int j = 0; j < NL; ++j)
         if (j < (int)p.n_loads) {
           const void* b = p.in[j];
           if constexpr (ROWS) b = row_start(b, row0, p.in_ld[j], p.in_dt[j]);
