@@ -56,3 +56,50 @@ def test_launch_on_pinned_host_buffers(spec, planned):
         for n in W.store_names(spec):
             got = host[n].numpy().view(specutil.NP[dts[n]])
             gpuutil.compare(got, want[n], dts[n], f"pinned host, call {call}: {n}")
+
+
+def test_padded_rows_on_pinned_host_buffers():
+    """Padded rows (the contiguous executor's row walk) over pinned host
+    memory."""
+    import test_gpu_rows as R
+    spec, bufs = R.padded_spec("rows_host", 37, 1024, {"x": ("f32", 1032), "y": ("bf16", 1088)},
+                               {"out": ("z", "f32", 1028)}, [("add", "z", "x", "y")], seed=4)
+    want = gpuutil.oracle_every_element(spec, bufs)
+    dts = W.tensor_dtypes(spec)
+    host = {n: _pinned(bufs[n], dts[n]) for n in bufs}
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    views = {tags[n]: T.TensorView(t.data_ptr(), spec["sizes"], spec["views"][n]["strides"]) for n, t in host.items()}
+    plan = k.plan(views)
+    assert plan["path"] == "contig" and plan["merged_rank"] == 2
+    k.launch(views)
+    k.sync()
+    torch.cuda.synchronize()
+    gpuutil.compare(host["out"].numpy().view(specutil.NP["f32"]), want["out"], "f32", "padded rows, pinned host")
+
+
+def test_shifted_loads_on_pinned_host_buffers():
+    """x one element and y three elements past a 16-byte boundary, out on
+    it (shifted loads) over pinned host memory."""
+    n = 50_021
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal(n).astype(np.float32)
+    y = rng.standard_normal(n).astype(np.float32)
+    spec = dict(name="shift_host", seed=0, sizes=(n,),
+                ops=[("load", "x", "f32"), ("load", "y", "f32"), ("exec", [("mul", "z", "x", "y")]),
+                     ("store", "out", "z", "f32")],
+                views={k: dict(strides=(1,), alloc=n) for k in ("x", "y", "out")}, inputs={})
+    bufs = {"x": x, "y": y, "out": specutil.sentinel_array("f32", n)}
+    want = gpuutil.oracle_every_element(spec, bufs)
+    hx = _pinned(np.concatenate([np.zeros(1, np.float32), x]), "f32")[1:]
+    hy = _pinned(np.concatenate([np.zeros(3, np.float32), y]), "f32")[3:]
+    ho = _pinned(bufs["out"], "f32")
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    views = {tags["x"]: hx, tags["y"]: hy, tags["out"]: ho}
+    assert k.plan(views)["path"] == "contig"
+    for call in range(2):
+        k.launch(views)
+        k.sync()
+        torch.cuda.synchronize()
+        gpuutil.compare(ho.numpy(), want["out"], "f32", f"shifted loads, pinned host, call {call}")
