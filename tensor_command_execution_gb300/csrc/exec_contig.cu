@@ -94,6 +94,8 @@ __device__ __forceinline__ void contig_shift(uint32_t (&x)[V], const void* a, in
   using M = LaneMap<V>;
   static_assert(M::G == 4, "shifted loads take groups of 4 elements");
   const bool last = lane == 31;
+  const bool r1 = r == 1, r2 = r == 2, hi = r >= 2;
+  const uint32_t sh = (r & 1) * 16;
   // the vector after the chunk (read by the last lane only)
   const int64_t e_after = e0 + 4 + (int64_t)(M::NG - 1) * 32 * M::G;
   if (dt == 0 || dt == 3) {
@@ -109,14 +111,12 @@ __device__ __forceinline__ void contig_shift(uint32_t (&x)[V], const void* a, in
         const uint32_t wrap = h + 1 < M::NG ? __shfl_sync(0xffffffffu, x[4 * (h + 1) + q], 0) : exw[q];
         n[q] = last ? wrap : dn;
       }
+      // elements r .. r + 3 of (m0 m1 m2 m3 n0 n1 n2), selected without branching
       const uint32_t m1 = x[4 * h + 1], m2 = x[4 * h + 2], m3 = x[4 * h + 3];
-      if (r == 1) {
-        x[4 * h] = m1; x[4 * h + 1] = m2; x[4 * h + 2] = m3; x[4 * h + 3] = n[0];
-      } else if (r == 2) {
-        x[4 * h] = m2; x[4 * h + 1] = m3; x[4 * h + 2] = n[0]; x[4 * h + 3] = n[1];
-      } else {
-        x[4 * h] = m3; x[4 * h + 1] = n[0]; x[4 * h + 2] = n[1]; x[4 * h + 3] = n[2];
-      }
+      x[4 * h] = r1 ? m1 : r2 ? m2 : m3;
+      x[4 * h + 1] = r1 ? m2 : r2 ? m3 : n[0];
+      x[4 * h + 2] = r1 ? m3 : r2 ? n[0] : n[1];
+      x[4 * h + 3] = r1 ? n[0] : r2 ? n[1] : n[2];
     }
   } else {
     uint2 ex = make_uint2(0, 0);
@@ -131,14 +131,12 @@ __device__ __forceinline__ void contig_shift(uint32_t (&x)[V], const void* a, in
         const uint32_t wrap = h + 1 < M::NG ? __shfl_sync(0xffffffffu, x[2 * (h + 1) + q], 0) : exw[q];
         n[q] = last ? wrap : dn;
       }
+      // elements r .. r + 3 (two to a word) of (m0 m1 n0 n1): words r / 2 ..
+      // shifted right by 16 (r % 2) bits, without branching
       const uint32_t m0 = x[2 * h], m1 = x[2 * h + 1];
-      if (r == 1) {
-        x[2 * h] = __funnelshift_r(m0, m1, 16); x[2 * h + 1] = __funnelshift_r(m1, n[0], 16);
-      } else if (r == 2) {
-        x[2 * h] = m1; x[2 * h + 1] = n[0];
-      } else {
-        x[2 * h] = __funnelshift_r(m1, n[0], 16); x[2 * h + 1] = __funnelshift_r(n[0], n[1], 16);
-      }
+      const uint32_t w0 = hi ? m1 : m0, w1 = hi ? n[0] : m1, w2 = hi ? n[1] : n[0];
+      x[2 * h] = __funnelshift_r(w0, w1, sh);
+      x[2 * h + 1] = __funnelshift_r(w1, w2, sh);
     }
   }
 }
