@@ -209,9 +209,9 @@ typedef enum cmd_path {
                            alignment by one number of elements (the few elements before
                            they align run per element): vector loads/stores. 1-D views
                            whose loads sit off the stores' alignment by other numbers of
-                           elements also take it in the 2- and 4-slot tiers (shifted
-                           loads; the first 4 to 7 and the last 4 or more elements run
-                           per element). With
+                           elements also take it, up to 16 live values (shifted loads;
+                           the first 4 to 7 and the last 4 or more elements run per
+                           element). With
                            merged_rank 2: rows, every view unit-stride along the columns,
                            each row starting on a 4-element boundary (a load's row stride
                            may be 0) and a whole number of warp chunks long (padded or

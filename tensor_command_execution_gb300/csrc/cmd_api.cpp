@@ -896,9 +896,9 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   // stores align, plus 4 elements; from there each load is read as aligned
   // vectors from up to 3 elements before it, each lane taking the end of its
   // elements from its right neighbour, and a tail of at least 4 elements is
-  // left, so that those vectors stay inside the views. (The 2- and 4-slot
-  // tiers, whose slots leave room for the extra vector; not with packed bits.)
-  if (m == 1 && !any_b1 && !pl->stores.empty() && (P.tier == cmdx::kTier2 || P.tier == cmdx::kTier4)) {
+  // left, so that those vectors stay inside the views. (Not in the 32-slot
+  // tier, whose lanes hold groups of 2 elements; not with packed bits.)
+  if (m == 1 && !any_b1 && !pl->stores.empty() && P.tier != cmdx::kTier32) {
     bool ok = true;
     int64_t sp = -1;
     for (size_t i = 0; i < all.size() && ok; ++i)

@@ -169,7 +169,7 @@ struct ContigParams {
   int32_t row_chunks;
   int64_t in_ld[kMaxLoads];
   int64_t out_ld[kMaxStores];
-  // Shifted launches (1-D, the 2- and 4-slot tiers): load j's first element
+  // Shifted launches (1-D, every tier but the 32-slot one): load j's first element
   // sits in_shift[j] elements past a vector boundary (0: aligned); every
   // store is aligned, and each view extends at least 4 elements before and
   // after the launch's range.

@@ -331,7 +331,11 @@ template <int TIER, bool EXT, bool ROWS, bool SHIFT = false>
 static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   // (the 2-slot tier's dense-range kernel fits 64 registers and so runs four
   // CTAs per SM; its row-walking one is held to the same)
-  constexpr int MINB = (CMDX_OCC4 || (ROWS && TIER == kTier2 && !EXT)) ? 4 : tier_min_blocks(TIER);
+  // (the 8-slot kernel with shifted loads is held to two CTAs per SM: at
+  // three it spilled 160 bytes)
+  constexpr int MINB = (CMDX_OCC4 || (ROWS && TIER == kTier2 && !EXT)) ? 4
+                       : (SHIFT && TIER == kTier8)                     ? 2
+                                                                       : tier_min_blocks(TIER);
   constexpr int V = contig_vec(TIER, EXT);
   constexpr int kBlock = 256;
   static DeviceCache grid_cache;  // (static storage: zero before first use)
@@ -347,10 +351,10 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   return launch_pdl(contig_kernel<TIER, EXT, MINB, ROWS, SHIFT>, grid, kBlock, 0, stream, p);
 }
 
-// Objects whose kernels take shifted loads: the 2- and 4-slot tiers (their
-// slots leave room for the extra vector per load), not the 16-element or
-// four-CTA builds.
-constexpr bool kShiftObject = (CMDX_TIER == kTier2 || CMDX_TIER == kTier4) && !CMDX_HALF16 && !CMDX_OCC4;
+// Objects whose kernels take shifted loads: every tier whose lanes hold
+// groups of 4 elements (not the 32-slot one), not the 16-element or
+// four-CTA builds (the host never sends them shifted launches).
+constexpr bool kShiftObject = CMDX_TIER != kTier32 && !CMDX_HALF16 && !CMDX_OCC4;
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
   if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);

@@ -133,3 +133,39 @@ def test_finite_difference_of_one_tensor():
     k.sync()
     torch.cuda.synchronize()
     gpuutil.compare(out.cpu().numpy(), want["out"], "f32", "x[1:] - x[:-1]")
+
+
+@pytest.mark.parametrize("offs", [{"a": 1, "c": 2}, {"b": 3, "out0": 2, "out1": 2}, {"f": 1, "e": 2, "d": 3}])
+def test_wide_dag_in_the_8_slot_tier(offs):
+    """The 16-op DAG (8-slot tier, its shifted kernel at two CTAs per SM),
+    fp32 and fp16 stores at one offset, loads at others."""
+    spec = W.wide_dag(60_013)
+    bufs = specutil.host_buffers(spec)
+    c, _ = T.command_from_spec(spec)
+    assert c.lower()[0]["tier"] == 2
+    _check(spec, bufs, offs)
+
+
+def test_extended_ops_in_the_8_slot_tier():
+    """The DAG with a division appended (the extended 8-slot kernel)."""
+    spec = W.wide_dag(40_009)
+    ops = list(spec["ops"])
+    i = next(k for k, o in enumerate(ops) if o[0] == "exec")
+    ops[i] = ("exec", list(ops[i][1]) + [("div", "t17", "t16", "t4")])
+    ops = [("store", "out0", "t17", "f32") if (o[0] == "store" and o[1] == "out0") else o for o in ops]
+    spec = dict(spec, ops=ops, name="wide_dag_div")
+    bufs = specutil.host_buffers(spec)
+    c, _ = T.command_from_spec(spec)
+    info = c.lower()[0]
+    assert info["tier"] == 2 and info["extended"] == 1, info
+    _check(spec, bufs, {"a": 2, "e": 1})
+
+
+@pytest.mark.parametrize("offs", [{"x0": 1}, {"x0": 1, "x5": 2, "x8": 3, "out": 1}])
+def test_sixteen_slot_tier_shifted(offs):
+    """Nine loads live at once (the 16-slot tier), shifted loads."""
+    spec = W.wide32_f32((1 << 16) + 7)
+    bufs = specutil.host_buffers(spec)
+    c, _ = T.command_from_spec(spec)
+    assert c.lower()[0]["tier"] == 4
+    _check(spec, bufs, offs)

@@ -314,10 +314,10 @@ def test_padded_rows_whole_chunks_long_take_the_contiguous_executor():
 
 def test_loads_off_the_stores_alignment_take_the_shifted_contiguous_path():
     """1-D unit-stride views whose loads sit off the stores' vector alignment
-    by other element counts run contiguous (shifted loads) in the 2- and
-    4-slot tiers once the launch is longer than its head (up to 7 elements),
-    one warp chunk and 4 more; otherwise, and for wider tiers, two stores at
-    different offsets, packed bits or a non-unit stride, per element."""
+    by other element counts run contiguous (shifted loads) once the launch
+    is longer than its head (up to 7 elements), one warp chunk and 4 more;
+    shorter, in the 32-slot tier, with two stores at different offsets,
+    packed bits or a non-unit stride, per element."""
     x_off = {"x": BASE + (1 << 28) + 4}                      # x one element past a 16-byte boundary
     p = _plan(W.add_f32(4096), ptrs=x_off)
     assert p["path"] == "contig" and p["merged_rank"] == 1
@@ -325,7 +325,11 @@ def test_loads_off_the_stores_alignment_take_the_shifted_contiguous_path():
     assert _plan(W.add_f32(512 + 6), ptrs=x_off)["path"] == "generic"   # shorter than head + chunk + 4
     out_off = {"out": BASE + 2 * (1 << 28) + 8}                # the store two elements in: head 2 + 4
     assert _plan(W.add_f32(4096), ptrs=out_off)["path"] == "contig"
-    assert _plan(W.wide_dag(4096), ptrs={"a": BASE + 4})["path"] == "generic"    # 8-slot tier
+    assert _plan(W.wide_dag(4096), ptrs={"a": BASE + 4})["path"] == "contig"     # 8-slot tier
+    wide = W.wide32_f32(4096)
+    c, _ = T.command_from_spec(wide)
+    assert c.lower()[0]["tier"] == 4                                             # 16 slots
+    assert _plan(wide, ptrs={"x0": BASE + 4})["path"] == "contig"
     two = W.add_f32(4096)
     two["ops"] = two["ops"] + [("store", "out2", "z", "f32")]
     two["views"]["out2"] = dict(strides=(1,), alloc=4096)
