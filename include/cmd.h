@@ -215,7 +215,9 @@ typedef enum cmd_path {
                            merged_rank 2: rows, every view unit-stride along the columns,
                            each row starting on a 4-element boundary (a load's row stride
                            may be 0) and a whole number of warp chunks long (padded or
-                           sliced row-major tensors) */
+                           sliced row-major tensors); or rows at offsets from that
+                           boundary with row strides of whole 4-element vectors, whose
+                           first and last few columns run per element */
   CMD_PATH_TILE2D = 2,  /* 2-D views, row-direct or transposed, staged through shared memory */
   CMD_PATH_GENERIC = 3  /* any other sizes/strides: per-element offsets */
 } cmd_path;

@@ -939,6 +939,35 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
       return CMD_OK;
     }
   }
+  // Shifted rows: as above, but the views' rows start at different offsets
+  // from the vector alignment (x[:, 1:] of a wider x, say); every row stride
+  // is a whole number of vectors, so each view keeps one offset on every
+  // row. Per row, the columns up to where the stores align plus 4, and a
+  // tail of at least 4, run per element; the columns between are whole warp
+  // chunks on the contiguous kernel's row walk with shifted loads. Taken
+  // only when the per-element columns are at most an eighth of a row.
+  if (m == 2 && !any_b1 && P.tier != cmdx::kTier32 && !pl->stores.empty()) {
+    bool ok = ms[0] < (int64_t(1) << 30);
+    int64_t sp = -1;
+    for (size_t i = 0; i < all.size() && ok; ++i)
+      if (wst[i][1] != 1 || wst[i][0] % 4 != 0) ok = false;
+    for (const View& v : pl->stores) {
+      const int64_t ph = (int64_t)((reinterpret_cast<uintptr_t>(v.ptr) / (uintptr_t)elem_size(v.dtype)) % 4);
+      if (sp < 0) sp = ph;
+      else if (ph != sp) ok = false;
+    }
+    const int64_t head = (4 - sp) % 4 + 4;
+    const int64_t W = cmdx::contig_chunk(P.tier, P.extended, false);
+    const int64_t cols = ms[1];
+    const int64_t main_cols = cols >= head + 4 ? (cols - head - 4) / W * W : 0;
+    if (ok && main_cols > 0 && 8 * (cols - main_cols) <= cols && main_cols / W < (int64_t(1) << 30)) {
+      pl->path = CMD_PATH_CONTIG;
+      pl->rows = ms[0];
+      pl->head = head;
+      pl->shifted = true;
+      return CMD_OK;
+    }
+  }
   // tile: two of the merged dims form the tile, the rest (at most two) are
   // batch dims. The column dim is the first store's unit-stride dim; the row
   // dim is the unit-stride dim of the loads that are not unit-stride along
@@ -1533,8 +1562,10 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     for (const auto& v : pl.loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
     const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended, half2);
     const int64_t head = pl.head;
-    // (all of it over rows; a shifted launch leaves at least 4 elements after)
-    const int64_t n_main = pl.shifted ? (pl.n - head - 4) / chunk * chunk : (pl.n - head) - (pl.n - head) % chunk;
+    // columns of a row walk; elements of a dense range (all of it over
+    // rows; a shifted launch leaves at least 4 elements after)
+    const int64_t cols = pl.rows > 1 ? pl.msizes[cmdx::kMaxRank - 1] : pl.n;
+    const int64_t n_main = pl.shifted ? (cols - head - 4) / chunk * chunk : (cols - head) - (cols - head) % chunk;
     // the generic executor over the 1-D elements [start, start + count),
     // skipping [start + gap_at, start + gap_at + gap)
     auto generic_range = [&](int64_t start, int64_t count, int64_t gap_at, int64_t gap) -> cudaError_t {
@@ -1579,14 +1610,14 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
       for (size_t j = 0; j < pl.stores.size(); ++j)
         p.out[j] = static_cast<char*>(pl.stores[j].ptr) + head * elem_size(pl.stores[j].dtype);
       std::memcpy(p.scal, pl.scal, sizeof p.scal);
-      p.n = n_main;
+      p.n = pl.rows > 1 ? pl.rows * n_main : n_main;
       p.prog = (uint32_t)k->slot;
       p.n_loads = (uint32_t)pl.loads.size();
       if (pl.rows > 1) {
         // merged dims are right-aligned: the row dim is the second to last
         const int rd = cmdx::kMaxRank - 2;
         p.rows = (int32_t)pl.rows;
-        p.row_chunks = (int32_t)(pl.msizes[rd + 1] / chunk);
+        p.row_chunks = (int32_t)(n_main / chunk);
         for (size_t j = 0; j < pl.loads.size(); ++j) p.in_ld[j] = pl.ml[j][rd];
         for (size_t j = 0; j < pl.stores.size(); ++j) p.out_ld[j] = pl.ms[j][rd];
       }
@@ -1597,9 +1628,41 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     // the tail from where the contiguous launch ends; with a head, head and
     // tail in one launch whose index space skips the contiguous launch's
     // elements (there are no packed-bit stores then: those index words by
-    // the launch's own element index)
-    if (e == cudaSuccess && pl.n > n_main)
+    // the launch's own element index). A row walk with shifted loads leaves
+    // each row's first `head` and last columns: two launches over those
+    // column ranges of every row.
+    if (pl.rows > 1 && pl.shifted) {
+      auto generic_cols = [&](int64_t c0, int64_t nc) -> cudaError_t {
+        cmdx::GenericParams p;
+        std::memset(&p, 0, sizeof p);
+        const int rd = cmdx::kMaxRank - 2;
+        for (size_t j = 0; j < pl.loads.size(); ++j) {
+          p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + c0 * elem_size(pl.loads[j].dtype);
+          p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
+          p.in_st[j][rd] = pl.ml[j][rd];
+          p.in_st[j][rd + 1] = 1;
+        }
+        for (size_t j = 0; j < pl.stores.size(); ++j) {
+          p.out[j] = static_cast<char*>(pl.stores[j].ptr) + c0 * elem_size(pl.stores[j].dtype);
+          p.out_st[j][rd] = pl.ms[j][rd];
+          p.out_st[j][rd + 1] = 1;
+        }
+        for (int d = 0; d < cmdx::kMaxRank; ++d) p.div[d] = make_fastdiv(1);
+        p.div[rd] = make_fastdiv(pl.rows);
+        p.div[rd + 1] = make_fastdiv(nc);
+        p.n = pl.rows * nc;
+        p.gap_at = p.n;  // no gap
+        p.top = (uint32_t)rd;
+        std::memcpy(p.scal, pl.scal, sizeof p.scal);
+        p.prog = (uint32_t)k->slot;
+        p.n_loads = (uint32_t)pl.loads.size();
+        return cmdx::generic_launch(P.tier, P.extended, p, stream);
+      };
+      if (e == cudaSuccess) e = generic_cols(0, head);
+      if (e == cudaSuccess) e = generic_cols(head + n_main, cols - head - n_main);
+    } else if (e == cudaSuccess && pl.n > n_main && pl.rows <= 1) {
       e = head == 0 ? generic_range(n_main, pl.n - n_main, pl.n, 0) : generic_range(0, pl.n - n_main, head, n_main);
+    }
   } else if (pl.path == CMD_PATH_TILE2D) {
     cmdx::Tile2dLaunch L;
     std::memset(&L, 0, sizeof L);

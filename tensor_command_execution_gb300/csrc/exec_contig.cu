@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(256, MINB) contig_kernel(const __grid_constant
     int row = (int)(w / rc), c = (int)(w % rc);
     const int drow = (int)(nwarps / rc), dc = (int)(nwarps % rc);
     while (row < p.rows) {
-      contig_run_chunk<TIER, EXT, true, false>(p, prog, (int64_t)c * M::W + (int64_t)lane * M::G, row);
+      contig_run_chunk<TIER, EXT, true, SHIFT>(p, prog, (int64_t)c * M::W + (int64_t)lane * M::G, row);
       c += dc;
       row += drow;
       if (c >= rc) {
@@ -333,7 +333,7 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   // CTAs per SM; its row-walking one is held to the same)
   // (the 8-slot kernel with shifted loads is held to two CTAs per SM: at
   // three it spilled 160 bytes)
-  constexpr int MINB = (CMDX_OCC4 || (ROWS && TIER == kTier2 && !EXT)) ? 4
+  constexpr int MINB = (CMDX_OCC4 || (ROWS && !SHIFT && TIER == kTier2 && !EXT)) ? 4
                        : (SHIFT && TIER == kTier8)                     ? 2
                                                                        : tier_min_blocks(TIER);
   constexpr int V = contig_vec(TIER, EXT);
@@ -357,11 +357,14 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
 constexpr bool kShiftObject = CMDX_TIER != kTier32 && !CMDX_HALF16 && !CMDX_OCC4;
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
-  if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);
   if (p.shifted) {
-    if constexpr (kShiftObject) return launch_tier<CMDX_TIER, CMDX_EXT != 0, false, true>(p, stream);
+    if constexpr (kShiftObject) {
+      if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true, true>(p, stream);
+      return launch_tier<CMDX_TIER, CMDX_EXT != 0, false, true>(p, stream);
+    }
     return cudaErrorInvalidValue;
   }
+  if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);
   return launch_tier<CMDX_TIER, CMDX_EXT != 0, false>(p, stream);
 }
 

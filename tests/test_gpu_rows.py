@@ -182,3 +182,73 @@ def test_sliced_torch_tensor():
     k.sync()
     torch.cuda.synchronize()
     gpuutil.compare(out.cpu().numpy().reshape(-1), want["out"], "f32", "x[:, :n] * y[:, :n]")
+
+
+def _shifted_rows_cases():
+    out = []
+    # x one element in, y and out aligned: 2-slot tier (512-element chunks), the
+    # row's first 4 and last 7 columns per element
+    out.append(("add_x1", 37, 2059, {"x": ("f32", 2064), "y": ("f32", 2060)}, {"out": ("z", "f32", 2060)},
+                [("add", "z", "x", "y")], (), {"x": 1}))
+    # bf16 chain (4-slot tier, 256-element chunks) with the store two elements in
+    out.append(("chain_bf16", 19, 2059, {"a": ("bf16", 2064), "b": ("bf16", 2080), "c": ("bf16", 2060)},
+                {"out": ("r", "bf16", 2064)}, CHAIN, (("s", "f32", 0.75),), {"a": 3, "b": 1, "out": 2}))
+    # a load read as one row for every row, at an offset
+    out.append(("bcast_i32", 29, 1037, {"x": ("i32", 1040), "y": ("i32", 0)}, {"o": ("t", "i32", 1044)},
+                [("mul", "t", "x", "y")], (), {"y": 2, "x": 1}))
+    # the wide DAG (8-slot tier)
+    wide_loads = {k: ("f32", 1040 + 4 * i) for i, k in enumerate("abcdef")}
+    out.append(("wide_dag", 11, 1037, wide_loads, {"out0": ("t16", "f32", 1040), "out1": ("t13", "f16", 1044)},
+                W.WIDE_DAG, (("s", "f32", 1.5), ("r", "f32", -0.25)), {"a": 1, "d": 2, "f": 3}))
+    return out
+
+
+@pytest.mark.parametrize("case", _shifted_rows_cases(), ids=lambda c: c[0])
+def test_rows_at_offsets_take_the_row_walk_with_shifted_loads(case):
+    """2-D views whose rows start at different offsets from the vector
+    alignment (x[:, 1:] of a wider x and the like; row strides whole vectors):
+    each row's first columns up to where the stores align plus 4 and its last
+    4 or more run per element, the rest on the row walk with shifted loads."""
+    name, rows, cols, loads, stores, block, scalars, offsets = case
+    spec, bufs = padded_spec(name, rows, cols, loads, stores, block, scalars, seed=rows + cols)
+    plan = gpuutil.parity(spec, bufs, offsets)
+    assert plan["path"] == "contig" and plan["merged_rank"] == 2, plan
+
+
+def test_rows_at_offsets_with_short_rows_run_per_element():
+    """More than an eighth of each row would run per element: the whole
+    launch does."""
+    spec, bufs = padded_spec("short_rows", 40, 700, {"x": ("f32", 704), "y": ("f32", 708)},
+                             {"out": ("z", "f32", 700)}, [("sub", "z", "x", "y")], seed=2)
+    plan = gpuutil.parity(spec, bufs, {"x": 1})
+    assert plan["path"] == "generic", plan
+
+
+def test_sliced_columns_of_torch_tensors():
+    """out[:, :n] = x[:, 1:n + 1] * y[:, :n] over (300, 4112) tensors: x's rows
+    start one element past a vector boundary."""
+    rows, wide, cols = 300, 4112, 4109
+    g = torch.Generator().manual_seed(8)
+    xw = torch.randn(rows, wide, generator=g)
+    yw = torch.randn(rows, wide, generator=g)
+    spec = dict(name="sliced_cols", seed=0, sizes=(rows, cols),
+                ops=[("load", "x", "f32"), ("load", "y", "f32"), ("exec", [("mul", "z", "x", "y")]),
+                     ("store", "out", "z", "f32")],
+                views={k: dict(strides=(wide, 1), alloc=(rows - 1) * wide + cols) for k in ("x", "y", "out")},
+                inputs={})
+    alloc = spec["views"]["x"]["alloc"]
+    bufs = {"x": xw.numpy().reshape(-1)[1:1 + alloc].copy(), "y": yw.numpy().reshape(-1)[:alloc].copy(),
+            "out": specutil.sentinel_array("f32", alloc)}
+    want = gpuutil.oracle_every_element(spec, bufs)["out"]
+    want = np.concatenate([want, np.zeros(wide - cols, np.float32)]).reshape(rows, wide)[:, :cols]
+    c, tags = T.command_from_spec(spec)
+    k = c.compile()
+    xd, yd = xw.cuda(), yw.cuda()
+    outw = torch.empty(rows, wide, device="cuda")
+    views = {tags["x"]: xd[:, 1:1 + cols], tags["y"]: yd[:, :cols], tags["out"]: outw[:, :cols]}
+    plan = k.plan(views)
+    assert plan["path"] == "contig" and plan["merged_rank"] == 2, plan
+    k.launch(views)
+    k.sync()
+    torch.cuda.synchronize()
+    gpuutil.compare(outw[:, :cols].cpu().numpy().reshape(-1), want.reshape(-1), "f32", "x[:, 1:n + 1] * y[:, :n]")
