@@ -44,6 +44,35 @@ __device__ __forceinline__ int64_t gen_offset(const GenericParams& p, const int6
   return off + (int64_t)rem * st[0];
 }
 
+// The row-major multi-index of linear element e, dims top .. kMaxRank - 1
+// (c[k] for k < top stays 0): computed once per element and dotted with each
+// view's strides by view_offset, so a launch with several loads divides once
+// per element, not once per view.
+__device__ __forceinline__ void gen_index(const GenericParams& p, int64_t e, int64_t (&c)[kMaxRank]) {
+  uint64_t rem = (uint64_t)e;
+#pragma unroll
+  for (int k = kMaxRank - 1; k >= 0; --k) {
+    c[k] = 0;
+    if (k < (int)p.top) continue;
+    if (k == (int)p.top || p.div[k].l == 0) {
+      c[k] = k == (int)p.top ? (int64_t)rem : 0;
+      if (k == (int)p.top) rem = 0;
+      continue;
+    }
+    const uint64_t q = fast_div(p.div[k], rem);
+    c[k] = (int64_t)(rem - q * (uint64_t)p.div[k].d);
+    rem = q;
+  }
+}
+
+__device__ __forceinline__ int64_t view_offset(const GenericParams& p, const int64_t (&c)[kMaxRank], const int64_t* st) {
+  int64_t off = c[kMaxRank - 1] * st[kMaxRank - 1];
+#pragma unroll
+  for (int k = 0; k < kMaxRank - 1; ++k)
+    if (k >= (int)p.top) off += c[k] * st[k];
+  return off;
+}
+
 template <int V>
 struct GenericStore {
   const GenericParams& p;
@@ -90,14 +119,33 @@ __global__ void __launch_bounds__(256, tier_min_blocks(TIER)) generic_kernel(con
     // every load of every view is issued before any is widened, so they are
     // all in flight at once (a widening right after each load would wait for
     // it before the next load issues)
+    if (p.top == kMaxRank - 1) {
+      // one dim: an element's offset in a view is one multiply
 #pragma unroll
-    for (int j = 0; j < NL; ++j) {
-      if (j < (int)p.n_loads) {
+      for (int j = 0; j < NL; ++j) {
+        if (j < (int)p.n_loads) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-          const int64_t e = base + 32 * v + lane;
-          r[j][v] = 0u;
-          if (e < p.n) r[j][v] = ld_elem(p.in[j], p.in_dt[j], gen_offset(p, p.in_st[j], e < p.gap_at ? e : e + p.gap));
+          for (int v = 0; v < V; ++v) {
+            const int64_t e = base + 32 * v + lane;
+            r[j][v] = 0u;
+            if (e < p.n)
+              r[j][v] = ld_elem(p.in[j], p.in_dt[j], (e < p.gap_at ? e : e + p.gap) * p.in_st[j][kMaxRank - 1]);
+          }
+        }
+      }
+    } else {
+      // several dims: the multi-index once per element, for every load
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int64_t e = base + 32 * v + lane;
+        int64_t c[kMaxRank];
+        gen_index(p, e < p.gap_at ? e : e + p.gap, c);
+#pragma unroll
+        for (int j = 0; j < NL; ++j) {
+          if (j < (int)p.n_loads) {
+            r[j][v] = 0u;
+            if (e < p.n) r[j][v] = ld_elem(p.in[j], p.in_dt[j], view_offset(p, c, p.in_st[j]));
+          }
         }
       }
     }
