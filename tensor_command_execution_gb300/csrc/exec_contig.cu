@@ -1,14 +1,19 @@
-// exec_contig.cu - contiguous executor: every view is dense row-major and
+// exec_contig.cu - contiguous executor: every view is unit-stride and
 // aligned for 4-element vectors, so each lane moves whole 16-byte (4-byte
 // types) or 8-byte (2-byte types) vectors, a warp's access is contiguous, and
 // the grid strides over warp-sized chunks of 32*V logical elements. It runs
 // whole chunks only: the host hands a ragged tail (fewer than 32*V elements),
 // and a head when every base is off the alignment by the same element count,
 // to the generic executor, so the hot loop carries no bounds checks.
+// Two more forms of the same kernel: a row walk over padded or sliced rows
+// whose length is a whole number of chunks (ROWS), and shifted loads for
+// views that sit off the stores' alignment by other element counts, read as
+// aligned vectors and assembled from neighbouring lanes (SHIFT).
 //
 // Compiled once per tier and op-set variant: CMDX_TIER and CMDX_EXT select
 // the kernel this object holds (and CMDX_OCC4 the four-CTA build of the
-// extended 2-slot kernel).
+// extended 2-slot kernel, CMDX_HALF16 the 16-element build of the base
+// 4-slot one).
 #include "exec_common.cuh"
 
 #if !defined(CMDX_TIER) || !defined(CMDX_EXT)
