@@ -939,35 +939,6 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
       return CMD_OK;
     }
   }
-  // Shifted rows: as above, but the views' rows start at different offsets
-  // from the vector alignment (x[:, 1:] of a wider x, say); every row stride
-  // is a whole number of vectors, so each view keeps one offset on every
-  // row. Per row, the columns up to where the stores align plus 4, and a
-  // tail of at least 4, run per element; the columns between are whole warp
-  // chunks on the contiguous kernel's row walk with shifted loads. Taken
-  // only when the per-element columns are at most an eighth of a row.
-  if (m == 2 && !any_b1 && P.tier != cmdx::kTier32 && !pl->stores.empty()) {
-    bool ok = ms[0] < (int64_t(1) << 30);
-    int64_t sp = -1;
-    for (size_t i = 0; i < all.size() && ok; ++i)
-      if (wst[i][1] != 1 || wst[i][0] % 4 != 0) ok = false;
-    for (const View& v : pl->stores) {
-      const int64_t ph = (int64_t)((reinterpret_cast<uintptr_t>(v.ptr) / (uintptr_t)elem_size(v.dtype)) % 4);
-      if (sp < 0) sp = ph;
-      else if (ph != sp) ok = false;
-    }
-    const int64_t head = (4 - sp) % 4 + 4;
-    const int64_t W = cmdx::contig_chunk(P.tier, P.extended, false);
-    const int64_t cols = ms[1];
-    const int64_t main_cols = cols >= head + 4 ? (cols - head - 4) / W * W : 0;
-    if (ok && main_cols > 0 && 8 * (cols - main_cols) <= cols && main_cols / W < (int64_t(1) << 30)) {
-      pl->path = CMD_PATH_CONTIG;
-      pl->rows = ms[0];
-      pl->head = head;
-      pl->shifted = true;
-      return CMD_OK;
-    }
-  }
   // tile: two of the merged dims form the tile, the rest (at most two) are
   // batch dims. The column dim is the first store's unit-stride dim; the row
   // dim is the unit-stride dim of the loads that are not unit-stride along
@@ -1042,6 +1013,36 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
       pl->n_batch = nbd;
       pl->batch[0] = bd[0];
       pl->batch[1] = bd[1];
+      return CMD_OK;
+    }
+  }
+  // Shifted rows: rows as above, but starting at different offsets from the
+  // vector alignment (x[:, 1:] of a wider x, say), views the tile executor
+  // cannot take either (its copies start on 16-byte boundaries); every row stride
+  // is a whole number of vectors, so each view keeps one offset on every
+  // row. Per row, the columns up to where the stores align plus 4, and a
+  // tail of at least 4, run per element; the columns between are whole warp
+  // chunks on the contiguous kernel's row walk with shifted loads. Taken
+  // only when the per-element columns are at most an eighth of a row.
+  if (m == 2 && !any_b1 && P.tier != cmdx::kTier32 && !pl->stores.empty()) {
+    bool ok = ms[0] < (int64_t(1) << 30);
+    int64_t sp = -1;
+    for (size_t i = 0; i < all.size() && ok; ++i)
+      if (wst[i][1] != 1 || wst[i][0] % 4 != 0) ok = false;
+    for (const View& v : pl->stores) {
+      const int64_t ph = (int64_t)((reinterpret_cast<uintptr_t>(v.ptr) / (uintptr_t)elem_size(v.dtype)) % 4);
+      if (sp < 0) sp = ph;
+      else if (ph != sp) ok = false;
+    }
+    const int64_t head = (4 - sp) % 4 + 4;
+    const int64_t W = cmdx::contig_chunk(P.tier, P.extended, false);
+    const int64_t cols = ms[1];
+    const int64_t main_cols = cols >= head + 4 ? (cols - head - 4) / W * W : 0;
+    if (ok && main_cols > 0 && 8 * (cols - main_cols) <= cols && main_cols / W < (int64_t(1) << 30)) {
+      pl->path = CMD_PATH_CONTIG;
+      pl->rows = ms[0];
+      pl->head = head;
+      pl->shifted = true;
       return CMD_OK;
     }
   }

@@ -306,6 +306,17 @@ def test_padded_rows_whole_chunks_long_take_the_contiguous_executor():
     ch["views"] = {k: dict(strides=(800, 1), alloc=10 * 800) for k in ("a", "b", "c", "out")}
     p = _plan(ch)
     assert p["path"] == "contig" and p["merged_rank"] == 2
+    # rows not a whole number of chunks: aligned views take the tile path, rows
+    # at an offset from the vector alignment (which tiles cannot start at) the
+    # row walk with shifted loads and their first and last columns per element
+    spec["sizes"] = (64, 8200)
+    spec["views"] = {"x": dict(strides=(8208, 1), alloc=64 * 8208), "y": dict(strides=(8204, 1), alloc=64 * 8204),
+                     "out": dict(strides=(8200, 1), alloc=64 * 8200)}
+    assert _plan(spec)["path"] == "tile2d"
+    p = _plan(spec, ptrs={"x": BASE + 4})
+    assert p["path"] == "contig" and p["merged_rank"] == 2
+    spec["sizes"] = (64, 700)                                     # a fifth of each row per element
+    assert _plan(spec, ptrs={"x": BASE + 4})["path"] == "generic"
     bits = W.threshold_bits(0)
     bits["sizes"] = (8, 1024)
     bits["views"] = {"x": dict(strides=(1040, 1), alloc=8 * 1040), "bits": dict(strides=(1024, 1), alloc=256)}
