@@ -356,7 +356,7 @@ cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* nee
 /* Validate args against the kernel and report the executor it would use,
  * without touching the GPU (and so without looking at where the memory lies:
  * cmd_launch runs a CMD_PATH_TILE2D plan on the generic executor when a load
- * is in pinned host memory). */
+ * is not in device memory). */
 cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_launch_plan* plan);
 
 /* Validate args and enqueue one fused pass on stream cuda_stream (a
@@ -366,9 +366,9 @@ cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_lau
  * be omitted. Stores must not overlap any other tensor argument (an identical
  * view of the same element type, used in place, is allowed) and must not
  * overlap themselves. Tensors may lie in pinned host memory (see
- * cmd_tensor_arg); views that would take the tile executor then run on the
- * generic one, since the tile executor's TMA copies are issued on device
- * memory only. Returns after the launch is enqueued (asynchronous). A
+ * cmd_tensor_arg); views that would take the tile executor run on the
+ * generic one whenever a load lies anywhere but in device memory, since the
+ * tile executor's TMA copies are issued on device memory only. Returns after the launch is enqueued (asynchronous). A
  * launch with zero elements does nothing. Safe to capture in a CUDA graph. */
 cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_stream);
 

@@ -1537,9 +1537,10 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     return fail(CMD_ERR_NOMEM, "out of host memory");
   }
   if (pl.path == CMD_PATH_NONE) return CMD_OK;
-  // A load in pinned host memory never takes the tile executor, whose loads
-  // are TMA copies that this library issues on device memory only; the
-  // generic executor reads the same views with plain loads.
+  // A load anywhere but in device memory (pinned or other host memory,
+  // managed memory) never takes the tile executor, whose loads are TMA
+  // copies that this library issues on device memory only; the generic
+  // executor reads the same views with plain loads.
   if (pl.path == CMD_PATH_TILE2D) {
     for (const View& v : pl.loads) {
       cudaPointerAttributes a;
@@ -1547,7 +1548,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
         cudaGetLastError();  // (an unknown pointer: left to the launch)
         continue;
       }
-      if (a.type == cudaMemoryTypeHost) {
+      if (a.type != cudaMemoryTypeDevice) {
         pl.path = CMD_PATH_GENERIC;
         break;
       }
