@@ -631,6 +631,27 @@ def spec_summary(spec):
     return f"{sizes} elements, {len(W.load_names(spec))} loads, {len(W.store_names(spec))} stores"
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine
+    type)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:  # lscpu missing or failing: fall through
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(spec, seconds):
     """The oracle, as it stands, on the host: single-threaded element walk over
     the first M elements of the same workload, M sized to about `seconds`."""
@@ -658,7 +679,7 @@ def cpu_baseline(spec, seconds):
     bpe = W.algorithmic_bytes(spec) / n_total
     return {"value": round(m * bpe / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {m} of {n_total} logical elements of the same workload, single thread, "
-                      f"{dt:.1f} s", "elements_per_s": round(m / dt, 1),
+                      f"{dt:.1f} s", "elements_per_s": round(m / dt, 1), "cpu_model": host_cpu_model(),
             "multicore": oracle_threads(oc, n_total, bpe, m / dt, seconds)}
 
 
@@ -728,7 +749,8 @@ def run_reference(args):
             "config": {"workload": f"{args.workload}: {spec_summary(spec)}"},
             "impl": "reference",
             "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{m} consecutive logical elements per step of {n_total}"},
+                             "sample": f"{m} consecutive logical elements per step of {n_total}",
+                             "cpu_model": host_cpu_model()},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
