@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define CMD_ABI_VERSION 2
+#define CMD_ABI_VERSION 3
 
 /* limits */
 #define CMD_MAX_RANK 4      /* logical dims of a tensor view */
@@ -229,6 +229,14 @@ typedef struct cmd_launch_plan {
   int64_t n_elements;     /* logical elements */
   int64_t bytes;          /* live loads read once + stores written once */
   int32_t n_transposed;   /* loads staged through shared memory (tile path) */
+  /* How a CMD_PATH_CONTIG launch splits (all 0 otherwise): the contiguous
+   * kernel runs contig_elements elements (of every row, for a row walk)
+   * starting head_elements in; the elements before and after them run per
+   * element. shifted_loads counts the loads read shifted (at another offset
+   * from the vector alignment than the stores). */
+  int64_t head_elements;
+  int64_t contig_elements;
+  int32_t shifted_loads;
 } cmd_launch_plan;
 
 int32_t cmd_abi_version(void);

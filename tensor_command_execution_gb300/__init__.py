@@ -79,12 +79,16 @@ class cmd_program_info(ctypes.Structure):
 class cmd_launch_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("merged_rank", ctypes.c_int32),
                 ("merged_sizes", ctypes.c_int64 * CMD_MAX_RANK), ("n_elements", ctypes.c_int64),
-                ("bytes", ctypes.c_int64), ("n_transposed", ctypes.c_int32)]
+                ("bytes", ctypes.c_int64), ("n_transposed", ctypes.c_int32),
+                ("head_elements", ctypes.c_int64), ("contig_elements", ctypes.c_int64),
+                ("shifted_loads", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {"path": PATHS.get(self.path, self.path), "merged_rank": self.merged_rank,
                 "merged_sizes": list(self.merged_sizes)[: self.merged_rank],
-                "n_elements": self.n_elements, "bytes": self.bytes, "n_transposed": self.n_transposed}
+                "n_elements": self.n_elements, "bytes": self.bytes, "n_transposed": self.n_transposed,
+                "head_elements": self.head_elements, "contig_elements": self.contig_elements,
+                "shifted_loads": self.shifted_loads}
 
 
 # Every symbol include/cmd.h declares, with (restype, argtypes).

@@ -1503,6 +1503,36 @@ cmd_status cmd_kernel_dump(cmd_kernel_t k, char* buf, int64_t size, int64_t* nee
   return CMD_OK;
 }
 
+// How a contiguous plan splits: the warp chunk of the kernel it runs, the
+// columns of a row walk (the elements of a dense range), and the elements
+// the contiguous kernel covers from `head` on (of every row for a row walk;
+// a shifted launch leaves at least 4 after them).
+namespace {
+struct ContigSplit {
+  bool half2;
+  int64_t chunk, cols, n_main;
+};
+
+ContigSplit contig_split(const Plan& pl, const Program& P) {
+  ContigSplit c;
+  c.half2 = !pl.shifted && !pl.loads.empty();
+  for (const auto& v : pl.loads) c.half2 = c.half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
+  c.chunk = cmdx::contig_chunk(P.tier, P.extended, c.half2);
+  c.cols = pl.rows > 1 ? pl.msizes[cmdx::kMaxRank - 1] : pl.n;
+  c.n_main = pl.shifted ? (c.cols - pl.head - 4) / c.chunk * c.chunk
+                        : (c.cols - pl.head) - (c.cols - pl.head) % c.chunk;
+  return c;
+}
+
+// Elements load j's first contiguous element sits past a vector boundary
+// (0 unless the launch is shifted).
+int load_shift(const Plan& pl, size_t j) {
+  if (!pl.shifted) return 0;
+  const int64_t es = elem_size(pl.loads[j].dtype);
+  return (int)(((reinterpret_cast<uintptr_t>(pl.loads[j].ptr) / (uintptr_t)es) + (uintptr_t)pl.head) % 4);
+}
+}  // namespace
+
 cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_launch_plan* plan) {
   if (!k || !plan) return fail(CMD_ERR_NULL, "k or plan is NULL");
   Plan pl;
@@ -1518,6 +1548,15 @@ cmd_status cmd_plan_launch(cmd_kernel_t k, const cmd_runtime_args* args, cmd_lau
   plan->n_elements = pl.n;
   plan->bytes = pl.bytes;
   plan->n_transposed = pl.n_trans;
+  plan->head_elements = 0;
+  plan->contig_elements = 0;
+  plan->shifted_loads = 0;
+  if (pl.path == CMD_PATH_CONTIG) {
+    const ContigSplit c = contig_split(pl, k->prog);
+    plan->head_elements = pl.head;
+    plan->contig_elements = c.n_main;
+    for (size_t j = 0; j < pl.loads.size(); ++j) plan->shifted_loads += load_shift(pl, j) != 0;
+  }
   return CMD_OK;
 }
 
@@ -1560,14 +1599,10 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
     // whole warp chunks on the contiguous executor; a head (the elements
     // before every pointer is vector-aligned) and a ragged tail (fewer than
     // one chunk of elements) on the generic one
-    bool half2 = !pl.shifted && !pl.loads.empty();
-    for (const auto& v : pl.loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
-    const int64_t chunk = cmdx::contig_chunk(P.tier, P.extended, half2);
+    const ContigSplit split = contig_split(pl, P);
+    const bool half2 = split.half2;
+    const int64_t chunk = split.chunk, cols = split.cols, n_main = split.n_main;
     const int64_t head = pl.head;
-    // columns of a row walk; elements of a dense range (all of it over
-    // rows; a shifted launch leaves at least 4 elements after)
-    const int64_t cols = pl.rows > 1 ? pl.msizes[cmdx::kMaxRank - 1] : pl.n;
-    const int64_t n_main = pl.shifted ? (cols - head - 4) / chunk * chunk : (cols - head) - (cols - head) % chunk;
     // the generic executor over the 1-D elements [start, start + count),
     // skipping [start + gap_at, start + gap_at + gap)
     auto generic_range = [&](int64_t start, int64_t count, int64_t gap_at, int64_t gap) -> cudaError_t {
@@ -1605,7 +1640,7 @@ cmd_status cmd_launch(cmd_kernel_t k, const cmd_runtime_args* args, void* cuda_s
         p.in[j] = static_cast<const char*>(pl.loads[j].ptr) + head * es;
         p.in_dt[j] = (uint8_t)pl.loads[j].dtype;
         if (pl.shifted) {
-          p.in_shift[j] = (uint8_t)((reinterpret_cast<uintptr_t>(p.in[j]) / (uintptr_t)es) % 4);
+          p.in_shift[j] = (uint8_t)load_shift(pl, j);
           p.shifted = 1;
         }
       }

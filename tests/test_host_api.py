@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(T.SIGNATURES), set(names) ^ set(T.SIGNATURES)
-    assert T.cmd_abi_version() == 2
+    assert T.cmd_abi_version() == 3
 
 
 def test_status_strings():

@@ -1,0 +1,73 @@
+"""How contiguous launches split, on the host (plans only, no GPU).
+
+Over random 1-D and 2-D layouts and programs (element offsets, padded and
+broadcast rows), each plan on the contiguous executor is checked against
+what keeps its accesses inside the views: the contiguous kernel's range is
+whole warp chunks inside the row or range; a launch that may read shifted
+(its head is 4 elements or more) leaves at least 4 elements after that
+range, so the aligned vectors read up to 3 elements before a shifted load's
+first element and up to 3 past the range's last stay inside; every load
+counted as shifted sits 1..3 elements off; otherwise the head is under one
+vector and what follows the range under one chunk (none in a row walk)."""
+from __future__ import annotations
+
+import pytest
+
+import tensor_command_execution_gb300 as T
+from inputgen import workloads as W
+import test_gpu_shifted as S  # random_layout_case: plain data, no GPU work
+
+BASE = 1 << 30
+# elements per slot per thread of the contiguous executor by tier
+VEC = {0: 16, 1: 8, 2: 8, 3: 2, 4: 4}
+
+
+def _plan(spec, offsets):
+    c, tags = T.command_from_spec(spec)
+    k = c.lower_kernel()
+    dts = W.tensor_dtypes(spec)
+    views, addr = {}, BASE
+    for n in W.load_names(spec) + W.store_names(spec):
+        es = 2 if dts[n] in ("f16", "bf16") else 4
+        views[tags[n]] = T.TensorView(addr + offsets.get(n, 0) * es, spec["sizes"], spec["views"][n]["strides"])
+        addr += 1 << 32
+    return k.plan(views, T.spec_scalars(spec, tags)), c.lower()[0], dts
+
+
+@pytest.mark.parametrize("seed", range(400))
+def test_contiguous_split_keeps_reads_inside_the_views(seed):
+    spec, _, offsets = S.random_layout_case(seed)
+    p, info, dts = _plan(spec, offsets)
+    if p["path"] != "contig":
+        assert p["head_elements"] == p["contig_elements"] == p["shifted_loads"] == 0
+        return
+    rows_walk = p["merged_rank"] == 2
+    cols = p["merged_sizes"][-1] if rows_walk else p["n_elements"]
+    head, main = p["head_elements"], p["contig_elements"]
+    half2 = all(dts[n] in ("f16", "bf16") for n in W.load_names(spec))
+    may_shift = head >= 4
+    v = 16 if (info["tier"] == 1 and not info["extended"] and half2 and not may_shift) else VEC[info["tier"]]
+    chunk = 32 * v
+    assert main % chunk == 0 and 0 <= head and head + main <= cols, p
+    if p["shifted_loads"]:
+        assert may_shift, p
+    if may_shift:
+        assert head <= 7 and cols - head - main >= 4 and main > 0, p
+        assert info["tier"] != 3, p   # the 32-slot tier never reads shifted
+    elif rows_walk:
+        assert head == 0 and main == cols, p
+    else:
+        assert head < 4 and cols - head - main < chunk, p
+
+
+def test_split_of_a_known_shifted_launch():
+    """4099 elements of the 2-slot tier (512-element chunks). x one element
+    in, y and out aligned: a head of 4, 3584 elements (7 chunks), 511 after.
+    Aligned: 4096 elements, 3 after. All three 3 elements in: a head of 1."""
+    spec = W.add_f32(4099)
+    p, _, _ = _plan(spec, {"x": 1})
+    assert (p["path"], p["head_elements"], p["contig_elements"], p["shifted_loads"]) == ("contig", 4, 3584, 1)
+    p, _, _ = _plan(spec, {})
+    assert (p["head_elements"], p["contig_elements"], p["shifted_loads"]) == (0, 4096, 0)
+    p, _, _ = _plan(spec, {"x": 3, "y": 3, "out": 3})   # one offset for all: a head of 1
+    assert (p["head_elements"], p["contig_elements"], p["shifted_loads"]) == (1, 4096, 0)
