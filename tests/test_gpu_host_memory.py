@@ -61,8 +61,8 @@ def test_launch_on_pinned_host_buffers(spec, planned):
 def test_padded_rows_on_pinned_host_buffers():
     """Padded rows (the contiguous executor's row walk) over pinned host
     memory."""
-    import test_gpu_rows as R
-    spec, bufs = R.padded_spec("rows_host", 37, 1024, {"x": ("f32", 1032), "y": ("bf16", 1088)},
+    import layouts
+    spec, bufs = layouts.padded_spec("rows_host", 37, 1024, {"x": ("f32", 1032), "y": ("bf16", 1088)},
                                {"out": ("z", "f32", 1028)}, [("add", "z", "x", "y")], seed=4)
     want = gpuutil.oracle_every_element(spec, bufs)
     dts = W.tensor_dtypes(spec)

@@ -14,6 +14,7 @@ import tensor_command_execution_gb300 as T
 from inputgen import workloads as W
 import gpuutil
 import oracle
+import layouts
 import specutil
 
 pytestmark = pytest.mark.gpu
@@ -21,36 +22,6 @@ pytestmark = pytest.mark.gpu
 # elements per slot per thread of the contiguous executor by tier (the base
 # 4-slot tier runs 16 when every load is 2-byte)
 VEC = {0: 16, 1: 8, 2: 8, 3: 2, 4: 4}
-
-
-def _values(rng, dt, n):
-    if dt == "i32":
-        return rng.integers(-2**31, 2**31, size=n).astype(np.int32)
-    f = (rng.standard_normal(n) * 3).astype(np.float32)
-    if dt == "f32":
-        return f
-    if dt == "f16":
-        return f.astype(np.float16)
-    return (f.view(np.uint32) >> 16).astype(np.uint16)
-
-
-def padded_spec(name, rows, cols, loads, stores, block, scalars=(), seed=0):
-    """loads: {name: (dtype, row stride)}; stores: {name: (source tag, dtype,
-    row stride)}; a row stride of 0 reads one row for every row."""
-    ops = [("load", n, dt) for n, (dt, _) in loads.items()]
-    ops += [("scalar", n, dt, v) for n, dt, v in scalars]
-    ops += [("exec", block)] + [("store", n, src, dt) for n, (src, dt, _) in stores.items()]
-    views = {}
-    for n, (dt, ld) in loads.items():
-        views[n] = dict(strides=(ld, 1), alloc=(rows - 1) * ld + cols)
-    for n, (_, dt, ld) in stores.items():
-        views[n] = dict(strides=(ld, 1), alloc=(rows - 1) * ld + cols)
-    spec = dict(name=name, seed=seed, sizes=(rows, cols), ops=ops, views=views, inputs={})
-    rng = np.random.default_rng(seed)
-    bufs = {n: _values(rng, dt, views[n]["alloc"]) for n, (dt, _) in loads.items()}
-    for n, (_, dt, _) in stores.items():
-        bufs[n] = specutil.sentinel_array(dt, views[n]["alloc"])
-    return spec, bufs
 
 
 def _chunk(spec):
@@ -117,7 +88,7 @@ def _cases():
 @pytest.mark.parametrize("case", _cases(), ids=lambda c: c[0])
 def test_padded_rows_on_the_contiguous_executor(case):
     name, rows, cols, loads, stores, block, scalars = case
-    spec, bufs = padded_spec(name, rows, cols, loads, stores, block, scalars, seed=len(name) * 7 + rows)
+    spec, bufs = layouts.padded_spec(name, rows, cols, loads, stores, block, scalars, seed=len(name) * 7 + rows)
     w, info = _chunk(spec)
     assert cols % w == 0, (cols, w, info)
     plan = gpuutil.parity(spec, bufs)
@@ -130,7 +101,7 @@ def test_row_walk_with_carries(rows, chunks):
     (row, chunk) pair is stepped by it with a carry): every row written
     once, the padding untouched. One row merges to a dense range."""
     cols = 512 * chunks
-    spec, bufs = padded_spec(f"walk{rows}x{chunks}", rows, cols, {"x": ("f32", cols + 16), "y": ("f32", cols + 4)},
+    spec, bufs = layouts.padded_spec(f"walk{rows}x{chunks}", rows, cols, {"x": ("f32", cols + 16), "y": ("f32", cols + 4)},
                              {"out": ("z", "f32", cols + 8)}, [("sub", "z", "x", "y")], seed=rows + chunks)
     plan = gpuutil.parity(spec, bufs)
     assert plan["path"] == "contig" and plan["merged_rank"] == (2 if rows > 1 else 1), plan
@@ -139,7 +110,7 @@ def test_row_walk_with_carries(rows, chunks):
 def test_padded_rows_in_place():
     """The store's view is the load's padded view (x = x * y + x, in place)."""
     rows, cols, ld = 40, 1024, 1040
-    spec, bufs = padded_spec("inplace", rows, cols, {"x": ("f32", ld), "y": ("f32", cols)},
+    spec, bufs = layouts.padded_spec("inplace", rows, cols, {"x": ("f32", ld), "y": ("f32", cols)},
                              {"xo": ("r", "f32", ld)}, [("mul", "p", "x", "y"), ("add", "r", "p", "x")], seed=3)
     ref = {k: v.copy() for k, v in bufs.items()}
     ref["xo"] = bufs["x"].copy()
@@ -210,7 +181,7 @@ def test_rows_at_offsets_take_the_row_walk_with_shifted_loads(case):
     each row's first columns up to where the stores align plus 4 and its last
     4 or more run per element, the rest on the row walk with shifted loads."""
     name, rows, cols, loads, stores, block, scalars, offsets = case
-    spec, bufs = padded_spec(name, rows, cols, loads, stores, block, scalars, seed=rows + cols)
+    spec, bufs = layouts.padded_spec(name, rows, cols, loads, stores, block, scalars, seed=rows + cols)
     plan = gpuutil.parity(spec, bufs, offsets)
     assert plan["path"] == "contig" and plan["merged_rank"] == 2, plan
 
@@ -218,7 +189,7 @@ def test_rows_at_offsets_take_the_row_walk_with_shifted_loads(case):
 def test_rows_at_offsets_with_short_rows_run_per_element():
     """More than an eighth of each row would run per element: the whole
     launch does."""
-    spec, bufs = padded_spec("short_rows", 40, 700, {"x": ("f32", 704), "y": ("f32", 708)},
+    spec, bufs = layouts.padded_spec("short_rows", 40, 700, {"x": ("f32", 704), "y": ("f32", 708)},
                              {"out": ("z", "f32", 700)}, [("sub", "z", "x", "y")], seed=2)
     plan = gpuutil.parity(spec, bufs, {"x": 1})
     assert plan["path"] == "generic", plan

@@ -15,7 +15,7 @@ import pytest
 
 import tensor_command_execution_gb300 as T
 from inputgen import workloads as W
-import test_gpu_shifted as S  # random_layout_case: plain data, no GPU work
+import layouts
 
 BASE = 1 << 30
 # elements per slot per thread of the contiguous executor by tier
@@ -36,7 +36,7 @@ def _plan(spec, offsets):
 
 @pytest.mark.parametrize("seed", range(400))
 def test_contiguous_split_keeps_reads_inside_the_views(seed):
-    spec, _, offsets = S.random_layout_case(seed)
+    spec, _, offsets = layouts.random_layout_case(seed)
     p, info, dts = _plan(spec, offsets)
     if p["path"] != "contig":
         assert p["head_elements"] == p["contig_elements"] == p["shifted_loads"] == 0
