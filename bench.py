@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=list(W.FULL) + list(W.PROFILE))
+    ap.add_argument("--workload", default=HEADLINE, choices=list(W.FULL) + list(W.LAYOUT) + list(W.PROFILE))
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -64,7 +64,7 @@ def parse():
 
 
 def make_spec(name, size):
-    f = W.FULL.get(name) or W.PROFILE[name]
+    f = W.FULL.get(name) or W.LAYOUT.get(name) or W.PROFILE[name]
     if not size:
         return f()
     if name == "strided_bf16":
@@ -73,6 +73,8 @@ def make_spec(name, size):
         return f(size, size)
     if name == "batched_transpose":
         return f(max(1, size // (1 << 20)))
+    if name == "rows_chain_f32":
+        return f(size, size)
     return f(size)
 
 
@@ -228,6 +230,14 @@ class Workload:
         self.dev = {n: t.to(device) for n, t in self.host.items()}
         for n in W.store_names(spec):
             self.dev[n] = torch.empty(spec["views"][n]["alloc"], dtype=torch_dtype(self.dts[n]), device=device)
+        # a tensor placed `off` elements into its allocation (spec offsets)
+        self._alloc = {}
+        for n, off in spec.get("offsets", {}).items():
+            t = self.dev[n]
+            big = torch.empty(t.numel() + off, dtype=t.dtype, device=device)
+            big[off:].copy_(t)
+            self._alloc[n] = big
+            self.dev[n] = big[off:]
         self.cmd, self.tags = T.command_from_spec(spec)
         self.kernel = self.cmd.compile()
         self.views = {self.tags[n]: self.view_of(n, t) for n, t in self.dev.items()}
@@ -478,7 +488,7 @@ DTYPE_OF = {"chain_f32": "f32", "add_f32": "f32", "wrap_i32": "int32", "strided_
             "tile4_f32": "f32", "wide32_f32": "f32",
             "wide_dag": "f32 (f32+f16 out)", "batched_transpose": "f32", "div_clamp_i32": "f32 (int32 out)",
             "threshold_u32": "u32 (int32 out)", "threshold_bits": "u32 (packed-bit out)",
-            "chain_bf16": "f32 (bf16 io)"}
+            "chain_bf16": "f32 (bf16 io)", "rows_chain_f32": "f32", "stencil_f32": "f32"}
 
 
 def run_ours(args):
@@ -549,7 +559,7 @@ def run_ours(args):
     # ---- other workloads, same kernels, full sizes (per-rank, informative) ---
     per = {}
     if not args.headline_only and rank == 0:
-        for name, f in W.FULL.items():
+        for name, f in list(W.FULL.items()) + list(W.LAYOUT.items()):
             if name == args.workload:
                 continue
             other = Workload(f(), device)

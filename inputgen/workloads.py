@@ -20,6 +20,9 @@ A workload ("spec") is a dict:
 ``views``     per load/store name: ``strides`` (elements) and ``alloc``
               (elements in the physical buffer; 32-bit words for a b1 store)
 ``inputs``    per load name: (distribution kind, lo, hi) for inputgen
+``offsets``   (optional) per tensor name: elements between its allocation's
+              start and the view's base (a view placed off the vector
+              alignment); absent names start at their allocation
 
 Nothing here computes the Command; the oracle side and the CUDA side each
 build their own Command from the same spec.
@@ -271,6 +274,36 @@ def wide32_f32(n: int = 1 << 24) -> dict:
     )
 
 
+def rows_chain_f32(m: int = 8192, n: int = 8192) -> dict:
+    """The chain Command over padded rows: a, b and c are m x n views of
+    wider row-major tensors (leading dimensions 8320, 8256 and 8200), out is
+    dense; normal(0,1), seed 12 (the contiguous executor's row walk)."""
+    lds = {"a": n + 128, "b": n + 64, "c": n + 8, "out": n}
+    spec = chain_f32(0)
+    spec.update(name="rows_chain_f32", seed=12, sizes=(m, n),
+                views={k: dict(strides=(ld, 1), alloc=(m - 1) * ld + n) for k, ld in lds.items()})
+    return spec
+
+
+def stencil_f32(n: int = 1 << 26) -> dict:
+    """out = (x1 - x0) * s + x2, s = 0.5, fp32, with x1 and x2 one and two
+    elements past the vector alignment and x0 and out on it (the layout of
+    a difference of neighbouring slices; normal(0,1), seed 13): the
+    contiguous executor with shifted loads. ``offsets`` gives each tensor's
+    element offset into its allocation."""
+    st, al = _dense((n,))
+    return dict(
+        name="stencil_f32", seed=13, sizes=(n,),
+        ops=[("load", "x0", "f32"), ("load", "x1", "f32"), ("load", "x2", "f32"),
+             ("scalar", "s", "f32", 0.5),
+             ("exec", [("sub", "d", "x1", "x0"), ("mul", "e", "d", "s"), ("add", "r", "e", "x2")]),
+             ("store", "out", "r", "f32")],
+        views={k: dict(strides=st, alloc=al) for k in ("x0", "x1", "x2", "out")},
+        inputs={k: ("normal_f32", 0.0, 0.0) for k in ("x0", "x1", "x2")},
+        offsets={"x1": 1, "x2": 2},
+    )
+
+
 # Full-size workloads, in the order they are listed for this path.
 FULL = {
     "add_f32": add_f32,
@@ -283,6 +316,14 @@ FULL = {
     "threshold_u32": threshold_u32,
     "threshold_bits": threshold_bits,
     "chain_bf16": chain_bf16,
+}
+
+# Layouts the contiguous executor takes beyond dense ranges (padded rows,
+# loads off the stores' alignment): the benchmark's per-workload table
+# lists them after the ones above.
+LAYOUT = {
+    "rows_chain_f32": rows_chain_f32,
+    "stencil_f32": stencil_f32,
 }
 
 # Cases that run the executor objects the workloads above do not reach (the

@@ -121,7 +121,7 @@ def full_parity(spec: dict) -> tuple:
     store buffer with the oracle (bit-exact; <= 1 ulp for 16-bit floats, and
     they are in fact exact). Returns (plan, elements compared, max ulp)."""
     bufs = specutil.host_buffers(spec)
-    got, plan = run_cuda(spec, bufs)
+    got, plan = run_cuda(spec, bufs, offsets=spec.get("offsets"))
     ref = oracle_every_element(spec, bufs)
     dts = W.tensor_dtypes(spec)
     checked, max_ulp = 0, 0

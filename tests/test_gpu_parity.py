@@ -64,6 +64,19 @@ def test_workload_full_size_every_element(name):
     assert max_ulp == 0
 
 
+@pytest.mark.parametrize("name", list(W.LAYOUT))
+def test_layout_workload_full_size_every_element(name):
+    """The benchmark's layout workloads at full size (the chain Command over
+    8192 x 8192 padded rows; the 2^26-element stencil with two loads off the
+    alignment), their offsets applied, every element against the oracle."""
+    spec = W.LAYOUT[name]()
+    plan, checked, max_ulp = gpuutil.full_parity(spec)
+    assert plan["path"] == "contig" and plan["merged_rank"] == (2 if name == "rows_chain_f32" else 1), plan
+    if name == "stencil_f32":
+        assert plan["shifted_loads"] == 2, plan
+    assert checked == sum(spec["views"][n]["alloc"] for n in W.store_names(spec))
+
+
 # ---- tile executor over dtypes, ragged tiles and several transposed loads -------------
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16", "i32"])
