@@ -897,8 +897,11 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   // vectors from up to 3 elements before it, each lane taking the end of its
   // elements from its right neighbour, and a tail of at least 4 elements is
   // left, so that those vectors stay inside the views. (Not in the 32-slot
-  // tier, whose lanes hold groups of 2 elements; not with packed bits.)
-  if (m == 1 && !any_b1 && !pl->stores.empty() && P.tier != cmdx::kTier32) {
+  // tier, whose lanes hold groups of 2 elements, nor in the extended 8-slot
+  // one, which is built with the dense-range kernel only; not with packed
+  // bits.)
+  const bool shift_tier = P.tier != cmdx::kTier32 && !(P.tier == cmdx::kTier8 && P.extended);
+  if (m == 1 && !any_b1 && !pl->stores.empty() && shift_tier) {
     bool ok = true;
     int64_t sp = -1;
     for (size_t i = 0; i < all.size() && ok; ++i)
@@ -923,8 +926,10 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   // for every row), and rows a whole number of the contiguous executor's
   // warp chunks long, so that no chunk crosses a row: the contiguous kernel
   // then walks (row, chunk) pairs. Padded and sliced row-major tensors
-  // (x[:, :n] of a wider x) take it. (Not with packed bits.)
-  if (m == 2 && !any_b1) {
+  // (x[:, :n] of a wider x) take it. (Not with packed bits, nor in the
+  // extended 8-slot tier, which is built with the dense-range kernel only.)
+  const bool dense_only = P.tier == cmdx::kTier8 && P.extended;
+  if (m == 2 && !any_b1 && !dense_only) {
     bool half2 = !pl->loads.empty();
     for (const auto& v : pl->loads) half2 = half2 && (v.dtype == CMD_F16 || v.dtype == CMD_BF16);
     const int64_t W = cmdx::contig_chunk(P.tier, P.extended, half2);
@@ -1024,7 +1029,7 @@ cmd_status plan_launch(const cmd_kernel* k, const cmd_runtime_args* args, Plan* 
   // tail of at least 4, run per element; the columns between are whole warp
   // chunks on the contiguous kernel's row walk with shifted loads. Taken
   // only when the per-element columns are at most an eighth of a row.
-  if (m == 2 && !any_b1 && P.tier != cmdx::kTier32 && !pl->stores.empty()) {
+  if (m == 2 && !any_b1 && shift_tier && !pl->stores.empty()) {
     bool ok = ms[0] < (int64_t(1) << 30);
     int64_t sp = -1;
     for (size_t i = 0; i < all.size() && ok; ++i)

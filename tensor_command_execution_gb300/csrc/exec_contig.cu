@@ -356,10 +356,16 @@ static cudaError_t launch_tier(const ContigParams& p, cudaStream_t stream) {
   return launch_pdl(contig_kernel<TIER, EXT, MINB, ROWS, SHIFT>, grid, kBlock, 0, stream, p);
 }
 
+// The extended 8-slot interpreter is the largest: each more form of its
+// kernel adds about half a minute to its object's compile, the build's
+// longest, so that object holds the dense-range kernel alone (the host
+// sends it no row walk and no shifted launch; such views take the tile or
+// generic executor).
+constexpr bool kDenseOnly = CMDX_TIER == kTier8 && CMDX_EXT;
 // Objects whose kernels take shifted loads: every tier whose lanes hold
 // groups of 4 elements (not the 32-slot one), not the 16-element or
 // four-CTA builds (the host never sends them shifted launches).
-constexpr bool kShiftObject = CMDX_TIER != kTier32 && !CMDX_HALF16 && !CMDX_OCC4;
+constexpr bool kShiftObject = CMDX_TIER != kTier32 && !kDenseOnly && !CMDX_HALF16 && !CMDX_OCC4;
 
 cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t stream) {
   if (p.shifted) {
@@ -369,7 +375,10 @@ cudaError_t CMDX_TIER_NAME(contig_launch_t)(const ContigParams& p, cudaStream_t 
     }
     return cudaErrorInvalidValue;
   }
-  if (p.rows > 1) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);
+  if (p.rows > 1) {
+    if constexpr (!kDenseOnly) return launch_tier<CMDX_TIER, CMDX_EXT != 0, true>(p, stream);
+    return cudaErrorInvalidValue;
+  }
   return launch_tier<CMDX_TIER, CMDX_EXT != 0, false>(p, stream);
 }
 

@@ -337,6 +337,12 @@ def test_loads_off_the_stores_alignment_take_the_shifted_contiguous_path():
     out_off = {"out": BASE + 2 * (1 << 28) + 8}                # the store two elements in: head 2 + 4
     assert _plan(W.add_f32(4096), ptrs=out_off)["path"] == "contig"
     assert _plan(W.wide_dag(4096), ptrs={"a": BASE + 4})["path"] == "contig"     # 8-slot tier
+    div = W.wide_dag(4096)   # with a division: the extended 8-slot tier, dense ranges only
+    i = next(k for k, o in enumerate(div["ops"]) if o[0] == "exec")
+    div["ops"][i] = ("exec", list(div["ops"][i][1]) + [("div", "t17", "t16", "t4")])
+    div["ops"] = [("store", "out0", "t17", "f32") if (o[0] == "store" and o[1] == "out0") else o for o in div["ops"]]
+    assert _plan(div)["path"] == "contig"
+    assert _plan(div, ptrs={"a": BASE + 4})["path"] == "generic"
     wide = W.wide32_f32(4096)
     c, _ = T.command_from_spec(wide)
     assert c.lower()[0]["tier"] == 4                                             # 16 slots

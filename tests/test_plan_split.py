@@ -49,6 +49,8 @@ def test_contiguous_split_keeps_reads_inside_the_views(seed):
     v = 16 if (info["tier"] == 1 and not info["extended"] and half2 and not may_shift) else VEC[info["tier"]]
     chunk = 32 * v
     assert main % chunk == 0 and 0 <= head and head + main <= cols, p
+    if info["tier"] == 2 and info["extended"]:   # built with the dense-range kernel only
+        assert not rows_walk and not may_shift, p
     if p["shifted_loads"]:
         assert may_shift, p
     if may_shift:
