@@ -73,3 +73,40 @@ def test_split_of_a_known_shifted_launch():
     assert (p["head_elements"], p["contig_elements"], p["shifted_loads"]) == (0, 4096, 0)
     p, _, _ = _plan(spec, {"x": 3, "y": 3, "out": 3})   # one offset for all: a head of 1
     assert (p["head_elements"], p["contig_elements"], p["shifted_loads"]) == (1, 4096, 0)
+
+
+def _with_division(spec):
+    """spec with a division appended to its T_Execute block and stored by its
+    first store: the extended variant of whatever tier the program lands in."""
+    ops = [list(o) if o[0] == "exec" else o for o in spec["ops"]]
+    i = next(k for k, o in enumerate(ops) if o[0] == "exec")
+    block = list(ops[i][1])
+    last = block[-1][1]
+    first_load = next(o[1] for o in ops if o[0] == "load")
+    block.append(("div", "Ediv", last, first_load))
+    ops[i] = ("exec", block)
+    j = next(k for k, o in enumerate(ops) if o[0] == "store")
+    ops[j] = ("store", ops[j][1], "Ediv", ops[j][3])
+    return dict(spec, ops=[tuple(o) for o in ops])
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_contiguous_split_with_extended_programs(seed):
+    """The same checks with a division in every program (the extended
+    variants; the extended 8-slot tier is built with the dense-range kernel
+    only, so it never plans a row walk or shifted loads)."""
+    spec, _, offsets = layouts.random_layout_case(seed)
+    spec = _with_division(spec)
+    p, info, dts = _plan(spec, offsets)
+    assert info["extended"] == 1
+    if p["path"] != "contig":
+        return
+    rows_walk = p["merged_rank"] == 2
+    cols = p["merged_sizes"][-1] if rows_walk else p["n_elements"]
+    head, main = p["head_elements"], p["contig_elements"]
+    chunk = 32 * VEC[info["tier"]]
+    assert main % chunk == 0 and head + main <= cols, p
+    if info["tier"] == 2:
+        assert not rows_walk and head < 4, p
+    if head >= 4:
+        assert head <= 7 and cols - head - main >= 4, p
